@@ -1,0 +1,251 @@
+/*
+ * Plain CPU oracle for the paged variable-length attention forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * CPU-baseline leg of the benchmark may load this code.  The product path
+ * (the CUDA library and its Python binding) never calls it, and this file
+ * shares no code, header, table or helper with that path.
+ *
+ * What it computes follows the pages literally, slowly and in order:
+ *
+ *   - "The attention backend and a reference implementation" (mini-sglang
+ *     from Scratch, ch. 5), section "Variable-length, paged attention with
+ *     prefixes": write this step's K/V into the pool first, then for each
+ *     request gather its whole KV through its page-table row, build the
+ *     [n, kv_len] bottom-right causal mask (query r sits at absolute position
+ *     kv_len - n + r and sees keys j <= kv_len - n + r), and apply
+ *     softmax(scale * Q K^T) V with grouped-query heads (enable_gqa).
+ *   - "Variable-length batching and one mixed forward pass", section
+ *     "Layout and metadata": query_start_loc / seq_lens / slot_mapping /
+ *     block tables; prefill, chunked prefill and decode are the same
+ *     computation with different (cached, new) lengths.
+ *
+ * Readings taken where the pages leave a step open (each restated in the
+ * design notes of the repository):
+ *   - page table entries are page ids; the pool slot of position j of
+ *     request i is page_table[i][j / page_size] * page_size + j % page_size
+ *     (with page_size 1 this is exactly the token-slot table of ch. 5);
+ *   - q head h uses kv head h / (Hq / Hkv) (the grouping of enable_gqa);
+ *   - LSE is the natural-log log-sum-exp of the scaled, masked scores;
+ *   - a slot_mapping entry of -1 means "no write" (padding token);
+ *   - arithmetic is fp32 (the precision the pages run their reference
+ *     backend in), sums taken in index order.
+ *
+ * Storage types: bf16 values are passed as their raw 16-bit patterns
+ * (uint16_t); bf16 -> fp32 is exact (the pattern becomes the high half).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static float bf16_bits_to_float(uint16_t b) {
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Number of OpenMP threads the attention loop will use (1 without OpenMP). */
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/*
+ * Pool slot of absolute position j of request i.
+ * Follows: page-level block tables ("Variable-length batching ...",
+ * section "Implementation": slot_mapping_for(table, pos, block_size)) and
+ * the ch. 5 page table read with page_size 1.
+ */
+static int64_t slot_of(const int32_t *page_table, int64_t ld, int page_size, int i, int64_t j) {
+    int64_t page = page_table[(int64_t)i * ld + j / page_size];
+    return page * page_size + j % page_size;
+}
+
+/*
+ * slot_mapping for this step's new tokens: request i's n_i new tokens are its
+ * last n_i positions kv_len_i - n_i .. kv_len_i - 1 ("The attention backend
+ * and a reference implementation", the worked example: out_loc is
+ * page_table[i, cached:len]).
+ * Returns 0, or -(i+1) if request i has n_i > kv_len_i or n_i < 0.
+ */
+int oracle_slot_mapping(int B, const int32_t *cu_seqlens_q, const int32_t *cache_seqlens,
+                        const int32_t *page_table, int64_t ld, int page_size, int64_t *slots_out) {
+    for (int i = 0; i < B; ++i) {
+        int n = cu_seqlens_q[i + 1] - cu_seqlens_q[i];
+        int L = cache_seqlens[i];
+        if (n < 0 || n > L) return -(i + 1);
+        for (int r = 0; r < n; ++r)
+            slots_out[cu_seqlens_q[i] + r] = slot_of(page_table, ld, page_size, i, (int64_t)(L - n + r));
+    }
+    return 0;
+}
+
+/*
+ * store_kvcache: pool[slot[t]][h][:] = new[t][h][:] for K and V, as raw bits.
+ * ("The attention backend ...", TorchAttnBackend.forward: store_kv before
+ * any read; "Attention backends: ...", step 2: do_kv_cache_update is a
+ * scatter by slot.)  slot -1 = skip.  Returns 0, or -(t+1) for the first
+ * token whose slot is out of range (nothing is written for that token).
+ */
+int oracle_store_kvcache(int64_t T, int Hkv, int D, const uint16_t *k, const uint16_t *v,
+                         const int64_t *slots, int64_t num_slots, uint16_t *k_pool, uint16_t *v_pool) {
+    int rc = 0;
+    const int64_t row = (int64_t)Hkv * D;
+    for (int64_t t = 0; t < T; ++t) {
+        int64_t s = slots[t];
+        if (s == -1) continue;
+        if (s < 0 || s >= num_slots) {
+            if (rc == 0) rc = (int)-(t + 1);
+            continue;
+        }
+        memcpy(k_pool + s * row, k + t * row, (size_t)row * sizeof(uint16_t));
+        memcpy(v_pool + s * row, v + t * row, (size_t)row * sizeof(uint16_t));
+    }
+    return rc;
+}
+
+/*
+ * The bottom-right causal mask of one request: M[r][j] = (j <= L - n + r),
+ * for r < n and j < L ("The attention backend and a reference
+ * implementation", the mask figure and "query r sits at absolute position
+ * kv_len - n + r").
+ */
+void oracle_causal_mask(int n, int L, uint8_t *mask_out) {
+    for (int r = 0; r < n; ++r)
+        for (int j = 0; j < L; ++j)
+            mask_out[(int64_t)r * L + j] = (uint8_t)(j <= L - n + r);
+}
+
+/*
+ * Attention over the paged pool, one request and one q head at a time.
+ *
+ *   for each request i with n = cu[i+1]-cu[i] > 0 and L = cache_seqlens[i]:
+ *     K_i[j], V_i[j] = pool[slot_of(i, j)]        j < L   (the page-table gather)
+ *     M = bottom-right causal mask [n, L]
+ *     for each q head h (kv head g = h / (Hq/Hkv)) and row r:
+ *       S[j] = scale * sum_d q[cu_i + r][h][d] * K_i[j][g][d]   (masked -> -inf)
+ *       m = max_j S[j];  p_j = exp(S[j] - m);  l = sum_j p_j
+ *       out[cu_i + r][h][:] = sum_j p_j V_i[j][g][:] / l
+ *       lse[cu_i + r][h]    = m + log(l)
+ *
+ * row_select (optional, [T*Hq] bytes): when given, only rows (t, h) with a
+ * nonzero byte are computed; others are left untouched.  This lets a test
+ * check sampled rows of a batch too large to compute whole.
+ *
+ * Returns 0, or -(i+1) when request i violates n <= L or reads a page id
+ * outside [0, num_pages).
+ */
+int oracle_attention(int B, const int32_t *cu_seqlens_q, const int32_t *cache_seqlens,
+                     const int32_t *page_table, int64_t ld, int page_size, int64_t num_pages,
+                     int Hq, int Hkv, int D, float scale,
+                     const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
+                     const uint8_t *row_select, float *out, float *lse) {
+    const int group = Hq / Hkv;
+    const int64_t kv_row = (int64_t)Hkv * D;
+
+    /* Validate first, so that the parallel loop below never reads out of range. */
+    for (int i = 0; i < B; ++i) {
+        int n = cu_seqlens_q[i + 1] - cu_seqlens_q[i];
+        int L = cache_seqlens[i];
+        if (n < 0 || n > L) return -(i + 1);
+        int64_t pages = n > 0 ? (L + page_size - 1) / page_size : 0;
+        for (int64_t p = 0; p < pages; ++p) {
+            int32_t id = page_table[(int64_t)i * ld + p];
+            if (id < 0 || id >= num_pages) return -(i + 1);
+        }
+    }
+
+    int rc = 0;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t work = 0; work < (int64_t)B * Hq; ++work) {
+        const int i = (int)(work / Hq);
+        const int h = (int)(work % Hq);
+        const int n = cu_seqlens_q[i + 1] - cu_seqlens_q[i];
+        const int L = cache_seqlens[i];
+        if (n == 0) continue;
+        const int q0 = cu_seqlens_q[i];
+        const int g = h / group;
+
+        if (row_select) {
+            int any = 0;
+            for (int r = 0; r < n && !any; ++r) any = row_select[(int64_t)(q0 + r) * Hq + h] != 0;
+            if (!any) continue;
+        }
+
+        /* gather this kv head's keys and values through the page table */
+        float *Ki = (float *)malloc(sizeof(float) * (size_t)L * D);
+        float *Vi = (float *)malloc(sizeof(float) * (size_t)L * D);
+        uint8_t *M = (uint8_t *)malloc((size_t)n * L);
+        float *S = (float *)malloc(sizeof(float) * (size_t)L);
+        float *qf = (float *)malloc(sizeof(float) * (size_t)D);
+        if (!Ki || !Vi || !M || !S || !qf) {
+            free(Ki); free(Vi); free(M); free(S); free(qf);
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            rc = -1000000;
+            continue;
+        }
+        for (int64_t j = 0; j < L; ++j) {
+            int64_t s = slot_of(page_table, ld, page_size, i, j);
+            const uint16_t *kr = k_pool + s * kv_row + (int64_t)g * D;
+            const uint16_t *vr = v_pool + s * kv_row + (int64_t)g * D;
+            for (int d = 0; d < D; ++d) {
+                Ki[j * D + d] = bf16_bits_to_float(kr[d]);
+                Vi[j * D + d] = bf16_bits_to_float(vr[d]);
+            }
+        }
+        oracle_causal_mask(n, L, M);
+
+        for (int r = 0; r < n; ++r) {
+            const int64_t t = q0 + r;
+            if (row_select && !row_select[t * Hq + h]) continue;
+            const uint16_t *qr = q + (t * Hq + h) * D;
+            for (int d = 0; d < D; ++d) qf[d] = bf16_bits_to_float(qr[d]);
+
+            float m = -INFINITY;
+            for (int64_t j = 0; j < L; ++j) {
+                if (!M[(int64_t)r * L + j]) {
+                    S[j] = -INFINITY;
+                    continue;
+                }
+                float acc = 0.0f;
+                for (int d = 0; d < D; ++d) acc += qf[d] * Ki[j * D + d];
+                S[j] = scale * acc;
+                if (S[j] > m) m = S[j];
+            }
+            float l = 0.0f;
+            float *o = out + (t * Hq + h) * D;
+            for (int d = 0; d < D; ++d) o[d] = 0.0f;
+            for (int64_t j = 0; j < L; ++j) {
+                if (!M[(int64_t)r * L + j]) continue;
+                float p = expf(S[j] - m);
+                l += p;
+                for (int d = 0; d < D; ++d) o[d] += p * Vi[j * D + d];
+            }
+            for (int d = 0; d < D; ++d) o[d] /= l;
+            if (lse) lse[t * Hq + h] = m + logf(l);
+        }
+        free(Ki); free(Vi); free(M); free(S); free(qf);
+    }
+    return rc;
+}
