@@ -1,0 +1,401 @@
+"""Benchmark: one step = prepare_metadata + one attn_forward (store + attention)
+over one synthetic batch, through the C ABI of libpva.so.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|mixed|cascade|worked]
+    python bench.py --impl reference ...     # the CPU oracle on a bounded sample
+
+Prints ONE JSON line.  Multi-GPU (torchrun, one process per GPU): every rank
+runs an independent replica of the workload (requests are independent; no
+collective in the data path), timing is max over ranks, `value` is the
+whole-job tokens/s (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged varlen attention tokens/s and % roofline (HBM for decode, TC for prefill)"
+L2_FLUSH_BYTES = 512 << 20  # > 4x the 129 MB L2
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="decode", choices=["worked", "decode", "prefill", "mixed", "cascade"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------------------ algorithmic work
+
+def algorithmic_work(wl):
+    """Bytes and FLOPs the step must move / compute, independent of the kernels.
+
+    bytes: every visible KV row once (unique pages), this step's Q read and O
+    write, the new K/V read and their pool write.  FLOPs: 4*D per visible
+    (query, key) pair per q head (QK^T and PV), causal pairs only.
+    """
+    import numpy as np
+
+    Hq, Hkv, D, ps = wl.num_qo_heads, wl.num_kv_heads, wl.head_dim, wl.page_size
+    row_kv = Hkv * D * 2  # bytes of one slot's K (or V) row, all kv heads
+    # unique KV rows read: positions < kv_len of each request, shared prefix pages counted once
+    seen = set()
+    kv_rows = 0
+    for i, L in enumerate(wl.kv_lens):
+        if wl.q_lens[i] == 0:
+            continue
+        full, rem = divmod(L, ps)
+        for p in range(full + (1 if rem else 0)):
+            pid = int(wl.page_table[i, p])
+            rows = ps if p < full else rem
+            key = (pid, rows)
+            if pid in seen:
+                continue
+            seen.add(pid)
+            kv_rows += rows
+    T = wl.total_tokens
+    kv_bytes = 2 * kv_rows * row_kv
+    q_bytes = T * Hq * D * 2
+    o_bytes = T * Hq * D * 2
+    new_kv_bytes = 2 * T * row_kv
+    store_bytes = 2 * new_kv_bytes  # read k,v + write pool
+    pairs = 0
+    for n, L in zip(wl.q_lens, wl.kv_lens):
+        # query r sees L - n + r + 1 keys
+        pairs += n * (L - n) + n * (n + 1) // 2
+    flops = 4 * D * Hq * pairs
+    no_share_kv = 2 * sum(L for n, L in zip(wl.q_lens, wl.kv_lens) if n) * row_kv
+    return {
+        "kv_bytes": kv_bytes, "q_bytes": q_bytes, "o_bytes": o_bytes, "store_bytes": store_bytes,
+        "attn_bytes": kv_bytes + q_bytes + o_bytes, "step_bytes": kv_bytes + q_bytes + o_bytes + store_bytes,
+        "flops": flops, "pairs": pairs, "kv_bytes_without_sharing": no_share_kv,
+    }
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, enabled: bool = True):
+        self.proc = None
+        self.path = None
+        if not enabled:
+            return
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = float(parts[2])
+                except ValueError:
+                    continue
+                for nm, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------------------ CPU oracle baseline
+
+def cpu_baseline(wl, tensors_cpu, budget_s: float):
+    """The oracle as it stands, timed on this host over a bounded sample of the
+    workload's requests (in order, until the estimated work reaches the budget)."""
+    import numpy as np
+
+    import oracle
+    from paged_variable_length_gb300 import workloads as W
+
+    oracle.build()
+    threads = oracle.num_threads()
+    # estimated oracle rate: ~0.5 GFLOP/s per thread on the plain loops (used only to size the sample)
+    rate = 0.5e9 * max(threads, 1)
+    chosen, est = [], 0.0
+    for i, (n, L) in enumerate(zip(wl.q_lens, wl.kv_lens)):
+        cost = 4.0 * wl.head_dim * wl.num_qo_heads * (n * L) + 1e6
+        if chosen and est + cost / rate > budget_s:
+            break
+        chosen.append(i)
+        est += cost / rate
+    cu = wl.cu_seqlens_q
+    rows = np.concatenate([np.arange(cu[i], cu[i + 1]) for i in chosen]) if chosen else np.zeros(0, np.int64)
+    sub_cu = np.concatenate([[0], np.cumsum([wl.q_lens[i] for i in chosen])]).astype(np.int32)
+    sub_lens = np.asarray([wl.kv_lens[i] for i in chosen], np.int32)
+    sub_table = wl.page_table[chosen]
+    q = tensors_cpu["q"][rows]
+    k = tensors_cpu["k"][rows]
+    v = tensors_cpu["v"][rows]
+    t0 = time.perf_counter()
+    oracle.forward(q, k, v, tensors_cpu["k_pool"], tensors_cpu["v_pool"], sub_cu, sub_lens, sub_table,
+                   wl.page_size)
+    dt = time.perf_counter() - t0
+    tokens = int(sub_cu[-1])
+    return {"value": tokens / dt if dt > 0 else None, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(chosen)} of {wl.batch} requests ({tokens} of {wl.total_tokens} new tokens), "
+                      f"one store+attention pass, {dt:.2f} s"}
+
+
+# ------------------------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from paged_variable_length_gb300 import workloads as W
+
+    wl = W.WORKLOADS[args.workload](args.seed)
+    t = W.make_tensors(wl, "cpu")
+    vals = []
+    base = None
+    budget = min(args.cpu_budget_s, 150.0 / max(args.steps + args.warmup, 1))
+    for i in range(args.warmup + args.steps):
+        base = cpu_baseline(wl, t, budget_s=budget)
+        if i >= args.warmup:
+            vals.append(base["value"])
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.description, "seed": args.seed},
+        "cpu_baseline": dict(base, value=value),
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+# ------------------------------------------------------------------------------ our arm
+
+def run_ours(args):
+    import torch
+
+    from paged_variable_length_gb300 import build as libbuild
+    from paged_variable_length_gb300 import pva
+    from paged_variable_length_gb300 import workloads as W
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    if rank == 0:
+        libbuild.build()
+    if dist is not None:
+        dist.barrier()
+    pva.load()
+
+    wl = W.WORKLOADS[args.workload](args.seed + rank)
+    work = algorithmic_work(wl)
+    dev = torch.device("cuda", local)
+    t = W.make_tensors(wl, dev)
+    max_q = max(wl.q_lens)
+    eng = pva.PagedAttention(wl.num_qo_heads, wl.num_kv_heads, wl.head_dim, wl.page_size, wl.num_pages,
+                             max_batch=wl.batch, max_tokens=wl.total_tokens, max_kv_len=max(wl.kv_lens),
+                             device=dev)
+    out = torch.empty_like(t["q"])
+    lse = torch.empty(t["q"].shape[:2], dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        eng.prepare(t["cu_seqlens_q"], t["cache_seqlens"], t["page_table"], wl.total_tokens, None, max_q)
+        eng.forward(t["q"], t["k"], t["v"], t["k_pool"], t["v_pool"], out, lse)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    bits = pva.attn_get_device_status(eng.meta)
+    if bits:
+        raise RuntimeError(f"device error bits: {pva.deverr_names(bits)}")
+    plan = pva.attn_debug_plan_counts(eng.meta)
+
+    # ---- timed region: K steps, L2 flushed before each (outside the events)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local, enabled=not args.no_clocks)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clock_info = clocks.stop()
+    times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(times) / len(times)
+    if dist is not None:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    value = world * wl.total_tokens / (ms / 1e3)
+
+    # ---- per-kernel durations (events between the library's launches), same steps
+    kev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    pev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    for e in kev + pev:
+        e.record(stream)
+    phase = {"prepare": [], "store": [], "prefill": [], "cascade": [], "decode": []}
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        pev[0].record(stream)
+        eng.prepare(t["cu_seqlens_q"], t["cache_seqlens"], t["page_table"], wl.total_tokens, None, max_q)
+        pev[1].record(stream)
+        pva.attn_set_timing_events(eng.meta, kev)
+        eng.forward(t["q"], t["k"], t["v"], t["k_pool"], t["v_pool"], out, lse)
+        torch.cuda.synchronize()
+        phase["prepare"].append(pev[0].elapsed_time(pev[1]))
+        for j, name in enumerate(["store", "prefill", "cascade", "decode"]):
+            phase[name].append(kev[j].elapsed_time(kev[j + 1]))
+    phase_ms = {k: (sum(v) / len(v) if v else 0.0) for k, v in phase.items()}
+
+    peaks = load_peaks()
+    # dominant kernel: the phase with the largest share of the step
+    dom = max(("prefill", "cascade", "decode"), key=lambda k: phase_ms[k])
+    if dom == "prefill" and work["flops"] > 0:
+        roof = {"bound": "tensor", "achieved": work["flops"] / (phase_ms[dom] / 1e3) / 1e12,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": work["attn_bytes"] / (phase_ms[dom] / 1e3) / 1e9,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["kernel"] = dom
+    roof["peak_source"] = peaks["source"]
+    roof_time_s = max(work["flops"] / (peaks["bf16_tflops"] * 1e12), work["step_bytes"] / (peaks["hbm_gbs"] * 1e9))
+
+    # ---- end to end through the public API with host buffers (pinned), copies inside the timed region
+    host_in = {k: t[k].cpu().pin_memory() for k in ("q", "k", "v", "cu_seqlens_q", "cache_seqlens", "page_table")}
+    dev_in = {k: torch.empty_like(t[k]) for k in host_in}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for k2, v2 in host_in.items():
+            dev_in[k2].copy_(v2, non_blocking=True)
+        eng.prepare(dev_in["cu_seqlens_q"], dev_in["cache_seqlens"], dev_in["page_table"], wl.total_tokens, None,
+                    max_q)
+        eng.forward(dev_in["q"], dev_in["k"], dev_in["v"], t["k_pool"], t["v_pool"], out, None)
+        host_out.copy_(out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        e_s[i].record(stream)
+        e2e_step()
+        e_e[i].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(s.elapsed_time(e) for s, e in zip(e_s, e_e)) / args.steps
+    if dist is not None:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        base = cpu_baseline(wl, {k: v.cpu() for k, v in t.items()}, args.cpu_budget_s)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {
+                "workload": wl.description, "seed": args.seed, "batch": wl.batch, "new_tokens": wl.total_tokens,
+                "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write, outside the timed events)",
+                "step": "attn_prepare_metadata + attn_forward (store_kvcache + attention), one layer",
+                "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+            },
+            "roofline": roof,
+            "step_roofline": {"roofline_time_us": roof_time_s * 1e6, "frac_of_step": roof_time_s / (ms / 1e3),
+                              "bytes": work["step_bytes"], "flops": work["flops"]},
+            "phases_ms": phase_ms,
+            "plan": plan,
+            "gpu_launches": int(args.steps * (1 + plan.get("kernels_per_forward", 2))),
+            "e2e": {"value": world * wl.total_tokens / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "clocks": clock_info,
+            "cpu_baseline": base,
+        }
+        print(json.dumps(line))
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

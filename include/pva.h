@@ -1,0 +1,219 @@
+/*
+ * pva.h -- C ABI of libpva.so: the paged variable-length attention forward
+ * of an LLM serving engine, for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (one flat, mixed batch of prefill, chunked-prefill and decode
+ * requests; all requests' new tokens packed end to end without padding):
+ *
+ *   once per batch   attn_prepare_metadata(...)  -> pva_meta
+ *   once per layer   attn_forward(q, k, v, k_pool, v_pool, out, lse, meta)
+ *                      = store this step's K/V into the paged pool, then
+ *                        causal, bottom-right-aligned GQA attention of every
+ *                        request over its cached prefix plus its new tokens.
+ *
+ * Where each piece is defined:
+ *   - "The attention backend and a reference implementation" (mini-sglang
+ *     from Scratch, ch. 5), section "The interface": prepare_metadata once
+ *     per batch (the metadata is the same for every layer), forward once per
+ *     layer, write-before-read.
+ *   - same page, section "Variable-length, paged attention with prefixes":
+ *     cu_seqlens_q, cache_seqlens (KV length INCLUDING this step's tokens),
+ *     the page table, and the bottom-right causal mask (query r of n sits at
+ *     absolute position kv_len - n + r and sees keys j <= kv_len - n + r).
+ *   - "Attention backends: backend, metadata builder and implementation"
+ *     (explain vLLM), step 2: the implementation writes into a caller-given
+ *     output, and the KV update is a scatter by slot (slot_mapping).
+ *   - "Source walkthrough: Attention backends" (SGLang learning notes),
+ *     sections 3.1 and 7: plan once into a preallocated workspace, run per
+ *     layer; section 3.3: shared-prefix (cascade) attention merged by
+ *     log-sum-exp.
+ *   - "Variable-length batching and one mixed forward pass", sections
+ *     "Layout and metadata" and "Exercises" (answer 2): prefill, chunked
+ *     prefill and decode differ only in (cached, new) lengths; long decodes
+ *     are split over the KV sequence and combined (split-KV).
+ *
+ * Conventions (all calls):
+ *   - Every pointer to batch data or pools is a DEVICE pointer on the current
+ *     CUDA device unless stated otherwise; the caller owns all memory.  The
+ *     library allocates no device memory and never synchronises a stream
+ *     (except attn_get_device_status, which is documented as syncing).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *   - bf16 tensors are row-major and contiguous:
+ *       q   [total_tokens, num_qo_heads, head_dim]
+ *       k,v [total_tokens, num_kv_heads, head_dim]   (this step's new tokens)
+ *       k_pool, v_pool [num_pages * page_size, num_kv_heads, head_dim]
+ *       out [total_tokens, num_qo_heads, head_dim]
+ *     lse is fp32 [total_tokens, num_qo_heads] (natural log of the sum of
+ *     exp of the scaled scores), or NULL.
+ *   - Index tensors are int32 except slot_mapping (int64).
+ *   - q head h reads kv head h / (num_qo_heads / num_kv_heads).
+ *   - Pool slot of position j of request i:
+ *       page_table[i * ld_page_table + j / page_size] * page_size + j % page_size.
+ *     Page-table columns past ceil(kv_len / page_size) are never read.
+ *   - Errors the host can see (null pointers, unsupported shapes, workspace
+ *     too small) return a status and launch nothing.  Errors that depend on
+ *     device data (non-monotone cu_seqlens_q, q_len > kv_len, page ids or
+ *     slots outside the pool, a batch larger than the planned limits) set
+ *     bits of a device error word in the workspace; the kernels then skip
+ *     the offending work and never trap.  attn_get_device_status reads it.
+ */
+#ifndef PVA_H
+#define PVA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PVA_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define PVA_API __attribute__((visibility("default")))
+#else
+#define PVA_API
+#endif
+
+typedef enum pva_status {
+    PVA_OK = 0,
+    PVA_ERR_INVALID_ARG = 1,          /* null pointer, negative size, bad layout */
+    PVA_ERR_UNSUPPORTED = 2,          /* head_dim, group size or page_size outside the built set */
+    PVA_ERR_WORKSPACE_TOO_SMALL = 3,  /* workspace_bytes < attn_workspace_size(cfg) */
+    PVA_ERR_CUDA = 4,                 /* a CUDA runtime call failed (launch, attribute, ...) */
+    PVA_ERR_DEVICE_CHECK = 5,         /* attn_get_device_status found device error bits set */
+    PVA_ERR_NOT_PREPARED = 6          /* meta was not filled by attn_prepare_metadata */
+} pva_status;
+
+/* Bits of the device error word (attn_get_device_status). */
+#define PVA_DEVERR_CU_SEQLENS 0x01u  /* cu_seqlens_q[0] != 0, decreasing, or cu[batch] != total_tokens */
+#define PVA_DEVERR_Q_GT_KV    0x02u  /* some request has q_len > kv_len (or kv_len < 0) */
+#define PVA_DEVERR_PAGE_ID    0x04u  /* a page id read for a position < kv_len lies outside [0, num_pages) */
+#define PVA_DEVERR_SLOT       0x08u  /* a slot_mapping entry lies outside [-1, num_pages * page_size) */
+#define PVA_DEVERR_LIMITS     0x10u  /* batch exceeds cfg.max_batch / max_tokens / max_kv_len or the max_q_len hint */
+#define PVA_DEVERR_TIMEOUT    0x20u  /* a bounded wait inside a kernel gave up (internal error) */
+
+/*
+ * Static description of the model's attention layer and of the largest batch
+ * the workspace is planned for.  Plain data; the caller fills every field.
+ */
+typedef struct pva_config {
+    int32_t num_qo_heads;       /* Hq */
+    int32_t num_kv_heads;       /* Hkv; Hq % Hkv == 0 and Hq / Hkv <= 16 */
+    int32_t head_dim;           /* D: 64 or 128 */
+    int32_t page_size;          /* 1, 2, 4, ..., 128 (a power of two) */
+    int64_t num_pages;          /* pool capacity in pages */
+    float sm_scale;             /* softmax scale; <= 0 selects 1/sqrt(head_dim) */
+    int32_t max_batch;          /* upper bound on requests per batch */
+    int32_t max_tokens;         /* upper bound on new tokens per batch */
+    int32_t max_kv_len;         /* upper bound on any request's kv_len */
+    int32_t enable_split_kv;    /* nonzero: split long KV ranges over several CTAs (LSE combine) */
+    int32_t enable_cascade;     /* nonzero: read prefixes shared by several decodes once */
+    int32_t min_cascade_pages;  /* shortest shared prefix (in pages) worth a cascade pass; <= 0 -> 8 */
+} pva_config;
+
+/*
+ * The prepared batch.  Host-side, caller-owned, filled by
+ * attn_prepare_metadata; it refers to device memory inside the workspace and
+ * stays valid until the next attn_prepare_metadata on the same workspace.
+ * Treat it as opaque.
+ */
+typedef struct pva_meta {
+    uint64_t opaque[64];
+} pva_meta;
+
+/* Version of this header the library was built from (PVA_ABI_VERSION). */
+PVA_API int32_t attn_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+PVA_API const char* attn_status_string(pva_status status);
+
+/*
+ * Device bytes the workspace must hold for batches within cfg's limits on the
+ * current device (the plan is sized by its SM count).  Returns 0 when cfg is
+ * invalid or unsupported.  Host-only: makes no CUDA call other than a device
+ * attribute query.
+ */
+PVA_API size_t attn_workspace_size(const pva_config* cfg);
+
+/*
+ * Once per batch: validate the batch on the device and build the plan inside
+ * `workspace` -- the slot mapping (derived when slot_mapping is NULL), the
+ * classification of each request (decode rows vs. prefill tiles), the
+ * per-tile work list with causal KV extents, the split-KV plan and the
+ * shared-prefix (cascade) groups.  One kernel launch on `stream`, no sync.
+ *
+ *   cu_seqlens_q   int32 [batch+1]  request i's new tokens are q[cu[i] : cu[i+1]]
+ *   cache_seqlens  int32 [batch]    kv_len of request i, including its new tokens
+ *   page_table     int32 [batch, ld_page_table]  page ids, row i = request i
+ *   slot_mapping   int64 [total_tokens] pool slot of each new token, -1 = do not
+ *                  store; or NULL to derive it from the page table (the new
+ *                  tokens are positions kv_len - q_len .. kv_len - 1)
+ *   batch, total_tokens   host values; total_tokens must equal cu[batch]
+ *   max_q_len      host upper bound on any request's q_len (<= 0: unknown,
+ *                  taken as total_tokens); lets the forward skip the prefill
+ *                  kernel for decode-only batches.  A request above it sets
+ *                  PVA_DEVERR_LIMITS and is skipped.
+ *   workspace      device buffer of at least attn_workspace_size(cfg) bytes,
+ *                  256-byte aligned, owned by the caller, not used
+ *                  concurrently by another prepare/forward.
+ * The arrays must stay unchanged until the last attn_forward using `meta`
+ * (page_table and slot_mapping are read by the forward kernels).
+ */
+PVA_API pva_status attn_prepare_metadata(const pva_config* cfg, const int32_t* cu_seqlens_q,
+                                 const int32_t* cache_seqlens, const int32_t* page_table,
+                                 int64_t ld_page_table, const int64_t* slot_mapping, int32_t batch,
+                                 int32_t total_tokens, int32_t max_q_len, void* workspace,
+                                 size_t workspace_bytes, void* stream, pva_meta* meta);
+
+/*
+ * Once per layer: store_kvcache, then attention, in stream order on `stream`.
+ * k_pool / v_pool are updated in place (bit-exact copies of k / v rows at
+ * their slots) and then read; out (and lse when not NULL) are fully written
+ * for every new token.  Requests with q_len == 0 write nothing.  q, k, v, out
+ * must be 16-byte aligned.  Several forwards may reuse one meta (one per
+ * layer); they must not run concurrently on the same workspace.
+ */
+PVA_API pva_status attn_forward(const pva_meta* meta, const void* q, const void* k, const void* v,
+                        void* k_pool, void* v_pool, void* out, float* lse, void* stream);
+
+/*
+ * store_kvcache alone: k_pool[slot[t], h, :] = k[t, h, :] and the same for v,
+ * for every new token t with slot != -1.  attn_forward already includes it.
+ */
+PVA_API pva_status attn_store_kvcache(const pva_meta* meta, const void* k, const void* v, void* k_pool,
+                              void* v_pool, void* stream);
+
+/*
+ * Debug/test helper: synchronises the stream of the last prepare/forward on
+ * meta's workspace, then reads the device error word into *error_bits
+ * (PVA_DEVERR_*).  Returns PVA_ERR_DEVICE_CHECK when any bit is set.
+ */
+PVA_API pva_status attn_get_device_status(const pva_meta* meta, uint32_t* error_bits);
+
+/*
+ * Profiling helper: with n > 0, every later attn_forward on this meta records
+ * caller-created events (cudaEvent_t passed as void*) on its stream:
+ * events[0] before its first kernel, then one after each phase --
+ * [1] store_kvcache, [2] tensor-core prefill tiles, [3] shared-prefix
+ * (cascade) pass, [4] decode / split-KV / combine.  A phase that launches
+ * nothing records at the same point as the previous one.  n must be 0 (off)
+ * or 5; the handles must outlive the forwards.  Timing only; it changes no
+ * result.
+ */
+PVA_API pva_status attn_set_timing_events(pva_meta* meta, void* const* events, int32_t n);
+
+/*
+ * Debug/test helper: copies plan counters to host (synchronising): counts[0]
+ * decode units, [1] decode merge groups, [2] prefill tiles, [3] cascade
+ * groups, [4] cascade prefix tiles, [5] split-KV chunk (keys), [6] partial
+ * slots used, [7] kernels one attn_forward launches.  Returns the number of
+ * entries written (<= n).
+ */
+PVA_API int32_t attn_debug_plan_counts(const pva_meta* meta, int64_t* counts, int32_t n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PVA_H */

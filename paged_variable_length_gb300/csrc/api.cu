@@ -1,0 +1,281 @@
+// The C ABI of libpva.so (declared in include/pva.h): argument checks that need
+// no GPU, workspace planning, and kernel launches.  The host never reads device
+// data here except in the two documented debug helpers.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+
+#include "pva_internal.h"
+
+namespace pva {
+namespace {
+
+int device_sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return sms;
+}
+
+bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+
+// Host-side validation of the static configuration.
+pva_status check_config(const pva_config* c) {
+    if (c == nullptr) return PVA_ERR_INVALID_ARG;
+    if (c->num_qo_heads <= 0 || c->num_kv_heads <= 0 || c->head_dim <= 0 || c->page_size <= 0 ||
+        c->num_pages <= 0 || c->max_batch <= 0 || c->max_tokens < 0 || c->max_kv_len < 0)
+        return PVA_ERR_INVALID_ARG;
+    if (c->num_qo_heads % c->num_kv_heads != 0) return PVA_ERR_INVALID_ARG;
+    if (!is_pow2(c->page_size) || c->page_size > 128) return PVA_ERR_UNSUPPORTED;
+    if (!decode_supported(c->num_qo_heads, c->num_kv_heads, c->head_dim)) return PVA_ERR_UNSUPPORTED;
+    if ((int64_t)c->num_pages * c->page_size > ((int64_t)1 << 40)) return PVA_ERR_UNSUPPORTED;
+    return PVA_OK;
+}
+
+Layout make_layout(const pva_config* c, int sm_count) {
+    Layout L{};
+    const int G = c->num_qo_heads / c->num_kv_heads;
+    const int TB = kDecRows / G;
+    const int TM = kPreRows / G;
+    const int cps = decode_ctas_per_sm(c->num_kv_heads, c->head_dim);
+    L.target_units = 4 * sm_count * cps;
+    L.max_dec_groups = (int32_t)(c->max_tokens / TB + c->max_batch + 1);
+    L.max_dec_units = L.max_dec_groups + L.target_units + 1;
+    L.max_partial = 2 * L.target_units + 2;
+    L.max_pre_tiles = (int32_t)((c->max_tokens / TM + c->max_batch + 1) * (int64_t)c->num_kv_heads);
+    L.rows_per_slot = kDecRows * c->num_kv_heads;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = off;
+        off = align_up(off + bytes, 256);
+        return at;
+    };
+    L.header = take(sizeof(PlanHeader));
+    L.dec_units = take(sizeof(DecUnit) * (size_t)L.max_dec_units);
+    L.dec_groups = take(sizeof(DecGroup) * (size_t)L.max_dec_groups);
+    L.pre_tiles = take(sizeof(PreTile) * (size_t)L.max_pre_tiles);
+    L.slots = take(sizeof(int64_t) * (size_t)(c->max_tokens + 1));
+    L.counters = take(sizeof(uint32_t) * (size_t)L.max_dec_groups);
+    L.partial_o = take(sizeof(float) * (size_t)L.max_partial * L.rows_per_slot * c->head_dim);
+    L.partial_lse = take(sizeof(float) * (size_t)L.max_partial * L.rows_per_slot);
+    L.req_scratch = take(sizeof(int32_t) * 4 * (size_t)c->max_batch);
+    L.total = off;
+    return L;
+}
+
+const MetaHost* meta_of(const pva_meta* m) {
+    if (m == nullptr) return nullptr;
+    const MetaHost* h = reinterpret_cast<const MetaHost*>(m->opaque);
+    return h->magic == kMetaMagic ? h : nullptr;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+ForwardParams forward_params(const MetaHost* h, const void* q, const void* k, const void* v, void* k_pool,
+                             void* v_pool, void* out, float* lse) {
+    ForwardParams fp{};
+    fp.q = static_cast<const uint16_t*>(q);
+    fp.k = static_cast<const uint16_t*>(k);
+    fp.v = static_cast<const uint16_t*>(v);
+    fp.k_pool = static_cast<uint16_t*>(k_pool);
+    fp.v_pool = static_cast<uint16_t*>(v_pool);
+    fp.out = static_cast<uint16_t*>(out);
+    fp.lse = lse;
+    fp.cu = h->cu;
+    fp.seqlens = h->seqlens;
+    fp.page_table = h->page_table;
+    fp.ld = h->ld;
+    fp.slots = h->slots;
+    fp.total_tokens = h->total_tokens;
+    fp.page_size = h->cfg.page_size;
+    fp.page_shift = ilog2(h->cfg.page_size);
+    fp.num_pages = h->cfg.num_pages;
+    fp.num_slots = h->cfg.num_pages * (int64_t)h->cfg.page_size;
+    fp.num_qo_heads = h->cfg.num_qo_heads;
+    fp.num_kv_heads = h->cfg.num_kv_heads;
+    fp.group = h->cfg.num_qo_heads / h->cfg.num_kv_heads;
+    const float scale = h->cfg.sm_scale > 0.f ? h->cfg.sm_scale : 1.0f / std::sqrt((float)h->cfg.head_dim);
+    fp.scale_log2 = scale * 1.4426950408889634f;
+    fp.ws = h->ws;
+    fp.lay = h->lay;
+    return fp;
+}
+
+}  // namespace
+}  // namespace pva
+
+using namespace pva;
+
+extern "C" {
+
+int32_t attn_abi_version(void) { return PVA_ABI_VERSION; }
+
+const char* attn_status_string(pva_status s) {
+    switch (s) {
+        case PVA_OK: return "PVA_OK";
+        case PVA_ERR_INVALID_ARG: return "PVA_ERR_INVALID_ARG: null pointer, bad size or bad layout";
+        case PVA_ERR_UNSUPPORTED: return "PVA_ERR_UNSUPPORTED: head_dim, group size or page_size not built";
+        case PVA_ERR_WORKSPACE_TOO_SMALL: return "PVA_ERR_WORKSPACE_TOO_SMALL";
+        case PVA_ERR_CUDA: return "PVA_ERR_CUDA: a CUDA runtime call failed";
+        case PVA_ERR_DEVICE_CHECK: return "PVA_ERR_DEVICE_CHECK: the device error word is nonzero";
+        case PVA_ERR_NOT_PREPARED: return "PVA_ERR_NOT_PREPARED: meta was not filled by attn_prepare_metadata";
+    }
+    return "unknown pva_status";
+}
+
+size_t attn_workspace_size(const pva_config* cfg) {
+    if (check_config(cfg) != PVA_OK) return 0;
+    const int sms = device_sm_count();
+    if (sms <= 0) return 0;
+    return make_layout(cfg, sms).total;
+}
+
+pva_status attn_prepare_metadata(const pva_config* cfg, const int32_t* cu_seqlens_q, const int32_t* cache_seqlens,
+                                 const int32_t* page_table, int64_t ld_page_table, const int64_t* slot_mapping,
+                                 int32_t batch, int32_t total_tokens, int32_t max_q_len, void* workspace,
+                                 size_t workspace_bytes, void* stream, pva_meta* meta) {
+    pva_status st = check_config(cfg);
+    if (st != PVA_OK) return st;
+    if (meta == nullptr || workspace == nullptr || cu_seqlens_q == nullptr || cache_seqlens == nullptr ||
+        page_table == nullptr)
+        return PVA_ERR_INVALID_ARG;
+    if (batch < 0 || total_tokens < 0 || ld_page_table <= 0) return PVA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PVA_ERR_INVALID_ARG;
+    if (batch > cfg->max_batch || total_tokens > cfg->max_tokens) return PVA_ERR_INVALID_ARG;
+    const int sms = device_sm_count();
+    if (sms <= 0) return PVA_ERR_CUDA;
+    const Layout lay = make_layout(cfg, sms);
+    if (workspace_bytes < lay.total) return PVA_ERR_WORKSPACE_TOO_SMALL;
+
+    const int G = cfg->num_qo_heads / cfg->num_kv_heads;
+    const int TB = kDecRows / G;
+    const int mq = max_q_len > 0 ? max_q_len : (total_tokens > 0 ? total_tokens : 1);
+
+    MetaHost h{};
+    h.magic = kMetaMagic;
+    h.cfg = *cfg;
+    if (h.cfg.min_cascade_pages <= 0) h.cfg.min_cascade_pages = 8;
+    h.batch = batch;
+    h.total_tokens = total_tokens;
+    h.max_q_len = mq;
+    h.sm_count = sms;
+    h.use_prefill = 0;  // the tensor-core prefill kernel is enabled per build below
+    (void)TB;
+    h.dec_ctas = sms * decode_ctas_per_sm(cfg->num_kv_heads, cfg->head_dim);
+    h.cu = cu_seqlens_q;
+    h.seqlens = cache_seqlens;
+    h.page_table = page_table;
+    h.ld = ld_page_table;
+    h.ws = static_cast<uint8_t*>(workspace);
+    h.slots = slot_mapping != nullptr ? slot_mapping : reinterpret_cast<const int64_t*>(h.ws + lay.slots);
+    h.stream = stream;
+    h.lay = lay;
+    h.n_events = 0;
+    h.kernels_per_forward = 2 + (h.use_prefill ? 1 : 0);  // store, [prefill], decode
+
+    PrepareParams pp{};
+    pp.cu = cu_seqlens_q;
+    pp.seqlens = cache_seqlens;
+    pp.page_table = page_table;
+    pp.ld = ld_page_table;
+    pp.user_slots = slot_mapping;
+    pp.derived_slots = slot_mapping != nullptr ? nullptr : reinterpret_cast<int64_t*>(h.ws + lay.slots);
+    pp.batch = batch;
+    pp.total_tokens = total_tokens;
+    pp.max_q_len = mq;
+    pp.page_size = cfg->page_size;
+    pp.num_pages = cfg->num_pages;
+    pp.num_qo_heads = cfg->num_qo_heads;
+    pp.num_kv_heads = cfg->num_kv_heads;
+    pp.group = G;
+    pp.dec_tokens = kDecRows / G;
+    pp.pre_tokens = kPreRows / G;
+    pp.use_prefill = h.use_prefill;
+    pp.split_kv = cfg->enable_split_kv ? 1 : 0;
+    pp.max_kv_len = cfg->max_kv_len;
+    pp.max_tokens = cfg->max_tokens;
+    pp.max_batch = cfg->max_batch;
+    pp.ws = h.ws;
+    pp.lay = lay;
+    if (launch_prepare(pp, static_cast<cudaStream_t>(stream)) != cudaSuccess) return PVA_ERR_CUDA;
+    std::memset(meta, 0, sizeof(*meta));
+    std::memcpy(meta->opaque, &h, sizeof(h));
+    return PVA_OK;
+}
+
+pva_status attn_store_kvcache(const pva_meta* meta, const void* k, const void* v, void* k_pool, void* v_pool,
+                              void* stream) {
+    const MetaHost* h = meta_of(meta);
+    if (h == nullptr) return PVA_ERR_NOT_PREPARED;
+    if (h->total_tokens > 0 && (k == nullptr || v == nullptr)) return PVA_ERR_INVALID_ARG;
+    if (k_pool == nullptr || v_pool == nullptr) return PVA_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_pool) || !aligned16(v_pool)) return PVA_ERR_INVALID_ARG;
+    ForwardParams fp = forward_params(h, nullptr, k, v, k_pool, v_pool, nullptr, nullptr);
+    if (launch_store(fp, h->cfg.head_dim, static_cast<cudaStream_t>(stream)) != cudaSuccess) return PVA_ERR_CUDA;
+    return PVA_OK;
+}
+
+pva_status attn_forward(const pva_meta* meta, const void* q, const void* k, const void* v, void* k_pool,
+                        void* v_pool, void* out, float* lse, void* stream) {
+    const MetaHost* h = meta_of(meta);
+    if (h == nullptr) return PVA_ERR_NOT_PREPARED;
+    if (h->total_tokens > 0 && (q == nullptr || k == nullptr || v == nullptr || out == nullptr))
+        return PVA_ERR_INVALID_ARG;
+    if (k_pool == nullptr || v_pool == nullptr) return PVA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(k_pool) ||
+        !aligned16(v_pool) || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+        return PVA_ERR_INVALID_ARG;
+    if (h->total_tokens == 0) return PVA_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    ForwardParams fp = forward_params(h, q, k, v, k_pool, v_pool, out, lse);
+    auto mark = [&](int i) {
+        return h->n_events == 5 ? cudaEventRecord(static_cast<cudaEvent_t>(h->events[i]), s) : cudaSuccess;
+    };
+    if (mark(0) != cudaSuccess) return PVA_ERR_CUDA;
+    if (launch_store(fp, h->cfg.head_dim, s) != cudaSuccess) return PVA_ERR_CUDA;
+    if (mark(1) != cudaSuccess || mark(2) != cudaSuccess || mark(3) != cudaSuccess) return PVA_ERR_CUDA;
+    if (launch_decode(fp, h->cfg.head_dim, h->dec_ctas, s) != cudaSuccess) return PVA_ERR_CUDA;
+    if (mark(4) != cudaSuccess) return PVA_ERR_CUDA;
+    return PVA_OK;
+}
+
+pva_status attn_get_device_status(const pva_meta* meta, uint32_t* error_bits) {
+    const MetaHost* h = meta_of(meta);
+    if (h == nullptr) return PVA_ERR_NOT_PREPARED;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(h->stream)) != cudaSuccess) return PVA_ERR_CUDA;
+    PlanHeader hdr{};
+    if (cudaMemcpy(&hdr, h->ws + h->lay.header, sizeof(hdr), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return PVA_ERR_CUDA;
+    if (error_bits) *error_bits = hdr.error_bits;
+    return hdr.error_bits ? PVA_ERR_DEVICE_CHECK : PVA_OK;
+}
+
+pva_status attn_set_timing_events(pva_meta* meta, void* const* events, int32_t n) {
+    if (meta == nullptr) return PVA_ERR_NOT_PREPARED;
+    MetaHost* h = reinterpret_cast<MetaHost*>(meta->opaque);
+    if (h->magic != kMetaMagic) return PVA_ERR_NOT_PREPARED;
+    if (n != 0 && n != 5) return PVA_ERR_INVALID_ARG;
+    if (n == 5 && events == nullptr) return PVA_ERR_INVALID_ARG;
+    for (int i = 0; i < 5; ++i) {
+        if (n == 5 && events[i] == nullptr) return PVA_ERR_INVALID_ARG;
+        h->events[i] = n == 5 ? events[i] : nullptr;
+    }
+    h->n_events = n;
+    return PVA_OK;
+}
+
+int32_t attn_debug_plan_counts(const pva_meta* meta, int64_t* counts, int32_t n) {
+    const MetaHost* h = meta_of(meta);
+    if (h == nullptr || counts == nullptr || n <= 0) return 0;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(h->stream)) != cudaSuccess) return 0;
+    PlanHeader hdr{};
+    if (cudaMemcpy(&hdr, h->ws + h->lay.header, sizeof(hdr), cudaMemcpyDeviceToHost) != cudaSuccess) return 0;
+    const int64_t vals[8] = {hdr.n_dec_units, hdr.n_dec_groups, hdr.n_pre_tiles, hdr.n_casc_groups,
+                             hdr.n_casc_tiles, hdr.split_chunk, hdr.n_partial_slots, h->kernels_per_forward};
+    const int m = n < 8 ? n : 8;
+    for (int i = 0; i < m; ++i) counts[i] = vals[i];
+    return m;
+}
+
+}  // extern "C"

@@ -1,0 +1,480 @@
+// K3 + K4: decode / small-row attention streaming the paged KV pool, with the
+// split-KV log-sum-exp combine fused as a "last CTA to finish merges" epilogue.
+//
+// What it computes is the ch. 5 reference forward ("The attention backend and
+// a reference implementation", section "Variable-length, paged attention with
+// prefixes") for requests with few new tokens: for every q head h of kv head
+// g, softmax(scale * q K^T) V over the request's keys 0..kv_len-1 gathered
+// through the page table, with the bottom-right causal mask.  Long KV ranges
+// are split over CTAs and recombined by LSE, the split-KV / Flash-Decoding
+// scheme "Variable-length batching and one mixed forward pass" (Exercises,
+// answer 2) names for decode batches.
+//
+// GB300 design (one CTA per SM-slot, persistent, dynamic work fetch):
+//   * a work unit is (decode group, key range); a group is up to floor(16/G)
+//     consecutive new tokens of one request, all q heads;
+//   * producer warp: fetches units with an atomic counter, and for every
+//     16-key stage issues one bulk async copy (TMA, 1-D) per key row --
+//     Hkv*D bf16 = all kv heads of one slot, 1-2 KiB contiguous in the pool --
+//     for K and for V into a ring of shared-memory stages (mbarrier
+//     complete_tx).  Rows land 16 bytes apart from a multiple of 128 so the
+//     per-head reads below are bank-conflict free;
+//   * consumer warp w owns kv head w: its G*ntok (<= 16) query rows are one
+//     m16 operand held in registers; S = Q K^T and O += P V run as
+//     m16n8k16 warp MMAs (fp32 accumulate) on the staged rows, with an online
+//     softmax in registers.  The tcgen05 tensor core's smallest M (64) would
+//     leave >= 87% of its rows idle here; the warp MMA keeps the CUDA cores
+//     free so the kernel stays bound by HBM, not by issue slots;
+//   * split groups write fp32 partial (O, LSE) to the workspace; the CTA that
+//     finishes a group's last split (atomic arrival count, no waiting) merges
+//     them: lse = log sum_s exp(lse_s), o = sum_s exp(lse_s - lse) o_s.
+// Every wait is bounded (PVA_DEVERR_TIMEOUT, then the CTA drains its copies
+// and leaves); nothing traps.
+#include <cuda_runtime.h>
+
+#include <cfloat>
+
+#include "device_utils.cuh"
+#include "pva_internal.h"
+
+namespace pva {
+namespace {
+
+constexpr int kMaxKvHeads = 8;
+constexpr int kStageKeys = kDecKeysPerStage;  // 16
+constexpr int kRowPad = 16;                    // bytes between consecutive staged rows beyond Hkv*D*2
+constexpr float kLn2 = 0.69314718055994530942f;
+
+struct StageInfo {
+    int32_t unit, group, k, k1;
+    int32_t tok0, ntok, qpos0, nsplit;
+    int32_t pbase, split, flags, hb;
+};
+constexpr int kFirst = 1, kLast = 2, kEnd = 4;
+
+struct DecSmemHead {
+    uint64_t full[8];
+    uint64_t empty[8];
+    StageInfo info[8];
+    int32_t last_flag;
+    int32_t abort_flag;
+};
+
+__device__ __forceinline__ void abort_cta(DecSmemHead* sh, uint32_t* err) {
+    sh->abort_flag = 1;
+    dev::set_error(err, kErrTimeout);
+}
+
+template <int D>
+__global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
+    decode_kernel(ForwardParams p, int stages, int row_stride) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    DecSmemHead* sh = reinterpret_cast<DecSmemHead*>(smem);
+    uint8_t* ring = smem + ((sizeof(DecSmemHead) + 127) / 128) * 128;
+    PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws + p.lay.header);
+    uint32_t* err = &hdr->error_bits;
+
+    // a CTA serves HB = min(Hkv, 8) kv heads ("head block"); work item = (unit, head block)
+    const int Hkv = p.num_kv_heads, G = p.group, Hq = p.num_qo_heads;
+    const int HB = Hkv < kMaxKvHeads ? Hkv : kMaxKvHeads;
+    const int n_hb = Hkv / HB;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row_bytes = HB * D * 2;
+    const int stage_bytes = 2 * kStageKeys * row_stride;
+    const int n_units = hdr->n_dec_units * n_hb;
+    if ((hdr->error_bits & kErrFatal) || n_units == 0) return;
+
+    // zero the ring once so rows past a range's end are finite (they are masked,
+    // and 0 * finite stays 0 in the P V product)
+    for (int i = threadIdx.x * 16; i < stages * stage_bytes; i += blockDim.x * 16)
+        *reinterpret_cast<int4*>(ring + i) = make_int4(0, 0, 0, 0);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            dev::mbar_init(&sh->full[s], 1);
+            dev::mbar_init(&sh->empty[s], HB);
+        }
+        sh->abort_flag = 0;
+        sh->last_flag = 0;
+        dev::fence_barrier_init();
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+
+    const DecUnit* units = reinterpret_cast<const DecUnit*>(p.ws + p.lay.dec_units);
+    const DecGroup* groups = reinterpret_cast<const DecGroup*>(p.ws + p.lay.dec_groups);
+    int32_t* sched = &hdr->pad[0];
+
+    if (warp == HB) {
+        // ================================================================ producer
+        int stage = 0;
+        uint32_t phase = 0;
+        const uint64_t policy = dev::policy_evict_first();
+        const int ps_mask = p.page_size - 1;
+        uint32_t armed = 0, armed_par = 0;  // stages with copies issued, and the parity of that phase
+        while (true) {
+            int u = 0;
+            if (lane == 0) u = atomicAdd(sched, 1);
+            u = __shfl_sync(0xffffffffu, u, 0);
+            if (!dev::mbar_wait(&sh->empty[stage], phase ^ 1)) {
+                abort_cta(sh, err);
+                break;
+            }
+            if (u >= n_units) {
+                if (lane == 0) {
+                    sh->info[stage].flags = kEnd;
+                    dev::mbar_arrive(&sh->full[stage]);
+                }
+                break;
+            }
+            const int hb = u % n_hb;
+            const DecUnit du = units[u / n_hb];
+            const DecGroup dg = groups[du.group];
+            const int32_t* prow = p.page_table + (int64_t)dg.req * p.ld;
+            // warm L2 with this group's query rows (read by the consumers at unit start)
+            {
+                const char* qbase = reinterpret_cast<const char*>(p.q + (int64_t)dg.tok0 * Hq * D);
+                const int qbytes = dg.ntok * Hq * D * 2;
+                for (int off = lane * 128; off < qbytes; off += 32 * 128)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(qbase + off));
+            }
+            for (int k = du.k0; k < du.k1; k += kStageKeys) {
+                if (k != du.k0) {
+                    if (!dev::mbar_wait(&sh->empty[stage], phase ^ 1)) {
+                        abort_cta(sh, err);
+                        goto producer_done;
+                    }
+                }
+                const int nk = min(kStageKeys, du.k1 - k);
+                if (lane == 0) {
+                    StageInfo& si = sh->info[stage];
+                    si.unit = u;
+                    si.group = du.group;
+                    si.k = k;
+                    si.k1 = du.k1;
+                    si.tok0 = dg.tok0;
+                    si.ntok = dg.ntok;
+                    si.qpos0 = dg.qpos0;
+                    si.nsplit = dg.nsplit;
+                    si.pbase = dg.pbase;
+                    si.split = du.split;
+                    si.hb = hb;
+                    si.flags = (k == du.k0 ? kFirst : 0) | (k + kStageKeys >= du.k1 ? kLast : 0);
+                    dev::mbar_arrive_expect_tx(&sh->full[stage], (uint32_t)(2 * nk * row_bytes));
+                }
+                armed |= 1u << stage;
+                armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+                __syncwarp();
+                const int r = lane & 15;
+                if (r < nk) {
+                    const int key = k + r;
+                    int64_t page = prow[key >> p.page_shift];
+                    if (page < 0 || page >= p.num_pages) {
+                        dev::set_error(err, kErrPage);
+                        page = 0;  // keep the transaction count; the result is flagged
+                    }
+                    const int64_t slot = (page << p.page_shift) + (key & ps_mask);
+                    const uint16_t* src =
+                        (lane < 16 ? p.k_pool : p.v_pool) + slot * (int64_t)(Hkv * D) + hb * HB * D;
+                    uint8_t* dst = ring + stage * stage_bytes + (lane < 16 ? 0 : kStageKeys * row_stride) +
+                                   r * row_stride;
+                    dev::bulk_g2s_hint(dst, src, (uint32_t)row_bytes, &sh->full[stage], policy);
+                }
+                if (++stage == stages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+    producer_done:
+        // drain: every copy this warp issued must land before the CTA may exit
+        if (sh->abort_flag) {
+            for (int s = 0; s < stages; ++s)
+                if (armed & (1u << s)) (void)dev::mbar_wait(&sh->full[s], (armed_par >> s) & 1u);
+        }
+        return;
+    }
+
+    // ==================================================================== consumers
+    const int gl = warp;           // kv head within the head block
+    const int gq = lane >> 2;      // fragment row group
+    const int cq = lane & 3;       // fragment column pair
+    constexpr int KS = D / 16;     // k-steps over the head dim
+    constexpr int NT = D / 8;      // n-tiles of the output
+    uint32_t qa[KS][4];
+    float o[NT][4];
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    int lim0 = 0, lim1 = 0;
+    const int r0 = gq, r1 = gq + 8;
+    const int consumer_threads = HB * 32;
+    int stage = 0;
+    uint32_t phase = 0;
+
+    while (true) {
+        if (!dev::mbar_wait(&sh->full[stage], phase)) {
+            abort_cta(sh, err);
+            return;
+        }
+        const StageInfo si = sh->info[stage];
+        if (si.flags & kEnd) break;
+        const int rows = si.ntok * G;
+        const int g = si.hb * HB + gl;  // kv head
+        if (si.flags & kFirst) {
+            // load this head's query rows as m16k16 A fragments (rows >= rows are zero)
+            const uint32_t* q32 = reinterpret_cast<const uint32_t*>(p.q);
+            const int64_t qrow0 = r0 < rows ? ((int64_t)(si.tok0 + r0 / G) * Hq + g * G + r0 % G) * D : -1;
+            const int64_t qrow1 = r1 < rows ? ((int64_t)(si.tok0 + r1 / G) * Hq + g * G + r1 % G) * D : -1;
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+                const int c = kk * 16 + 2 * cq;
+                qa[kk][0] = qrow0 >= 0 ? q32[(qrow0 + c) >> 1] : 0u;
+                qa[kk][1] = qrow1 >= 0 ? q32[(qrow1 + c) >> 1] : 0u;
+                qa[kk][2] = qrow0 >= 0 ? q32[(qrow0 + c + 8) >> 1] : 0u;
+                qa[kk][3] = qrow1 >= 0 ? q32[(qrow1 + c + 8) >> 1] : 0u;
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+            m0 = m1 = -INFINITY;
+            l0 = l1 = 0.f;
+            // causal limit of each fragment row (rows past `rows` see nothing)
+            lim0 = r0 < rows ? si.qpos0 + r0 / G : -1;
+            lim1 = r1 < rows ? si.qpos0 + r1 / G : -1;
+        }
+
+        const uint8_t* Ks = ring + stage * stage_bytes + gl * D * 2;
+        const uint8_t* Vs = Ks + kStageKeys * row_stride;
+        const uint32_t ks_base = dev::smem_u32(Ks);
+        const uint32_t vs_base = dev::smem_u32(Vs);
+
+        // ---- S = Q K^T over the stage's 16 keys (two n8 tiles)
+        float s[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+        for (int kk2 = 0; kk2 < KS / 2; ++kk2) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const uint32_t addr =
+                    ks_base + (nt * 8 + (lane & 7)) * row_stride + (kk2 * 32 + (lane >> 3) * 8) * 2;
+                uint32_t b0, b1, b2, b3;
+                dev::ldsm_x4(addr, b0, b1, b2, b3);
+                dev::mma_bf16_16816(s[nt], qa[2 * kk2], b0, b1);
+                dev::mma_bf16_16816(s[nt], qa[2 * kk2 + 1], b2, b3);
+            }
+        }
+
+        // ---- scale, mask (range end and causal diagonal), online softmax
+        const float sl = p.scale_log2;
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int key = si.k + nt * 8 + 2 * cq + (e & 1);
+                const int lim = e < 2 ? lim0 : lim1;
+                float x = s[nt][e] * sl;
+                if (key >= si.k1 || key > lim) x = -INFINITY;
+                s[nt][e] = x;
+            }
+            mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
+            mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
+        }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+        const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float al0 = dev::fast_exp2(m0 - mu0);  // m0 = -inf -> 0
+        const float al1 = dev::fast_exp2(m1 - mu1);
+        m0 = mn0;
+        m1 = mn1;
+        float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            s[nt][0] = dev::fast_exp2(s[nt][0] - mu0);
+            s[nt][1] = dev::fast_exp2(s[nt][1] - mu0);
+            s[nt][2] = dev::fast_exp2(s[nt][2] - mu1);
+            s[nt][3] = dev::fast_exp2(s[nt][3] - mu1);
+            ps0 += s[nt][0] + s[nt][1];
+            ps1 += s[nt][2] + s[nt][3];
+        }
+        l0 = l0 * al0 + ps0;
+        l1 = l1 * al1 + ps1;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            o[nt][0] *= al0;
+            o[nt][1] *= al0;
+            o[nt][2] *= al1;
+            o[nt][3] *= al1;
+        }
+        uint32_t pa[4];
+        pa[0] = dev::pack_bf16x2(s[0][0], s[0][1]);
+        pa[1] = dev::pack_bf16x2(s[0][2], s[0][3]);
+        pa[2] = dev::pack_bf16x2(s[1][0], s[1][1]);
+        pa[3] = dev::pack_bf16x2(s[1][2], s[1][3]);
+
+        // ---- O += P V (V rows are the k dimension: transposed fragment loads)
+#pragma unroll
+        for (int dt = 0; dt < D / 16; ++dt) {
+            const uint32_t addr =
+                vs_base + ((lane & 7) + ((lane >> 3) & 1) * 8) * row_stride + (dt * 16 + (lane >> 4) * 8) * 2;
+            uint32_t v0, v1, v2, v3;
+            dev::ldsm_x4_t(addr, v0, v1, v2, v3);
+            dev::mma_bf16_16816(o[2 * dt], pa, v0, v1);
+            dev::mma_bf16_16816(o[2 * dt + 1], pa, v2, v3);
+        }
+
+        __syncwarp();
+        if (lane == 0) dev::mbar_arrive(&sh->empty[stage]);
+        if (++stage == stages) {
+            stage = 0;
+            phase ^= 1;
+        }
+        if (!(si.flags & kLast)) continue;
+
+        // ================================================================ unit epilogue
+        float lt0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
+        lt0 += __shfl_xor_sync(0xffffffffu, lt0, 2);
+        float lt1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
+        lt1 += __shfl_xor_sync(0xffffffffu, lt1, 2);
+        const float inv0 = lt0 > 0.f ? 1.f / lt0 : 0.f;
+        const float inv1 = lt1 > 0.f ? 1.f / lt1 : 0.f;
+        const float lse0 = lt0 > 0.f ? m0 + __log2f(lt0) : -INFINITY;  // log2 domain
+        const float lse1 = lt1 > 0.f ? m1 + __log2f(lt1) : -INFINITY;
+
+        if (si.nsplit == 1) {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int r = half ? r1 : r0;
+                if (r >= rows) continue;
+                const int64_t orow = (int64_t)(si.tok0 + r / G) * Hq + g * G + r % G;
+                uint32_t* dst = reinterpret_cast<uint32_t*>(p.out + orow * D);
+                const float inv = half ? inv1 : inv0;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    dst[(nt * 8 + 2 * cq) >> 1] = dev::pack_bf16x2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
+                if (p.lse != nullptr && cq == 0) p.lse[orow] = (half ? lse1 : lse0) * kLn2;
+            }
+            continue;
+        }
+
+        // split group: fp32 partial (normalised O, log2-domain LSE) into its slot
+        const int slot = si.pbase + si.split;
+        float* po = reinterpret_cast<float*>(p.ws + p.lay.partial_o) + (int64_t)slot * p.lay.rows_per_slot * D;
+        float* pl = reinterpret_cast<float*>(p.ws + p.lay.partial_lse) + (int64_t)slot * p.lay.rows_per_slot;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int r = half ? r1 : r0;
+            if (r >= rows) continue;
+            const int prow = (r / G) * Hq + g * G + r % G;  // (token, q head) within the group
+            const float inv = half ? inv1 : inv0;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                *reinterpret_cast<float2*>(po + (int64_t)prow * D + nt * 8 + 2 * cq) =
+                    make_float2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
+            if (cq == 0) pl[prow] = half ? lse1 : lse0;
+        }
+        __threadfence();
+        dev::named_bar_sync(1, consumer_threads);
+        uint32_t* counters = reinterpret_cast<uint32_t*>(p.ws + p.lay.counters);
+        if (threadIdx.x == 0) {
+            const uint32_t prev = atomicAdd(&counters[si.group], 1u);
+            sh->last_flag = (prev == (uint32_t)(si.nsplit * n_hb - 1));
+            if (sh->last_flag) {
+                counters[si.group] = 0;  // ready for the next forward on this plan
+                __threadfence();
+            }
+        }
+        dev::named_bar_sync(1, consumer_threads);
+        if (sh->last_flag) {
+            // merge the group's splits: rows (token, q head), 4 columns per thread item
+            const int grows = si.ntok * Hq;
+            const float* pob =
+                reinterpret_cast<const float*>(p.ws + p.lay.partial_o) + (int64_t)si.pbase * p.lay.rows_per_slot * D;
+            const float* plb =
+                reinterpret_cast<const float*>(p.ws + p.lay.partial_lse) + (int64_t)si.pbase * p.lay.rows_per_slot;
+            const int items = grows * (D / 4);
+            for (int it = threadIdx.x; it < items; it += consumer_threads) {
+                const int row = it / (D / 4), c4 = (it % (D / 4)) * 4;
+                float mx = -INFINITY;
+                for (int sp = 0; sp < si.nsplit; ++sp) mx = fmaxf(mx, __ldcg(plb + sp * p.lay.rows_per_slot + row));
+                const float mu = mx == -INFINITY ? 0.f : mx;
+                float wsum = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+                for (int sp = 0; sp < si.nsplit; ++sp) {
+                    const float w = dev::fast_exp2(__ldcg(plb + sp * p.lay.rows_per_slot + row) - mu);
+                    const float4 v =
+                        __ldcg(reinterpret_cast<const float4*>(pob + ((int64_t)sp * p.lay.rows_per_slot + row) * D + c4));
+                    wsum += w;
+                    a0 += w * v.x;
+                    a1 += w * v.y;
+                    a2 += w * v.z;
+                    a3 += w * v.w;
+                }
+                const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+                const int64_t orow = (int64_t)(si.tok0 + row / Hq) * Hq + row % Hq;
+                uint2 packed;
+                packed.x = dev::pack_bf16x2(a0 * inv, a1 * inv);
+                packed.y = dev::pack_bf16x2(a2 * inv, a3 * inv);
+                *reinterpret_cast<uint2*>(p.out + orow * D + c4) = packed;
+                if (p.lse != nullptr && c4 == 0) p.lse[orow] = wsum > 0.f ? (mu + __log2f(wsum)) * kLn2 : -INFINITY;
+            }
+        }
+        dev::named_bar_sync(1, consumer_threads);
+    }
+}
+
+template <int D>
+int stage_count(int num_kv_heads, int ctas_per_sm) {
+    const int hb = num_kv_heads < kMaxKvHeads ? num_kv_heads : kMaxKvHeads;
+    const int row_stride = hb * D * 2 + kRowPad;
+    const int stage_bytes = 2 * kStageKeys * row_stride;
+    const int budget = 220 * 1024 / ctas_per_sm - 1024;
+    int st = budget / stage_bytes;
+    return st < 2 ? 2 : (st > 8 ? 8 : st);
+}
+
+template <int D>
+size_t smem_bytes(int num_kv_heads, int stages) {
+    const int hb = num_kv_heads < kMaxKvHeads ? num_kv_heads : kMaxKvHeads;
+    const int row_stride = hb * D * 2 + kRowPad;
+    return ((sizeof(DecSmemHead) + 127) / 128) * 128 + (size_t)stages * 2 * kStageKeys * row_stride;
+}
+
+template <int D>
+cudaError_t launch_d(const ForwardParams& p, int ctas, cudaStream_t s) {
+    const int cps = decode_ctas_per_sm(p.num_kv_heads, D);
+    const int stages = stage_count<D>(p.num_kv_heads, cps);
+    const size_t smem = smem_bytes<D>(p.num_kv_heads, stages);
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int hb = p.num_kv_heads < kMaxKvHeads ? p.num_kv_heads : kMaxKvHeads;
+    const int row_stride = hb * D * 2 + kRowPad;
+    decode_kernel<D><<<ctas, 32 * (hb + 1), smem, s>>>(p, stages, row_stride);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int decode_ctas_per_sm(int num_kv_heads, int head_dim) {
+    (void)head_dim;
+    const int hb = num_kv_heads < kMaxKvHeads ? num_kv_heads : kMaxKvHeads;
+    int c = 8 / (hb > 0 ? hb : 1);
+    return c < 1 ? 1 : (c > 4 ? 4 : c);
+}
+
+bool decode_supported(int num_qo_heads, int num_kv_heads, int head_dim) {
+    if (num_kv_heads < 1) return false;
+    if (num_kv_heads > kMaxKvHeads && num_kv_heads % kMaxKvHeads != 0) return false;
+    if (num_qo_heads % num_kv_heads != 0) return false;
+    if (num_qo_heads / num_kv_heads > kDecRows) return false;
+    return head_dim == 64 || head_dim == 128;
+}
+
+cudaError_t launch_decode(const ForwardParams& p, int head_dim, int ctas, cudaStream_t s) {
+    if (head_dim == 128) return launch_d<128>(p, ctas, s);
+    if (head_dim == 64) return launch_d<64>(p, ctas, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pva

@@ -1,0 +1,215 @@
+// Internal plan layout shared by the host API and the kernels of libpva.so.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/pva.h"
+
+namespace pva {
+
+// ---------------------------------------------------------------- tiling constants
+
+// Decode/row-block kernel: keys per pipeline stage and maximum rows (q tokens x
+// q heads of one kv head) one warp holds -- the M of one m16n8k16 tile.
+constexpr int kDecKeysPerStage = 16;
+constexpr int kDecRows = 16;
+// Tensor-core prefill kernel: rows per tile (M of tcgen05.mma) and keys per KV tile.
+constexpr int kPreRows = 128;
+constexpr int kPreKeys = 128;
+// Smallest split-KV chunk (keys) worth a separate CTA.
+constexpr int kMinSplitChunk = 256;
+
+// Error bits the kernels OR into the plan's error word (same values as pva.h).
+constexpr uint32_t kErrCu = PVA_DEVERR_CU_SEQLENS;
+constexpr uint32_t kErrQgtKv = PVA_DEVERR_Q_GT_KV;
+constexpr uint32_t kErrPage = PVA_DEVERR_PAGE_ID;
+constexpr uint32_t kErrSlot = PVA_DEVERR_SLOT;
+constexpr uint32_t kErrLimits = PVA_DEVERR_LIMITS;
+constexpr uint32_t kErrTimeout = PVA_DEVERR_TIMEOUT;
+// Errors that make the whole batch description untrustworthy: nothing runs.
+constexpr uint32_t kErrFatal = kErrCu | kErrQgtKv | kErrLimits;
+
+// ---------------------------------------------------------------- device plan records
+
+// Header at offset 0 of the workspace, written by the prepare kernel.
+struct PlanHeader {
+    uint32_t error_bits;
+    int32_t n_dec_units;
+    int32_t n_dec_groups;
+    int32_t n_pre_tiles;
+    int32_t n_casc_groups;
+    int32_t n_casc_tiles;
+    int32_t split_chunk;
+    int32_t n_partial_slots;
+    int32_t n_casc_units;
+    int32_t pad[55];
+};
+static_assert(sizeof(PlanHeader) == 256, "header is one 256-byte line");
+
+// A decode group: up to floor(16 / G) consecutive new tokens of one request,
+// all q heads.  One merge (LSE combine) per group when it is split.
+struct DecGroup {
+    int32_t req;
+    int32_t tok0;        // global index of the first token (row of q)
+    int32_t ntok;        // tokens in the group (>= 1)
+    int32_t qpos0;       // absolute position of the first token: kv_len - q_len + (tok0 - cu[req])
+    int32_t nsplit;      // number of units (key ranges) covering the group
+    int32_t pbase;       // first partial slot (valid when nsplit > 1)
+    int32_t kv_end;      // keys [0, kv_end) are visible to some token of the group
+    int32_t casc;        // cascade group id feeding a prefix partial, or -1
+};
+
+// One CTA work item of the decode kernel: keys [k0, k1) of a group.
+struct DecUnit {
+    int32_t group;
+    int32_t k0;
+    int32_t k1;
+    int32_t split;       // index among the group's units (partial slot pbase + split)
+};
+
+// One tile of the tensor-core prefill kernel: kPreRows rows = tokens x q heads of
+// one kv head, keys [0, kv_end) with the causal diagonal.
+struct PreTile {
+    int32_t req;
+    int32_t kvh;
+    int32_t tok0;        // global index of the first token of the tile
+    int32_t ntok;        // tokens in the tile
+    int32_t qpos0;       // absolute position of the first token
+    int32_t kv_end;      // keys [0, kv_end)
+    int32_t pad0, pad1;
+};
+
+// Workspace carve-up (byte offsets from the workspace base); computed on the host.
+struct Layout {
+    size_t header;
+    size_t dec_units;
+    size_t dec_groups;
+    size_t pre_tiles;
+    size_t slots;        // int64 [max_tokens] derived slot mapping
+    size_t counters;     // uint32 [max_dec_groups] merge arrival counters
+    size_t partial_o;    // fp32 [max_partial][rows_per_slot][D]
+    size_t partial_lse;  // fp32 [max_partial][rows_per_slot]
+    size_t req_scratch;  // int32 [max_batch * 4] prepare scratch
+    size_t total;
+    int32_t max_dec_units;
+    int32_t max_dec_groups;
+    int32_t max_pre_tiles;
+    int32_t max_partial;
+    int32_t rows_per_slot;
+    int32_t target_units;
+};
+
+// Parameters of the prepare kernel (by value).
+struct PrepareParams {
+    const int32_t* cu;
+    const int32_t* seqlens;
+    const int32_t* page_table;
+    int64_t ld;
+    const int64_t* user_slots;   // may be null
+    int64_t* derived_slots;
+    int32_t batch;
+    int32_t total_tokens;
+    int32_t max_q_len;
+    int32_t page_size;
+    int64_t num_pages;
+    int32_t num_qo_heads;
+    int32_t num_kv_heads;
+    int32_t group;               // Hq / Hkv
+    int32_t dec_tokens;          // tokens per decode group = 16 / group
+    int32_t pre_tokens;          // tokens per prefill tile = 128 / group
+    int32_t use_prefill;         // 1: requests with q_len > dec_tokens go to the prefill kernel
+    int32_t split_kv;
+    int32_t max_kv_len;
+    int32_t max_tokens;
+    int32_t max_batch;
+    uint8_t* ws;
+    Layout lay;
+};
+
+// Parameters common to the forward kernels (by value).
+struct ForwardParams {
+    const uint16_t* q;           // bf16 bits [T, Hq, D]
+    const uint16_t* k;           // [T, Hkv, D]
+    const uint16_t* v;
+    uint16_t* k_pool;            // [slots, Hkv, D]
+    uint16_t* v_pool;
+    uint16_t* out;               // [T, Hq, D]
+    float* lse;                  // [T, Hq] or null
+    const int32_t* cu;
+    const int32_t* seqlens;
+    const int32_t* page_table;
+    int64_t ld;
+    const int64_t* slots;        // user or derived
+    int32_t total_tokens;
+    int32_t page_size;
+    int32_t page_shift;          // log2(page_size)
+    int64_t num_pages;
+    int64_t num_slots;
+    int32_t num_qo_heads;
+    int32_t num_kv_heads;
+    int32_t group;
+    float scale_log2;            // sm_scale * log2(e)
+    uint8_t* ws;
+    Layout lay;
+};
+
+// Host view of a prepared batch, stored inside pva_meta::opaque.
+struct MetaHost {
+    uint64_t magic;
+    pva_config cfg;
+    int32_t batch;
+    int32_t total_tokens;
+    int32_t max_q_len;
+    int32_t sm_count;
+    int32_t use_prefill;
+    int32_t dec_ctas;
+    const int32_t* cu;
+    const int32_t* seqlens;
+    const int32_t* page_table;
+    int64_t ld;
+    const int64_t* slots;
+    uint8_t* ws;
+    void* stream;
+    void* events[5];           // optional timing events (attn_set_timing_events)
+    int32_t n_events;
+    int32_t kernels_per_forward;
+    Layout lay;
+};
+static_assert(sizeof(MetaHost) <= sizeof(pva_meta), "MetaHost must fit in pva_meta");
+constexpr uint64_t kMetaMagic = 0x5056414d45544131ull;  // "PVAMETA1"
+
+// ---------------------------------------------------------------- host helpers
+
+inline int ilog2(int x) {
+    int r = 0;
+    while ((1 << r) < x) ++r;
+    return r;
+}
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Split a key range of `ext` keys into near-equal chunks of whole 16-key stages,
+// about `chunk` keys each; returns the number of (non-empty) chunks and their length.
+#ifdef __CUDACC__
+__host__ __device__
+#endif
+inline int split_ranges(int ext, int chunk, int* per_out) {
+    int s = (ext + chunk - 1) / chunk;
+    if (s < 1) s = 1;
+    int per = ((ext + s - 1) / s + kDecKeysPerStage - 1) / kDecKeysPerStage * kDecKeysPerStage;
+    if (per < kDecKeysPerStage) per = kDecKeysPerStage;
+    *per_out = per;
+    return (ext + per - 1) / per;
+}
+
+// Launchers (defined in the .cu files).
+cudaError_t launch_prepare(const PrepareParams& p, cudaStream_t s);
+cudaError_t launch_store(const ForwardParams& p, int head_dim, cudaStream_t s);
+cudaError_t launch_decode(const ForwardParams& p, int head_dim, int ctas, cudaStream_t s);
+int decode_ctas_per_sm(int num_kv_heads, int head_dim);
+bool decode_supported(int num_qo_heads, int num_kv_heads, int head_dim);
+
+}  // namespace pva

@@ -1,0 +1,53 @@
+// K1: store_kvcache -- this step's K and V rows scattered into the paged pool.
+//
+// "The attention backend and a reference implementation" (section
+// "Variable-length, paged attention with prefixes"): the forward writes this
+// step's K/V into the pool before reading any of it back; "Attention backends:
+// backend, metadata builder and implementation" (step 2) describes the same
+// update as a scatter by slot.  A slot row holds all kv heads of one token,
+// Hkv * D bf16 = 1-2 KiB contiguous in both the source and the pool, so one
+// warp moves one token's K row (or V row) with 16-byte vector accesses: reads
+// stream past L1, writes stay in L2 for the attention kernels that follow.
+#include <cuda_runtime.h>
+
+#include "device_utils.cuh"
+#include "pva_internal.h"
+
+namespace pva {
+namespace {
+
+constexpr int kThreads = 256;
+
+__global__ void __launch_bounds__(kThreads) store_kernel(ForwardParams p, int row_vecs) {
+    PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws + p.lay.header);
+    // the decode kernel that follows fetches work from this counter
+    if (blockIdx.x == 0 && threadIdx.x == 0) hdr->pad[0] = 0;
+    if (hdr->error_bits & kErrFatal) return;
+    const int lane = threadIdx.x & 31;
+    const int64_t job = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);  // (token, K|V)
+    if (job >= 2 * (int64_t)p.total_tokens) return;
+    const int64_t t = job >> 1;
+    const bool is_v = job & 1;
+    const int64_t slot = p.slots[t];
+    if (slot == -1) return;
+    if (slot < 0 || slot >= p.num_slots) {
+        if (lane == 0 && !is_v) dev::set_error(&hdr->error_bits, kErrSlot);
+        return;
+    }
+    const int4* src = reinterpret_cast<const int4*>(is_v ? p.v : p.k) + t * row_vecs;
+    int4* dst = reinterpret_cast<int4*>(is_v ? p.v_pool : p.k_pool) + slot * row_vecs;
+    for (int i = lane; i < row_vecs; i += 32) dst[i] = dev::ld_stream_v4(src + i);
+}
+
+}  // namespace
+
+cudaError_t launch_store(const ForwardParams& p, int head_dim, cudaStream_t s) {
+    if (p.total_tokens <= 0) return cudaSuccess;
+    const int row_vecs = p.num_kv_heads * head_dim * 2 / 16;
+    const int64_t jobs = 2 * (int64_t)p.total_tokens;
+    const int64_t blocks = (jobs + kThreads / 32 - 1) / (kThreads / 32);
+    store_kernel<<<(unsigned)blocks, kThreads, 0, s>>>(p, row_vecs);
+    return cudaGetLastError();
+}
+
+}  // namespace pva

@@ -1,0 +1,222 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle on the
+same seeded inputs.  KV pool bit-exact after the write; bf16 output within
+2e-2 + 1e-2*|ref|; LSE within 1e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from harness import assert_close, host_copy, make_engine, pool_bits, run_cuda, run_oracle
+from paged_variable_length_gb300 import pva
+from paged_variable_length_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _full_check(wl, poison=True, slot_mapping=False, max_q_len=0, engine=None, **eng_kw):
+    t = W.make_tensors(wl, DEV, poison_unused=poison)
+    h = host_copy(t)
+    slots = oracle.slot_mapping(wl.cu_seqlens_q, wl.cache_seqlens, wl.page_table, wl.page_size)
+    sm = torch.as_tensor(slots, device=DEV) if slot_mapping else None
+    eng = engine or make_engine(wl, **eng_kw)
+    out, lse, eng = run_cuda(wl, t, engine=eng, slot_mapping=sm, max_q_len=max_q_len)
+    ref_o, ref_l, ref_kp, ref_vp = run_oracle(wl, h, slots=slots)
+    assert np.array_equal(pool_bits(t["k_pool"]), ref_kp), "K pool differs from the oracle's"
+    assert np.array_equal(pool_bits(t["v_pool"]), ref_vp), "V pool differs from the oracle's"
+    err = assert_close(out, lse, ref_o, ref_l)
+    assert pva.attn_get_device_status(eng.meta) == 0
+    return err, eng
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_worked_example(seed):
+    _full_check(W.worked_example(seed))
+
+
+def test_pages_literal_layout():
+    """The ch. 5 example layout: H 16, Hkv 8, D 128, page rows 0-5 / 40-43,20-22 / 50-58."""
+    table = np.zeros((3, 16), np.int32)
+    table[0, :6] = np.arange(6)
+    table[1, :7] = [40, 41, 42, 43, 20, 21, 22]
+    table[2, :9] = np.arange(50, 59)
+    wl = W.Workload("literal", [6, 3, 1], [6, 7, 9], 16, 8, 128, 1, 64, table)
+    _full_check(wl, poison=False)
+    _full_check(wl, poison=False, slot_mapping=True)
+
+
+CASES = [
+    # (Hq, Hkv, D, ps, q_lens, kv_lens)
+    (4, 2, 64, 1, [6, 3, 1], [6, 7, 9]),
+    (32, 8, 128, 16, [1, 1, 1, 1, 3], [1, 16, 17, 700, 33]),
+    (28, 4, 128, 1, [1, 2, 1, 1], [5, 2, 1000, 257]),
+    (8, 8, 64, 4, [1, 9, 0, 16, 1], [3, 20, 5, 16, 77]),
+    (32, 8, 128, 16, [40, 1, 130], [40, 2000, 300]),          # prefills and a long decode in one batch
+    (16, 1, 128, 32, [1, 5, 1], [4096, 5, 31]),                # MQA
+    (16, 16, 64, 2, [1, 1, 7], [9, 1, 7]),                     # MHA (group 1)
+    (32, 2, 128, 8, [1, 1], [3000, 5]),                        # group 16
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"{c[0]}-{c[1]}-{c[2]}-ps{c[3]}-{i}" for i, c in enumerate(CASES)])
+@pytest.mark.parametrize("explicit_slots", [False, True])
+def test_random_batches(case, explicit_slots):
+    Hq, Hkv, D, ps, ql, kl = case
+    wl = W.custom(ql, kl, Hq, Hkv, D, ps, seed=len(ql) + D)
+    _full_check(wl, slot_mapping=explicit_slots)
+
+
+def test_split_kv_off_matches_on():
+    wl = W.custom([1, 1, 4], [3000, 700, 2500], 32, 8, 128, 16, seed=5)
+    e1, _ = _full_check(wl, enable_split_kv=True)
+    e2, _ = _full_check(wl, enable_split_kv=False)
+
+
+def test_many_layers_reuse_one_plan():
+    """prepare once, forward per layer (different pools and activations)."""
+    wl = W.custom([1, 5, 1, 12], [900, 5, 64, 40], 32, 8, 128, 16, seed=11)
+    eng = make_engine(wl)
+    t0 = W.make_tensors(wl, DEV)
+    eng.prepare(t0["cu_seqlens_q"], t0["cache_seqlens"], t0["page_table"], wl.total_tokens)
+    for layer in range(3):
+        wl.seed = 100 + layer
+        t = W.make_tensors(wl, DEV)
+        h = host_copy(t)
+        out = torch.empty_like(t["q"])
+        lse = torch.empty(t["q"].shape[:2], dtype=torch.float32, device=DEV)
+        eng.forward(t["q"], t["k"], t["v"], t["k_pool"], t["v_pool"], out, lse)
+        torch.cuda.synchronize()
+        ref_o, ref_l, ref_kp, _ = run_oracle(wl, h)
+        assert np.array_equal(pool_bits(t["k_pool"]), ref_kp)
+        assert_close(out, lse, ref_o, ref_l)
+
+
+def test_deterministic():
+    wl = W.custom([1, 1, 3], [5000, 1200, 800], 32, 8, 128, 16, seed=9)
+    t = W.make_tensors(wl, DEV)
+    outs = []
+    for _ in range(2):
+        tt = {k: v.clone() for k, v in t.items()}
+        out, lse, _ = run_cuda(wl, tt)
+        outs.append((out.clone(), lse.clone()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+def test_store_only_is_bit_exact():
+    wl = W.custom([3, 1, 7], [3, 9, 20], 8, 2, 128, 4, seed=4)
+    t = W.make_tensors(wl, DEV)
+    h = host_copy(t)
+    eng = make_engine(wl)
+    eng.prepare(t["cu_seqlens_q"], t["cache_seqlens"], t["page_table"], wl.total_tokens)
+    pva.attn_store_kvcache(eng.meta, t["k"], t["v"], t["k_pool"], t["v_pool"])
+    torch.cuda.synchronize()
+    slots = oracle.slot_mapping(wl.cu_seqlens_q, wl.cache_seqlens, wl.page_table, wl.page_size)
+    kp, vp = oracle.store_kvcache(h["k"], h["v"], slots, h["k_pool"], h["v_pool"])
+    assert np.array_equal(pool_bits(t["k_pool"]), kp) and np.array_equal(pool_bits(t["v_pool"]), vp)
+
+
+def test_padding_slots_are_skipped():
+    wl = W.custom([2, 1], [2, 6], 8, 2, 64, 1, seed=6)
+    t = W.make_tensors(wl, DEV)
+    h = host_copy(t)
+    slots = oracle.slot_mapping(wl.cu_seqlens_q, wl.cache_seqlens, wl.page_table, wl.page_size)
+    slots[1] = -1  # a padding token: not stored
+    eng = make_engine(wl)
+    eng.prepare(t["cu_seqlens_q"], t["cache_seqlens"], t["page_table"], wl.total_tokens,
+                torch.as_tensor(slots, device=DEV))
+    out = torch.empty_like(t["q"])
+    eng.forward(t["q"], t["k"], t["v"], t["k_pool"], t["v_pool"], out)
+    torch.cuda.synchronize()
+    kp, _ = oracle.store_kvcache(h["k"], h["v"], slots, h["k_pool"], h["v_pool"])
+    assert np.array_equal(pool_bits(t["k_pool"]), kp)
+
+
+# ------------------------------------------------------------------ device-checked errors
+
+
+def _error_bits(wl, t, slot_mapping=None, max_q_len=0):
+    eng = make_engine(wl)
+    eng.prepare(t["cu_seqlens_q"], t["cache_seqlens"], t["page_table"], wl.total_tokens, slot_mapping, max_q_len)
+    out = torch.zeros_like(t["q"])
+    eng.forward(t["q"], t["k"], t["v"], t["k_pool"], t["v_pool"], out)
+    return pva.attn_get_device_status(eng.meta), out
+
+
+def test_q_len_above_kv_len_is_flagged_not_run():
+    wl = W.custom([3, 1], [3, 4], 8, 2, 64, 1, seed=1)
+    t = W.make_tensors(wl, DEV)
+    t["cache_seqlens"][0] = 2  # 3 new tokens but a KV length of 2
+    bits, out = _error_bits(wl, t)
+    assert bits & 0x02
+    assert torch.count_nonzero(out) == 0
+
+
+def test_decreasing_cu_seqlens_is_flagged():
+    wl = W.custom([3, 1], [3, 4], 8, 2, 64, 1, seed=1)
+    t = W.make_tensors(wl, DEV)
+    t["cu_seqlens_q"][1] = 5
+    bits, _ = _error_bits(wl, t)
+    assert bits & 0x01
+
+
+def test_page_id_outside_pool_is_flagged():
+    wl = W.custom([1], [40], 8, 2, 64, 4, seed=2)
+    t = W.make_tensors(wl, DEV)
+    t["page_table"][0, 3] = wl.num_pages + 7
+    bits, _ = _error_bits(wl, t)
+    assert bits & 0x04
+
+
+def test_slot_outside_pool_is_flagged():
+    wl = W.custom([2], [2], 8, 2, 64, 1, seed=3)
+    t = W.make_tensors(wl, DEV)
+    sm = torch.tensor([0, wl.num_slots + 3], dtype=torch.int64, device=DEV)
+    bits, _ = _error_bits(wl, t, slot_mapping=sm)
+    assert bits & 0x08
+
+
+def test_q_len_above_hint_is_flagged():
+    wl = W.custom([5, 1], [9, 4], 8, 2, 64, 1, seed=3)
+    t = W.make_tensors(wl, DEV)
+    bits, _ = _error_bits(wl, t, max_q_len=2)
+    assert bits & 0x10
+
+
+# ------------------------------------------------------------------ full-size workloads (sampled rows)
+
+
+def _sampled_check(wl, n_rows=3000, seed=0):
+    t = W.make_tensors(wl, DEV)
+    slots = oracle.slot_mapping(wl.cu_seqlens_q, wl.cache_seqlens, wl.page_table, wl.page_size)
+    written = np.unique(slots)
+    k_in = t["k"].cpu()
+    v_in = t["v"].cpu()
+    q_h = t["q"].cpu()
+    eng = make_engine(wl)
+    out, lse, eng = run_cuda(wl, t, engine=eng, max_q_len=max(wl.q_lens))
+    assert pva.attn_get_device_status(eng.meta) == 0
+    # pool: the written rows are bit-exact copies of this step's K/V
+    kp = t["k_pool"][torch.as_tensor(slots, device=DEV)].cpu()
+    vp = t["v_pool"][torch.as_tensor(slots, device=DEV)].cpu()
+    assert torch.equal(kp, k_in) and torch.equal(vp, v_in)
+    assert written.size == slots.size
+    # output: sampled rows recomputed by the oracle over the written pool
+    rng = np.random.default_rng(seed)
+    T, Hq = wl.total_tokens, wl.num_qo_heads
+    sel = np.zeros((T, Hq), bool)
+    if T * Hq <= n_rows:
+        sel[:] = True
+    else:
+        idx = rng.choice(T * Hq, size=n_rows, replace=False)
+        sel.reshape(-1)[idx] = True
+        sel[np.asarray(wl.cu_seqlens_q[1:]) - 1, :] = True  # every request's last token, all heads
+    ref_o, ref_l = oracle.attention(q_h, t["k_pool"].cpu(), t["v_pool"].cpu(), wl.cu_seqlens_q, wl.cache_seqlens,
+                                    wl.page_table, wl.page_size, row_select=sel)
+    return assert_close(out, lse, ref_o, ref_l, mask=sel)
+
+
+@pytest.mark.parametrize("name", ["decode", "mixed", "cascade", "prefill"])
+def test_full_size_workload(name):
+    _sampled_check(W.WORKLOADS[name](0))
