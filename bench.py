@@ -115,10 +115,20 @@ class ClockSampler:
             self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+
+    def wait_first_sample(self, timeout_s: float = 3.0):
+        if self.proc is None:
+            return
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < timeout_s:
+            self.f.flush()
+            if os.path.getsize(self.path) > 0:
+                return
+            time.sleep(0.05)
 
     def stop(self):
         if self.proc is None:
@@ -271,6 +281,7 @@ def run_ours(args):
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     clocks = ClockSampler(local, enabled=not args.no_clocks)
+    clocks.wait_first_sample()
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -282,6 +293,13 @@ def run_ours(args):
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
+    # the timed region is short next to the sampler's period: keep the same step
+    # running (no flush) for ~1 s more so the clock record covers the load
+    t_end = time.perf_counter() + 1.0
+    while time.perf_counter() < t_end:
+        for _ in range(20):
+            step()
+        torch.cuda.synchronize()
     clock_info = clocks.stop()
     times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = sum(times) / len(times)

@@ -160,9 +160,14 @@ pva_status attn_prepare_metadata(const pva_config* cfg, const int32_t* cu_seqlen
     h.total_tokens = total_tokens;
     h.max_q_len = mq;
     h.sm_count = sms;
-    h.use_prefill = 0;  // the tensor-core prefill kernel is enabled per build below
-    (void)TB;
+    // requests with more than TB new tokens run on the tensor-core prefill kernel
+    h.use_prefill = (mq > TB && prefill_supported(cfg->num_qo_heads, cfg->num_kv_heads, cfg->head_dim)) ? 1 : 0;
     h.dec_ctas = sms * decode_ctas_per_sm(cfg->num_kv_heads, cfg->head_dim);
+    {
+        const int64_t TM = kPreRows / G;
+        const int64_t bound = ((int64_t)total_tokens / TM + batch + 1) * cfg->num_kv_heads;
+        h.pre_ctas = h.use_prefill ? (int32_t)(bound < sms ? bound : sms) : 0;
+    }
     h.cu = cu_seqlens_q;
     h.seqlens = cache_seqlens;
     h.page_table = page_table;
@@ -234,7 +239,9 @@ pva_status attn_forward(const pva_meta* meta, const void* q, const void* k, cons
     };
     if (mark(0) != cudaSuccess) return PVA_ERR_CUDA;
     if (launch_store(fp, h->cfg.head_dim, s) != cudaSuccess) return PVA_ERR_CUDA;
-    if (mark(1) != cudaSuccess || mark(2) != cudaSuccess || mark(3) != cudaSuccess) return PVA_ERR_CUDA;
+    if (mark(1) != cudaSuccess) return PVA_ERR_CUDA;
+    if (h->use_prefill && launch_prefill(fp, h->cfg.head_dim, h->pre_ctas, s) != cudaSuccess) return PVA_ERR_CUDA;
+    if (mark(2) != cudaSuccess || mark(3) != cudaSuccess) return PVA_ERR_CUDA;
     if (launch_decode(fp, h->cfg.head_dim, h->dec_ctas, s) != cudaSuccess) return PVA_ERR_CUDA;
     if (mark(4) != cudaSuccess) return PVA_ERR_CUDA;
     return PVA_OK;

@@ -101,7 +101,6 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
     __syncthreads();
 
     const DecUnit* units = reinterpret_cast<const DecUnit*>(p.ws + p.lay.dec_units);
-    const DecGroup* groups = reinterpret_cast<const DecGroup*>(p.ws + p.lay.dec_groups);
     int32_t* sched = &hdr->pad[0];
 
     if (warp == HB) {
@@ -111,10 +110,26 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
         const uint64_t policy = dev::policy_evict_first();
         const int ps_mask = p.page_size - 1;
         uint32_t armed = 0, armed_par = 0;  // stages with copies issued, and the parity of that phase
+        // Dynamic work fetch, one unit ahead but late: the ticket for the next unit is
+        // taken four stages before the current unit ends, its record read two stages
+        // before, its first page id one stage before.  A CTA so holds a unit in
+        // reserve only briefly (a long reservation starves the tail of the grid), and
+        // no global round trip sits between a freed ring slot and the copies that
+        // refill it.  Page ids inside a unit are read one stage ahead.
+        auto page_of = [&](const int32_t* prow, int key) -> int64_t {
+            int64_t page = prow[key >> p.page_shift];
+            if (page < 0 || page >= p.num_pages) {
+                dev::set_error(err, kErrPage);
+                page = 0;  // keep the transaction count; the result is flagged
+            }
+            return page;
+        };
+        const int r = lane & 15;
+        int u = __shfl_sync(0xffffffffu, lane == 0 ? atomicAdd(sched, 1) : 0, 0);
+        DecUnit du{};
+        if (u < n_units) du = units[u / n_hb];
+        int64_t page_first = -1;  // page of the unit's first stage, when already fetched
         while (true) {
-            int u = 0;
-            if (lane == 0) u = atomicAdd(sched, 1);
-            u = __shfl_sync(0xffffffffu, u, 0);
             if (!dev::mbar_wait(&sh->empty[stage], phase ^ 1)) {
                 abort_cta(sh, err);
                 break;
@@ -127,18 +142,33 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
                 break;
             }
             const int hb = u % n_hb;
-            const DecUnit du = units[u / n_hb];
-            const DecGroup dg = groups[du.group];
-            const int32_t* prow = p.page_table + (int64_t)dg.req * p.ld;
-            // warm L2 with this group's query rows (read by the consumers at unit start)
+            const int32_t* prow = p.page_table + (int64_t)du.req * p.ld;
+            // warm L2 with this unit's query rows (read by the consumers at unit start)
             {
-                const char* qbase = reinterpret_cast<const char*>(p.q + (int64_t)dg.tok0 * Hq * D);
-                const int qbytes = dg.ntok * Hq * D * 2;
+                const char* qbase = reinterpret_cast<const char*>(p.q + (int64_t)du.tok0 * Hq * D);
+                const int qbytes = du.ntok * Hq * D * 2;
                 for (int off = lane * 128; off < qbytes; off += 32 * 128)
                     asm volatile("prefetch.global.L2 [%0];" ::"l"(qbase + off));
             }
-            for (int k = du.k0; k < du.k1; k += kStageKeys) {
-                if (k != du.k0) {
+            int64_t page_next = page_first >= 0 ? page_first : ((du.k0 + r < du.k1) ? page_of(prow, du.k0 + r) : 0);
+            page_first = -1;
+            const int nst = (du.k1 - du.k0 + kStageKeys - 1) / kStageKeys;
+            int ticket = 0, u_next = n_units;
+            DecUnit du_next{};
+            for (int si_ = 0; si_ < nst; ++si_) {
+                const int k = du.k0 + si_ * kStageKeys;
+                if (si_ == max(nst - 4, 0) && lane == 0) ticket = atomicAdd(sched, 1);
+                if (si_ == max(nst - 2, 0)) {
+                    u_next = __shfl_sync(0xffffffffu, ticket, 0);
+                    if (u_next < n_units) du_next = units[u_next / n_hb];
+                }
+                const int64_t page = page_next;
+                if (k + kStageKeys + r < du.k1) {
+                    page_next = page_of(prow, k + kStageKeys + r);
+                } else if (si_ == nst - 1 && u_next < n_units && du_next.k0 + r < du_next.k1) {
+                    page_first = page_of(p.page_table + (int64_t)du_next.req * p.ld, du_next.k0 + r);
+                }
+                if (si_ != 0) {
                     if (!dev::mbar_wait(&sh->empty[stage], phase ^ 1)) {
                         abort_cta(sh, err);
                         goto producer_done;
@@ -151,28 +181,21 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
                     si.group = du.group;
                     si.k = k;
                     si.k1 = du.k1;
-                    si.tok0 = dg.tok0;
-                    si.ntok = dg.ntok;
-                    si.qpos0 = dg.qpos0;
-                    si.nsplit = dg.nsplit;
-                    si.pbase = dg.pbase;
+                    si.tok0 = du.tok0;
+                    si.ntok = du.ntok;
+                    si.qpos0 = du.qpos0;
+                    si.nsplit = du.nsplit;
+                    si.pbase = du.pbase;
                     si.split = du.split;
                     si.hb = hb;
-                    si.flags = (k == du.k0 ? kFirst : 0) | (k + kStageKeys >= du.k1 ? kLast : 0);
+                    si.flags = (si_ == 0 ? kFirst : 0) | (si_ == nst - 1 ? kLast : 0);
                     dev::mbar_arrive_expect_tx(&sh->full[stage], (uint32_t)(2 * nk * row_bytes));
                 }
                 armed |= 1u << stage;
                 armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
                 __syncwarp();
-                const int r = lane & 15;
                 if (r < nk) {
-                    const int key = k + r;
-                    int64_t page = prow[key >> p.page_shift];
-                    if (page < 0 || page >= p.num_pages) {
-                        dev::set_error(err, kErrPage);
-                        page = 0;  // keep the transaction count; the result is flagged
-                    }
-                    const int64_t slot = (page << p.page_shift) + (key & ps_mask);
+                    const int64_t slot = (page << p.page_shift) + ((k + r) & ps_mask);
                     const uint16_t* src =
                         (lane < 16 ? p.k_pool : p.v_pool) + slot * (int64_t)(Hkv * D) + hb * HB * D;
                     uint8_t* dst = ring + stage * stage_bytes + (lane < 16 ? 0 : kStageKeys * row_stride) +
@@ -184,6 +207,8 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
                     phase ^= 1;
                 }
             }
+            u = u_next;
+            du = du_next;
         }
     producer_done:
         // drain: every copy this warp issued must land before the CTA may exit

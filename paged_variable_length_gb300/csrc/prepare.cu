@@ -204,6 +204,13 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
                     du.k0 = min(ext, u * per);
                     du.k1 = min(ext, (u + 1) * per);
                     du.split = u;
+                    du.req = i;
+                    du.tok0 = dg.tok0;
+                    du.ntok = dg.ntok;
+                    du.qpos0 = dg.qpos0;
+                    du.nsplit = dg.nsplit;
+                    du.pbase = dg.pbase;
+                    du.pad0 = du.pad1 = 0;
                     units[ui++] = du;
                 }
                 if (s > 1) pi += s;

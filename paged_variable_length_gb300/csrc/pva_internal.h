@@ -62,12 +62,20 @@ struct DecGroup {
     int32_t casc;        // cascade group id feeding a prefix partial, or -1
 };
 
-// One CTA work item of the decode kernel: keys [k0, k1) of a group.
+// One CTA work item of the decode kernel: keys [k0, k1) of a group.  The group's
+// fields are repeated here so that one load brings everything a unit needs.
 struct DecUnit {
     int32_t group;
     int32_t k0;
     int32_t k1;
     int32_t split;       // index among the group's units (partial slot pbase + split)
+    int32_t req;
+    int32_t tok0;
+    int32_t ntok;
+    int32_t qpos0;
+    int32_t nsplit;
+    int32_t pbase;
+    int32_t pad0, pad1;
 };
 
 // One tile of the tensor-core prefill kernel: kPreRows rows = tokens x q heads of
@@ -166,6 +174,7 @@ struct MetaHost {
     int32_t sm_count;
     int32_t use_prefill;
     int32_t dec_ctas;
+    int32_t pre_ctas;
     const int32_t* cu;
     const int32_t* seqlens;
     const int32_t* page_table;
@@ -209,6 +218,8 @@ inline int split_ranges(int ext, int chunk, int* per_out) {
 cudaError_t launch_prepare(const PrepareParams& p, cudaStream_t s);
 cudaError_t launch_store(const ForwardParams& p, int head_dim, cudaStream_t s);
 cudaError_t launch_decode(const ForwardParams& p, int head_dim, int ctas, cudaStream_t s);
+cudaError_t launch_prefill(const ForwardParams& p, int head_dim, int ctas, cudaStream_t s);
+bool prefill_supported(int num_qo_heads, int num_kv_heads, int head_dim);
 int decode_ctas_per_sm(int num_kv_heads, int head_dim);
 bool decode_supported(int num_qo_heads, int num_kv_heads, int head_dim);
 
