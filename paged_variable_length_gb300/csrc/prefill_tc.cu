@@ -7,22 +7,27 @@
 // (query r of n sees keys j <= kv_len - n + r), softmax, O = P V.  It is the
 // dense contraction of the path, so it runs as tcgen05 MMAs:
 //
-//   * a tile is 128 rows = floor(128/G) consecutive new tokens x the G q heads
-//     of one kv head (GQA packing: every K/V tile loaded serves all G heads);
-//     keys run in 128-key tiles up to the tile's causal end (later keys are
-//     never loaded: causal tile skipping), only tiles crossing the diagonal
-//     get an elementwise mask;
-//   * warp 0 (producer) loads Q once per tile and K/V tiles through TMA from
-//     the paged pool: one 3-D box per page (rows of one kv head, 128-byte
-//     swizzle) and single-row boxes for the valid rows of a partial last page,
-//     so no slot past kv_len is read; two K and two V stages;
-//   * warp 1 issues the MMAs from one thread: S_j = Q K_j^T into one of two
-//     TMEM buffers (fp32, 128 lanes x 128 columns), then O += P_{j-1} V_{j-1}
-//     into a TMEM accumulator, so the next S overlaps the current softmax;
-//   * warps 2-5 (one TMEM lane = one row per thread) run the online softmax:
-//     tcgen05.ld of S, mask, running max, exp2, P as bf16 into shared memory
-//     (the A operand of the P V product); O in TMEM is rescaled only when a
-//     row's max grows by more than 2^8, and normalised once at the end.
+//   * a Q tile is 128 rows = floor(128/G) consecutive new tokens x the G q
+//     heads of one kv head (GQA packing: every K/V tile loaded serves all G
+//     heads); a CTA work unit holds two consecutive Q tiles of one request and
+//     kv head, which share every K/V tile;
+//   * keys run in 128-key tiles up to each Q tile's causal end (later keys
+//     are never loaded or multiplied: causal tile skipping); only tiles that
+//     cross the diagonal get an elementwise mask;
+//   * warp 9 (producer) loads Q and K/V tiles with TMA from the paged pool:
+//     one 3-D box per page (rows of one kv head, 128-byte swizzle) plus
+//     single-row boxes for the valid rows of a partial last page, so no slot
+//     past kv_len is read; two K and two V stages;
+//   * warp 8 issues the MMAs from one thread, in the order
+//     PV0(j), S0(j+1), PV1(j), S1(j+1): while one softmax warpgroup works on
+//     its S tile the tensor core runs the other tile's products;
+//   * warps 0-3 / 4-7 are the softmax warpgroups of Q tile 0 / 1, one row per
+//     thread (TMEM lane = row): tcgen05.ld of S, mask, running max, exp2, and
+//     P as packed bf16 written back into the S columns of TMEM, where the
+//     P V MMA reads it as its A operand.  O (fp32, TMEM) is rescaled only when
+//     a row's max grows by more than 2^8, and normalised once at the end.
+// TMEM: per Q tile h, S_h at columns 256h .. 256h+127 (P_h aliases its first
+// 64 columns) and O_h at 256h+128 .. 256h+255.
 // Every wait is bounded; a timeout sets PVA_DEVERR_TIMEOUT and the CTA winds
 // down (outstanding copies and MMAs waited for, TMEM freed) without trapping.
 #include <cuda.h>
@@ -37,35 +42,32 @@
 namespace pva {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // 8 softmax warps, MMA warp, producer warp
+constexpr int kMmaWarp = 8;
+constexpr int kProducerWarp = 9;
 constexpr int kRegion = 128 * 128;  // one 128-row x 128-byte swizzled region (64 bf16 columns)
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
-struct Layout2 {
+struct SmemMap {
     static constexpr int kHalves = D / 64;
     static constexpr int kTile = kRegion * kHalves;
-    static constexpr int kQ = 0;
-    static constexpr int kK = kQ + kTile;
-    static constexpr int kV = kK + 2 * kTile;
-    static constexpr int kP = kV + 2 * kTile;
-    static constexpr int kBytes = kP + 2 * kRegion;
+    static constexpr int kQ = 0;                 // two Q tiles
+    static constexpr int kK = kQ + 2 * kTile;    // two K stages
+    static constexpr int kV = kK + 2 * kTile;    // two V stages
+    static constexpr int kBytes = kV + 2 * kTile;
 };
 
 struct Bars {
     uint64_t q_full, q_empty;
     uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
-    uint64_t s_full[2];
-    uint64_t p_full, pv_done, o_free, drain;
+    uint64_t s_full[2], p_full[2], o_ready[2], o_free[2];
+    uint64_t drain;
     uint32_t tmem_base;
     int32_t abort_flag;
 };
-
-__device__ __forceinline__ uint32_t sw128(int row, int col16) {  // byte offset of 16-byte chunk col16 of a row
-    return row * 128 + (((col16 ^ (row & 7)) & 7) << 4);
-}
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Bars* b, uint32_t* err) {
     if (dev::mbar_wait(bar, parity)) return true;
@@ -74,22 +76,27 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ba
     return false;
 }
 
+// Number of 128-key tiles Q tile h of a unit walks (0 when the tile is empty).
+__device__ __forceinline__ int kv_tiles(int kv_end, int ntok) {
+    return ntok > 0 ? (kv_end + kPreKeys - 1) / kPreKeys : 0;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const ForwardParams p, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k_page, const __grid_constant__ CUtensorMap tm_v_page,
                    const __grid_constant__ CUtensorMap tm_k_row, const __grid_constant__ CUtensorMap tm_v_row,
                    int rows_page) {
-    using L = Layout2<D>;
+    using L = SmemMap<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ Bars bars;
     Bars* b = &bars;
     PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws + p.lay.header);
     uint32_t* err = &hdr->error_bits;
-    const int n_tiles = hdr->n_pre_tiles;
-    if ((hdr->error_bits & kErrFatal) || n_tiles == 0 || (int)blockIdx.x >= n_tiles) return;
-    const PreTile* tiles = reinterpret_cast<const PreTile*>(p.ws + p.lay.pre_tiles);
+    const int n_units = hdr->n_pre_tiles;
+    if ((hdr->error_bits & kErrFatal) || n_units == 0 || (int)blockIdx.x >= n_units) return;
+    const PreTile* units = reinterpret_cast<const PreTile*>(p.ws + p.lay.pre_tiles);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.group, Hq = p.num_qo_heads;
@@ -107,15 +114,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             dev::mbar_init(&b->v_full[s], 1);
             dev::mbar_init(&b->v_empty[s], 1);
             dev::mbar_init(&b->s_full[s], 1);
+            dev::mbar_init(&b->p_full[s], 4);
+            dev::mbar_init(&b->o_ready[s], 1);
+            dev::mbar_init(&b->o_free[s], 4);
         }
-        dev::mbar_init(&b->p_full, 4);
-        dev::mbar_init(&b->pv_done, 1);
-        dev::mbar_init(&b->o_free, 4);
         dev::mbar_init(&b->drain, 1);
         b->abort_flag = 0;
         dev::fence_barrier_init();
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tc::tmem_alloc(&b->tmem_base, kTmemCols);
         tc::tmem_relinquish();
     }
@@ -123,17 +130,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = b->tmem_base;
-    const uint32_t t_s[2] = {tmem, tmem + 128};
-    const uint32_t t_o = tmem + 256;
 
-    if (warp == 0) {
+    if (warp == kProducerWarp) {
         // ============================================================== producer (TMA)
         if (lane == 0) {
             tc::prefetch_tmap(&tm_q);
             tc::prefetch_tmap(&tm_k_page);
             tc::prefetch_tmap(&tm_v_page);
         }
-        const uint64_t pol_kv = dev::policy_evict_last();  // K/V tiles are re-read by the request's other tiles
+        const uint64_t pol_kv = dev::policy_evict_last();  // K/V tiles are re-read by the request's other units
         uint32_t it = 0;
         int uc = 0;
         // barriers this warp armed with copies, and the parity of the phase each last armed
@@ -143,24 +148,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             armed_par = (armed_par & ~(1u << bit)) | (par << bit);
         };
         const int ps = p.page_size, ps_mask = p.page_size - 1;
-        for (int u = blockIdx.x; u < n_tiles && !b->abort_flag; u += gridDim.x, ++uc) {
-            const PreTile pt = tiles[u];
+        for (int u = blockIdx.x; u < n_units && !b->abort_flag; u += gridDim.x, ++uc) {
+            const PreTile pt = units[u];
             const int32_t* prow = p.page_table + (int64_t)pt.req * p.ld;
+            const int ntiles_q = pt.ntok1 > 0 ? 2 : 1;
             if (uc > 0 && !wait_or_abort(&b->q_empty, (uc - 1) & 1, b, err)) break;
             if (lane == 0) {
-                dev::mbar_arrive_expect_tx(&b->q_full, (uint32_t)(L::kHalves * 128 * G * TM));
-                for (int h = 0; h < L::kHalves; ++h)
-                    tc::tma_load_3d(smem + L::kQ + h * kRegion, &tm_q, h * 64, pt.kvh * G, pt.tok0, &b->q_full);
+                dev::mbar_arrive_expect_tx(&b->q_full, (uint32_t)(ntiles_q * L::kHalves * 128 * G * TM));
+                for (int h = 0; h < ntiles_q; ++h)
+                    for (int x = 0; x < L::kHalves; ++x)
+                        tc::tma_load_3d(smem + L::kQ + h * L::kTile + x * kRegion, &tm_q, x * 64, pt.kvh * G,
+                                        pt.tok0 + h * TM, &b->q_full);
             }
             arm(0, uc & 1);
-            const int nkt = (pt.kv_end + kPreKeys - 1) / kPreKeys;
+            const int kv_end = pt.ntok1 > 0 ? pt.kv_end1 : pt.kv_end0;
+            const int nkt = (kv_end + kPreKeys - 1) / kPreKeys;
             for (int j = 0; j < nkt; ++j, ++it) {
                 const int st = it & 1;
                 const uint32_t ph = (it >> 1) & 1;
                 const int key0 = j * kPreKeys;
-                const int nkeys = min(kPreKeys, pt.kv_end - key0);
-                const int nfull = nkeys / rows_page;              // whole boxes of rows_page rows
-                const int npart = nkeys - nfull * rows_page;     // valid rows of a partial last page
+                const int nkeys = min(kPreKeys, kv_end - key0);
+                const int nfull = nkeys / rows_page;           // whole boxes of rows_page rows
+                const int npart = nkeys - nfull * rows_page;  // valid rows of a partial last page
                 // slots of this lane's boxes/rows (ops lane, lane+32, ...; at most 128 ops)
                 int64_t slot[4];
 #pragma unroll
@@ -171,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (op < nfull) key = key0 + op * rows_page;
                     else if (op < nfull + npart) key = key0 + nfull * rows_page + (op - nfull);
                     if (key >= 0) {
-                        int64_t page = prow[key / ps];
+                        int64_t page = prow[key >> p.page_shift];
                         if (page < 0 || page >= p.num_pages) {
                             dev::set_error(err, kErrPage);
                             page = 0;
@@ -197,8 +206,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (slot[i] < 0) continue;
                         const bool whole = op < nfull;
                         const int row = whole ? op * rows_page : nfull * rows_page + (op - nfull);
-                        for (int h = 0; h < L::kHalves; ++h)
-                            tc::tma_load_3d_hint(base + h * kRegion + row * 128, whole ? tm_page : tm_row, h * 64,
+                        for (int x = 0; x < L::kHalves; ++x)
+                            tc::tma_load_3d_hint(base + x * kRegion + row * 128, whole ? tm_page : tm_row, x * 64,
                                                  pt.kvh, (int)slot[i], full, pol_kv);
                     }
                 }
@@ -211,62 +220,94 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 5; ++i)
                 if (armed & (1u << i)) (void)dev::mbar_wait(bars_armed[i], (armed_par >> i) & 1u);
         }
-    } else if (warp == 1) {
+    } else if (warp == kMmaWarp) {
         // ============================================================== MMA issuer (one thread)
-        const uint32_t id_qk = tc::idesc_bf16_f32(128, 128, 0, 0);
-        const uint32_t id_pv = tc::idesc_bf16_f32(128, D, 0, 1);
-        const uint32_t sq = dev::smem_u32(smem + L::kQ);
-        const uint32_t sp = dev::smem_u32(smem + L::kP);
-        uint32_t it = 0;
-        int uc = 0;
-        bool ok = true;
-        auto pv = [&](uint32_t t, bool first_of_unit, int ucount) -> bool {
-            if (!wait_or_abort(&b->p_full, t & 1, b, err)) return false;
-            if (!wait_or_abort(&b->v_full[t & 1], (t >> 1) & 1, b, err)) return false;
-            if (first_of_unit && ucount > 0 && !wait_or_abort(&b->o_free, (ucount - 1) & 1, b, err)) return false;
-            tc::fence_after_sync();
-            const uint32_t sv = dev::smem_u32(smem + L::kV + (t & 1) * L::kTile);
-#pragma unroll
-            for (int kk = 0; kk < kPreKeys / 16; ++kk) {
-                const uint64_t ad = tc::smem_desc(sp + (kk >> 2) * kRegion + (kk & 3) * 32, 16, 1024, tc::kSwizzle128B);
-                const uint64_t bd = tc::smem_desc(sv + kk * 2048, kRegion, 1024, tc::kSwizzle128B);
-                tc::mma_ss(t_o, ad, bd, id_pv, (first_of_unit && kk == 0) ? 0u : 1u);
-            }
-            tc::mma_commit(&b->pv_done);
-            tc::mma_commit(&b->v_empty[t & 1]);
-            return true;
-        };
         if (lane == 0) {
-            for (int u = blockIdx.x; u < n_tiles && ok; u += gridDim.x, ++uc) {
-                const PreTile pt = tiles[u];
-                const int nkt = (pt.kv_end + kPreKeys - 1) / kPreKeys;
+            const uint32_t id_qk = tc::idesc_bf16_f32(128, 128, 0, 0);
+            const uint32_t id_pv = tc::idesc_bf16_f32(128, D, 0, 1);
+            uint32_t it = 0;                      // KV tiles across units
+            uint32_t n_p[2] = {0, 0};             // P tiles consumed per Q tile
+            uint32_t n_units_h[2] = {0, 0};       // units that had Q tile h
+            int uc = 0;
+            bool ok = true;
+            auto issue_s = [&](int h, int st) {
+                const uint32_t sq = dev::smem_u32(smem + L::kQ + h * L::kTile);
+                const uint32_t sk = dev::smem_u32(smem + L::kK + st * L::kTile);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t ad =
+                        tc::smem_desc(sq + (kk >> 2) * kRegion + (kk & 3) * 32, 16, 1024, tc::kSwizzle128B);
+                    const uint64_t bd =
+                        tc::smem_desc(sk + (kk >> 2) * kRegion + (kk & 3) * 32, 16, 1024, tc::kSwizzle128B);
+                    tc::mma_ss(tmem + 256 * h, ad, bd, id_qk, kk > 0 ? 1u : 0u);
+                }
+                tc::mma_commit(&b->s_full[h]);
+            };
+            // O_h += P_h V(st); P_h is read from TMEM (the first 64 columns of S_h)
+            auto issue_pv = [&](int h, int st, bool first) -> bool {
+                if (!wait_or_abort(&b->p_full[h], n_p[h] & 1, b, err)) return false;
+                ++n_p[h];
+                if (first && n_units_h[h] > 0 && !wait_or_abort(&b->o_free[h], (n_units_h[h] - 1) & 1, b, err))
+                    return false;
+                tc::fence_after_sync();
+                const uint32_t sv = dev::smem_u32(smem + L::kV + st * L::kTile);
+#pragma unroll
+                for (int kk = 0; kk < kPreKeys / 16; ++kk) {
+                    const uint64_t bd = tc::smem_desc(sv + kk * 2048, kRegion, 1024, tc::kSwizzle128B);
+                    tc::mma_ts(tmem + 256 * h + 128, tmem + 256 * h + kk * 8, bd, id_pv,
+                               (first && kk == 0) ? 0u : 1u);
+                }
+                return true;
+            };
+            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
+                const PreTile pt = units[u];
+                const int nkt0 = kv_tiles(pt.kv_end0, pt.ntok0);
+                const int nkt1 = kv_tiles(pt.kv_end1, pt.ntok1);
+                const int nkt = nkt1 > nkt0 ? nkt1 : nkt0;
                 if (!wait_or_abort(&b->q_full, uc & 1, b, err)) {
                     ok = false;
                     break;
                 }
+                // prologue: S_h(0) for both tiles
+                if (!wait_or_abort(&b->k_full[it & 1], (it >> 1) & 1, b, err)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                if (nkt0 > 0) issue_s(0, it & 1);
+                if (nkt1 > 0) issue_s(1, it & 1);
+                tc::mma_commit(&b->k_empty[it & 1]);
+                if (nkt == 1) tc::mma_commit(&b->q_empty);
                 for (int j = 0; j < nkt && ok; ++j) {
                     const uint32_t t = it + j;
-                    const int st = t & 1;
-                    if (!wait_or_abort(&b->k_full[st], (t >> 1) & 1, b, err)) {
+                    const int st = t & 1, st1 = (t + 1) & 1;
+                    if (!wait_or_abort(&b->v_full[st], (t >> 1) & 1, b, err)) {
+                        ok = false;
+                        break;
+                    }
+                    const bool next = j + 1 < nkt;
+                    if (next && !wait_or_abort(&b->k_full[st1], ((t + 1) >> 1) & 1, b, err)) {
                         ok = false;
                         break;
                     }
                     tc::fence_after_sync();
-                    const uint32_t sk = dev::smem_u32(smem + L::kK + st * L::kTile);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t ad =
-                            tc::smem_desc(sq + (kk >> 2) * kRegion + (kk & 3) * 32, 16, 1024, tc::kSwizzle128B);
-                        const uint64_t bd =
-                            tc::smem_desc(sk + (kk >> 2) * kRegion + (kk & 3) * 32, 16, 1024, tc::kSwizzle128B);
-                        tc::mma_ss(t_s[st], ad, bd, id_qk, kk > 0 ? 1u : 0u);
+                    for (int h = 0; h < 2 && ok; ++h) {
+                        const int nk = h ? nkt1 : nkt0;
+                        if (j >= nk) continue;
+                        ok = issue_pv(h, st, j == 0);
+                        if (!ok) break;
+                        if (j == nk - 1) tc::mma_commit(&b->o_ready[h]);
+                        if (j + 1 < nk) issue_s(h, st1);
                     }
-                    tc::mma_commit(&b->s_full[st]);
-                    tc::mma_commit(&b->k_empty[st]);
-                    if (j == nkt - 1) tc::mma_commit(&b->q_empty);
-                    if (j > 0) ok = pv(t - 1, j - 1 == 0, uc);
+                    if (!ok) break;
+                    tc::mma_commit(&b->v_empty[st]);
+                    if (next) {
+                        tc::mma_commit(&b->k_empty[st1]);
+                        if (j + 1 == nkt - 1) tc::mma_commit(&b->q_empty);
+                    }
                 }
-                if (ok) ok = pv(it + nkt - 1, nkt == 1, uc);
+                if (nkt0 > 0) ++n_units_h[0];
+                if (nkt1 > 0) ++n_units_h[1];
                 it += nkt;
             }
             // every MMA issued must complete before TMEM is released
@@ -276,141 +317,137 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ============================================================== softmax (one row per thread)
+        const int h = warp >> 2;  // Q tile of this warpgroup
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const uint32_t t_s = tmem + 256 * h + lane_base;
+        const uint32_t t_o = t_s + 128;
         const float sl = p.scale_log2;
-        uint32_t it = 0;
-        int uc = 0;
-        for (int u = blockIdx.x; u < n_tiles && !b->abort_flag; u += gridDim.x, ++uc) {
-            const PreTile pt = tiles[u];
-            const int nkt = (pt.kv_end + kPreKeys - 1) / kPreKeys;
-            const bool valid = row < pt.ntok * G;
-            const int limit = valid ? pt.qpos0 + row / G : -1;
+        uint32_t n_s = 0;   // S tiles seen by this warpgroup
+        uint32_t n_u = 0;   // units with this Q tile
+        for (int u = blockIdx.x; u < n_units && !b->abort_flag; u += gridDim.x) {
+            const PreTile pt = units[u];
+            const int ntok = h ? pt.ntok1 : pt.ntok0;
+            const int nk = kv_tiles(h ? pt.kv_end1 : pt.kv_end0, ntok);
+            if (nk == 0) continue;
+            const int qpos = pt.qpos0 + h * TM;
+            const bool valid = row < ntok * G;
+            const int limit = valid ? qpos + row / G : -1;
             float m = -INFINITY, l = 0.f;
             bool ok = true;
-            for (int j = 0; j < nkt; ++j) {
-                const uint32_t t = it + j;
-                const int st = t & 1;
-                if (!wait_or_abort(&b->s_full[st], (t >> 1) & 1, b, err)) {
+            for (int j = 0; j < nk; ++j, ++n_s) {
+                if (!wait_or_abort(&b->s_full[h], n_s & 1, b, err)) {
                     ok = false;
                     break;
                 }
                 tc::fence_after_sync();
-                float s[kPreKeys];
+                // the whole S row: four 32-column TMEM loads in flight, one wait
+                float s[kPreKeys / 32][32];
 #pragma unroll
-                for (int c = 0; c < kPreKeys / 32; ++c) {
-                    float v[32];
-                    tc::tmem_ld32(t_s[st] + lane_base + c * 32, v);
-                    tc::tmem_wait_ld();
+                for (int c = 0; c < kPreKeys / 32; ++c) tc::tmem_ld32_async(t_s + c * 32, s[c]);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) s[c * 32 + i] = v[i];
-                }
+                for (int c = 0; c < kPreKeys / 32; ++c) tc::tmem_wait_ld_regs(s[c]);
                 const int key0 = j * kPreKeys;
-                const bool need_mask = key0 + kPreKeys - 1 > pt.qpos0;
-                float mx = -INFINITY;
+                const bool need_mask = key0 + kPreKeys - 1 > qpos;
+                float mxa[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mxa[i] = -INFINITY;
 #pragma unroll
                 for (int c = 0; c < kPreKeys; ++c) {
-                    float x = s[c] * sl;
+                    float x = s[c >> 5][c & 31];
                     if (need_mask && key0 + c > limit) x = -INFINITY;
-                    s[c] = x;
-                    mx = fmaxf(mx, x);
+                    s[c >> 5][c & 31] = x;
+                    mxa[c & 7] = fmaxf(mxa[c & 7], x);
                 }
-                const float m_new = fmaxf(m, mx);
-                bool waited = false;
+                const float mx = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
+                                       fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
+                const float m_new = fmaxf(m, mx * sl);  // log2 units (sl = scale * log2 e > 0)
                 if (j == 0) {
                     m = m_new;
                 } else {
+                    // O_h is stable here: P_h(j-1) V was issued before S_h(j), whose
+                    // completion this thread has just observed
                     const bool resc = m_new > m + kRescaleThreshold;
                     if (__any_sync(0xffffffffu, resc)) {
-                        if (!wait_or_abort(&b->pv_done, (t - 1) & 1, b, err)) {
-                            ok = false;
-                            break;
-                        }
-                        waited = true;
-                        tc::fence_after_sync();
                         const float alpha = resc ? dev::fast_exp2(m - m_new) : 1.f;
 #pragma unroll
                         for (int c = 0; c < D / 32; ++c) {
                             float v[32];
-                            tc::tmem_ld32(t_o + lane_base + c * 32, v);
-                            tc::tmem_wait_ld();
+                            tc::tmem_ld32_async(t_o + c * 32, v);
+                            tc::tmem_wait_ld_regs(v);
 #pragma unroll
                             for (int i = 0; i < 32; ++i) v[i] *= alpha;
-                            tc::tmem_st32(t_o + lane_base + c * 32, v);
+                            tc::tmem_st32(t_o + c * 32, v);
                         }
-                        tc::tmem_wait_st();
                         if (resc) {
                             l *= alpha;
                             m = m_new;
                         }
                     }
                 }
-                const float mu = m == -INFINITY ? 0.f : m;
-                float ls = 0.f;
+                const float nmu = m == -INFINITY ? 0.f : -m;
+                float lsa[8];
 #pragma unroll
-                for (int c = 0; c < kPreKeys; ++c) {
-                    s[c] = dev::fast_exp2(s[c] - mu);
-                    ls += s[c];
-                }
-                l += ls;
-                if (j > 0 && !waited) {
-                    if (!wait_or_abort(&b->pv_done, (t - 1) & 1, b, err)) {
-                        ok = false;
-                        break;
+                for (int i = 0; i < 8; ++i) lsa[i] = 0.f;
+                // P = exp2(s * sl - m) as packed bf16 pairs, 32 columns (64 keys) per TMEM store
+#pragma unroll
+                for (int c2 = 0; c2 < kPreKeys / 64; ++c2) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int c = c2 * 64 + 2 * i;
+                        const float e0 = dev::fast_exp2(fmaf(s[c >> 5][c & 31], sl, nmu));
+                        const float e1 = dev::fast_exp2(fmaf(s[(c + 1) >> 5][(c + 1) & 31], sl, nmu));
+                        lsa[i & 7] += e0 + e1;
+                        pk[i] = dev::pack_bf16x2(e0, e1);
                     }
+                    tc::tmem_st32u(t_s + c2 * 32, pk);
                 }
-                // P row -> shared memory, bf16, 128-byte swizzle (A operand of P V, K-major)
-                uint8_t* prow_s = smem + L::kP;
-#pragma unroll
-                for (int c16 = 0; c16 < kPreKeys / 8; ++c16) {
-                    uint4 w;
-                    w.x = dev::pack_bf16x2(s[c16 * 8 + 0], s[c16 * 8 + 1]);
-                    w.y = dev::pack_bf16x2(s[c16 * 8 + 2], s[c16 * 8 + 3]);
-                    w.z = dev::pack_bf16x2(s[c16 * 8 + 4], s[c16 * 8 + 5]);
-                    w.w = dev::pack_bf16x2(s[c16 * 8 + 6], s[c16 * 8 + 7]);
-                    *reinterpret_cast<uint4*>(prow_s + (c16 >> 3) * kRegion + sw128(row, c16 & 7)) = w;
-                }
-                tc::fence_proxy_async_smem();
+                l += ((lsa[0] + lsa[1]) + (lsa[2] + lsa[3])) + ((lsa[4] + lsa[5]) + (lsa[6] + lsa[7]));
+                tc::tmem_wait_st();
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) dev::mbar_arrive(&b->p_full);
+                if (lane == 0) dev::mbar_arrive(&b->p_full[h]);
             }
             if (!ok) break;
             // ---- epilogue: O / l -> bf16 rows of out, LSE
-            const uint32_t t_last = it + nkt - 1;
-            if (!wait_or_abort(&b->pv_done, t_last & 1, b, err)) break;
+            if (!wait_or_abort(&b->o_ready[h], n_u & 1, b, err)) break;
             tc::fence_after_sync();
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            const int64_t orow = valid ? ((int64_t)(pt.tok0 + row / G) * Hq + pt.kvh * G + row % G) : 0;
+            const int64_t orow =
+                valid ? ((int64_t)(pt.tok0 + h * TM + row / G) * Hq + pt.kvh * G + row % G) : 0;
+            float o[D / 32][32];
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                float v[32];
-                tc::tmem_ld32(t_o + lane_base + c * 32, v);
-                tc::tmem_wait_ld();
-                if (valid) {
+            for (int c = 0; c < D / 32; ++c) tc::tmem_ld32_async(t_o + c * 32, o[c]);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) tc::tmem_wait_ld_regs(o[c]);
+            // O is in registers: the accumulator may be overwritten by the next unit
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) dev::mbar_arrive(&b->o_free[h]);
+            ++n_u;
+            if (valid) {
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
                     uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D + c * 32);
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
                         uint4 w;
-                        w.x = dev::pack_bf16x2(v[q4 * 8 + 0] * inv, v[q4 * 8 + 1] * inv);
-                        w.y = dev::pack_bf16x2(v[q4 * 8 + 2] * inv, v[q4 * 8 + 3] * inv);
-                        w.z = dev::pack_bf16x2(v[q4 * 8 + 4] * inv, v[q4 * 8 + 5] * inv);
-                        w.w = dev::pack_bf16x2(v[q4 * 8 + 6] * inv, v[q4 * 8 + 7] * inv);
+                        w.x = dev::pack_bf16x2(o[c][q4 * 8 + 0] * inv, o[c][q4 * 8 + 1] * inv);
+                        w.y = dev::pack_bf16x2(o[c][q4 * 8 + 2] * inv, o[c][q4 * 8 + 3] * inv);
+                        w.z = dev::pack_bf16x2(o[c][q4 * 8 + 4] * inv, o[c][q4 * 8 + 5] * inv);
+                        w.w = dev::pack_bf16x2(o[c][q4 * 8 + 6] * inv, o[c][q4 * 8 + 7] * inv);
                         dst[q4] = w;
                     }
                 }
+                if (p.lse != nullptr) p.lse[orow] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
             }
-            if (valid && p.lse != nullptr) p.lse[orow] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) dev::mbar_arrive(&b->o_free);
-            it += nkt;
         }
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
     }
@@ -462,7 +499,7 @@ cudaError_t launch_p(const ForwardParams& p, int ctas, cudaStream_t s) {
         !make_map(&tkr, p.k_pool, D, p.num_kv_heads, (uint64_t)p.num_slots, 1, 1) ||
         !make_map(&tvr, p.v_pool, D, p.num_kv_heads, (uint64_t)p.num_slots, 1, 1))
         return cudaErrorInvalidValue;
-    const size_t smem = Layout2<D>::kBytes + 1024;
+    const size_t smem = SmemMap<D>::kBytes + 1024;
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     prefill_kernel<D><<<ctas, kThreads, smem, s>>>(p, tq, tkp, tvp, tkr, tvr, rows_page);

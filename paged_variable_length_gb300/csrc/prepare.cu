@@ -26,6 +26,7 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
+constexpr int kBuckets = 256;  // cost classes for the longest-first ordering of work items
 
 // Exclusive scan of N counters across the block; each thread contributes v[k].
 template <int N>
@@ -80,6 +81,8 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     __shared__ unsigned long long s_work;
     __shared__ int s_tmp3[kWarps][3];
     __shared__ int s_tmp2[kWarps][2];
+    __shared__ int s_hist_u[kBuckets];
+    __shared__ int s_hist_t[kBuckets];
     const int tid = threadIdx.x;
     if (tid == 0) {
         s_err = 0;
@@ -108,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         if (L > p.max_kv_len || n > p.max_q_len) err |= kErrLimits;
         if (n <= 0 || n > L || L > p.max_kv_len || n > p.max_q_len) continue;
         if (p.use_prefill && n > TB) {
-            cnt[1] += (int)((n + TM - 1) / TM) * Hkv;
+            cnt[1] += (int)((((n + TM - 1) / TM) + 1) / 2) * Hkv;  // units of two Q tiles
         } else {
             const int ng = (n + TB - 1) / TB;
             cnt[0] += ng;
@@ -157,66 +160,106 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     __syncthreads();
     const bool run = (s_err & kErrFatal) == 0;
 
-    // ---- pass 3: write groups, units, tiles
-    if (run) {
-        int gi = cnt[0], ti = cnt[1], ui = cnt2[0], pi = cnt2[1];
-        for (int i = r0; i < r1; ++i) {
-            const int c0 = p.cu[i], n = p.cu[i + 1] - c0, L = p.seqlens[i];
-            if (n <= 0) continue;
-            if (p.use_prefill && n > TB) {
-                const int nt = (n + TM - 1) / TM;
-                for (int t = nt - 1; t >= 0; --t) {  // costliest (latest) tile first
-                    const int a0 = t * TM, na = min(TM, n - a0);
-                    for (int h = 0; h < Hkv; ++h) {
-                        PreTile pt;
-                        pt.req = i;
-                        pt.kvh = h;
-                        pt.tok0 = c0 + a0;
-                        pt.ntok = na;
-                        pt.qpos0 = L - n + a0;
-                        pt.kv_end = L - n + a0 + na;
-                        pt.pad0 = pt.pad1 = 0;
-                        tiles[ti++] = pt;
+    // ---- pass 3: write groups; units and tiles go out longest first (a counting sort on
+    // their cost), so that the kernels' in-order work fetch ends with the short items and
+    // the grid finishes together (longest-processing-time-first).  The position of a
+    // unit in the list never changes a result: each split writes its own partial slot and
+    // the merge walks the slots in split order.
+    for (int b = tid; b < kBuckets; b += kThreads) {
+        s_hist_u[b] = 0;
+        s_hist_t[b] = 0;
+    }
+    __syncthreads();
+    for (int emit = 0; emit < 2; ++emit) {
+        if (run) {
+            int gi = cnt[0], pi = cnt2[1];
+            for (int i = r0; i < r1; ++i) {
+                const int c0 = p.cu[i], n = p.cu[i + 1] - c0, L = p.seqlens[i];
+                if (n <= 0) continue;
+                if (p.use_prefill && n > TB) {
+                    const int nt = (n + TM - 1) / TM;
+                    for (int t = 0; t < nt; t += 2) {  // a unit: Q tiles t and t+1
+                        const int a0 = t * TM, na0 = min(TM, n - a0);
+                        const int na1 = t + 1 < nt ? min(TM, n - a0 - TM) : 0;
+                        const int kv_end0 = L - n + a0 + na0;
+                        const int kv_end1 = na1 > 0 ? kv_end0 + na1 : kv_end0;
+                        const int b = kBuckets - 1 - min(kBuckets - 1, (kv_end1 + kPreKeys - 1) / kPreKeys);
+                        for (int h = 0; h < Hkv; ++h) {
+                            if (!emit) {
+                                atomicAdd(&s_hist_t[b], 1);
+                                continue;
+                            }
+                            PreTile pt;
+                            pt.req = i;
+                            pt.kvh = h;
+                            pt.tok0 = c0 + a0;
+                            pt.ntok0 = na0;
+                            pt.ntok1 = na1;
+                            pt.qpos0 = L - n + a0;
+                            pt.kv_end0 = kv_end0;
+                            pt.kv_end1 = kv_end1;
+                            tiles[atomicAdd(&s_hist_t[b], 1)] = pt;
+                        }
                     }
+                    continue;
                 }
-                continue;
-            }
-            const int ng = (n + TB - 1) / TB;
-            for (int g = 0; g < ng; ++g) {
-                const int a0 = g * TB, na = min(TB, n - a0);
-                const int ext = L - n + a0 + na;
-                int per;
-                const int s = split_ranges(ext, chunk, &per);
-                DecGroup dg;
-                dg.req = i;
-                dg.tok0 = c0 + a0;
-                dg.ntok = na;
-                dg.qpos0 = L - n + a0;
-                dg.nsplit = s;
-                dg.pbase = s > 1 ? pi : -1;
-                dg.kv_end = ext;
-                dg.casc = -1;
-                groups[gi] = dg;
-                counters[gi] = 0;
-                for (int u = 0; u < s; ++u) {
-                    DecUnit du;
-                    du.group = gi;
-                    du.k0 = min(ext, u * per);
-                    du.k1 = min(ext, (u + 1) * per);
-                    du.split = u;
-                    du.req = i;
-                    du.tok0 = dg.tok0;
-                    du.ntok = dg.ntok;
-                    du.qpos0 = dg.qpos0;
-                    du.nsplit = dg.nsplit;
-                    du.pbase = dg.pbase;
-                    du.pad0 = du.pad1 = 0;
-                    units[ui++] = du;
+                const int ng = (n + TB - 1) / TB;
+                for (int g = 0; g < ng; ++g) {
+                    const int a0 = g * TB, na = min(TB, n - a0);
+                    const int ext = L - n + a0 + na;
+                    int per;
+                    const int s = split_ranges(ext, chunk, &per);
+                    DecGroup dg;
+                    dg.req = i;
+                    dg.tok0 = c0 + a0;
+                    dg.ntok = na;
+                    dg.qpos0 = L - n + a0;
+                    dg.nsplit = s;
+                    dg.pbase = s > 1 ? pi : -1;
+                    dg.kv_end = ext;
+                    dg.casc = -1;
+                    if (emit) {
+                        groups[gi] = dg;
+                        counters[gi] = 0;
+                    }
+                    for (int u = 0; u < s; ++u) {
+                        DecUnit du;
+                        du.group = gi;
+                        du.k0 = min(ext, u * per);
+                        du.k1 = min(ext, (u + 1) * per);
+                        const int b = kBuckets - 1 - min(kBuckets - 1, (du.k1 - du.k0 + kDecKeysPerStage - 1) /
+                                                                           kDecKeysPerStage);
+                        if (!emit) {
+                            atomicAdd(&s_hist_u[b], 1);
+                            continue;
+                        }
+                        du.split = u;
+                        du.req = i;
+                        du.tok0 = dg.tok0;
+                        du.ntok = dg.ntok;
+                        du.qpos0 = dg.qpos0;
+                        du.nsplit = dg.nsplit;
+                        du.pbase = dg.pbase;
+                        du.pad0 = du.pad1 = 0;
+                        units[atomicAdd(&s_hist_u[b], 1)] = du;
+                    }
+                    if (s > 1) pi += s;
+                    ++gi;
                 }
-                if (s > 1) pi += s;
-                ++gi;
             }
         }
+        __syncthreads();
+        if (!emit && tid == 0) {  // bucket counts -> first position of each bucket (bucket 0 = costliest)
+            int au = 0, at = 0;
+            for (int b = 0; b < kBuckets; ++b) {
+                const int cu_ = s_hist_u[b], ct = s_hist_t[b];
+                s_hist_u[b] = au;
+                s_hist_t[b] = at;
+                au += cu_;
+                at += ct;
+            }
+        }
+        __syncthreads();
     }
 
     // ---- derived slot mapping: the new tokens are each request's last q_len positions

@@ -78,16 +78,19 @@ struct DecUnit {
     int32_t pad0, pad1;
 };
 
-// One tile of the tensor-core prefill kernel: kPreRows rows = tokens x q heads of
-// one kv head, keys [0, kv_end) with the causal diagonal.
+// One work unit of the tensor-core prefill kernel: two consecutive Q tiles of one
+// request and kv head.  A Q tile is kPreRows rows = floor(kPreRows / G) tokens x the
+// G q heads; tile h covers tokens tok0 + h*TM ..; it sees keys [0, kv_end_h) with the
+// causal diagonal.  ntok1 == 0 when the request has no second tile here.
 struct PreTile {
     int32_t req;
     int32_t kvh;
-    int32_t tok0;        // global index of the first token of the tile
-    int32_t ntok;        // tokens in the tile
-    int32_t qpos0;       // absolute position of the first token
-    int32_t kv_end;      // keys [0, kv_end)
-    int32_t pad0, pad1;
+    int32_t tok0;        // global index of the first token of tile 0
+    int32_t ntok0;       // tokens in tile 0 (>= 1)
+    int32_t ntok1;       // tokens in tile 1 (0: absent)
+    int32_t qpos0;       // absolute position of the first token of tile 0
+    int32_t kv_end0;     // keys [0, kv_end0) for tile 0
+    int32_t kv_end1;     // keys [0, kv_end1) for tile 1
 };
 
 // Workspace carve-up (byte offsets from the workspace base); computed on the host.
