@@ -14,10 +14,9 @@
 //   * keys run in 128-key tiles up to each Q tile's causal end (later keys
 //     are never loaded or multiplied: causal tile skipping); only tiles that
 //     cross the diagonal get an elementwise mask;
-//   * warp 9 (producer) loads Q and K/V tiles with TMA from the paged pool:
-//     one 3-D box per page (rows of one kv head, 128-byte swizzle) plus
-//     single-row boxes for the valid rows of a partial last page, so no slot
-//     past kv_len is read; two K and two V stages;
+//   * warps 9-11 (producers) gather Q and K/V tiles row by row from the paged
+//     pool with 16-byte async copies into the 128-byte-swizzled layout of the
+//     MMA operands (rows past kv_len are not read); two K and two V stages;
 //   * warp 8 issues the MMAs from one thread, in the order
 //     PV0(j), S0(j+1), PV1(j), S1(j+1): while one softmax warpgroup works on
 //     its S tile the tensor core runs the other tile's products;
@@ -30,10 +29,7 @@
 // 64 columns) and O_h at 256h+128 .. 256h+255.
 // Every wait is bounded; a timeout sets PVA_DEVERR_TIMEOUT and the CTA winds
 // down (outstanding copies and MMAs waited for, TMEM freed) without trapping.
-#include <cuda.h>
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "device_utils.cuh"
 #include "pva_internal.h"
@@ -42,9 +38,22 @@
 namespace pva {
 namespace {
 
-constexpr int kThreads = 320;  // 8 softmax warps, MMA warp, producer warp
+// 12 warps = three warpgroups: softmax of Q tile 0 (warps 0-3), of Q tile 1 (4-7), and
+// the control group (warp 8: MMA issuer, warps 9-11: producers).  Registers move from
+// the control group to the softmax groups with setmaxnreg: launched at kRegsLaunch
+// each, the control warps drop to kRegsCtrl and the softmax warps rise to kRegsSoftmax
+// (8 x kRegsSoftmax + 4 x kRegsCtrl == 12 x kRegsLaunch, so the increase never waits
+// for registers that are not there).
+constexpr int kThreads = 384;
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsSoftmax = 208;
+constexpr int kRegsCtrl = 88;
+static_assert(8 * kRegsSoftmax + 4 * kRegsCtrl == 12 * kRegsLaunch, "register split must balance");
 constexpr int kMmaWarp = 8;
-constexpr int kProducerWarp = 9;
+constexpr int kProducerWarp0 = 9;
+constexpr int kProducerThreads = 96;
+// Readers of every work-queue entry: 3 producer warps, the MMA thread, 8 softmax warps.
+constexpr int kQueueReaders = 3 + 1 + 8;
 constexpr int kRegion = 128 * 128;  // one 128-row x 128-byte swizzled region (64 bf16 columns)
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -65,6 +74,8 @@ struct Bars {
     uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
     uint64_t s_full[2], p_full[2], o_ready[2], o_free[2];
     uint64_t drain;
+    uint64_t uq_full[4], uq_empty[4];  // work queue: unit indices fetched from the global counter
+    int32_t uq[4];
     uint32_t tmem_base;
     int32_t abort_flag;
 };
@@ -76,6 +87,35 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ba
     return false;
 }
 
+// Work queue.  Units are handed out dynamically, longest first (the plan lists them in
+// that order), one at a time: entry k is filled by one producer thread when the CTA
+// starts its unit k-1, so a CTA never holds more than one unit in reserve and the
+// grid finishes together.  Every role reads every entry; -1 ends the kernel.
+__device__ __forceinline__ void queue_push(Bars* b, int k, int32_t* counter, int n_units, uint32_t* err) {
+    if (k >= 4 && !dev::mbar_wait(&b->uq_empty[k & 3], ((k >> 2) & 1) ^ 1)) {
+        b->abort_flag = 1;
+        dev::set_error(err, kErrTimeout);
+    }
+    const int v = b->abort_flag ? n_units : atomicAdd(counter, 1);
+    b->uq[k & 3] = v < n_units ? v : -1;
+    dev::mbar_arrive(&b->uq_full[k & 3]);
+}
+
+// All lanes of the calling warp read entry k and lane 0 releases it (single: only the
+// calling thread reads, for a role that runs on one thread).
+__device__ __forceinline__ int queue_read(Bars* b, int k, int lane, uint32_t* err, bool single = false) {
+    int v = -1;
+    if (dev::mbar_wait(&b->uq_full[k & 3], (k >> 2) & 1)) {
+        v = b->uq[k & 3];
+    } else {
+        b->abort_flag = 1;
+        dev::set_error(err, kErrTimeout);
+    }
+    if (!single) __syncwarp();
+    if (single || lane == 0) dev::mbar_arrive(&b->uq_empty[k & 3]);
+    return v;
+}
+
 // Number of 128-key tiles Q tile h of a unit walks (0 when the tile is empty).
 __device__ __forceinline__ int kv_tiles(int kv_end, int ntok) {
     return ntok > 0 ? (kv_end + kPreKeys - 1) / kPreKeys : 0;
@@ -83,10 +123,7 @@ __device__ __forceinline__ int kv_tiles(int kv_end, int ntok) {
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_kernel(const ForwardParams p, const __grid_constant__ CUtensorMap tm_q,
-                   const __grid_constant__ CUtensorMap tm_k_page, const __grid_constant__ CUtensorMap tm_v_page,
-                   const __grid_constant__ CUtensorMap tm_k_row, const __grid_constant__ CUtensorMap tm_v_row,
-                   int rows_page) {
+    prefill_kernel(const ForwardParams p) {
     using L = SmemMap<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -97,6 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_units = hdr->n_pre_tiles;
     if ((hdr->error_bits & kErrFatal) || n_units == 0 || (int)blockIdx.x >= n_units) return;
     const PreTile* units = reinterpret_cast<const PreTile*>(p.ws + p.lay.pre_tiles);
+    int32_t* counter = &hdr->pad[1];  // zeroed by the store kernel of this forward
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.group, Hq = p.num_qo_heads;
@@ -106,12 +144,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<int4*>(smem + i) = make_int4(0, 0, 0, 0);
     tc::fence_proxy_async_smem();
     if (threadIdx.x == 0) {
-        dev::mbar_init(&b->q_full, 1);
+        dev::mbar_init(&b->q_full, kProducerThreads / 32);
         dev::mbar_init(&b->q_empty, 1);
         for (int s = 0; s < 2; ++s) {
-            dev::mbar_init(&b->k_full[s], 1);
+            dev::mbar_init(&b->k_full[s], kProducerThreads / 32);
             dev::mbar_init(&b->k_empty[s], 1);
-            dev::mbar_init(&b->v_full[s], 1);
+            dev::mbar_init(&b->v_full[s], kProducerThreads / 32);
             dev::mbar_init(&b->v_empty[s], 1);
             dev::mbar_init(&b->s_full[s], 1);
             dev::mbar_init(&b->p_full[s], 4);
@@ -119,6 +157,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             dev::mbar_init(&b->o_free[s], 4);
         }
         dev::mbar_init(&b->drain, 1);
+        for (int s = 0; s < 4; ++s) {
+            dev::mbar_init(&b->uq_full[s], 1);
+            dev::mbar_init(&b->uq_empty[s], kQueueReaders);
+        }
         b->abort_flag = 0;
         dev::fence_barrier_init();
     }
@@ -131,95 +173,115 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after_sync();
     const uint32_t tmem = b->tmem_base;
 
-    if (warp == kProducerWarp) {
-        // ============================================================== producer (TMA)
-        if (lane == 0) {
-            tc::prefetch_tmap(&tm_q);
-            tc::prefetch_tmap(&tm_k_page);
-            tc::prefetch_tmap(&tm_v_page);
-        }
-        const uint64_t pol_kv = dev::policy_evict_last();  // K/V tiles are re-read by the request's other units
-        uint32_t it = 0;
-        int uc = 0;
-        // barriers this warp armed with copies, and the parity of the phase each last armed
-        uint32_t armed = 0, armed_par = 0;  // bit 0: q, bits 1-2: k stages, bits 3-4: v stages
-        auto arm = [&](int bit, uint32_t par) {
-            armed |= 1u << bit;
-            armed_par = (armed_par & ~(1u << bit)) | (par << bit);
+    if (warp >= 8) {
+        // control warpgroups: give registers to the softmax warpgroups
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtrl));
+    if (warp >= kProducerWarp0) {
+        // ============================================================== producer (cp.async gathers)
+        // Thread r of these warps moves rows r and r + 96 of every Q / K / V tile: a 256-byte row
+        // (one kv head of one slot, or one q head of one token) as 16-byte async copies
+        // into the 128-byte-swizzled layout the MMA descriptors expect.  A page of a
+        // few rows per kv head is too small a box for TMA to stream efficiently, and
+        // rows past kv_len are simply not copied.  Each tile is one commit group;
+        // a group is signalled (wait, proxy fence, arrive) once the next group has
+        // been issued, so two tiles are in flight.
+        const int r0 = threadIdx.x - kProducerWarp0 * 32;  // 0..95
+        const int ps_mask = p.page_size - 1;
+        uint64_t* pending[2] = {nullptr, nullptr};  // barriers of issued, not yet signalled groups
+        int npend = 0;
+        auto signal = [&](int keep) {  // signal all but the newest `keep` groups
+            if (npend <= keep) return;
+            if (keep == 0) asm volatile("cp.async.wait_group 0;" ::: "memory");
+            else asm volatile("cp.async.wait_group 1;" ::: "memory");
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            while (npend > keep) {
+                if (lane == 0) dev::mbar_arrive(pending[0]);
+                pending[0] = pending[1];
+                --npend;
+            }
         };
-        const int ps = p.page_size, ps_mask = p.page_size - 1;
-        for (int u = blockIdx.x; u < n_units && !b->abort_flag; u += gridDim.x, ++uc) {
+        auto issue = [&](uint64_t* full) {
+            asm volatile("cp.async.commit_group;" ::: "memory");
+            pending[npend++] = full;
+            signal(1);
+        };
+        // 256-byte row -> swizzled smem row r of a tile (two 64-column regions)
+        auto copy_row = [&](uint8_t* tile, int r, const uint16_t* src) {
+            const uint32_t d0 = dev::smem_u32(tile) + r * 128;
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c) {
+                const uint32_t dst = d0 + (c >> 3) * kRegion + ((((c & 7) ^ (r & 7)) & 7) << 4);
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + c * 8) : "memory");
+            }
+        };
+        uint32_t it = 0;
+        const bool fetcher = warp == kProducerWarp0 && lane == 0;
+        if (fetcher) queue_push(b, 0, counter, n_units, err);
+        for (int uc = 0;; ++uc) {
+            const int u = queue_read(b, uc, lane, err);
+            if (u < 0 || b->abort_flag) break;
+            if (fetcher) queue_push(b, uc + 1, counter, n_units, err);
             const PreTile pt = units[u];
             const int32_t* prow = p.page_table + (int64_t)pt.req * p.ld;
-            const int ntiles_q = pt.ntok1 > 0 ? 2 : 1;
+            // ---- Q: row r = token r / G, head r % G of each tile
             if (uc > 0 && !wait_or_abort(&b->q_empty, (uc - 1) & 1, b, err)) break;
-            if (lane == 0) {
-                dev::mbar_arrive_expect_tx(&b->q_full, (uint32_t)(ntiles_q * L::kHalves * 128 * G * TM));
-                for (int h = 0; h < ntiles_q; ++h)
-                    for (int x = 0; x < L::kHalves; ++x)
-                        tc::tma_load_3d(smem + L::kQ + h * L::kTile + x * kRegion, &tm_q, x * 64, pt.kvh * G,
-                                        pt.tok0 + h * TM, &b->q_full);
+            for (int h = 0; h < 2; ++h) {
+                const int ntok = h ? pt.ntok1 : pt.ntok0;
+                for (int r = r0; r < kPreRows; r += kProducerThreads) {
+                    const int t = r / G;
+                    if (t < ntok) {
+                        const uint16_t* src =
+                            p.q + ((int64_t)(pt.tok0 + h * TM + t) * Hq + pt.kvh * G + (r - t * G)) * D;
+                        copy_row(smem + L::kQ + h * L::kTile, r, src);
+                    }
+                }
             }
-            arm(0, uc & 1);
+            issue(&b->q_full);
+            // ---- K and V tiles
             const int kv_end = pt.ntok1 > 0 ? pt.kv_end1 : pt.kv_end0;
             const int nkt = (kv_end + kPreKeys - 1) / kPreKeys;
-            for (int j = 0; j < nkt; ++j, ++it) {
+            bool ok = true;
+            for (int j = 0; j < nkt && ok; ++j, ++it) {
                 const int st = it & 1;
                 const uint32_t ph = (it >> 1) & 1;
-                const int key0 = j * kPreKeys;
-                const int nkeys = min(kPreKeys, kv_end - key0);
-                const int nfull = nkeys / rows_page;           // whole boxes of rows_page rows
-                const int npart = nkeys - nfull * rows_page;  // valid rows of a partial last page
-                // slots of this lane's boxes/rows (ops lane, lane+32, ...; at most 128 ops)
-                int64_t slot[4];
+                // element offsets of this thread's (at most two) rows; -1: past kv_len
+                int64_t off[2] = {-1, -1};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int op = lane + 32 * i;
-                    slot[i] = -1;
-                    int key = -1;
-                    if (op < nfull) key = key0 + op * rows_page;
-                    else if (op < nfull + npart) key = key0 + nfull * rows_page + (op - nfull);
-                    if (key >= 0) {
+                for (int i = 0; i < 2; ++i) {
+                    const int r = r0 + i * kProducerThreads;
+                    const int key = j * kPreKeys + r;
+                    if (r < kPreRows && key < kv_end) {
                         int64_t page = prow[key >> p.page_shift];
                         if (page < 0 || page >= p.num_pages) {
                             dev::set_error(err, kErrPage);
                             page = 0;
                         }
-                        slot[i] = page * ps + (key & ps_mask);
+                        off[i] = (((page << p.page_shift) + (key & ps_mask)) * p.num_kv_heads + pt.kvh) * D;
                     }
                 }
-                const uint32_t bytes = (uint32_t)(nkeys * 128 * L::kHalves);
-#pragma unroll
-                for (int kv = 0; kv < 2; ++kv) {
-                    uint64_t* full = kv ? &b->v_full[st] : &b->k_full[st];
-                    uint64_t* empty = kv ? &b->v_empty[st] : &b->k_empty[st];
-                    const CUtensorMap* tm_page = kv ? &tm_v_page : &tm_k_page;
-                    const CUtensorMap* tm_row = kv ? &tm_v_row : &tm_k_row;
-                    uint8_t* base = smem + (kv ? L::kV : L::kK) + st * L::kTile;
-                    if (!wait_or_abort(empty, ph ^ 1, b, err)) goto producer_out;
-                    if (lane == 0) dev::mbar_arrive_expect_tx(full, bytes);
-                    __syncwarp();
-                    arm(kv ? 3 + st : 1 + st, ph);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int op = lane + 32 * i;
-                        if (slot[i] < 0) continue;
-                        const bool whole = op < nfull;
-                        const int row = whole ? op * rows_page : nfull * rows_page + (op - nfull);
-                        for (int x = 0; x < L::kHalves; ++x)
-                            tc::tma_load_3d_hint(base + x * kRegion + row * 128, whole ? tm_page : tm_row, x * 64,
-                                                 pt.kvh, (int)slot[i], full, pol_kv);
-                    }
+                if (!wait_or_abort(&b->k_empty[st], ph ^ 1, b, err)) {
+                    ok = false;
+                    break;
                 }
+#pragma unroll
+                for (int i = 0; i < 2; ++i)
+                    if (off[i] >= 0) copy_row(smem + L::kK + st * L::kTile, r0 + i * kProducerThreads, p.k_pool + off[i]);
+                issue(&b->k_full[st]);
+                if (!wait_or_abort(&b->v_empty[st], ph ^ 1, b, err)) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll
+                for (int i = 0; i < 2; ++i)
+                    if (off[i] >= 0) copy_row(smem + L::kV + st * L::kTile, r0 + i * kProducerThreads, p.v_pool + off[i]);
+                issue(&b->v_full[st]);
             }
+            signal(0);  // the unit's last tile must not wait for the next unit's first group
+            if (!ok) break;
         }
-    producer_out:
         // copies still in flight must land before the CTA may leave
-        if (b->abort_flag) {
-            uint64_t* bars_armed[5] = {&b->q_full, &b->k_full[0], &b->k_full[1], &b->v_full[0], &b->v_full[1]};
-            for (int i = 0; i < 5; ++i)
-                if (armed & (1u << i)) (void)dev::mbar_wait(bars_armed[i], (armed_par >> i) & 1u);
-        }
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
     } else if (warp == kMmaWarp) {
         // ============================================================== MMA issuer (one thread)
         if (lane == 0) {
@@ -259,7 +321,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 return true;
             };
-            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
+            for (uc = 0; ok; ++uc) {
+                const int u = queue_read(b, uc, lane, err, true);
+                if (u < 0) break;
                 const PreTile pt = units[u];
                 const int nkt0 = kv_tiles(pt.kv_end0, pt.ntok0);
                 const int nkt1 = kv_tiles(pt.kv_end1, pt.ntok1);
@@ -315,7 +379,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             (void)dev::mbar_wait(&b->drain, 0);
         }
         __syncwarp();
+    }  // warps 10-11: idle
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
         // ============================================================== softmax (one row per thread)
         const int h = warp >> 2;  // Q tile of this warpgroup
         const int quarter = warp & 3;
@@ -326,7 +392,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sl = p.scale_log2;
         uint32_t n_s = 0;   // S tiles seen by this warpgroup
         uint32_t n_u = 0;   // units with this Q tile
-        for (int u = blockIdx.x; u < n_units && !b->abort_flag; u += gridDim.x) {
+        for (int k = 0;; ++k) {
+            const int u = queue_read(b, k, lane, err);
+            if (u < 0 || b->abort_flag) break;
             const PreTile pt = units[u];
             const int ntok = h ? pt.ntok1 : pt.ntok0;
             const int nk = kv_tiles(h ? pt.kv_end1 : pt.kv_end0, ntok);
@@ -353,12 +421,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float mxa[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) mxa[i] = -INFINITY;
+                if (need_mask) {  // a tile crossing the diagonal (or the end of the keys)
 #pragma unroll
-                for (int c = 0; c < kPreKeys; ++c) {
-                    float x = s[c >> 5][c & 31];
-                    if (need_mask && key0 + c > limit) x = -INFINITY;
-                    s[c >> 5][c & 31] = x;
-                    mxa[c & 7] = fmaxf(mxa[c & 7], x);
+                    for (int c = 0; c < kPreKeys; ++c) {
+                        float x = s[c >> 5][c & 31];
+                        if (key0 + c > limit) x = -INFINITY;
+                        s[c >> 5][c & 31] = x;
+                        mxa[c & 7] = fmaxf(mxa[c & 7], x);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kPreKeys; ++c) mxa[c & 7] = fmaxf(mxa[c & 7], s[c >> 5][c & 31]);
                 }
                 const float mx = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
                                        fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
@@ -453,56 +526,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// ---------------------------------------------------------------- host side: tensor maps
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(f);
-    });
-    return fn;
-}
-
-// 3-D bf16 map over [outer][mid][D] with a box of {64, box_mid, box_outer} and 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t D, uint64_t mid, uint64_t outer, uint32_t box_mid,
-              uint32_t box_outer) {
-    EncodeTiledFn fn = encode_fn();
-    if (fn == nullptr) return false;
-    cuuint64_t dims[3] = {D, mid, outer};
-    cuuint64_t strides[2] = {D * 2, mid * D * 2};
-    cuuint32_t box[3] = {64, box_mid, box_outer};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D>
 cudaError_t launch_p(const ForwardParams& p, int ctas, cudaStream_t s) {
-    const int G = p.group;
-    const int TM = kPreRows / G;
-    const int rows_page = p.page_size < kPreKeys ? p.page_size : kPreKeys;
-    CUtensorMap tq, tkp, tvp, tkr, tvr;
-    if (!make_map(&tq, p.q, D, p.num_qo_heads, (uint64_t)p.total_tokens, (uint32_t)G, (uint32_t)TM) ||
-        !make_map(&tkp, p.k_pool, D, p.num_kv_heads, (uint64_t)p.num_slots, 1, (uint32_t)rows_page) ||
-        !make_map(&tvp, p.v_pool, D, p.num_kv_heads, (uint64_t)p.num_slots, 1, (uint32_t)rows_page) ||
-        !make_map(&tkr, p.k_pool, D, p.num_kv_heads, (uint64_t)p.num_slots, 1, 1) ||
-        !make_map(&tvr, p.v_pool, D, p.num_kv_heads, (uint64_t)p.num_slots, 1, 1))
-        return cudaErrorInvalidValue;
     const size_t smem = SmemMap<D>::kBytes + 1024;
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    prefill_kernel<D><<<ctas, kThreads, smem, s>>>(p, tq, tkp, tvp, tkr, tvr, rows_page);
+    // The register split inside the kernel assumes the launch allocates exactly
+    // kRegsLaunch registers per thread; with fewer, the softmax warps' increase
+    // could not be satisfied.  Refuse to launch rather than risk that.
+    static int launch_regs = -1;
+    if (launch_regs < 0) {
+        cudaFuncAttributes attr{};
+        e = cudaFuncGetAttributes(&attr, prefill_kernel<D>);
+        if (e != cudaSuccess) return e;
+        launch_regs = attr.numRegs;
+    }
+    if (launch_regs != kRegsLaunch) return cudaErrorInvalidConfiguration;
+    prefill_kernel<D><<<ctas, kThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 
@@ -511,7 +551,7 @@ cudaError_t launch_p(const ForwardParams& p, int ctas, cudaStream_t s) {
 bool prefill_supported(int num_qo_heads, int num_kv_heads, int head_dim) {
     if (head_dim != 64 && head_dim != 128) return false;
     const int G = num_qo_heads / num_kv_heads;
-    return G >= 1 && G <= 16 && encode_fn() != nullptr;
+    return G >= 1 && G <= 16;
 }
 
 cudaError_t launch_prefill(const ForwardParams& p, int head_dim, int ctas, cudaStream_t s) {

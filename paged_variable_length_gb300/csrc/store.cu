@@ -20,8 +20,11 @@ constexpr int kThreads = 256;
 
 __global__ void __launch_bounds__(kThreads) store_kernel(ForwardParams p, int row_vecs) {
     PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws + p.lay.header);
-    // the decode kernel that follows fetches work from this counter
-    if (blockIdx.x == 0 && threadIdx.x == 0) hdr->pad[0] = 0;
+    // the attention kernels that follow fetch their work from these counters
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        hdr->pad[0] = 0;  // decode kernel work counter
+        hdr->pad[1] = 0;  // prefill kernel work counter
+    }
     if (hdr->error_bits & kErrFatal) return;
     const int lane = threadIdx.x & 31;
     const int64_t job = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);  // (token, K|V)
