@@ -144,12 +144,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<int4*>(smem + i) = make_int4(0, 0, 0, 0);
     tc::fence_proxy_async_smem();
     if (threadIdx.x == 0) {
-        dev::mbar_init(&b->q_full, kProducerThreads / 32);
+        dev::mbar_init(&b->q_full, kProducerThreads);
         dev::mbar_init(&b->q_empty, 1);
         for (int s = 0; s < 2; ++s) {
-            dev::mbar_init(&b->k_full[s], kProducerThreads / 32);
+            dev::mbar_init(&b->k_full[s], kProducerThreads);
             dev::mbar_init(&b->k_empty[s], 1);
-            dev::mbar_init(&b->v_full[s], kProducerThreads / 32);
+            dev::mbar_init(&b->v_full[s], kProducerThreads);
             dev::mbar_init(&b->v_empty[s], 1);
             dev::mbar_init(&b->s_full[s], 1);
             dev::mbar_init(&b->p_full[s], 4);
@@ -182,29 +182,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (one kv head of one slot, or one q head of one token) as 16-byte async copies
         // into the 128-byte-swizzled layout the MMA descriptors expect.  A page of a
         // few rows per kv head is too small a box for TMA to stream efficiently, and
-        // rows past kv_len are simply not copied.  Each tile is one commit group;
-        // a group is signalled (wait, proxy fence, arrive) once the next group has
-        // been issued, so two tiles are in flight.
+        // rows past kv_len are simply not copied.  The MMA thread orders these
+        // generic-proxy writes before its tensor-core reads with a proxy fence after
+        // it has waited on the tile's barrier.
         const int r0 = threadIdx.x - kProducerWarp0 * 32;  // 0..95
         const int ps_mask = p.page_size - 1;
-        uint64_t* pending[2] = {nullptr, nullptr};  // barriers of issued, not yet signalled groups
-        int npend = 0;
-        auto signal = [&](int keep) {  // signal all but the newest `keep` groups
-            if (npend <= keep) return;
-            if (keep == 0) asm volatile("cp.async.wait_group 0;" ::: "memory");
-            else asm volatile("cp.async.wait_group 1;" ::: "memory");
-            tc::fence_proxy_async_smem();
-            __syncwarp();
-            while (npend > keep) {
-                if (lane == 0) dev::mbar_arrive(pending[0]);
-                pending[0] = pending[1];
-                --npend;
-            }
-        };
+        // every producer thread arrives on a tile's barrier when its own copies of that
+        // tile have landed (hardware-tracked: the producer never waits for its loads)
         auto issue = [&](uint64_t* full) {
-            asm volatile("cp.async.commit_group;" ::: "memory");
-            pending[npend++] = full;
-            signal(1);
+            asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(dev::smem_u32(full))
+                         : "memory");
         };
         // 256-byte row -> swizzled smem row r of a tile (two 64-column regions)
         auto copy_row = [&](uint8_t* tile, int r, const uint16_t* src) {
@@ -277,7 +264,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (off[i] >= 0) copy_row(smem + L::kV + st * L::kTile, r0 + i * kProducerThreads, p.v_pool + off[i]);
                 issue(&b->v_full[st]);
             }
-            signal(0);  // the unit's last tile must not wait for the next unit's first group
             if (!ok) break;
         }
         // copies still in flight must land before the CTA may leave
@@ -338,6 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc::fence_after_sync();
+                tc::fence_proxy_async_smem();  // the producers' generic-proxy copies -> MMA operand reads
                 if (nkt0 > 0) issue_s(0, it & 1);
                 if (nkt1 > 0) issue_s(1, it & 1);
                 tc::mma_commit(&b->k_empty[it & 1]);
@@ -355,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc::fence_after_sync();
+                    tc::fence_proxy_async_smem();
                     for (int h = 0; h < 2 && ok; ++h) {
                         const int nk = h ? nkt1 : nkt0;
                         if (j >= nk) continue;
