@@ -20,6 +20,10 @@ int device_sm_count() {
 
 bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 
+// Batches up to this size keep their per-request arrays in the prepare kernel's shared
+// memory; shared-prefix detection needs it.
+constexpr int kPrepareSmemBatch = 4096;
+
 // Host-side validation of the static configuration.
 pva_status check_config(const pva_config* c) {
     if (c == nullptr) return PVA_ERR_INVALID_ARG;
@@ -44,6 +48,15 @@ Layout make_layout(const pva_config* c, int sm_count) {
     L.max_dec_units = L.max_dec_groups + L.target_units + 1;
     L.max_partial = 2 * L.target_units + 2;
     L.max_pre_tiles = (int32_t)((c->max_tokens / TM + c->max_batch + 1) * (int64_t)c->num_kv_heads);
+    L.max_casc_groups = c->enable_cascade ? c->max_batch / 2 + 1 : 1;
+    L.casc_target = sm_count;
+    if (c->enable_cascade) {
+        // every member of a group takes one partial slot per prefix chunk; the prefix pass
+        // has at most (member tiles / 2 + groups) x kv heads x chunks units
+        L.max_partial += c->max_batch * kMaxCascChunks;
+        L.max_pre_tiles += (int32_t)((c->max_batch / (2 * TM) + L.max_casc_groups + 1) * (int64_t)c->num_kv_heads *
+                                     kMaxCascChunks);
+    }
     L.rows_per_slot = kDecRows * c->num_kv_heads;
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -59,7 +72,9 @@ Layout make_layout(const pva_config* c, int sm_count) {
     L.counters = take(sizeof(uint32_t) * (size_t)L.max_dec_groups);
     L.partial_o = take(sizeof(float) * (size_t)L.max_partial * L.rows_per_slot * c->head_dim);
     L.partial_lse = take(sizeof(float) * (size_t)L.max_partial * L.rows_per_slot);
-    L.req_scratch = take(sizeof(int32_t) * 4 * (size_t)c->max_batch);
+    L.req_scratch = take(sizeof(int32_t) * 4 * (size_t)(c->max_batch + 1));
+    L.casc_groups = take(sizeof(CascGroup) * (size_t)L.max_casc_groups);
+    L.casc_members = take(sizeof(int32_t) * (size_t)c->max_batch);
     L.total = off;
     return L;
 }
@@ -160,13 +175,17 @@ pva_status attn_prepare_metadata(const pva_config* cfg, const int32_t* cu_seqlen
     h.total_tokens = total_tokens;
     h.max_q_len = mq;
     h.sm_count = sms;
-    // requests with more than TB new tokens run on the tensor-core prefill kernel
-    h.use_prefill = (mq > TB && prefill_supported(cfg->num_qo_heads, cfg->num_kv_heads, cfg->head_dim)) ? 1 : 0;
+    // requests with more than TB new tokens run on the tensor-core prefill kernel, which
+    // also runs the prefix pass of shared-prefix groups
+    const bool tc_ok = prefill_supported(cfg->num_qo_heads, cfg->num_kv_heads, cfg->head_dim);
+    h.use_prefill = (mq > TB && tc_ok) ? 1 : 0;
+    h.use_cascade = (cfg->enable_cascade && tc_ok && batch >= 2 && batch <= kPrepareSmemBatch) ? 1 : 0;
     h.dec_ctas = sms * decode_ctas_per_sm(cfg->num_kv_heads, cfg->head_dim);
     {
         const int64_t TM = kPreRows / G;
         const int64_t bound = ((int64_t)total_tokens / TM + batch + 1) * cfg->num_kv_heads;
         h.pre_ctas = h.use_prefill ? (int32_t)(bound < sms ? bound : sms) : 0;
+        if (h.use_cascade) h.pre_ctas = sms;
     }
     h.cu = cu_seqlens_q;
     h.seqlens = cache_seqlens;
@@ -177,7 +196,7 @@ pva_status attn_prepare_metadata(const pva_config* cfg, const int32_t* cu_seqlen
     h.stream = stream;
     h.lay = lay;
     h.n_events = 0;
-    h.kernels_per_forward = 2 + (h.use_prefill ? 1 : 0);  // store, [prefill], decode
+    h.kernels_per_forward = 2 + ((h.use_prefill || h.use_cascade) ? 1 : 0);  // store, [prefill], decode
 
     PrepareParams pp{};
     pp.cu = cu_seqlens_q;
@@ -197,6 +216,9 @@ pva_status attn_prepare_metadata(const pva_config* cfg, const int32_t* cu_seqlen
     pp.dec_tokens = kDecRows / G;
     pp.pre_tokens = kPreRows / G;
     pp.use_prefill = h.use_prefill;
+    pp.use_cascade = h.use_cascade;
+    pp.min_cascade_pages = h.cfg.min_cascade_pages;
+    pp.smem_batch = batch <= kPrepareSmemBatch ? batch : 0;
     pp.split_kv = cfg->enable_split_kv ? 1 : 0;
     pp.max_kv_len = cfg->max_kv_len;
     pp.max_tokens = cfg->max_tokens;
@@ -234,13 +256,20 @@ pva_status attn_forward(const pva_meta* meta, const void* q, const void* k, cons
     if (h->total_tokens == 0) return PVA_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     ForwardParams fp = forward_params(h, q, k, v, k_pool, v_pool, out, lse);
+    // inside a stream capture the events become graph nodes that still time the replay
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    if (h->n_events == 5 && cudaStreamIsCapturing(s, &capture) != cudaSuccess) return PVA_ERR_CUDA;
     auto mark = [&](int i) {
-        return h->n_events == 5 ? cudaEventRecord(static_cast<cudaEvent_t>(h->events[i]), s) : cudaSuccess;
+        if (h->n_events != 5) return cudaSuccess;
+        cudaEvent_t ev = static_cast<cudaEvent_t>(h->events[i]);
+        return capture == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal)
+                                                        : cudaEventRecord(ev, s);
     };
     if (mark(0) != cudaSuccess) return PVA_ERR_CUDA;
     if (launch_store(fp, h->cfg.head_dim, s) != cudaSuccess) return PVA_ERR_CUDA;
     if (mark(1) != cudaSuccess) return PVA_ERR_CUDA;
-    if (h->use_prefill && launch_prefill(fp, h->cfg.head_dim, h->pre_ctas, s) != cudaSuccess) return PVA_ERR_CUDA;
+    if ((h->use_prefill || h->use_cascade) && launch_prefill(fp, h->cfg.head_dim, h->pre_ctas, s) != cudaSuccess)
+        return PVA_ERR_CUDA;
     if (mark(2) != cudaSuccess || mark(3) != cudaSuccess) return PVA_ERR_CUDA;
     if (launch_decode(fp, h->cfg.head_dim, h->dec_ctas, s) != cudaSuccess) return PVA_ERR_CUDA;
     if (mark(4) != cudaSuccess) return PVA_ERR_CUDA;

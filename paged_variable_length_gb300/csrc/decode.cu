@@ -27,7 +27,10 @@
 //     free so the kernel stays bound by HBM, not by issue slots;
 //   * split groups write fp32 partial (O, LSE) to the workspace; the CTA that
 //     finishes a group's last split (atomic arrival count, no waiting) merges
-//     them: lse = log sum_s exp(lse_s), o = sum_s exp(lse_s - lse) o_s.
+//     them: lse = log sum_s exp(lse_s), o = sum_s exp(lse_s - lse) o_s.  For a
+//     member of a shared-prefix group the units cover only the keys after the
+//     prefix, and the merge also takes the prefix-pass partials that the
+//     tensor-core kernel (launched before this one on the same stream) wrote.
 // Every wait is bounded (PVA_DEVERR_TIMEOUT, then the CTA drains its copies
 // and leaves); nothing traps.
 #include <cuda_runtime.h>
@@ -49,6 +52,7 @@ struct StageInfo {
     int32_t unit, group, k, k1;
     int32_t tok0, ntok, qpos0, nsplit;
     int32_t pbase, split, flags, hb;
+    int32_t nparts, pad0, pad1, pad2;
 };
 constexpr int kFirst = 1, kLast = 2, kEnd = 4;
 
@@ -188,6 +192,7 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
                     si.pbase = du.pbase;
                     si.split = du.split;
                     si.hb = hb;
+                    si.nparts = du.nparts;
                     si.flags = (si_ == 0 ? kFirst : 0) | (si_ == nst - 1 ? kLast : 0);
                     dev::mbar_arrive_expect_tx(&sh->full[stage], (uint32_t)(2 * nk * row_bytes));
                 }
@@ -368,7 +373,7 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
         const float lse0 = lt0 > 0.f ? m0 + __log2f(lt0) : -INFINITY;  // log2 domain
         const float lse1 = lt1 > 0.f ? m1 + __log2f(lt1) : -INFINITY;
 
-        if (si.nsplit == 1) {
+        if (si.nparts == 1) {
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 const int r = half ? r1 : r0;
@@ -423,10 +428,10 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
             for (int it = threadIdx.x; it < items; it += consumer_threads) {
                 const int row = it / (D / 4), c4 = (it % (D / 4)) * 4;
                 float mx = -INFINITY;
-                for (int sp = 0; sp < si.nsplit; ++sp) mx = fmaxf(mx, __ldcg(plb + sp * p.lay.rows_per_slot + row));
+                for (int sp = 0; sp < si.nparts; ++sp) mx = fmaxf(mx, __ldcg(plb + sp * p.lay.rows_per_slot + row));
                 const float mu = mx == -INFINITY ? 0.f : mx;
                 float wsum = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-                for (int sp = 0; sp < si.nsplit; ++sp) {
+                for (int sp = 0; sp < si.nparts; ++sp) {
                     const float w = dev::fast_exp2(__ldcg(plb + sp * p.lay.rows_per_slot + row) - mu);
                     const float4 v =
                         __ldcg(reinterpret_cast<const float4*>(pob + ((int64_t)sp * p.lay.rows_per_slot + row) * D + c4));

@@ -116,9 +116,27 @@ __device__ __forceinline__ int queue_read(Bars* b, int k, int lane, uint32_t* er
     return v;
 }
 
-// Number of 128-key tiles Q tile h of a unit walks (0 when the tile is empty).
-__device__ __forceinline__ int kv_tiles(int kv_end, int ntok) {
-    return ntok > 0 ? (kv_end + kPreKeys - 1) / kPreKeys : 0;
+// What a unit asks for, for either kind: a prefill tile pair (keys [0, kv_end_h) of Q
+// tile h, causal) or a cascade prefix-pass unit (keys [k0, k1) of the shared prefix for
+// both member tiles, no causal mask).
+struct UnitView {
+    bool casc;
+    int key_base;   // first key of the unit (a multiple of kPreKeys)
+    int key_end;    // keys [key_base, key_end) are loaded
+    int end[2];     // keys visible to tile h end here
+    int nk[2];      // 128-key tiles tile h walks (0: tile absent)
+};
+
+__device__ __forceinline__ UnitView unit_view(const PreTile& pt) {
+    UnitView v;
+    v.casc = pt.req < 0;
+    v.key_base = v.casc ? pt.kv_end0 : 0;
+    v.end[0] = v.casc ? pt.kv_end1 : pt.kv_end0;
+    v.end[1] = pt.kv_end1;
+    v.key_end = pt.ntok1 > 0 ? v.end[1] : v.end[0];
+    v.nk[0] = pt.ntok0 > 0 ? (v.end[0] - v.key_base + kPreKeys - 1) / kPreKeys : 0;
+    v.nk[1] = pt.ntok1 > 0 ? (v.end[1] - v.key_base + kPreKeys - 1) / kPreKeys : 0;
+    return v;
 }
 
 template <int D>
@@ -135,6 +153,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if ((hdr->error_bits & kErrFatal) || n_units == 0 || (int)blockIdx.x >= n_units) return;
     const PreTile* units = reinterpret_cast<const PreTile*>(p.ws + p.lay.pre_tiles);
     int32_t* counter = &hdr->pad[1];  // zeroed by the store kernel of this forward
+    const DecGroup* groups = reinterpret_cast<const DecGroup*>(p.ws + p.lay.dec_groups);
+    const CascGroup* cgroups = reinterpret_cast<const CascGroup*>(p.ws + p.lay.casc_groups);
+    const int32_t* cmembers = reinterpret_cast<const int32_t*>(p.ws + p.lay.casc_members);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.group, Hq = p.num_qo_heads;
@@ -210,24 +231,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (u < 0 || b->abort_flag) break;
             if (fetcher) queue_push(b, uc + 1, counter, n_units, err);
             const PreTile pt = units[u];
-            const int32_t* prow = p.page_table + (int64_t)pt.req * p.ld;
-            // ---- Q: row r = token r / G, head r % G of each tile
+            const UnitView uv = unit_view(pt);
+            const int32_t* prow =
+                p.page_table + (int64_t)(uv.casc ? cgroups[-1 - pt.req].leader : pt.req) * p.ld;
+            // ---- Q: row r = token (or cascade member) r / G, head r % G of each tile
             if (uc > 0 && !wait_or_abort(&b->q_empty, (uc - 1) & 1, b, err)) break;
             for (int h = 0; h < 2; ++h) {
                 const int ntok = h ? pt.ntok1 : pt.ntok0;
                 for (int r = r0; r < kPreRows; r += kProducerThreads) {
                     const int t = r / G;
                     if (t < ntok) {
-                        const uint16_t* src =
-                            p.q + ((int64_t)(pt.tok0 + h * TM + t) * Hq + pt.kvh * G + (r - t * G)) * D;
+                        const int token = uv.casc ? groups[cmembers[pt.tok0 + h * TM + t]].tok0 : pt.tok0 + h * TM + t;
+                        const uint16_t* src = p.q + ((int64_t)token * Hq + pt.kvh * G + (r - t * G)) * D;
                         copy_row(smem + L::kQ + h * L::kTile, r, src);
                     }
                 }
             }
             issue(&b->q_full);
             // ---- K and V tiles
-            const int kv_end = pt.ntok1 > 0 ? pt.kv_end1 : pt.kv_end0;
-            const int nkt = (kv_end + kPreKeys - 1) / kPreKeys;
+            const int kv_end = uv.key_end;
+            const int nkt = (kv_end - uv.key_base + kPreKeys - 1) / kPreKeys;
             bool ok = true;
             for (int j = 0; j < nkt && ok; ++j, ++it) {
                 const int st = it & 1;
@@ -237,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
                     const int r = r0 + i * kProducerThreads;
-                    const int key = j * kPreKeys + r;
+                    const int key = uv.key_base + j * kPreKeys + r;
                     if (r < kPreRows && key < kv_end) {
                         int64_t page = prow[key >> p.page_shift];
                         if (page < 0 || page >= p.num_pages) {
@@ -310,9 +333,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (uc = 0; ok; ++uc) {
                 const int u = queue_read(b, uc, lane, err, true);
                 if (u < 0) break;
-                const PreTile pt = units[u];
-                const int nkt0 = kv_tiles(pt.kv_end0, pt.ntok0);
-                const int nkt1 = kv_tiles(pt.kv_end1, pt.ntok1);
+                const UnitView uv = unit_view(units[u]);
+                const int nkt0 = uv.nk[0];
+                const int nkt1 = uv.nk[1];
                 const int nkt = nkt1 > nkt0 ? nkt1 : nkt0;
                 if (!wait_or_abort(&b->q_full, uc & 1, b, err)) {
                     ok = false;
@@ -384,12 +407,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int u = queue_read(b, k, lane, err);
             if (u < 0 || b->abort_flag) break;
             const PreTile pt = units[u];
+            const UnitView uv = unit_view(pt);
             const int ntok = h ? pt.ntok1 : pt.ntok0;
-            const int nk = kv_tiles(h ? pt.kv_end1 : pt.kv_end0, ntok);
+            const int nk = uv.nk[h];
             if (nk == 0) continue;
-            const int qpos = pt.qpos0 + h * TM;
             const bool valid = row < ntok * G;
-            const int limit = valid ? qpos + row / G : -1;
+            // last visible key of this row, and the first key some row may not see
+            const int qpos = pt.qpos0 + h * TM;
+            const int limit = !valid ? -1 : (uv.casc ? uv.end[h] - 1 : qpos + row / G);
+            const int mask_from = uv.casc ? uv.end[h] : qpos + 1;
             float m = -INFINITY, l = 0.f;
             bool ok = true;
             for (int j = 0; j < nk; ++j, ++n_s) {
@@ -404,8 +430,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < kPreKeys / 32; ++c) tc::tmem_ld32_async(t_s + c * 32, s[c]);
 #pragma unroll
                 for (int c = 0; c < kPreKeys / 32; ++c) tc::tmem_wait_ld_regs(s[c]);
-                const int key0 = j * kPreKeys;
-                const bool need_mask = key0 + kPreKeys - 1 > qpos;
+                const int key0 = uv.key_base + j * kPreKeys;
+                const bool need_mask = key0 + kPreKeys - 1 >= mask_from;
                 float mxa[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) mxa[i] = -INFINITY;
@@ -476,8 +502,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!wait_or_abort(&b->o_ready[h], n_u & 1, b, err)) break;
             tc::fence_after_sync();
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            const int64_t orow =
-                valid ? ((int64_t)(pt.tok0 + h * TM + row / G) * Hq + pt.kvh * G + row % G) : 0;
+            const int64_t orow = (valid && !uv.casc)
+                                     ? ((int64_t)(pt.tok0 + h * TM + row / G) * Hq + pt.kvh * G + row % G)
+                                     : 0;
             float o[D / 32][32];
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) tc::tmem_ld32_async(t_o + c * 32, o[c]);
@@ -488,7 +515,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) dev::mbar_arrive(&b->o_free[h]);
             ++n_u;
-            if (valid) {
+            if (valid && uv.casc) {
+                // prefix-pass partial of a cascade member: normalised O and the log2-domain
+                // LSE into the member's slot for this key chunk (merged by the decode kernel)
+                const DecGroup dg = groups[cmembers[pt.tok0 + h * TM + row / G]];
+                const int slot = dg.pbase + dg.nsplit + pt.qpos0;
+                const int prow = pt.kvh * G + row % G;  // one new token: row = q head
+                float* po = reinterpret_cast<float*>(p.ws + p.lay.partial_o) +
+                            ((int64_t)slot * p.lay.rows_per_slot + prow) * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 8; ++q4)
+                        reinterpret_cast<float4*>(po + c * 32)[q4] =
+                            make_float4(o[c][q4 * 4] * inv, o[c][q4 * 4 + 1] * inv, o[c][q4 * 4 + 2] * inv,
+                                        o[c][q4 * 4 + 3] * inv);
+                }
+                reinterpret_cast<float*>(p.ws + p.lay.partial_lse)[(int64_t)slot * p.lay.rows_per_slot + prow] =
+                    l > 0.f ? m + __log2f(l) : -INFINITY;
+            } else if (valid) {
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D + c * 32);

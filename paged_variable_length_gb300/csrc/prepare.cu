@@ -8,14 +8,18 @@
 // and one mixed forward pass", section "Inference view": metadata building is
 // CPU work that can rival the GPU's compute time).
 //
-//   1. validate cu_seqlens_q / cache_seqlens (error word, never a trap);
-//   2. classify each request: q_len * G <= 16 rows -> decode groups (the
+//   0. shared-prefix (cascade) groups: single-token decodes whose page tables start
+//      with the same run of pages ("Source walkthrough: Attention backends",
+//      section 3.3: the shared part is computed once and merged by log-sum-exp);
+//   1. validate cu_seqlens_q / cache_seqlens (error word, never a trap) and
+//      classify each request: q_len * G <= 16 rows -> decode groups (the
 //      warp-MMA streaming kernel), otherwise -> 128-row tensor-core tiles;
-//   3. split-KV plan: choose one chunk length so that the decode work fills the
-//      GPU, split each group's visible key range into near-equal chunks;
-//   4. prefill tiles: causal KV extent of each tile (keys past the tile's last
-//      query are never loaded);
-//   5. derive slot_mapping from the page table when the caller passed none.
+//   2. split-KV plan: one chunk length so that the decode work fills the GPU;
+//      each group's visible key range (after the prefix, for cascade members) is
+//      cut into near-equal chunks;
+//   3. work lists, longest item first: decode units, prefill tile pairs with
+//      their causal KV extents, and the prefix-pass units of the cascade groups;
+//   4. slot_mapping derived from the page table when the caller passed none.
 #include <cuda_runtime.h>
 
 #include "device_utils.cuh"
@@ -27,6 +31,22 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBuckets = 256;  // cost classes for the longest-first ordering of work items
+
+// Per-request shared-memory arrays (dynamic shared memory, batch <= smem_batch).
+enum SmemArray { kCu = 0, kLen, kToff, kFirst, kLeader, kLcp, kCnt, kCgid, kGoff, kMpos, kNumArrays };
+
+// atomicAdd(addr, 1) for every active lane, with one atomic per distinct key in the
+// warp (lanes incrementing the same bucket share one); returns the lane's old value.
+__device__ __forceinline__ int warp_agg_inc(int* addr, int key) {
+    const unsigned active = __activemask();
+    const unsigned peers = __match_any_sync(active, key);
+    const int lane = threadIdx.x & 31;
+    const int leader = __ffs(peers) - 1;
+    int base = 0;
+    if (lane == leader) base = atomicAdd(addr, __popc(peers));
+    base = __shfl_sync(peers, base, leader);
+    return base + __popc(peers & ((1u << lane) - 1u));
+}
 
 // Exclusive scan of N counters across the block; each thread contributes v[k].
 template <int N>
@@ -70,59 +90,231 @@ __device__ void block_scan(int (&v)[N], int (&total)[N], int (*warp_tmp)[N]) {
     __syncthreads();
 }
 
+// Index i with off[i] <= x < off[i+1] (off ascending, off[0] <= x).
+__device__ __forceinline__ int find_bucket(const int32_t* off, int count, int x) {
+    int lo = 0, hi = count - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (off[mid] <= x) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ int cost_bucket(int cost) { return kBuckets - 1 - min(kBuckets - 1, cost); }
+
+__device__ __forceinline__ bool is_group_leader(const int32_t* leader, const int32_t* cnt, const int32_t* lcp,
+                                                int i, int min_pages) {
+    return leader[i] == i && cnt[i] >= 2 && lcp[i] >= min_pages;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws + p.lay.header);
     DecUnit* units = reinterpret_cast<DecUnit*>(p.ws + p.lay.dec_units);
     DecGroup* groups = reinterpret_cast<DecGroup*>(p.ws + p.lay.dec_groups);
     PreTile* tiles = reinterpret_cast<PreTile*>(p.ws + p.lay.pre_tiles);
     uint32_t* counters = reinterpret_cast<uint32_t*>(p.ws + p.lay.counters);
+    CascGroup* cgroups = reinterpret_cast<CascGroup*>(p.ws + p.lay.casc_groups);
+    int32_t* cmembers = reinterpret_cast<int32_t*>(p.ws + p.lay.casc_members);
 
+    extern __shared__ int32_t dyn[];
     __shared__ uint32_t s_err;
     __shared__ unsigned long long s_work;
     __shared__ int s_tmp3[kWarps][3];
     __shared__ int s_tmp2[kWarps][2];
     __shared__ int s_hist_u[kBuckets];
     __shared__ int s_hist_t[kBuckets];
+    __shared__ int s_ngroups, s_casc_units;
+
     const int tid = threadIdx.x;
+    const int B = p.batch;
+    const int TB = p.dec_tokens, TM = p.pre_tokens, Hkv = p.num_kv_heads, ps = p.page_size;
+    const bool small = p.smem_batch >= B;  // per-request arrays fit in shared memory
+    const int stride = p.smem_batch + 1;
+    int32_t* sa[kNumArrays];
+#pragma unroll
+    for (int a = 0; a < kNumArrays; ++a) sa[a] = dyn + a * stride;
     if (tid == 0) {
         s_err = 0;
         s_work = 0;
+        s_ngroups = 0;
+        s_casc_units = 0;
+    }
+    if (small) {
+        for (int i = tid; i <= B; i += kThreads) {
+            sa[kCu][i] = p.cu[i];
+            if (i < B) sa[kLen][i] = p.seqlens[i];
+            sa[kCgid][i] = -1;
+        }
     }
     __syncthreads();
+    const int32_t* cu = small ? sa[kCu] : p.cu;
+    const int32_t* lens = small ? sa[kLen] : p.seqlens;
+    auto valid_req = [&](int n, int L) { return n >= 0 && n <= L && L <= p.max_kv_len && n <= p.max_q_len; };
 
-    const int B = p.batch;
-    const int TB = p.dec_tokens, TM = p.pre_tokens, Hkv = p.num_kv_heads;
+    // ---- pass 0: shared-prefix groups among single-token decodes.  Requests are keyed
+    // by their first page; the first request with a key leads its group; the group's
+    // prefix is the run of pages every member shares with the leader (whole pages that
+    // lie strictly before each member's query, so no causal mask ever applies to it).
+    const bool casc = p.use_cascade && small && B >= 2;
+    if (casc) {
+        int32_t* first = sa[kFirst];
+        int32_t* leader = sa[kLeader];
+        int32_t* lcp = sa[kLcp];
+        int32_t* cnt = sa[kCnt];
+        for (int i = tid; i < B; i += kThreads) {
+            const int n = cu[i + 1] - cu[i], L = lens[i];
+            const int pages = (L - n) / ps;  // whole pages strictly before the query
+            const bool cand = n == 1 && valid_req(n, L) && pages >= p.min_cascade_pages;
+            const int f = cand ? p.page_table[(int64_t)i * p.ld] : -1;
+            first[i] = (cand && f >= 0) ? f : -1;
+            lcp[i] = cand ? pages : 0;
+            cnt[i] = 0;
+        }
+        __syncthreads();
+        for (int i = tid; i < B; i += kThreads) {
+            int ld = -1;
+            if (first[i] >= 0)
+                for (int j = 0; j <= i && ld < 0; ++j)
+                    if (first[j] == first[i]) ld = j;
+            leader[i] = ld;
+        }
+        __syncthreads();
+        for (int i = tid; i < B; i += kThreads) {
+            const int ld = leader[i];
+            if (ld < 0) continue;
+            atomicAdd(&cnt[ld], 1);
+            if (ld == i) continue;
+            const int lim = min(lcp[i], lcp[ld]);
+            const int32_t* ri = p.page_table + (int64_t)i * p.ld;
+            const int32_t* rl = p.page_table + (int64_t)ld * p.ld;
+            int k = 1;
+            while (k < lim && ri[k] == rl[k]) ++k;
+            atomicMin(&lcp[ld], k);
+        }
+        __syncthreads();
+        // group ids in leader order (a deterministic plan); member slots per group
+        if (tid == 0) {
+            int gid = 0, moff = 0;
+            for (int i = 0; i < B; ++i) {
+                if (!is_group_leader(leader, cnt, lcp, i, p.min_cascade_pages)) continue;
+                sa[kCgid][i] = gid;
+                CascGroup cg;
+                cg.leader = i;
+                cg.prefix_len = lcp[i] * ps;
+                cg.n_members = cnt[i];
+                cg.member_off = moff;
+                cg.n_chunks = 0;
+                cg.chunk_keys = 0;
+                cg.unit_off = 0;
+                cg.n_units = 0;
+                cgroups[gid] = cg;
+                sa[kMpos][i] = moff;  // next free member slot of the group
+                moff += cnt[i];
+                ++gid;
+            }
+            s_ngroups = gid;
+        }
+        __syncthreads();
+        // members take the group id of their leader (-1 when the leader leads no group)
+        for (int i = tid; i < B; i += kThreads) {
+            const int ld = leader[i];
+            if (ld >= 0 && ld != i) sa[kCgid][i] = is_group_leader(leader, cnt, lcp, ld, p.min_cascade_pages)
+                                                       ? sa[kCgid][ld]
+                                                       : -1;
+        }
+        __syncthreads();
+    }
+    auto casc_of = [&](int i) { return casc ? sa[kCgid][i] : -1; };
+    // prefix length (keys) of request i when it is a cascade member, else 0
+    auto prefix_of = [&](int i) {
+        const int g = casc_of(i);
+        return g >= 0 ? cgroups[g].prefix_len : 0;
+    };
+
     const int chunk_req = (B + kThreads - 1) / kThreads;
     const int r0 = min(B, tid * chunk_req), r1 = min(B, r0 + chunk_req);
 
     // ---- pass 1: validate, count decode groups and prefill tiles, sum decode key extents
     uint32_t err = 0;
-    int cnt[3] = {0, 0, 0};  // groups, tiles, (unused)
+    int cnt[3] = {0, 0, 0};  // decode groups, prefill tile pairs x kv heads, (unused)
     unsigned long long work = 0;
     if (tid == 0 && p.cu[0] != 0) err |= kErrCu;
     if (tid == 0 && B > p.max_batch) err |= kErrLimits;
     if (tid == 0 && p.total_tokens > p.max_tokens) err |= kErrLimits;
     for (int i = r0; i < r1; ++i) {
-        const int c0 = p.cu[i], c1 = p.cu[i + 1], L = p.seqlens[i];
+        const int c0 = cu[i], c1 = cu[i + 1], L = lens[i];
         const int n = c1 - c0;
         if (n < 0) err |= kErrCu;
         if (i == B - 1 && c1 != p.total_tokens) err |= kErrCu;
         if (L < 0 || n > L) err |= kErrQgtKv;
         if (L > p.max_kv_len || n > p.max_q_len) err |= kErrLimits;
-        if (n <= 0 || n > L || L > p.max_kv_len || n > p.max_q_len) continue;
+        if (n <= 0 || !valid_req(n, L)) continue;
         if (p.use_prefill && n > TB) {
             cnt[1] += (int)((((n + TM - 1) / TM) + 1) / 2) * Hkv;  // units of two Q tiles
         } else {
             const int ng = (n + TB - 1) / TB;
             cnt[0] += ng;
-            for (int g = 0; g < ng; ++g) work += (unsigned long long)(L - n + min((g + 1) * TB, n));
+            const int lp = prefix_of(i);
+            for (int g = 0; g < ng; ++g) work += (unsigned long long)(L - n + min((g + 1) * TB, n) - lp);
         }
     }
     if (err) atomicOr(&s_err, err);
-    if (work) atomicAdd(&s_work, work);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) work += __shfl_xor_sync(0xffffffffu, work, o);
+    if ((tid & 31) == 0 && work) atomicAdd(&s_work, work);
     int tot3[3];
     block_scan<3>(cnt, tot3, s_tmp3);  // cnt now holds this thread's exclusive offsets
-    if (tot3[0] > p.lay.max_dec_groups || tot3[1] > p.lay.max_pre_tiles) {
+    // first prefill unit and first decode group of each request: the emission below runs
+    // in parallel over units and finds a unit's request by binary search
+    int32_t* tile_off = small ? sa[kToff] : reinterpret_cast<int32_t*>(p.ws + p.lay.req_scratch);
+    {
+        int toff = cnt[1], goff = cnt[0];
+        for (int i = r0; i < r1; ++i) {
+            tile_off[i] = toff;
+            if (small) sa[kGoff][i] = goff;
+            const int n = cu[i + 1] - cu[i], L = lens[i];
+            if (n > 0 && valid_req(n, L)) {
+                if (p.use_prefill && n > TB) toff += (int)((((n + TM - 1) / TM) + 1) / 2) * Hkv;
+                else goff += (n + TB - 1) / TB;
+            }
+        }
+        if (tid == 0) tile_off[B] = tot3[1];
+    }
+    __syncthreads();
+
+    // ---- cascade groups: key chunks of each prefix, prefix-pass units, member lists
+    if (casc && tid == 0) {
+        const int ng = s_ngroups;
+        // about casc_target prefix units in total (roughly one per SM)
+        int pair_units = 0;
+        for (int g = 0; g < ng; ++g) pair_units += (((cgroups[g].n_members + TM - 1) / TM) + 1) / 2 * Hkv;
+        int uoff = 0;
+        for (int g = 0; g < ng; ++g) {
+            CascGroup cg = cgroups[g];
+            const int pu = (((cg.n_members + TM - 1) / TM) + 1) / 2 * Hkv;
+            int nc = (p.lay.casc_target + pair_units - 1) / max(pair_units, 1);
+            nc = max(1, min(nc, min(kMaxCascChunks, (cg.prefix_len + kPreKeys - 1) / kPreKeys)));
+            const int ck = ((cg.prefix_len + nc - 1) / nc + kPreKeys - 1) / kPreKeys * kPreKeys;
+            cg.chunk_keys = ck;
+            cg.n_chunks = (cg.prefix_len + ck - 1) / ck;
+            cg.unit_off = uoff;
+            cg.n_units = cg.n_chunks * pu;
+            uoff += cg.n_units;
+            cgroups[g] = cg;
+        }
+        s_casc_units = uoff;
+    }
+    __syncthreads();
+    if (casc) {
+        for (int i = tid; i < B; i += kThreads) {
+            if (sa[kCgid][i] < 0) continue;
+            const int slot = atomicAdd(&sa[kMpos][sa[kLeader][i]], 1);
+            cmembers[slot] = sa[kGoff][i];  // a member (one new token) has exactly one decode group
+        }
+    }
+    const int tiles_total = tot3[1] + s_casc_units;
+    if (tot3[0] > p.lay.max_dec_groups || tiles_total > p.lay.max_pre_tiles) {
         if (tid == 0) atomicOr(&s_err, kErrLimits);
     }
     __syncthreads();
@@ -140,15 +332,18 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     int cnt2[2] = {0, 0};  // units, partial slots
     if (!fatal) {
         for (int i = r0; i < r1; ++i) {
-            const int n = p.cu[i + 1] - p.cu[i], L = p.seqlens[i];
+            const int n = cu[i + 1] - cu[i], L = lens[i];
             if (n <= 0 || (p.use_prefill && n > TB)) continue;
             const int ng = (n + TB - 1) / TB;
+            const int lp = prefix_of(i);
+            const int cg = casc_of(i);
             for (int g = 0; g < ng; ++g) {
-                const int ext = L - n + min((g + 1) * TB, n);
+                const int ext = L - n + min((g + 1) * TB, n) - lp;
                 int per;
                 const int s = split_ranges(ext, chunk, &per);
+                const int nparts = s + (cg >= 0 ? cgroups[cg].n_chunks : 0);
                 cnt2[0] += s;
-                if (s > 1) cnt2[1] += s;
+                if (nparts > 1) cnt2[1] += nparts;
             }
         }
     }
@@ -174,50 +369,30 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         if (run) {
             int gi = cnt[0], pi = cnt2[1];
             for (int i = r0; i < r1; ++i) {
-                const int c0 = p.cu[i], n = p.cu[i + 1] - c0, L = p.seqlens[i];
+                const int c0 = cu[i], n = cu[i + 1] - c0, L = lens[i];
                 if (n <= 0) continue;
-                if (p.use_prefill && n > TB) {
-                    const int nt = (n + TM - 1) / TM;
-                    for (int t = 0; t < nt; t += 2) {  // a unit: Q tiles t and t+1
-                        const int a0 = t * TM, na0 = min(TM, n - a0);
-                        const int na1 = t + 1 < nt ? min(TM, n - a0 - TM) : 0;
-                        const int kv_end0 = L - n + a0 + na0;
-                        const int kv_end1 = na1 > 0 ? kv_end0 + na1 : kv_end0;
-                        const int b = kBuckets - 1 - min(kBuckets - 1, (kv_end1 + kPreKeys - 1) / kPreKeys);
-                        for (int h = 0; h < Hkv; ++h) {
-                            if (!emit) {
-                                atomicAdd(&s_hist_t[b], 1);
-                                continue;
-                            }
-                            PreTile pt;
-                            pt.req = i;
-                            pt.kvh = h;
-                            pt.tok0 = c0 + a0;
-                            pt.ntok0 = na0;
-                            pt.ntok1 = na1;
-                            pt.qpos0 = L - n + a0;
-                            pt.kv_end0 = kv_end0;
-                            pt.kv_end1 = kv_end1;
-                            tiles[atomicAdd(&s_hist_t[b], 1)] = pt;
-                        }
-                    }
-                    continue;
-                }
+                if (p.use_prefill && n > TB) continue;  // prefill units: emitted below
                 const int ng = (n + TB - 1) / TB;
+                const int lp = prefix_of(i);
+                const int cg = casc_of(i);
                 for (int g = 0; g < ng; ++g) {
                     const int a0 = g * TB, na = min(TB, n - a0);
-                    const int ext = L - n + a0 + na;
+                    const int kv_end = L - n + a0 + na;
                     int per;
-                    const int s = split_ranges(ext, chunk, &per);
+                    const int s = split_ranges(kv_end - lp, chunk, &per);
+                    const int nparts = s + (cg >= 0 ? cgroups[cg].n_chunks : 0);
                     DecGroup dg;
                     dg.req = i;
                     dg.tok0 = c0 + a0;
                     dg.ntok = na;
                     dg.qpos0 = L - n + a0;
                     dg.nsplit = s;
-                    dg.pbase = s > 1 ? pi : -1;
-                    dg.kv_end = ext;
-                    dg.casc = -1;
+                    dg.pbase = nparts > 1 ? pi : -1;
+                    dg.kv_end = kv_end;
+                    dg.casc = cg;
+                    dg.nparts = nparts;
+                    dg.tail0 = lp;
+                    dg.pad0 = dg.pad1 = dg.pad2 = dg.pad3 = dg.pad4 = dg.pad5 = 0;
                     if (emit) {
                         groups[gi] = dg;
                         counters[gi] = 0;
@@ -225,12 +400,11 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
                     for (int u = 0; u < s; ++u) {
                         DecUnit du;
                         du.group = gi;
-                        du.k0 = min(ext, u * per);
-                        du.k1 = min(ext, (u + 1) * per);
-                        const int b = kBuckets - 1 - min(kBuckets - 1, (du.k1 - du.k0 + kDecKeysPerStage - 1) /
-                                                                           kDecKeysPerStage);
+                        du.k0 = min(kv_end, lp + u * per);
+                        du.k1 = min(kv_end, lp + (u + 1) * per);
+                        const int b = cost_bucket((du.k1 - du.k0 + kDecKeysPerStage - 1) / kDecKeysPerStage);
                         if (!emit) {
-                            atomicAdd(&s_hist_u[b], 1);
+                            warp_agg_inc(&s_hist_u[b], b);
                             continue;
                         }
                         du.split = u;
@@ -238,23 +412,89 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
                         du.tok0 = dg.tok0;
                         du.ntok = dg.ntok;
                         du.qpos0 = dg.qpos0;
-                        du.nsplit = dg.nsplit;
+                        du.nsplit = s;
                         du.pbase = dg.pbase;
-                        du.pad0 = du.pad1 = 0;
-                        units[atomicAdd(&s_hist_u[b], 1)] = du;
+                        du.nparts = nparts;
+                        du.pad1 = 0;
+                        units[warp_agg_inc(&s_hist_u[b], b)] = du;
                     }
-                    if (s > 1) pi += s;
+                    if (nparts > 1) pi += nparts;
                     ++gi;
                 }
             }
+            // prefill tile pairs, then cascade prefix units, in parallel over the unit index
+            for (int x = tid; x < tiles_total; x += kThreads) {
+                PreTile pt;
+                int cost;
+                if (x < tot3[1]) {  // unit index -> (request, pair of Q tiles, kv head)
+                    const int i = find_bucket(tile_off, B, x);
+                    const int lx = x - tile_off[i];
+                    const int c0 = cu[i], n = cu[i + 1] - c0, L = lens[i];
+                    const int nt = (n + TM - 1) / TM;
+                    const int t = 2 * (lx / Hkv), h = lx % Hkv;  // Q tiles t and t+1
+                    const int a0 = t * TM, na0 = min(TM, n - a0);
+                    const int na1 = t + 1 < nt ? min(TM, n - a0 - TM) : 0;
+                    pt.req = i;
+                    pt.kvh = h;
+                    pt.tok0 = c0 + a0;
+                    pt.ntok0 = na0;
+                    pt.ntok1 = na1;
+                    pt.qpos0 = L - n + a0;
+                    pt.kv_end0 = L - n + a0 + na0;
+                    pt.kv_end1 = na1 > 0 ? pt.kv_end0 + na1 : pt.kv_end0;
+                    cost = (pt.kv_end1 + kPreKeys - 1) / kPreKeys;
+                } else {  // -> (cascade group, key chunk, pair of member tiles, kv head)
+                    const int y = x - tot3[1];
+                    int g = 0;
+                    while (g + 1 < s_ngroups && cgroups[g + 1].unit_off <= y) ++g;
+                    const CascGroup cgr = cgroups[g];
+                    const int ly = y - cgr.unit_off;
+                    const int pu = (((cgr.n_members + TM - 1) / TM) + 1) / 2 * Hkv;
+                    const int c = ly / pu, rest = ly % pu;
+                    const int pair = rest / Hkv, h = rest % Hkv;
+                    const int m0 = pair * 2 * TM;
+                    pt.req = -1 - g;
+                    pt.kvh = h;
+                    pt.tok0 = cgr.member_off + m0;
+                    pt.ntok0 = min(TM, cgr.n_members - m0);
+                    pt.ntok1 = max(0, min(TM, cgr.n_members - m0 - TM));
+                    pt.qpos0 = c;
+                    pt.kv_end0 = c * cgr.chunk_keys;
+                    pt.kv_end1 = min(cgr.prefix_len, (c + 1) * cgr.chunk_keys);
+                    cost = (pt.kv_end1 - pt.kv_end0 + kPreKeys - 1) / kPreKeys;
+                }
+                const int b = cost_bucket(cost);
+                if (!emit) {
+                    warp_agg_inc(&s_hist_t[b], b);
+                    continue;
+                }
+                tiles[warp_agg_inc(&s_hist_t[b], b)] = pt;
+            }
         }
         __syncthreads();
-        if (!emit && tid == 0) {  // bucket counts -> first position of each bucket (bucket 0 = costliest)
-            int au = 0, at = 0;
-            for (int b = 0; b < kBuckets; ++b) {
-                const int cu_ = s_hist_u[b], ct = s_hist_t[b];
-                s_hist_u[b] = au;
-                s_hist_t[b] = at;
+        if (!emit && tid < 32) {  // bucket counts -> first position of each bucket (bucket 0 = costliest)
+            constexpr int kPer = kBuckets / 32;
+            int su = 0, st = 0;
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) {
+                su += s_hist_u[tid * kPer + k];
+                st += s_hist_t[tid * kPer + k];
+            }
+            int iu = su, itt = st;  // inclusive warp scan
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int yu = __shfl_up_sync(0xffffffffu, iu, o), yt = __shfl_up_sync(0xffffffffu, itt, o);
+                if (tid >= o) {
+                    iu += yu;
+                    itt += yt;
+                }
+            }
+            int au = iu - su, at = itt - st;
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) {
+                const int cu_ = s_hist_u[tid * kPer + k], ct = s_hist_t[tid * kPer + k];
+                s_hist_u[tid * kPer + k] = au;
+                s_hist_t[tid * kPer + k] = at;
                 au += cu_;
                 at += ct;
             }
@@ -266,19 +506,13 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     if (run && p.derived_slots != nullptr) {
         uint32_t perr = 0;
         for (int t = tid; t < p.total_tokens; t += kThreads) {
-            int lo = 0, hi = B - 1;  // request i with cu[i] <= t < cu[i+1]
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (p.cu[mid] <= t) lo = mid;
-                else hi = mid - 1;
-            }
-            const int i = lo;
-            const int n = p.cu[i + 1] - p.cu[i], L = p.seqlens[i];
-            const int pos = L - n + (t - p.cu[i]);
-            const int64_t page = p.page_table[(int64_t)i * p.ld + pos / p.page_size];
+            const int i = find_bucket(cu, B, t);  // request i with cu[i] <= t < cu[i+1]
+            const int n = cu[i + 1] - cu[i], L = lens[i];
+            const int pos = L - n + (t - cu[i]);
+            const int64_t page = p.page_table[(int64_t)i * p.ld + pos / ps];
             int64_t slot = -1;
             if (page < 0 || page >= p.num_pages) perr |= kErrPage;
-            else slot = page * p.page_size + pos % p.page_size;
+            else slot = page * ps + pos % ps;
             p.derived_slots[t] = slot;
         }
         if (perr) atomicOr(&s_err, perr);
@@ -288,20 +522,27 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         const bool ok = (s_err & kErrFatal) == 0;
         hdr->error_bits = s_err;
         hdr->n_dec_groups = ok ? tot3[0] : 0;
-        hdr->n_pre_tiles = ok ? tot3[1] : 0;
+        hdr->n_pre_tiles = ok ? tiles_total : 0;
         hdr->n_dec_units = ok ? tot2[0] : 0;
         hdr->n_partial_slots = ok ? tot2[1] : 0;
         hdr->split_chunk = chunk;
-        hdr->n_casc_groups = 0;
-        hdr->n_casc_tiles = 0;
-        hdr->n_casc_units = 0;
+        hdr->n_casc_groups = ok ? s_ngroups : 0;
+        hdr->n_casc_tiles = ok ? s_casc_units : 0;
+        hdr->n_casc_units = ok ? s_casc_units : 0;
     }
 }
 
 }  // namespace
 
+size_t prepare_smem_bytes(int smem_batch) { return (size_t)kNumArrays * (smem_batch + 1) * sizeof(int32_t); }
+
 cudaError_t launch_prepare(const PrepareParams& p, cudaStream_t s) {
-    prepare_kernel<<<1, kThreads, 0, s>>>(p);
+    const size_t smem = prepare_smem_bytes(p.smem_batch);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(prepare_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    prepare_kernel<<<1, kThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 

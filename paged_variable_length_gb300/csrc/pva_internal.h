@@ -21,6 +21,8 @@ constexpr int kPreRows = 128;
 constexpr int kPreKeys = 128;
 // Smallest split-KV chunk (keys) worth a separate CTA.
 constexpr int kMinSplitChunk = 256;
+// Most key chunks one shared prefix is cut into for the cascade prefix pass.
+constexpr int kMaxCascChunks = 8;
 
 // Error bits the kernels OR into the plan's error word (same values as pva.h).
 constexpr uint32_t kErrCu = PVA_DEVERR_CU_SEQLENS;
@@ -59,8 +61,12 @@ struct DecGroup {
     int32_t nsplit;      // number of units (key ranges) covering the group
     int32_t pbase;       // first partial slot (valid when nsplit > 1)
     int32_t kv_end;      // keys [0, kv_end) are visible to some token of the group
-    int32_t casc;        // cascade group id feeding a prefix partial, or -1
+    int32_t casc;        // cascade group id feeding prefix partials, or -1
+    int32_t nparts;      // partial slots of the group (see DecUnit::nparts)
+    int32_t tail0;       // first key the decode units cover (the prefix length of a cascade member)
+    int32_t pad0, pad1, pad2, pad3, pad4, pad5;
 };
+static_assert(sizeof(DecGroup) == 64, "DecGroup is one 64-byte record");
 
 // One CTA work item of the decode kernel: keys [k0, k1) of a group.  The group's
 // fields are repeated here so that one load brings everything a unit needs.
@@ -73,9 +79,25 @@ struct DecUnit {
     int32_t tok0;
     int32_t ntok;
     int32_t qpos0;
-    int32_t nsplit;
+    int32_t nsplit;      // units (CTAs) that arrive on the group's counter
     int32_t pbase;
-    int32_t pad0, pad1;
+    int32_t nparts;      // partial slots merged: nsplit, plus the prefix chunks of a cascade member
+    int32_t pad1;
+};
+
+// A shared-prefix (cascade) group: decode requests whose page tables start with the
+// same prefix_len / page_size pages.  The prefix pass attends every member's query
+// rows to the prefix keys once per chunk of keys; the members' decode units cover only
+// the keys after the prefix, and the merge combines both by log-sum-exp.
+struct CascGroup {
+    int32_t leader;       // request whose page-table row addresses the prefix
+    int32_t prefix_len;   // keys [0, prefix_len) are shared
+    int32_t n_members;
+    int32_t member_off;   // members[member_off ..] hold the members' decode-group indices
+    int32_t n_chunks;     // prefix pass key chunks
+    int32_t chunk_keys;   // keys per chunk (multiple of kPreKeys)
+    int32_t unit_off;     // first prefix-pass unit of the group (relative to the cascade units)
+    int32_t n_units;
 };
 
 // One work unit of the tensor-core prefill kernel: two consecutive Q tiles of one
@@ -92,6 +114,10 @@ struct PreTile {
     int32_t kv_end0;     // keys [0, kv_end0) for tile 0
     int32_t kv_end1;     // keys [0, kv_end1) for tile 1
 };
+// A cascade prefix-pass unit reuses PreTile: req = -1 - cascade group, tok0 = first
+// member (index into the member list), ntok0 / ntok1 = members in Q tile 0 / 1, qpos0 =
+// key chunk, kv_end0 / kv_end1 = the chunk's keys [k0, k1).  No causal mask applies:
+// the prefix lies before every member's query.
 
 // Workspace carve-up (byte offsets from the workspace base); computed on the host.
 struct Layout {
@@ -104,6 +130,8 @@ struct Layout {
     size_t partial_o;    // fp32 [max_partial][rows_per_slot][D]
     size_t partial_lse;  // fp32 [max_partial][rows_per_slot]
     size_t req_scratch;  // int32 [max_batch * 4] prepare scratch
+    size_t casc_groups;  // CascGroup [max_casc_groups]
+    size_t casc_members; // int32 [max_batch]
     size_t total;
     int32_t max_dec_units;
     int32_t max_dec_groups;
@@ -111,6 +139,8 @@ struct Layout {
     int32_t max_partial;
     int32_t rows_per_slot;
     int32_t target_units;
+    int32_t max_casc_groups;
+    int32_t casc_target;  // prefix-pass units aimed for (about one per SM)
 };
 
 // Parameters of the prepare kernel (by value).
@@ -132,6 +162,9 @@ struct PrepareParams {
     int32_t dec_tokens;          // tokens per decode group = 16 / group
     int32_t pre_tokens;          // tokens per prefill tile = 128 / group
     int32_t use_prefill;         // 1: requests with q_len > dec_tokens go to the prefill kernel
+    int32_t use_cascade;         // 1: detect shared prefixes among decodes
+    int32_t min_cascade_pages;
+    int32_t smem_batch;          // per-request arrays live in shared memory when batch <= this
     int32_t split_kv;
     int32_t max_kv_len;
     int32_t max_tokens;
@@ -176,6 +209,7 @@ struct MetaHost {
     int32_t max_q_len;
     int32_t sm_count;
     int32_t use_prefill;
+    int32_t use_cascade;
     int32_t dec_ctas;
     int32_t pre_ctas;
     const int32_t* cu;
@@ -219,6 +253,7 @@ inline int split_ranges(int ext, int chunk, int* per_out) {
 
 // Launchers (defined in the .cu files).
 cudaError_t launch_prepare(const PrepareParams& p, cudaStream_t s);
+size_t prepare_smem_bytes(int smem_batch);
 cudaError_t launch_store(const ForwardParams& p, int head_dim, cudaStream_t s);
 cudaError_t launch_decode(const ForwardParams& p, int head_dim, int ctas, cudaStream_t s);
 cudaError_t launch_prefill(const ForwardParams& p, int head_dim, int ctas, cudaStream_t s);

@@ -220,3 +220,80 @@ def _sampled_check(wl, n_rows=3000, seed=0):
 @pytest.mark.parametrize("name", ["decode", "mixed", "cascade", "prefill"])
 def test_full_size_workload(name):
     _sampled_check(W.WORKLOADS[name](0))
+
+
+# ------------------------------------------------------------------ shared-prefix (cascade) path
+
+
+def _table_workload(q_lens, kv_lens, rows, Hq, Hkv, D, ps, num_pages, seed):
+    """A workload with explicit page-table rows (lists of page ids)."""
+    width = max(len(r) for r in rows)
+    table = np.zeros((len(rows), width), np.int32)
+    for i, r in enumerate(rows):
+        table[i, :len(r)] = r
+    return W.Workload("table", list(q_lens), list(kv_lens), Hq, Hkv, D, ps, num_pages, table, 1.0, seed)
+
+
+def _cascade_batch(seed=0, Hq=32, Hkv=8, D=128, ps=16):
+    """Two prefix groups (12 and 9 shared pages), a member sharing only part of its
+    group's prefix, an unrelated decode, a decode too short for a prefix, a prefill."""
+    rng = np.random.default_rng(seed)
+    P = 400
+    perm = list(rng.permutation(P))
+    take = lambda k: [int(perm.pop()) for _ in range(k)]
+    pre_a, pre_b = take(12), take(9)
+    rows, q_lens, kv_lens = [], [], []
+    for tail in (1, 5, 16, 40, 17):            # group A: prefix 12 pages, tails of 1..40 keys
+        L = 12 * ps + tail
+        rows.append(pre_a + take((L + ps - 1) // ps - 12)); q_lens.append(1); kv_lens.append(L)
+    for tail in (3, 30, 64):                    # group B
+        L = 9 * ps + tail
+        rows.append(pre_b + take((L + ps - 1) // ps - 9)); q_lens.append(1); kv_lens.append(L)
+    L = 12 * ps + 7                             # shares only 10 of group A's pages
+    rows.append(pre_a[:10] + take((L + ps - 1) // ps - 10)); q_lens.append(1); kv_lens.append(L)
+    L = 300                                     # unrelated decode
+    rows.append(take((L + ps - 1) // ps)); q_lens.append(1); kv_lens.append(L)
+    L = 5 * ps                                  # group A's first pages but too short a prefix
+    rows.append(pre_a[:5]); q_lens.append(1); kv_lens.append(L)
+    L = 200                                     # a prefill in the same batch
+    rows.append(take((L + ps - 1) // ps)); q_lens.append(L); kv_lens.append(L)
+    return _table_workload(q_lens, kv_lens, rows, Hq, Hkv, D, ps, P, seed)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_cascade_groups_match_the_oracle(seed):
+    wl = _cascade_batch(seed)
+    err, eng = _full_check(wl)
+    counts = pva.attn_debug_plan_counts(eng.meta)
+    assert counts["casc_groups"] == 2 and counts["casc_tiles"] > 0
+
+
+def test_cascade_on_equals_off_within_tolerance():
+    wl = _cascade_batch(3)
+    _, eng_on = _full_check(wl, enable_cascade=True)
+    _, eng_off = _full_check(wl, enable_cascade=False)
+    assert pva.attn_debug_plan_counts(eng_off.meta)["casc_groups"] == 0
+
+
+def test_cascade_group_size_and_tile_edges():
+    """A group larger than one member tile pair (G 4: 32 members per tile) with ragged
+    member counts and a prefix that is not a multiple of 128 keys."""
+    ps = 16
+    rng = np.random.default_rng(7)
+    P = 3000
+    perm = list(rng.permutation(P))
+    take = lambda k: [int(perm.pop()) for _ in range(k)]
+    pre = take(27)  # 432 keys
+    rows, ql, kl = [], [], []
+    for m in range(70):
+        tail = int(rng.integers(1, 80))
+        L = 27 * ps + tail
+        rows.append(pre + take((L + ps - 1) // ps - 27)); ql.append(1); kl.append(L)
+    wl = _table_workload(ql, kl, rows, 32, 8, 128, ps, P, 7)
+    _, eng = _full_check(wl, poison=True)
+    assert pva.attn_debug_plan_counts(eng.meta)["casc_groups"] == 1
+
+
+def test_cascade_with_group_of_seven_heads():
+    wl = _cascade_batch(4, Hq=28, Hkv=4, D=128, ps=16)
+    _full_check(wl)
