@@ -324,7 +324,7 @@ def run_ours(args):
     pev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
     for e in kev + pev:
         e.record(stream)
-    phase = {"prepare": [], "store": [], "prefill": [], "cascade": [], "decode": []}
+    phase = {"prepare": [], "store": [], "tensor_core": [], "decode": [], "merge": []}
     pgraph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(pgraph):
         pev[0].record()
@@ -338,14 +338,14 @@ def run_ours(args):
         pgraph.replay()
         torch.cuda.synchronize()
         phase["prepare"].append(pev[0].elapsed_time(pev[1]))
-        for j, name in enumerate(["store", "prefill", "cascade", "decode"]):
+        for j, name in enumerate(["store", "tensor_core", "decode", "merge"]):
             phase[name].append(kev[j].elapsed_time(kev[j + 1]))
     phase_ms = {k: (sum(v) / len(v) if v else 0.0) for k, v in phase.items()}
 
     peaks = load_peaks()
     # dominant kernel: the phase with the largest share of the step
-    dom = max(("prefill", "cascade", "decode"), key=lambda k: phase_ms[k])
-    if dom == "prefill" and work["flops"] > 0:
+    dom = max(("tensor_core", "decode"), key=lambda k: phase_ms[k])
+    if dom == "tensor_core" and work["flops"] > 0:
         roof = {"bound": "tensor", "achieved": work["flops"] / (phase_ms[dom] / 1e3) / 1e12,
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
     else:

@@ -195,9 +195,11 @@ PVA_API pva_status attn_get_device_status(const pva_meta* meta, uint32_t* error_
  * Profiling helper: with n > 0, every later attn_forward on this meta records
  * caller-created events (cudaEvent_t passed as void*) on its stream:
  * events[0] before its first kernel, then one after each phase --
- * [1] store_kvcache, [2] tensor-core prefill tiles, [3] shared-prefix
- * (cascade) pass, [4] decode / split-KV / combine.  A phase that launches
- * nothing records at the same point as the previous one.  n must be 0 (off)
+ * [1] store_kvcache, [2] tensor-core pass (prefill tiles and the
+ * shared-prefix pass), [3] decode / split-KV units, [4] LSE combine of the
+ * split groups.  A phase that launches nothing records at the same point as
+ * the previous one; recording the events also keeps the kernels from
+ * overlapping their launch with the kernel before them.  n must be 0 (off)
  * or 5; the handles must outlive the forwards.  Timing only; it changes no
  * result.
  */

@@ -21,8 +21,10 @@ int device_sm_count() {
 bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 
 // Batches up to this size keep their per-request arrays in the prepare kernel's shared
-// memory; shared-prefix detection needs it.
+// memory; shared-prefix detection needs them there, with its hash table beside them,
+// which bounds it to smaller batches.
 constexpr int kPrepareSmemBatch = 4096;
+constexpr int kCascadeMaxBatch = 2048;
 
 // Host-side validation of the static configuration.
 pva_status check_config(const pva_config* c) {
@@ -69,7 +71,6 @@ Layout make_layout(const pva_config* c, int sm_count) {
     L.dec_groups = take(sizeof(DecGroup) * (size_t)L.max_dec_groups);
     L.pre_tiles = take(sizeof(PreTile) * (size_t)L.max_pre_tiles);
     L.slots = take(sizeof(int64_t) * (size_t)(c->max_tokens + 1));
-    L.counters = take(sizeof(uint32_t) * (size_t)L.max_dec_groups);
     L.partial_o = take(sizeof(float) * (size_t)L.max_partial * L.rows_per_slot * c->head_dim);
     L.partial_lse = take(sizeof(float) * (size_t)L.max_partial * L.rows_per_slot);
     L.req_scratch = take(sizeof(int32_t) * 4 * (size_t)(c->max_batch + 1));
@@ -179,7 +180,7 @@ pva_status attn_prepare_metadata(const pva_config* cfg, const int32_t* cu_seqlen
     // also runs the prefix pass of shared-prefix groups
     const bool tc_ok = prefill_supported(cfg->num_qo_heads, cfg->num_kv_heads, cfg->head_dim);
     h.use_prefill = (mq > TB && tc_ok) ? 1 : 0;
-    h.use_cascade = (cfg->enable_cascade && tc_ok && batch >= 2 && batch <= kPrepareSmemBatch) ? 1 : 0;
+    h.use_cascade = (cfg->enable_cascade && tc_ok && batch >= 2 && batch <= kCascadeMaxBatch) ? 1 : 0;
     h.dec_ctas = sms * decode_ctas_per_sm(cfg->num_kv_heads, cfg->head_dim);
     {
         const int64_t TM = kPreRows / G;
@@ -196,7 +197,10 @@ pva_status attn_prepare_metadata(const pva_config* cfg, const int32_t* cu_seqlen
     h.stream = stream;
     h.lay = lay;
     h.n_events = 0;
-    h.kernels_per_forward = 2 + ((h.use_prefill || h.use_cascade) ? 1 : 0);  // store, [prefill], decode
+    // groups can have partial slots to combine only with split-KV or shared prefixes
+    h.use_merge = (cfg->enable_split_kv || h.use_cascade) ? 1 : 0;
+    // store, [prefill / prefix pass], decode, [combine]
+    h.kernels_per_forward = 2 + ((h.use_prefill || h.use_cascade) ? 1 : 0) + h.use_merge;
 
     PrepareParams pp{};
     pp.cu = cu_seqlens_q;
@@ -270,8 +274,10 @@ pva_status attn_forward(const pva_meta* meta, const void* q, const void* k, cons
     if (mark(1) != cudaSuccess) return PVA_ERR_CUDA;
     if ((h->use_prefill || h->use_cascade) && launch_prefill(fp, h->cfg.head_dim, h->pre_ctas, s) != cudaSuccess)
         return PVA_ERR_CUDA;
-    if (mark(2) != cudaSuccess || mark(3) != cudaSuccess) return PVA_ERR_CUDA;
+    if (mark(2) != cudaSuccess) return PVA_ERR_CUDA;
     if (launch_decode(fp, h->cfg.head_dim, h->dec_ctas, s) != cudaSuccess) return PVA_ERR_CUDA;
+    if (mark(3) != cudaSuccess) return PVA_ERR_CUDA;
+    if (h->use_merge && launch_merge(fp, h->cfg.head_dim, h->sm_count, s) != cudaSuccess) return PVA_ERR_CUDA;
     if (mark(4) != cudaSuccess) return PVA_ERR_CUDA;
     return PVA_OK;
 }

@@ -1,5 +1,5 @@
-// K3 + K4: decode / small-row attention streaming the paged KV pool, with the
-// split-KV log-sum-exp combine fused as a "last CTA to finish merges" epilogue.
+// K3 + K4: decode / small-row attention streaming the paged KV pool, and the
+// split-KV log-sum-exp combine as a small kernel right after it.
 //
 // What it computes is the ch. 5 reference forward ("The attention backend and
 // a reference implementation", section "Variable-length, paged attention with
@@ -25,12 +25,15 @@
 //     softmax in registers.  The tcgen05 tensor core's smallest M (64) would
 //     leave >= 87% of its rows idle here; the warp MMA keeps the CUDA cores
 //     free so the kernel stays bound by HBM, not by issue slots;
-//   * split groups write fp32 partial (O, LSE) to the workspace; the CTA that
-//     finishes a group's last split (atomic arrival count, no waiting) merges
-//     them: lse = log sum_s exp(lse_s), o = sum_s exp(lse_s - lse) o_s.  For a
-//     member of a shared-prefix group the units cover only the keys after the
-//     prefix, and the merge also takes the prefix-pass partials that the
-//     tensor-core kernel (launched before this one on the same stream) wrote.
+//   * split groups write fp32 partial (O, LSE) to the workspace and the CTA
+//     moves straight on (no fence, no arrival count, no waiting); the merge
+//     kernel then combines every group: lse = log sum_s exp(lse_s),
+//     o = sum_s exp(lse_s - lse) o_s.  For a member of a shared-prefix group the
+//     units cover only the keys after the prefix, and the merge also takes the
+//     prefix-pass partials that the tensor-core kernel wrote.  A merge inside the
+//     decode kernel (by the CTA finishing a group last) kept that CTA's
+//     consumers from the ring for the whole combine, and the arrival protocol
+//     stalled every split unit on a fence and an atomic round trip.
 // Every wait is bounded (PVA_DEVERR_TIMEOUT, then the CTA drains its copies
 // and leaves); nothing traps.
 #include <cuda_runtime.h>
@@ -60,7 +63,6 @@ struct DecSmemHead {
     uint64_t full[8];
     uint64_t empty[8];
     StageInfo info[8];
-    int32_t last_flag;
     int32_t abort_flag;
 };
 
@@ -85,8 +87,14 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row_bytes = HB * D * 2;
     const int stage_bytes = 2 * kStageKeys * row_stride;
+    // Plan from the prepare kernel (finished before the store kernel began); pool rows,
+    // the work counter and the prefix-pass partials only after grid_dep_wait.
+    dev::grid_dep_launch();
     const int n_units = hdr->n_dec_units * n_hb;
-    if ((hdr->error_bits & kErrFatal) || n_units == 0) return;
+    if ((hdr->error_bits & kErrFatal) || n_units == 0) {
+        dev::grid_dep_wait();
+        return;
+    }
 
     // zero the ring once so rows past a range's end are finite (they are masked,
     // and 0 * finite stays 0 in the P V product)
@@ -98,11 +106,11 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
             dev::mbar_init(&sh->empty[s], HB);
         }
         sh->abort_flag = 0;
-        sh->last_flag = 0;
         dev::fence_barrier_init();
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
+    dev::grid_dep_wait();
 
     const DecUnit* units = reinterpret_cast<const DecUnit*>(p.ws + p.lay.dec_units);
     int32_t* sched = &hdr->pad[0];
@@ -389,7 +397,9 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
             continue;
         }
 
-        // split group: fp32 partial (normalised O, log2-domain LSE) into its slot
+        // split group: fp32 partial (normalised O, log2-domain LSE) into its slot; the
+        // merge kernel that follows combines the group's slots.  Plain stores: nothing
+        // in this kernel reads them back, so the consumers move on to the next unit.
         const int slot = si.pbase + si.split;
         float* po = reinterpret_cast<float*>(p.ws + p.lay.partial_o) + (int64_t)slot * p.lay.rows_per_slot * D;
         float* pl = reinterpret_cast<float*>(p.ws + p.lay.partial_lse) + (int64_t)slot * p.lay.rows_per_slot;
@@ -405,52 +415,93 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
                     make_float2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
             if (cq == 0) pl[prow] = half ? lse1 : lse0;
         }
-        __threadfence();
-        dev::named_bar_sync(1, consumer_threads);
-        uint32_t* counters = reinterpret_cast<uint32_t*>(p.ws + p.lay.counters);
-        if (threadIdx.x == 0) {
-            const uint32_t prev = atomicAdd(&counters[si.group], 1u);
-            sh->last_flag = (prev == (uint32_t)(si.nsplit * n_hb - 1));
-            if (sh->last_flag) {
-                counters[si.group] = 0;  // ready for the next forward on this plan
-                __threadfence();
-            }
-        }
-        dev::named_bar_sync(1, consumer_threads);
-        if (sh->last_flag) {
-            // merge the group's splits: rows (token, q head), 4 columns per thread item
-            const int grows = si.ntok * Hq;
-            const float* pob =
-                reinterpret_cast<const float*>(p.ws + p.lay.partial_o) + (int64_t)si.pbase * p.lay.rows_per_slot * D;
-            const float* plb =
-                reinterpret_cast<const float*>(p.ws + p.lay.partial_lse) + (int64_t)si.pbase * p.lay.rows_per_slot;
-            const int items = grows * (D / 4);
-            for (int it = threadIdx.x; it < items; it += consumer_threads) {
-                const int row = it / (D / 4), c4 = (it % (D / 4)) * 4;
-                float mx = -INFINITY;
-                for (int sp = 0; sp < si.nparts; ++sp) mx = fmaxf(mx, __ldcg(plb + sp * p.lay.rows_per_slot + row));
-                const float mu = mx == -INFINITY ? 0.f : mx;
-                float wsum = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-                for (int sp = 0; sp < si.nparts; ++sp) {
-                    const float w = dev::fast_exp2(__ldcg(plb + sp * p.lay.rows_per_slot + row) - mu);
-                    const float4 v =
-                        __ldcg(reinterpret_cast<const float4*>(pob + ((int64_t)sp * p.lay.rows_per_slot + row) * D + c4));
-                    wsum += w;
-                    a0 += w * v.x;
-                    a1 += w * v.y;
-                    a2 += w * v.z;
-                    a3 += w * v.w;
+    }
+}
+
+// K4: log-sum-exp combine of the split groups (and of the prefix-pass partials of
+// shared-prefix members): for every row (token, q head) of a group with nparts > 1,
+// lse = log2 sum_s 2^lse_s, o = sum_s 2^(lse_s - lse) o_s over the group's slots
+// pbase .. pbase + nparts - 1, in slot order (deterministic).  One warp per row: lane s
+// holds part s's LSE, so the maximum and the normaliser are two warp reductions, and
+// lane c accumulates columns [c * D/32, (c+1) * D/32) of every part with independent
+// loads (the partials are L2-resident: written by the kernels just before).  Launched
+// programmatically after the decode kernel, whose grid it waits for.
+constexpr int kMergeThreads = 1024;
+
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(ForwardParams p) {
+    constexpr int kPer = D / 32;  // output columns per lane
+    dev::grid_dep_launch();
+    PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws + p.lay.header);
+    const int n_groups = hdr->n_dec_groups;
+    if ((hdr->error_bits & kErrFatal) || n_groups == 0 || hdr->n_partial_slots == 0) {
+        dev::grid_dep_wait();
+        return;
+    }
+    dev::grid_dep_wait();
+    const DecGroup* groups = reinterpret_cast<const DecGroup*>(p.ws + p.lay.dec_groups);
+    const float* plse = reinterpret_cast<const float*>(p.ws + p.lay.partial_lse);
+    const float* pout = reinterpret_cast<const float*>(p.ws + p.lay.partial_o);
+    const int rps = p.lay.rows_per_slot, Hq = p.num_qo_heads;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int gi = blockIdx.x; gi < n_groups; gi += gridDim.x) {
+        const DecGroup dg = groups[gi];
+        const int np = dg.nparts;
+        if (np <= 1) continue;
+        const int rows = dg.ntok * Hq;
+        const float* plb = plse + (int64_t)dg.pbase * rps;
+        const float* pob = pout + (int64_t)dg.pbase * rps * D;
+        for (int row = warp; row < rows; row += kMergeThreads / 32) {
+            const float lfirst = lane < np ? __ldcg(plb + (int64_t)lane * rps + row) : -INFINITY;
+            float mx = lfirst;
+            for (int s0 = 32; s0 < np; s0 += 32)
+                if (s0 + lane < np) mx = fmaxf(mx, __ldcg(plb + (int64_t)(s0 + lane) * rps + row));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            const float mu = mx == -INFINITY ? 0.f : mx;
+            float acc[kPer];
+#pragma unroll
+            for (int c = 0; c < kPer; ++c) acc[c] = 0.f;
+            float wsum = 0.f;
+            for (int s0 = 0; s0 < np; s0 += 32) {
+                const float l = s0 == 0 ? lfirst : (s0 + lane < np ? __ldcg(plb + (int64_t)(s0 + lane) * rps + row)
+                                                                    : -INFINITY);
+                const float w = dev::fast_exp2(l - mu);  // 0 for an empty part (lse -inf)
+                wsum += w;
+                const int cnt = min(32, np - s0);
+                const float* src = pob + ((int64_t)s0 * rps + row) * D + lane * kPer;
+#pragma unroll 8
+                for (int k = 0; k < cnt; ++k) {
+                    const float wk = __shfl_sync(0xffffffffu, w, k);
+                    const float* sp = src + (int64_t)k * rps * D;
+                    if constexpr (kPer == 4) {
+                        const float4 v = __ldcg(reinterpret_cast<const float4*>(sp));
+                        acc[0] += wk * v.x;
+                        acc[1] += wk * v.y;
+                        acc[2] += wk * v.z;
+                        acc[3] += wk * v.w;
+                    } else {
+                        const float2 v = __ldcg(reinterpret_cast<const float2*>(sp));
+                        acc[0] += wk * v.x;
+                        acc[1] += wk * v.y;
+                    }
                 }
-                const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-                const int64_t orow = (int64_t)(si.tok0 + row / Hq) * Hq + row % Hq;
-                uint2 packed;
-                packed.x = dev::pack_bf16x2(a0 * inv, a1 * inv);
-                packed.y = dev::pack_bf16x2(a2 * inv, a3 * inv);
-                *reinterpret_cast<uint2*>(p.out + orow * D + c4) = packed;
-                if (p.lse != nullptr && c4 == 0) p.lse[orow] = wsum > 0.f ? (mu + __log2f(wsum)) * kLn2 : -INFINITY;
             }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+            const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+            const int64_t orow = (int64_t)(dg.tok0 + row / Hq) * Hq + row % Hq;
+            uint16_t* dst = p.out + orow * D + lane * kPer;
+            if constexpr (kPer == 4) {
+                uint2 packed;
+                packed.x = dev::pack_bf16x2(acc[0] * inv, acc[1] * inv);
+                packed.y = dev::pack_bf16x2(acc[2] * inv, acc[3] * inv);
+                *reinterpret_cast<uint2*>(dst) = packed;
+            } else {
+                *reinterpret_cast<uint32_t*>(dst) = dev::pack_bf16x2(acc[0] * inv, acc[1] * inv);
+            }
+            if (p.lse != nullptr && lane == 0) p.lse[orow] = wsum > 0.f ? (mu + __log2f(wsum)) * kLn2 : -INFINITY;
         }
-        dev::named_bar_sync(1, consumer_threads);
     }
 }
 
@@ -480,8 +531,12 @@ cudaError_t launch_d(const ForwardParams& p, int ctas, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const int hb = p.num_kv_heads < kMaxKvHeads ? p.num_kv_heads : kMaxKvHeads;
     const int row_stride = hb * D * 2 + kRowPad;
-    decode_kernel<D><<<ctas, 32 * (hb + 1), smem, s>>>(p, stages, row_stride);
-    return cudaGetLastError();
+    return launch_programmatic(decode_kernel<D>, (unsigned)ctas, 32u * (hb + 1), smem, s, p, stages, row_stride);
+}
+
+template <int D>
+cudaError_t launch_m(const ForwardParams& p, int ctas, cudaStream_t s) {
+    return launch_programmatic(merge_kernel<D>, (unsigned)ctas, (unsigned)kMergeThreads, 0, s, p);
 }
 
 }  // namespace
@@ -504,6 +559,12 @@ bool decode_supported(int num_qo_heads, int num_kv_heads, int head_dim) {
 cudaError_t launch_decode(const ForwardParams& p, int head_dim, int ctas, cudaStream_t s) {
     if (head_dim == 128) return launch_d<128>(p, ctas, s);
     if (head_dim == 64) return launch_d<64>(p, ctas, s);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_merge(const ForwardParams& p, int head_dim, int ctas, cudaStream_t s) {
+    if (head_dim == 128) return launch_m<128>(p, ctas, s);
+    if (head_dim == 64) return launch_m<64>(p, ctas, s);
     return cudaErrorInvalidValue;
 }
 

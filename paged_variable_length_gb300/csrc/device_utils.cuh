@@ -170,5 +170,15 @@ __device__ __forceinline__ int4 ld_stream_v4(const void* p) {
 
 __device__ __forceinline__ void set_error(uint32_t* word, uint32_t bits) { atomicOr(word, bits); }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// Let the next kernel of the stream (launched with programmatic stream serialization)
+// start its CTAs while this grid still runs; they stop at grid_dep_wait.
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Wait until the grid this kernel depends on has finished and its writes are visible.
+// A kernel launched without the attribute returns at once.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 }  // namespace dev
 }  // namespace pva

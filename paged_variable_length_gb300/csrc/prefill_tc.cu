@@ -149,8 +149,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     Bars* b = &bars;
     PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws + p.lay.header);
     uint32_t* err = &hdr->error_bits;
+    // The plan was written by the prepare kernel, which finished before the store
+    // kernel began; the pool rows and the work counter come from the store kernel, which
+    // may still run (programmatic launch): they are read only after grid_dep_wait.  An
+    // idle CTA waits too, so that this grid never completes before its predecessor.
+    dev::grid_dep_launch();
     const int n_units = hdr->n_pre_tiles;
-    if ((hdr->error_bits & kErrFatal) || n_units == 0 || (int)blockIdx.x >= n_units) return;
+    if ((hdr->error_bits & kErrFatal) || n_units == 0 || (int)blockIdx.x >= n_units) {
+        dev::grid_dep_wait();
+        return;
+    }
     const PreTile* units = reinterpret_cast<const PreTile*>(p.ws + p.lay.pre_tiles);
     int32_t* counter = &hdr->pad[1];  // zeroed by the store kernel of this forward
     const DecGroup* groups = reinterpret_cast<const DecGroup*>(p.ws + p.lay.dec_groups);
@@ -193,6 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = b->tmem_base;
+    dev::grid_dep_wait();
 
     if (warp >= 8) {
         // control warpgroups: give registers to the softmax warpgroups
@@ -575,8 +584,7 @@ cudaError_t launch_p(const ForwardParams& p, int ctas, cudaStream_t s) {
         launch_regs = attr.numRegs;
     }
     if (launch_regs != kRegsLaunch) return cudaErrorInvalidConfiguration;
-    prefill_kernel<D><<<ctas, kThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_programmatic(prefill_kernel<D>, (unsigned)ctas, (unsigned)kThreads, smem, s, p);
 }
 
 }  // namespace

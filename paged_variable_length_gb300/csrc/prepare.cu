@@ -31,21 +31,29 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBuckets = 256;  // cost classes for the longest-first ordering of work items
+constexpr int kCmpPages = 8;   // page ids one thread compares per step of the shared-prefix search
 
-// Per-request shared-memory arrays (dynamic shared memory, batch <= smem_batch).
-enum SmemArray { kCu = 0, kLen, kToff, kFirst, kLeader, kLcp, kCnt, kCgid, kGoff, kMpos, kNumArrays };
+// Per-request shared-memory arrays (dynamic shared memory, batch <= smem_batch), followed
+// by the open-addressing table of the shared-prefix search when cascade detection runs.
+enum SmemArray { kCu = 0, kLen, kToff, kFirst, kLeader, kLcp, kCnt, kCgid, kGoff, kMpos, kCUoff, kNumArrays };
 
-// atomicAdd(addr, 1) for every active lane, with one atomic per distinct key in the
-// warp (lanes incrementing the same bucket share one); returns the lane's old value.
-__device__ __forceinline__ int warp_agg_inc(int* addr, int key) {
-    const unsigned active = __activemask();
-    const unsigned peers = __match_any_sync(active, key);
-    const int lane = threadIdx.x & 31;
-    const int leader = __ffs(peers) - 1;
-    int base = 0;
-    if (lane == leader) base = atomicAdd(addr, __popc(peers));
-    base = __shfl_sync(peers, base, leader);
-    return base + __popc(peers & ((1u << lane) - 1u));
+// Write a plan record as whole 16-byte words (a record is 32, 48 or 64 bytes, and the
+// record arrays start on 256-byte boundaries): one 16-byte store per word instead of
+// one 4-byte store per field keeps the single CTA's store traffic in few L2
+// transactions.
+template <class T>
+__device__ __forceinline__ void store_record(T* dst, const T& v) {
+    static_assert(sizeof(T) % 16 == 0, "records are whole 16-byte words");
+    int4 w[sizeof(T) / 16];
+    memcpy(w, &v, sizeof(T));
+    int4* d = reinterpret_cast<int4*>(dst);
+#pragma unroll
+    for (int k = 0; k < (int)(sizeof(T) / 16); ++k) d[k] = w[k];
+}
+
+// Fibonacci hashing of a page id into a table of 2^bits entries.
+__device__ __forceinline__ uint32_t page_hash(int32_t page, int bits) {
+    return ((uint32_t)page * 2654435761u) >> (32 - bits);
 }
 
 // Exclusive scan of N counters across the block; each thread contributes v[k].
@@ -90,7 +98,8 @@ __device__ void block_scan(int (&v)[N], int (&total)[N], int (*warp_tmp)[N]) {
     __syncthreads();
 }
 
-// Index i with off[i] <= x < off[i+1] (off ascending, off[0] <= x).
+// Index i with off[i] <= x < off[i+1] (off ascending, off[0] <= x); among equal offsets
+// the last one, so that entries of width zero are passed over.
 __device__ __forceinline__ int find_bucket(const int32_t* off, int count, int x) {
     int lo = 0, hi = count - 1;
     while (lo < hi) {
@@ -108,12 +117,16 @@ __device__ __forceinline__ bool is_group_leader(const int32_t* leader, const int
     return leader[i] == i && cnt[i] >= 2 && lcp[i] >= min_pages;
 }
 
+// Prefix-pass units of a group with m members: pairs of member tiles x kv heads.
+__device__ __forceinline__ int casc_pair_units(int members, int TM, int Hkv) {
+    return (((members + TM - 1) / TM) + 1) / 2 * Hkv;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws + p.lay.header);
     DecUnit* units = reinterpret_cast<DecUnit*>(p.ws + p.lay.dec_units);
     DecGroup* groups = reinterpret_cast<DecGroup*>(p.ws + p.lay.dec_groups);
     PreTile* tiles = reinterpret_cast<PreTile*>(p.ws + p.lay.pre_tiles);
-    uint32_t* counters = reinterpret_cast<uint32_t*>(p.ws + p.lay.counters);
     CascGroup* cgroups = reinterpret_cast<CascGroup*>(p.ws + p.lay.casc_groups);
     int32_t* cmembers = reinterpret_cast<int32_t*>(p.ws + p.lay.casc_members);
 
@@ -122,9 +135,10 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     __shared__ unsigned long long s_work;
     __shared__ int s_tmp3[kWarps][3];
     __shared__ int s_tmp2[kWarps][2];
+    __shared__ int s_tmp1[kWarps][1];
     __shared__ int s_hist_u[kBuckets];
     __shared__ int s_hist_t[kBuckets];
-    __shared__ int s_ngroups, s_casc_units;
+    __shared__ int s_casc_units;
 
     const int tid = threadIdx.x;
     const int B = p.batch;
@@ -137,7 +151,6 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     if (tid == 0) {
         s_err = 0;
         s_work = 0;
-        s_ngroups = 0;
         s_casc_units = 0;
     }
     if (small) {
@@ -151,52 +164,122 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     const int32_t* cu = small ? sa[kCu] : p.cu;
     const int32_t* lens = small ? sa[kLen] : p.seqlens;
     auto valid_req = [&](int n, int L) { return n >= 0 && n <= L && L <= p.max_kv_len && n <= p.max_q_len; };
+    // each thread owns a contiguous run of requests for the counting passes
+    const int chunk_req = (B + kThreads - 1) / kThreads;
+    const int r0 = min(B, tid * chunk_req), r1 = min(B, r0 + chunk_req);
 
     // ---- pass 0: shared-prefix groups among single-token decodes.  Requests are keyed
-    // by their first page; the first request with a key leads its group; the group's
-    // prefix is the run of pages every member shares with the leader (whole pages that
-    // lie strictly before each member's query, so no causal mask ever applies to it).
+    // by their first page; the lowest-numbered request with a key leads its group; the
+    // group's prefix is the run of pages every member shares with the leader (whole pages
+    // that lie strictly before each member's query, so no causal mask ever applies to it).
     const bool casc = p.use_cascade && small && B >= 2;
+    int n_cgroups = 0;
     if (casc) {
         int32_t* first = sa[kFirst];
         int32_t* leader = sa[kLeader];
         int32_t* lcp = sa[kLcp];
         int32_t* cnt = sa[kCnt];
+        int32_t* lim = sa[kMpos];   // pages compared per member (until the groups are numbered)
+        int32_t* boff = sa[kToff];  // first compare block of each member (until pass 1)
+        const int hbits = casc_hash_bits(p.smem_batch);
+        const int HT = 1 << hbits;  // > 2 * batch: the probe below always meets a free entry
+        int32_t* hkey = dyn + kNumArrays * stride;
+        int32_t* hval = hkey + HT;
+        for (int h = tid; h < HT; h += kThreads) {
+            hkey[h] = -1;
+            hval[h] = 0x7fffffff;
+        }
         for (int i = tid; i < B; i += kThreads) {
             const int n = cu[i + 1] - cu[i], L = lens[i];
-            const int pages = (L - n) / ps;  // whole pages strictly before the query
-            const bool cand = n == 1 && valid_req(n, L) && pages >= p.min_cascade_pages;
-            const int f = cand ? p.page_table[(int64_t)i * p.ld] : -1;
-            first[i] = (cand && f >= 0) ? f : -1;
-            lcp[i] = cand ? pages : 0;
+            const bool ok = n == 1 && valid_req(n, L);
+            const int pages = ok ? (L - n) / ps : 0;  // whole pages strictly before the query
+            const int f = (ok && pages >= p.min_cascade_pages) ? p.page_table[(int64_t)i * p.ld] : -1;
+            first[i] = (f >= 0 && f < p.num_pages) ? f : -1;
+            lcp[i] = pages;
             cnt[i] = 0;
+            leader[i] = -1;
         }
         __syncthreads();
         for (int i = tid; i < B; i += kThreads) {
-            int ld = -1;
-            if (first[i] >= 0)
-                for (int j = 0; j <= i && ld < 0; ++j)
-                    if (first[j] == first[i]) ld = j;
+            const int f = first[i];
+            if (f < 0) continue;
+            uint32_t h = page_hash(f, hbits);
+            while (true) {
+                const int prev = atomicCAS(&hkey[h], -1, f);
+                if (prev == -1 || prev == f) break;
+                h = (h + 1) & (HT - 1);
+            }
+            atomicMin(&hval[h], i);
+            leader[i] = (int)h;
+        }
+        __syncthreads();
+        for (int i = tid; i < B; i += kThreads) {
+            if (first[i] < 0) continue;
+            const int ld = hval[leader[i]];
             leader[i] = ld;
+            atomicAdd(&cnt[ld], 1);
         }
         __syncthreads();
-        for (int i = tid; i < B; i += kThreads) {
+        // every member compares pages 1 .. lim-1 of its row with the leader's, in blocks
+        // of kCmpPages spread over the whole CTA; the group prefix is the smallest
+        // mismatch (or the smallest member's page count)
+        int nb[1] = {0};
+        for (int i = r0; i < r1; ++i) {
             const int ld = leader[i];
-            if (ld < 0) continue;
-            atomicAdd(&cnt[ld], 1);
-            if (ld == i) continue;
-            const int lim = min(lcp[i], lcp[ld]);
+            int l = 0;
+            if (ld >= 0 && ld != i) {
+                l = min(lcp[i], lcp[ld]);
+                nb[0] += (l - 1 + kCmpPages - 1) / kCmpPages;
+            }
+            lim[i] = l;
+        }
+        int nbt[1];
+        block_scan<1>(nb, nbt, s_tmp1);
+        {
+            int off = nb[0];
+            for (int i = r0; i < r1; ++i) {
+                boff[i] = off;
+                const int l = lim[i];
+                if (l > 0) {
+                    off += (l - 1 + kCmpPages - 1) / kCmpPages;
+                    atomicMin(&lcp[leader[i]], l);
+                }
+            }
+        }
+        __syncthreads();
+        for (int x = tid; x < nbt[0]; x += kThreads) {
+            const int i = find_bucket(boff, B, x);
+            const int ld = leader[i];
+            const int k0 = 1 + (x - boff[i]) * kCmpPages;
+            const int k1 = min(lim[i], k0 + kCmpPages);
             const int32_t* ri = p.page_table + (int64_t)i * p.ld;
             const int32_t* rl = p.page_table + (int64_t)ld * p.ld;
-            int k = 1;
-            while (k < lim && ri[k] == rl[k]) ++k;
-            atomicMin(&lcp[ld], k);
+            int a[kCmpPages], b[kCmpPages];
+#pragma unroll
+            for (int k = 0; k < kCmpPages; ++k) {
+                const bool in = k0 + k < k1;
+                a[k] = in ? ri[k0 + k] : 0;
+                b[k] = in ? rl[k0 + k] : 0;
+            }
+            int mis = k1;
+#pragma unroll
+            for (int k = kCmpPages - 1; k >= 0; --k)
+                if (k0 + k < k1 && a[k] != b[k]) mis = k0 + k;
+            if (mis < k1) atomicMin(&lcp[ld], mis);
         }
         __syncthreads();
-        // group ids in leader order (a deterministic plan); member slots per group
-        if (tid == 0) {
-            int gid = 0, moff = 0;
-            for (int i = 0; i < B; ++i) {
+        // group ids in leader order (a deterministic plan) and member slot ranges
+        int gv[2] = {0, 0};
+        for (int i = r0; i < r1; ++i)
+            if (is_group_leader(leader, cnt, lcp, i, p.min_cascade_pages)) {
+                gv[0] += 1;
+                gv[1] += cnt[i];
+            }
+        int gt[2];
+        block_scan<2>(gv, gt, s_tmp2);
+        {
+            int gid = gv[0], moff = gv[1];
+            for (int i = r0; i < r1; ++i) {
                 if (!is_group_leader(leader, cnt, lcp, i, p.min_cascade_pages)) continue;
                 sa[kCgid][i] = gid;
                 CascGroup cg;
@@ -208,20 +291,19 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
                 cg.chunk_keys = 0;
                 cg.unit_off = 0;
                 cg.n_units = 0;
-                cgroups[gid] = cg;
+                store_record(&cgroups[gid], cg);
                 sa[kMpos][i] = moff;  // next free member slot of the group
                 moff += cnt[i];
                 ++gid;
             }
-            s_ngroups = gid;
         }
+        n_cgroups = gt[0];
         __syncthreads();
         // members take the group id of their leader (-1 when the leader leads no group)
         for (int i = tid; i < B; i += kThreads) {
             const int ld = leader[i];
-            if (ld >= 0 && ld != i) sa[kCgid][i] = is_group_leader(leader, cnt, lcp, ld, p.min_cascade_pages)
-                                                       ? sa[kCgid][ld]
-                                                       : -1;
+            if (ld >= 0 && ld != i)
+                sa[kCgid][i] = is_group_leader(leader, cnt, lcp, ld, p.min_cascade_pages) ? sa[kCgid][ld] : -1;
         }
         __syncthreads();
     }
@@ -231,9 +313,6 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         const int g = casc_of(i);
         return g >= 0 ? cgroups[g].prefix_len : 0;
     };
-
-    const int chunk_req = (B + kThreads - 1) / kThreads;
-    const int r0 = min(B, tid * chunk_req), r1 = min(B, r0 + chunk_req);
 
     // ---- pass 1: validate, count decode groups and prefill tiles, sum decode key extents
     uint32_t err = 0;
@@ -281,38 +360,51 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         }
         if (tid == 0) tile_off[B] = tot3[1];
     }
-    __syncthreads();
 
-    // ---- cascade groups: key chunks of each prefix, prefix-pass units, member lists
-    if (casc && tid == 0) {
-        const int ng = s_ngroups;
-        // about casc_target prefix units in total (roughly one per SM)
-        int pair_units = 0;
-        for (int g = 0; g < ng; ++g) pair_units += (((cgroups[g].n_members + TM - 1) / TM) + 1) / 2 * Hkv;
-        int uoff = 0;
-        for (int g = 0; g < ng; ++g) {
+    // ---- cascade groups: key chunks of each prefix (about casc_target prefix-pass units
+    // in total, roughly one per SM), unit ranges, member lists
+    if (casc) {
+        const int ng = n_cgroups;
+        const int gch = (ng + kThreads - 1) / kThreads;
+        const int g0 = min(ng, tid * gch), g1 = min(ng, g0 + gch);
+        int pv[1] = {0};
+        for (int g = g0; g < g1; ++g) pv[0] += casc_pair_units(cgroups[g].n_members, TM, Hkv);
+        int pt[1];
+        block_scan<1>(pv, pt, s_tmp1);
+        const int pair_units = max(pt[0], 1);
+        int uv[1] = {0};
+        for (int g = g0; g < g1; ++g) {
+            const CascGroup cg = cgroups[g];
+            int nc = (p.lay.casc_target + pair_units - 1) / pair_units;
+            nc = max(1, min(nc, min(kMaxCascChunks, (cg.prefix_len + kPreKeys - 1) / kPreKeys)));
+            const int ck = ((cg.prefix_len + nc - 1) / nc + kPreKeys - 1) / kPreKeys * kPreKeys;
+            uv[0] += (cg.prefix_len + ck - 1) / ck * casc_pair_units(cg.n_members, TM, Hkv);
+        }
+        int ut[1];
+        block_scan<1>(uv, ut, s_tmp1);
+        int uoff = uv[0];
+        for (int g = g0; g < g1; ++g) {
             CascGroup cg = cgroups[g];
-            const int pu = (((cg.n_members + TM - 1) / TM) + 1) / 2 * Hkv;
-            int nc = (p.lay.casc_target + pair_units - 1) / max(pair_units, 1);
+            int nc = (p.lay.casc_target + pair_units - 1) / pair_units;
             nc = max(1, min(nc, min(kMaxCascChunks, (cg.prefix_len + kPreKeys - 1) / kPreKeys)));
             const int ck = ((cg.prefix_len + nc - 1) / nc + kPreKeys - 1) / kPreKeys * kPreKeys;
             cg.chunk_keys = ck;
             cg.n_chunks = (cg.prefix_len + ck - 1) / ck;
             cg.unit_off = uoff;
-            cg.n_units = cg.n_chunks * pu;
+            cg.n_units = cg.n_chunks * casc_pair_units(cg.n_members, TM, Hkv);
+            sa[kCUoff][g] = uoff;
             uoff += cg.n_units;
-            cgroups[g] = cg;
+            store_record(&cgroups[g], cg);
         }
-        s_casc_units = uoff;
-    }
-    __syncthreads();
-    if (casc) {
+        if (tid == 0) s_casc_units = ut[0];
+        // members are listed by their decode group (a member has one new token, so exactly one)
         for (int i = tid; i < B; i += kThreads) {
             if (sa[kCgid][i] < 0) continue;
             const int slot = atomicAdd(&sa[kMpos][sa[kLeader][i]], 1);
-            cmembers[slot] = sa[kGoff][i];  // a member (one new token) has exactly one decode group
+            cmembers[slot] = sa[kGoff][i];
         }
     }
+    __syncthreads();
     const int tiles_total = tot3[1] + s_casc_units;
     if (tot3[0] > p.lay.max_dec_groups || tiles_total > p.lay.max_pre_tiles) {
         if (tid == 0) atomicOr(&s_err, kErrLimits);
@@ -328,7 +420,13 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         chunk = (int)(c > (unsigned long long)kMinSplitChunk ? c : (unsigned long long)kMinSplitChunk);
     }
 
-    // ---- pass 2: units and partial slots per thread's requests
+    // ---- pass 2: units and partial slots per thread's requests, and the unit cost
+    // histogram (a group's units all have length `per` but the last)
+    for (int b = tid; b < kBuckets; b += kThreads) {
+        s_hist_u[b] = 0;
+        s_hist_t[b] = 0;
+    }
+    __syncthreads();
     int cnt2[2] = {0, 0};  // units, partial slots
     if (!fatal) {
         for (int i = r0; i < r1; ++i) {
@@ -344,162 +442,154 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
                 const int nparts = s + (cg >= 0 ? cgroups[cg].n_chunks : 0);
                 cnt2[0] += s;
                 if (nparts > 1) cnt2[1] += nparts;
+                const int last = max(0, ext - (s - 1) * per);
+                if (s <= 0) continue;
+                if (s > 1) atomicAdd(&s_hist_u[cost_bucket(per / kDecKeysPerStage)], s - 1);
+                atomicAdd(&s_hist_u[cost_bucket((last + kDecKeysPerStage - 1) / kDecKeysPerStage)], 1);
             }
         }
     }
     int tot2[2];
     block_scan<2>(cnt2, tot2, s_tmp2);
-    if (tot2[0] > p.lay.max_dec_units || tot2[1] > p.lay.max_partial) {
-        if (tid == 0) atomicOr(&s_err, kErrLimits);
+    const bool over = tot2[0] > p.lay.max_dec_units || tot2[1] > p.lay.max_partial;
+    if (over && tid == 0) atomicOr(&s_err, kErrLimits);
+    const bool run = !fatal && !over;
+
+    // tile pair / prefix-pass unit x -> its record and cost
+    auto make_tile = [&](int x, PreTile& pt) -> int {
+        if (x < tot3[1]) {  // (request, pair of Q tiles, kv head)
+            const int i = find_bucket(tile_off, B, x);
+            const int lx = x - tile_off[i];
+            const int c0 = cu[i], n = cu[i + 1] - c0, L = lens[i];
+            const int nt = (n + TM - 1) / TM;
+            const int t = 2 * (lx / Hkv), h = lx % Hkv;  // Q tiles t and t+1
+            const int a0 = t * TM, na0 = min(TM, n - a0);
+            const int na1 = t + 1 < nt ? min(TM, n - a0 - TM) : 0;
+            pt.req = i;
+            pt.kvh = h;
+            pt.tok0 = c0 + a0;
+            pt.ntok0 = na0;
+            pt.ntok1 = na1;
+            pt.qpos0 = L - n + a0;
+            pt.kv_end0 = L - n + a0 + na0;
+            pt.kv_end1 = na1 > 0 ? pt.kv_end0 + na1 : pt.kv_end0;
+            return (pt.kv_end1 + kPreKeys - 1) / kPreKeys;
+        }
+        // (cascade group, key chunk, pair of member tiles, kv head)
+        const int y = x - tot3[1];
+        const int g = find_bucket(sa[kCUoff], n_cgroups, y);
+        const CascGroup cgr = cgroups[g];
+        const int ly = y - cgr.unit_off;
+        const int pu = casc_pair_units(cgr.n_members, TM, Hkv);
+        const int c = ly / pu, rest = ly % pu;
+        const int pair = rest / Hkv, h = rest % Hkv;
+        const int m0 = pair * 2 * TM;
+        pt.req = -1 - g;
+        pt.kvh = h;
+        pt.tok0 = cgr.member_off + m0;
+        pt.ntok0 = min(TM, cgr.n_members - m0);
+        pt.ntok1 = max(0, min(TM, cgr.n_members - m0 - TM));
+        pt.qpos0 = c;
+        pt.kv_end0 = c * cgr.chunk_keys;
+        pt.kv_end1 = min(cgr.prefix_len, (c + 1) * cgr.chunk_keys);
+        return (pt.kv_end1 - pt.kv_end0 + kPreKeys - 1) / kPreKeys;
+    };
+    if (run) {
+        for (int x = tid; x < tiles_total; x += kThreads) {
+            PreTile pt;
+            atomicAdd(&s_hist_t[cost_bucket(make_tile(x, pt))], 1);
+        }
     }
     __syncthreads();
-    const bool run = (s_err & kErrFatal) == 0;
 
     // ---- pass 3: write groups; units and tiles go out longest first (a counting sort on
     // their cost), so that the kernels' in-order work fetch ends with the short items and
     // the grid finishes together (longest-processing-time-first).  The position of a
     // unit in the list never changes a result: each split writes its own partial slot and
     // the merge walks the slots in split order.
-    for (int b = tid; b < kBuckets; b += kThreads) {
-        s_hist_u[b] = 0;
-        s_hist_t[b] = 0;
+    if (tid < 32) {  // bucket counts -> first position of each bucket (bucket 0 = costliest)
+        constexpr int kPer = kBuckets / 32;
+        int su = 0, st = 0;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            su += s_hist_u[tid * kPer + k];
+            st += s_hist_t[tid * kPer + k];
+        }
+        int iu = su, itt = st;  // inclusive warp scan
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int yu = __shfl_up_sync(0xffffffffu, iu, o), yt = __shfl_up_sync(0xffffffffu, itt, o);
+            if (tid >= o) {
+                iu += yu;
+                itt += yt;
+            }
+        }
+        int au = iu - su, at = itt - st;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int cu_ = s_hist_u[tid * kPer + k], ct = s_hist_t[tid * kPer + k];
+            s_hist_u[tid * kPer + k] = au;
+            s_hist_t[tid * kPer + k] = at;
+            au += cu_;
+            at += ct;
+        }
     }
     __syncthreads();
-    for (int emit = 0; emit < 2; ++emit) {
-        if (run) {
-            int gi = cnt[0], pi = cnt2[1];
-            for (int i = r0; i < r1; ++i) {
-                const int c0 = cu[i], n = cu[i + 1] - c0, L = lens[i];
-                if (n <= 0) continue;
-                if (p.use_prefill && n > TB) continue;  // prefill units: emitted below
-                const int ng = (n + TB - 1) / TB;
-                const int lp = prefix_of(i);
-                const int cg = casc_of(i);
-                for (int g = 0; g < ng; ++g) {
-                    const int a0 = g * TB, na = min(TB, n - a0);
-                    const int kv_end = L - n + a0 + na;
-                    int per;
-                    const int s = split_ranges(kv_end - lp, chunk, &per);
-                    const int nparts = s + (cg >= 0 ? cgroups[cg].n_chunks : 0);
-                    DecGroup dg;
-                    dg.req = i;
-                    dg.tok0 = c0 + a0;
-                    dg.ntok = na;
-                    dg.qpos0 = L - n + a0;
-                    dg.nsplit = s;
-                    dg.pbase = nparts > 1 ? pi : -1;
-                    dg.kv_end = kv_end;
-                    dg.casc = cg;
-                    dg.nparts = nparts;
-                    dg.tail0 = lp;
-                    dg.pad0 = dg.pad1 = dg.pad2 = dg.pad3 = dg.pad4 = dg.pad5 = 0;
-                    if (emit) {
-                        groups[gi] = dg;
-                        counters[gi] = 0;
-                    }
-                    for (int u = 0; u < s; ++u) {
-                        DecUnit du;
-                        du.group = gi;
-                        du.k0 = min(kv_end, lp + u * per);
-                        du.k1 = min(kv_end, lp + (u + 1) * per);
-                        const int b = cost_bucket((du.k1 - du.k0 + kDecKeysPerStage - 1) / kDecKeysPerStage);
-                        if (!emit) {
-                            warp_agg_inc(&s_hist_u[b], b);
-                            continue;
-                        }
-                        du.split = u;
-                        du.req = i;
-                        du.tok0 = dg.tok0;
-                        du.ntok = dg.ntok;
-                        du.qpos0 = dg.qpos0;
-                        du.nsplit = s;
-                        du.pbase = dg.pbase;
-                        du.nparts = nparts;
-                        du.pad1 = 0;
-                        units[warp_agg_inc(&s_hist_u[b], b)] = du;
-                    }
-                    if (nparts > 1) pi += nparts;
-                    ++gi;
+    if (run) {
+        int gi = cnt[0], pi = cnt2[1];
+        for (int i = r0; i < r1; ++i) {
+            const int c0 = cu[i], n = cu[i + 1] - c0, L = lens[i];
+            if (n <= 0) continue;
+            if (p.use_prefill && n > TB) continue;  // prefill units: emitted below
+            const int ng = (n + TB - 1) / TB;
+            const int lp = prefix_of(i);
+            const int cg = casc_of(i);
+            for (int g = 0; g < ng; ++g) {
+                const int a0 = g * TB, na = min(TB, n - a0);
+                const int kv_end = L - n + a0 + na;
+                int per;
+                const int s = split_ranges(kv_end - lp, chunk, &per);
+                const int nparts = s + (cg >= 0 ? cgroups[cg].n_chunks : 0);
+                DecGroup dg;
+                dg.req = i;
+                dg.tok0 = c0 + a0;
+                dg.ntok = na;
+                dg.qpos0 = L - n + a0;
+                dg.nsplit = s;
+                dg.pbase = nparts > 1 ? pi : -1;
+                dg.kv_end = kv_end;
+                dg.casc = cg;
+                dg.nparts = nparts;
+                dg.tail0 = lp;
+                dg.pad0 = dg.pad1 = dg.pad2 = dg.pad3 = dg.pad4 = dg.pad5 = 0;
+                store_record(&groups[gi], dg);
+                for (int u = 0; u < s; ++u) {
+                    DecUnit du;
+                    du.group = gi;
+                    du.k0 = min(kv_end, lp + u * per);
+                    du.k1 = min(kv_end, lp + (u + 1) * per);
+                    du.split = u;
+                    du.req = i;
+                    du.tok0 = dg.tok0;
+                    du.ntok = dg.ntok;
+                    du.qpos0 = dg.qpos0;
+                    du.nsplit = s;
+                    du.pbase = dg.pbase;
+                    du.nparts = nparts;
+                    du.pad1 = 0;
+                    const int b = cost_bucket((du.k1 - du.k0 + kDecKeysPerStage - 1) / kDecKeysPerStage);
+                    store_record(&units[atomicAdd(&s_hist_u[b], 1)], du);
                 }
-            }
-            // prefill tile pairs, then cascade prefix units, in parallel over the unit index
-            for (int x = tid; x < tiles_total; x += kThreads) {
-                PreTile pt;
-                int cost;
-                if (x < tot3[1]) {  // unit index -> (request, pair of Q tiles, kv head)
-                    const int i = find_bucket(tile_off, B, x);
-                    const int lx = x - tile_off[i];
-                    const int c0 = cu[i], n = cu[i + 1] - c0, L = lens[i];
-                    const int nt = (n + TM - 1) / TM;
-                    const int t = 2 * (lx / Hkv), h = lx % Hkv;  // Q tiles t and t+1
-                    const int a0 = t * TM, na0 = min(TM, n - a0);
-                    const int na1 = t + 1 < nt ? min(TM, n - a0 - TM) : 0;
-                    pt.req = i;
-                    pt.kvh = h;
-                    pt.tok0 = c0 + a0;
-                    pt.ntok0 = na0;
-                    pt.ntok1 = na1;
-                    pt.qpos0 = L - n + a0;
-                    pt.kv_end0 = L - n + a0 + na0;
-                    pt.kv_end1 = na1 > 0 ? pt.kv_end0 + na1 : pt.kv_end0;
-                    cost = (pt.kv_end1 + kPreKeys - 1) / kPreKeys;
-                } else {  // -> (cascade group, key chunk, pair of member tiles, kv head)
-                    const int y = x - tot3[1];
-                    int g = 0;
-                    while (g + 1 < s_ngroups && cgroups[g + 1].unit_off <= y) ++g;
-                    const CascGroup cgr = cgroups[g];
-                    const int ly = y - cgr.unit_off;
-                    const int pu = (((cgr.n_members + TM - 1) / TM) + 1) / 2 * Hkv;
-                    const int c = ly / pu, rest = ly % pu;
-                    const int pair = rest / Hkv, h = rest % Hkv;
-                    const int m0 = pair * 2 * TM;
-                    pt.req = -1 - g;
-                    pt.kvh = h;
-                    pt.tok0 = cgr.member_off + m0;
-                    pt.ntok0 = min(TM, cgr.n_members - m0);
-                    pt.ntok1 = max(0, min(TM, cgr.n_members - m0 - TM));
-                    pt.qpos0 = c;
-                    pt.kv_end0 = c * cgr.chunk_keys;
-                    pt.kv_end1 = min(cgr.prefix_len, (c + 1) * cgr.chunk_keys);
-                    cost = (pt.kv_end1 - pt.kv_end0 + kPreKeys - 1) / kPreKeys;
-                }
-                const int b = cost_bucket(cost);
-                if (!emit) {
-                    warp_agg_inc(&s_hist_t[b], b);
-                    continue;
-                }
-                tiles[warp_agg_inc(&s_hist_t[b], b)] = pt;
+                if (nparts > 1) pi += nparts;
+                ++gi;
             }
         }
-        __syncthreads();
-        if (!emit && tid < 32) {  // bucket counts -> first position of each bucket (bucket 0 = costliest)
-            constexpr int kPer = kBuckets / 32;
-            int su = 0, st = 0;
-#pragma unroll
-            for (int k = 0; k < kPer; ++k) {
-                su += s_hist_u[tid * kPer + k];
-                st += s_hist_t[tid * kPer + k];
-            }
-            int iu = su, itt = st;  // inclusive warp scan
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int yu = __shfl_up_sync(0xffffffffu, iu, o), yt = __shfl_up_sync(0xffffffffu, itt, o);
-                if (tid >= o) {
-                    iu += yu;
-                    itt += yt;
-                }
-            }
-            int au = iu - su, at = itt - st;
-#pragma unroll
-            for (int k = 0; k < kPer; ++k) {
-                const int cu_ = s_hist_u[tid * kPer + k], ct = s_hist_t[tid * kPer + k];
-                s_hist_u[tid * kPer + k] = au;
-                s_hist_t[tid * kPer + k] = at;
-                au += cu_;
-                at += ct;
-            }
+        // prefill tile pairs, then cascade prefix units, in parallel over the unit index
+        for (int x = tid; x < tiles_total; x += kThreads) {
+            PreTile pt;
+            const int b = cost_bucket(make_tile(x, pt));
+            store_record(&tiles[atomicAdd(&s_hist_t[b], 1)], pt);
         }
-        __syncthreads();
     }
 
     // ---- derived slot mapping: the new tokens are each request's last q_len positions
@@ -526,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         hdr->n_dec_units = ok ? tot2[0] : 0;
         hdr->n_partial_slots = ok ? tot2[1] : 0;
         hdr->split_chunk = chunk;
-        hdr->n_casc_groups = ok ? s_ngroups : 0;
+        hdr->n_casc_groups = ok ? n_cgroups : 0;
         hdr->n_casc_tiles = ok ? s_casc_units : 0;
         hdr->n_casc_units = ok ? s_casc_units : 0;
     }
@@ -534,10 +624,14 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
 
 }  // namespace
 
-size_t prepare_smem_bytes(int smem_batch) { return (size_t)kNumArrays * (smem_batch + 1) * sizeof(int32_t); }
+size_t prepare_smem_bytes(int smem_batch, bool cascade) {
+    size_t words = (size_t)kNumArrays * (smem_batch + 1);
+    if (cascade) words += 2 * ((size_t)1 << casc_hash_bits(smem_batch));
+    return words * sizeof(int32_t);
+}
 
 cudaError_t launch_prepare(const PrepareParams& p, cudaStream_t s) {
-    const size_t smem = prepare_smem_bytes(p.smem_batch);
+    const size_t smem = prepare_smem_bytes(p.smem_batch, p.use_cascade != 0);
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(prepare_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;

@@ -126,7 +126,6 @@ struct Layout {
     size_t dec_groups;
     size_t pre_tiles;
     size_t slots;        // int64 [max_tokens] derived slot mapping
-    size_t counters;     // uint32 [max_dec_groups] merge arrival counters
     size_t partial_o;    // fp32 [max_partial][rows_per_slot][D]
     size_t partial_lse;  // fp32 [max_partial][rows_per_slot]
     size_t req_scratch;  // int32 [max_batch * 4] prepare scratch
@@ -210,6 +209,7 @@ struct MetaHost {
     int32_t sm_count;
     int32_t use_prefill;
     int32_t use_cascade;
+    int32_t use_merge;
     int32_t dec_ctas;
     int32_t pre_ctas;
     const int32_t* cu;
@@ -251,11 +251,44 @@ inline int split_ranges(int ext, int chunk, int* per_out) {
     return (ext + per - 1) / per;
 }
 
+// Entries (log2) of the prepare kernel's shared-memory hash table for shared-prefix
+// detection: more than twice the batch, so that open addressing always finds a free entry.
+#ifdef __CUDACC__
+__host__ __device__
+#endif
+inline int casc_hash_bits(int batch) {
+    int b = 6;
+    while ((1 << b) < 2 * (batch + 1)) ++b;
+    return b;
+}
+
+// Launch with programmatic stream serialization: the kernel's CTAs may start while the
+// previous kernel of the stream is still running (that kernel lets them with
+// grid_dep_launch); the kernel reads nothing the previous one writes before its
+// grid_dep_wait.  This hides the launch and set-up of the attention kernels behind the
+// kernel before them.
+template <class... Params, class... Args>
+cudaError_t launch_programmatic(void (*kernel)(Params...), unsigned grid, unsigned block, size_t smem,
+                                cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Launchers (defined in the .cu files).
 cudaError_t launch_prepare(const PrepareParams& p, cudaStream_t s);
-size_t prepare_smem_bytes(int smem_batch);
+size_t prepare_smem_bytes(int smem_batch, bool cascade);
 cudaError_t launch_store(const ForwardParams& p, int head_dim, cudaStream_t s);
 cudaError_t launch_decode(const ForwardParams& p, int head_dim, int ctas, cudaStream_t s);
+cudaError_t launch_merge(const ForwardParams& p, int head_dim, int ctas, cudaStream_t s);
 cudaError_t launch_prefill(const ForwardParams& p, int head_dim, int ctas, cudaStream_t s);
 bool prefill_supported(int num_qo_heads, int num_kv_heads, int head_dim);
 int decode_ctas_per_sm(int num_kv_heads, int head_dim);

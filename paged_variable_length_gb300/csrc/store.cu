@@ -20,6 +20,9 @@ constexpr int kThreads = 256;
 
 __global__ void __launch_bounds__(kThreads) store_kernel(ForwardParams p, int row_vecs) {
     PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws + p.lay.header);
+    // the attention kernel that follows may set up its CTAs now; it reads nothing this
+    // kernel writes before its grid_dep_wait
+    dev::grid_dep_launch();
     // the attention kernels that follow fetch their work from these counters
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         hdr->pad[0] = 0;  // decode kernel work counter
