@@ -41,6 +41,62 @@ def parse():
     return ap.parse_args()
 
 
+# ------------------------------------------------------------------------------ ncu traffic
+
+# DRAM bytes (read + write) per launch from the committed ncu captures, keyed by
+# (kernel phase, workload).  A figure is used only while the kernel's sources hash to
+# what they were at capture time; after any change the roofline reports null.
+NCU_TRAFFIC = {
+    ("decode", "decode"): {
+        "bytes": 619.825152e6,
+        "sources": ["paged_variable_length_gb300/csrc/decode.cu", "paged_variable_length_gb300/csrc/device_utils.cuh",
+                    "paged_variable_length_gb300/csrc/pva_internal.h"],
+        "sha256_16": "117427c2844f34db",
+        "summary": "profiles/decode_kernel_decode_workload.md",
+    },
+}
+
+
+def ncu_traffic(phase: str, workload: str):
+    import hashlib
+
+    entry = NCU_TRAFFIC.get((phase, workload))
+    if entry is None:
+        return None
+    h = hashlib.sha256()
+    for f in entry["sources"]:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return entry["bytes"] if h.hexdigest()[:16] == entry["sha256_16"] else None
+
+
+# ------------------------------------------------------------------------------ multi-rank helpers
+
+def max_over_ranks(x: float, dist=None, device="cpu") -> float:
+    """The largest x over all ranks (x itself without a process group)."""
+    if dist is None:
+        return float(x)
+    import torch
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job throughput: every rank runs its own replica of the batch (weak scaling)."""
+    return world * tokens_per_rank / (ms / 1e3)
+
+
+def job_config(wl, args, world: int) -> dict:
+    return {
+        "workload": wl.description, "seed": args.seed, "batch": wl.batch, "new_tokens": wl.total_tokens,
+        "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write, outside the timed events)",
+        "step": "attn_prepare_metadata + attn_forward (store_kvcache + attention), one layer",
+        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+    }
+
+
 # ------------------------------------------------------------------------------ algorithmic work
 
 def algorithmic_work(wl):
@@ -220,7 +276,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": wl.description, "seed": args.seed},
+        "config": job_config(wl, args, args.gpus),
         "cpu_baseline": dict(base, value=value),
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -313,11 +369,8 @@ def run_ours(args):
     clock_info = clocks.stop()
     times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = sum(times) / len(times)
-    if dist is not None:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-    value = world * wl.total_tokens / (ms / 1e3)
+    ms = max_over_ranks(ms, dist, dev)
+    value = job_tokens_per_s(wl.total_tokens, world, ms)
 
     # ---- per-kernel durations (events between the library's launches), same steps
     kev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
@@ -352,7 +405,7 @@ def run_ours(args):
         roof = {"bound": "hbm", "achieved": work["attn_bytes"] / (phase_ms[dom] / 1e3) / 1e9,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = ncu_traffic(dom, args.workload)
     roof["kernel"] = dom
     roof["peak_source"] = peaks["source"]
     roof_time_s = max(work["flops"] / (peaks["bf16_tflops"] * 1e12), work["step_bytes"] / (peaks["hbm_gbs"] * 1e9))
@@ -384,10 +437,7 @@ def run_ours(args):
         e_e[i].record(stream)
     torch.cuda.synchronize()
     e2e_ms = sum(s.elapsed_time(e) for s, e in zip(e_s, e_e)) / args.steps
-    if dist is not None:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
 
     base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -398,19 +448,14 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {
-                "workload": wl.description, "seed": args.seed, "batch": wl.batch, "new_tokens": wl.total_tokens,
-                "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write, outside the timed events)",
-                "step": "attn_prepare_metadata + attn_forward (store_kvcache + attention), one layer",
-                "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-            },
+            "config": job_config(wl, args, world),
             "roofline": roof,
             "step_roofline": {"roofline_time_us": roof_time_s * 1e6, "frac_of_step": roof_time_s / (ms / 1e3),
                               "bytes": work["step_bytes"], "flops": work["flops"]},
             "phases_ms": phase_ms,
             "plan": plan,
             "gpu_launches": int(args.steps * (1 + plan.get("kernels_per_forward", 2))),
-            "e2e": {"value": world * wl.total_tokens / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+            "e2e": {"value": job_tokens_per_s(wl.total_tokens, world, e2e_ms), "unit": "tokens/s", "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "clocks": clock_info,
             "cpu_baseline": base,
