@@ -166,6 +166,43 @@ PVA_API pva_status attn_prepare_metadata(const pva_config* cfg, const int32_t* c
                                  int32_t total_tokens, int32_t max_q_len, void* workspace,
                                  size_t workspace_bytes, void* stream, pva_meta* meta);
 
+/* Bytes of the scratch area built into the library for attn_prepare_metadata_static. */
+#define PVA_STATIC_WORKSPACE_BYTES ((size_t)64 << 20)
+
+/*
+ * attn_prepare_metadata without a caller workspace: the plan is built in a
+ * fixed scratch area of PVA_STATIC_WORKSPACE_BYTES compiled into this
+ * library (one per device), so the call allocates no device memory at all.
+ * It is meant for callers that cannot hand the library a device buffer: a
+ * host program whose device memory belongs to an allocator it may not call on
+ * this path, or a plugin inside a framework that exposes no allocation hook.
+ * None of the pages this library follows describes such a call; it is an
+ * addition for those callers.
+ *
+ * Arguments and results are those of attn_prepare_metadata minus workspace /
+ * workspace_bytes; the returned meta is used with attn_forward as usual.
+ * Limits and behaviour:
+ *   - The first call on a device looks up that device's copy of the scratch
+ *     area (with that device current); make that first call before any stream
+ *     capture on the device.
+ *   - When the plan for cfg does not fit, the number of split-KV units is
+ *     lowered (down to one per SM) until it does; when it still does not fit,
+ *     the call returns PVA_ERR_WORKSPACE_TOO_SMALL and launches nothing.
+ *     attn_workspace_size(cfg) above PVA_STATIC_WORKSPACE_BYTES is the sign
+ *     that this can happen.
+ *   - Nothing in the scratch area has to start at zero: every plan record is
+ *     written by the prepare kernel before the forward reads it, and the work
+ *     counters are reset by each forward's first kernel.
+ *   - There is one scratch area per device, shared by every caller in the
+ *     process: a prepare or forward using it that overlaps another one on the
+ *     same device (another stream, another thread) races with it, and each
+ *     call invalidates the meta of the previous one on that device.
+ */
+PVA_API pva_status attn_prepare_metadata_static(const pva_config* cfg, const int32_t* cu_seqlens_q,
+                                        const int32_t* cache_seqlens, const int32_t* page_table,
+                                        int64_t ld_page_table, const int64_t* slot_mapping, int32_t batch,
+                                        int32_t total_tokens, int32_t max_q_len, void* stream, pva_meta* meta);
+
 /*
  * Once per layer: store_kvcache, then attention, in stream order on `stream`.
  * k_pool / v_pool are updated in place (bit-exact copies of k / v rows at

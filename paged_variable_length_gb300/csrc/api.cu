@@ -5,6 +5,7 @@
 
 #include <cmath>
 #include <cstring>
+#include <mutex>
 
 #include "pva_internal.h"
 
@@ -39,13 +40,15 @@ pva_status check_config(const pva_config* c) {
     return PVA_OK;
 }
 
-Layout make_layout(const pva_config* c, int sm_count) {
+// target_units > 0 replaces the number of split-KV units the plan aims for (and with
+// it the partial-slot capacity); 0 keeps the default of four per decode CTA.
+Layout make_layout(const pva_config* c, int sm_count, int target_units = 0) {
     Layout L{};
     const int G = c->num_qo_heads / c->num_kv_heads;
     const int TB = kDecRows / G;
     const int TM = kPreRows / G;
     const int cps = decode_ctas_per_sm(c->num_kv_heads, c->head_dim);
-    L.target_units = 4 * sm_count * cps;
+    L.target_units = target_units > 0 ? target_units : 4 * sm_count * cps;
     L.max_dec_groups = (int32_t)(c->max_tokens / TB + c->max_batch + 1);
     L.max_dec_units = L.max_dec_groups + L.target_units + 1;
     L.max_partial = 2 * L.target_units + 2;
@@ -147,23 +150,34 @@ size_t attn_workspace_size(const pva_config* cfg) {
     return make_layout(cfg, sms).total;
 }
 
-pva_status attn_prepare_metadata(const pva_config* cfg, const int32_t* cu_seqlens_q, const int32_t* cache_seqlens,
-                                 const int32_t* page_table, int64_t ld_page_table, const int64_t* slot_mapping,
-                                 int32_t batch, int32_t total_tokens, int32_t max_q_len, void* workspace,
-                                 size_t workspace_bytes, void* stream, pva_meta* meta) {
+namespace {
+
+// Scratch area of attn_prepare_metadata_static: a plan workspace that exists in every
+// device's copy of this module, for callers that cannot allocate one.
+static __device__ __align__(256) uint8_t g_static_workspace[PVA_STATIC_WORKSPACE_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxDevices];  // device address of g_static_workspace, per device, once looked up
+
+// Host checks of attn_prepare_metadata's arguments other than the workspace.
+pva_status check_prepare_args(const pva_config* cfg, const int32_t* cu_seqlens_q, const int32_t* cache_seqlens,
+                              const int32_t* page_table, int64_t ld_page_table, int32_t batch, int32_t total_tokens,
+                              pva_meta* meta) {
     pva_status st = check_config(cfg);
     if (st != PVA_OK) return st;
-    if (meta == nullptr || workspace == nullptr || cu_seqlens_q == nullptr || cache_seqlens == nullptr ||
-        page_table == nullptr)
+    if (meta == nullptr || cu_seqlens_q == nullptr || cache_seqlens == nullptr || page_table == nullptr)
         return PVA_ERR_INVALID_ARG;
     if (batch < 0 || total_tokens < 0 || ld_page_table <= 0) return PVA_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PVA_ERR_INVALID_ARG;
     if (batch > cfg->max_batch || total_tokens > cfg->max_tokens) return PVA_ERR_INVALID_ARG;
-    const int sms = device_sm_count();
-    if (sms <= 0) return PVA_ERR_CUDA;
-    const Layout lay = make_layout(cfg, sms);
-    if (workspace_bytes < lay.total) return PVA_ERR_WORKSPACE_TOO_SMALL;
+    return PVA_OK;
+}
 
+// The plan for one batch in `workspace` (carved up by `lay`); arguments already checked.
+pva_status prepare_in_workspace(const pva_config* cfg, const int32_t* cu_seqlens_q, const int32_t* cache_seqlens,
+                                const int32_t* page_table, int64_t ld_page_table, const int64_t* slot_mapping,
+                                int32_t batch, int32_t total_tokens, int32_t max_q_len, void* workspace,
+                                const Layout& lay, int sms, void* stream, pva_meta* meta) {
     const int G = cfg->num_qo_heads / cfg->num_kv_heads;
     const int TB = kDecRows / G;
     const int mq = max_q_len > 0 ? max_q_len : (total_tokens > 0 ? total_tokens : 1);
@@ -235,6 +249,25 @@ pva_status attn_prepare_metadata(const pva_config* cfg, const int32_t* cu_seqlen
     return PVA_OK;
 }
 
+}  // namespace
+
+pva_status attn_prepare_metadata(const pva_config* cfg, const int32_t* cu_seqlens_q, const int32_t* cache_seqlens,
+                                 const int32_t* page_table, int64_t ld_page_table, const int64_t* slot_mapping,
+                                 int32_t batch, int32_t total_tokens, int32_t max_q_len, void* workspace,
+                                 size_t workspace_bytes, void* stream, pva_meta* meta) {
+    pva_status st = check_prepare_args(cfg, cu_seqlens_q, cache_seqlens, page_table, ld_page_table, batch,
+                                       total_tokens, meta);
+    if (st != PVA_OK) return st;
+    if (workspace == nullptr) return PVA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PVA_ERR_INVALID_ARG;
+    const int sms = device_sm_count();
+    if (sms <= 0) return PVA_ERR_CUDA;
+    const Layout lay = make_layout(cfg, sms);
+    if (workspace_bytes < lay.total) return PVA_ERR_WORKSPACE_TOO_SMALL;
+    return prepare_in_workspace(cfg, cu_seqlens_q, cache_seqlens, page_table, ld_page_table, slot_mapping, batch,
+                                total_tokens, max_q_len, workspace, lay, sms, stream, meta);
+}
+
 pva_status attn_store_kvcache(const pva_meta* meta, const void* k, const void* v, void* k_pool, void* v_pool,
                               void* stream) {
     const MetaHost* h = meta_of(meta);
@@ -245,6 +278,39 @@ pva_status attn_store_kvcache(const pva_meta* meta, const void* k, const void* v
     ForwardParams fp = forward_params(h, nullptr, k, v, k_pool, v_pool, nullptr, nullptr);
     if (launch_store(fp, h->cfg.head_dim, static_cast<cudaStream_t>(stream)) != cudaSuccess) return PVA_ERR_CUDA;
     return PVA_OK;
+}
+
+pva_status attn_prepare_metadata_static(const pva_config* cfg, const int32_t* cu_seqlens_q,
+                                        const int32_t* cache_seqlens, const int32_t* page_table,
+                                        int64_t ld_page_table, const int64_t* slot_mapping, int32_t batch,
+                                        int32_t total_tokens, int32_t max_q_len, void* stream, pva_meta* meta) {
+    pva_status st = check_prepare_args(cfg, cu_seqlens_q, cache_seqlens, page_table, ld_page_table, batch,
+                                       total_tokens, meta);
+    if (st != PVA_OK) return st;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PVA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return PVA_ERR_UNSUPPORTED;
+    void* ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_static_mu);
+        if (g_static_ptr[dev] == nullptr) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || p == nullptr) return PVA_ERR_CUDA;
+            g_static_ptr[dev] = p;
+        }
+        ws = g_static_ptr[dev];
+    }
+    const int sms = device_sm_count();
+    if (sms <= 0) return PVA_ERR_CUDA;
+    // the default plan, or one aiming for fewer split-KV units when that does not fit
+    Layout lay = make_layout(cfg, sms);
+    for (int t = lay.target_units; lay.total > PVA_STATIC_WORKSPACE_BYTES && t > sms;) {
+        t = t / 2 > sms ? t / 2 : sms;
+        lay = make_layout(cfg, sms, t);
+    }
+    if (lay.total > PVA_STATIC_WORKSPACE_BYTES) return PVA_ERR_WORKSPACE_TOO_SMALL;
+    return prepare_in_workspace(cfg, cu_seqlens_q, cache_seqlens, page_table, ld_page_table, slot_mapping, batch,
+                                total_tokens, max_q_len, ws, lay, sms, stream, meta);
 }
 
 pva_status attn_forward(const pva_meta* meta, const void* q, const void* k, const void* v, void* k_pool,

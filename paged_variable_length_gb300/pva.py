@@ -26,7 +26,7 @@ DEVERR = {
 # Every function include/pva.h declares; the CPU tests check the library exports each one.
 EXPORTS = ("attn_abi_version", "attn_status_string", "attn_workspace_size", "attn_prepare_metadata",
            "attn_forward", "attn_store_kvcache", "attn_get_device_status", "attn_debug_plan_counts",
-           "attn_set_timing_events")
+           "attn_set_timing_events", "attn_prepare_metadata_static")
 
 
 class PvaError(RuntimeError):
@@ -72,6 +72,8 @@ def load(path: str | None = None):
         lib.attn_workspace_size.argtypes, lib.attn_workspace_size.restype = [CP], sz
         lib.attn_prepare_metadata.argtypes = [CP, P, P, P, i64, P, i32, i32, i32, P, sz, P, MP]
         lib.attn_prepare_metadata.restype = ctypes.c_int
+        lib.attn_prepare_metadata_static.argtypes = [CP, P, P, P, i64, P, i32, i32, i32, P, MP]
+        lib.attn_prepare_metadata_static.restype = ctypes.c_int
         lib.attn_forward.argtypes = [MP, P, P, P, P, P, P, P, P]
         lib.attn_forward.restype = ctypes.c_int
         lib.attn_store_kvcache.argtypes = [MP, P, P, P, P, P]
@@ -132,6 +134,17 @@ def attn_prepare_metadata(cfg: Config, cu_seqlens_q, cache_seqlens, page_table, 
         _ptr(slot_mapping), int(batch), int(total_tokens), int(max_q_len), _ptr(workspace),
         int(workspace.numel() * workspace.element_size()), _stream(stream), ctypes.byref(meta))
     _check(st, "attn_prepare_metadata")
+    return meta
+
+
+def attn_prepare_metadata_static(cfg: Config, cu_seqlens_q, cache_seqlens, page_table, slot_mapping, batch: int,
+                                 total_tokens: int, max_q_len: int, stream=None) -> Meta:
+    """attn_prepare_metadata with the plan in the library's built-in scratch area (no workspace)."""
+    meta = Meta()
+    st = load().attn_prepare_metadata_static(
+        ctypes.byref(cfg), _ptr(cu_seqlens_q), _ptr(cache_seqlens), _ptr(page_table), int(page_table.stride(0)),
+        _ptr(slot_mapping), int(batch), int(total_tokens), int(max_q_len), _stream(stream), ctypes.byref(meta))
+    _check(st, "attn_prepare_metadata_static")
     return meta
 
 
