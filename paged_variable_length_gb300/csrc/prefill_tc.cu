@@ -66,7 +66,8 @@ struct SmemMap {
     static constexpr int kQ = 0;                 // two Q tiles
     static constexpr int kK = kQ + 2 * kTile;    // two K stages
     static constexpr int kV = kK + 2 * kTile;    // two V stages
-    static constexpr int kBytes = kV + 2 * kTile;
+    static constexpr int kOff = kV + 2 * kTile;  // per producer warp: source offsets of its rows (64 x int64)
+    static constexpr int kBytes = kOff + 3 * 64 * 8;
 };
 
 struct Bars {
@@ -208,32 +209,92 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtrl));
     if (warp >= kProducerWarp0) {
         // ============================================================== producer (cp.async gathers)
-        // Thread r of these warps moves rows r and r + 96 of every Q / K / V tile: a 256-byte row
-        // (one kv head of one slot, or one q head of one token) as 16-byte async copies
-        // into the 128-byte-swizzled layout the MMA descriptors expect.  A page of a
-        // few rows per kv head is too small a box for TMA to stream efficiently, and
-        // rows past kv_len are simply not copied.  The MMA thread orders these
-        // generic-proxy writes before its tensor-core reads with a proxy fence after
-        // it has waited on the tile's barrier.
-        const int r0 = threadIdx.x - kProducerWarp0 * 32;  // 0..95
+        // The three producer warps move the rows of every Q / K / V tile: a row is one kv
+        // head of one slot (or one q head of one token), D*2 bytes, copied as 16-byte async
+        // copies into the 128-byte-swizzled layout the MMA descriptors expect.  The lanes of
+        // a copy instruction take consecutive 16-byte chunks of kRowsPerCopy whole rows, so
+        // every instruction touches whole 128-byte lines on both sides (one lane per row
+        // made each instruction touch 32 lines, eight times the shared-memory wavefronts the
+        // data needs, and those bursts slowed the tensor core's operand reads).  Each lane
+        // computes the source offsets of two of its warp's rows into the warp's own table in
+        // shared memory, which the copy loop reads back (one broadcast load per copy).
+        // With pages of 16 or more slots, K and V rows are instead copied one thread per row
+        // (16 chunks each): there a copy instruction's 32 rows lie in two pages, so address
+        // translation stays local, and that mapping measured about 10 % faster; with small
+        // pages (a token-slot pool) 32 rows per instruction meant 32 random translations,
+        // and the two-rows-per-instruction mapping is 3.7 times faster.  A page of a few rows per kv head is too small a box for TMA
+        // to stream efficiently, and rows past kv_len are not copied.  The MMA thread orders
+        // these generic-proxy writes before its tensor-core reads with a proxy fence after it
+        // has waited on the tile's barrier.
+        constexpr int kChunks = D / 8;              // 16-byte chunks per row
+        constexpr int kRowsPerCopy = 32 / kChunks;  // rows one copy instruction moves
+        constexpr int kStride = 3 * kRowsPerCopy;   // rows the three warps move per step
+        constexpr int kCopyIters = (kPreRows + kStride - 1) / kStride;
+        static_assert(kCopyIters * kRowsPerCopy <= 64, "two row offsets per lane");
+        const int pwarp = warp - kProducerWarp0;  // 0..2
+        const int pt_id = pwarp * 32 + lane;       // 0..95
+        const int chunk = lane % kChunks, sub = lane / kChunks;
+        const bool row_per_thread = p.page_size >= 16;
         const int ps_mask = p.page_size - 1;
+        // row of a tile held by this warp's row index k (k = copy step * kRowsPerCopy + sub)
+        auto row_of = [&](int k) { return pwarp * kRowsPerCopy + (k % kRowsPerCopy) + (k / kRowsPerCopy) * kStride; };
         // every producer thread arrives on a tile's barrier when its own copies of that
         // tile have landed (hardware-tracked: the producer never waits for its loads)
         auto issue = [&](uint64_t* full) {
             asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(dev::smem_u32(full))
                          : "memory");
         };
-        // 256-byte row -> swizzled smem row r of a tile (two 64-column regions)
+        // the warp's rows of a tile; o0 / o1: element offsets (from base) of row indices lane
+        // and lane + 32, -1 for a row that is not copied
+        // table entry of row index k: the rows one lane copies (k = i * kRowsPerCopy + sub)
+        // sit next to each other, so that the unrolled copy loop reads them as vectors
+        int64_t* offs = reinterpret_cast<int64_t*>(smem + L::kOff) + pwarp * 64;
+        auto slot_of = [](int k) { return (k % kRowsPerCopy) * kCopyIters + k / kRowsPerCopy; };
+        auto copy_tile = [&](uint8_t* tile, int64_t o0, int64_t o1, const uint16_t* base) {
+            __syncwarp();  // the previous tile's copy loop has read the table
+            if (lane < kCopyIters * kRowsPerCopy) offs[slot_of(lane)] = o0;
+            if (lane + 32 < kCopyIters * kRowsPerCopy) offs[slot_of(lane + 32)] = o1;
+            __syncwarp();
+            const uint32_t t0 = dev::smem_u32(tile) + (chunk >> 3) * kRegion;
+            const uint16_t* src0 = base + chunk * 8;
+            const int64_t* mine = offs + sub * kCopyIters;
+#pragma unroll
+            for (int i = 0; i < kCopyIters; ++i) {
+                const int r = pwarp * kRowsPerCopy + sub + i * kStride;
+                const int64_t o = mine[i];
+                if (r < kPreRows && o >= 0) {
+                    const uint32_t dst = t0 + r * 128 + (((chunk & 7) ^ (r & 7)) << 4);
+                    // no memory clobber: the table reads above may then be hoisted and batched;
+                    // the copies are ordered by the __syncwarp before the table is rewritten and
+                    // by the mbarrier arrive that follows every tile
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src0 + o));
+                }
+            }
+        };
+        // one thread per row: a row -> its 16-byte chunks, swizzled
         auto copy_row = [&](uint8_t* tile, int r, const uint16_t* src) {
             const uint32_t d0 = dev::smem_u32(tile) + r * 128;
 #pragma unroll
             for (int c = 0; c < D / 8; ++c) {
-                const uint32_t dst = d0 + (c >> 3) * kRegion + ((((c & 7) ^ (r & 7)) & 7) << 4);
+                const uint32_t dst = d0 + (c >> 3) * kRegion + (((c & 7) ^ (r & 7)) << 4);
                 asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + c * 8) : "memory");
             }
         };
+        // the K / V rows this lane computes offsets for (i = 0, 1)
+        auto kv_row = [&](int i) { return row_per_thread ? pt_id + i * kProducerThreads : row_of(lane + 32 * i); };
+        auto copy_kv = [&](uint8_t* tile, const int64_t (&off)[2], const uint16_t* base) {
+            if (row_per_thread) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int r = pt_id + i * kProducerThreads;
+                    if (r < kPreRows && off[i] >= 0) copy_row(tile, r, base + off[i]);
+                }
+            } else {
+                copy_tile(tile, off[0], off[1], base);
+            }
+        };
         uint32_t it = 0;
-        const bool fetcher = warp == kProducerWarp0 && lane == 0;
+        const bool fetcher = pwarp == 0 && lane == 0;
         if (fetcher) queue_push(b, 0, counter, n_units, err);
         for (int uc = 0;; ++uc) {
             const int u = queue_read(b, uc, lane, err);
@@ -247,53 +308,70 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (uc > 0 && !wait_or_abort(&b->q_empty, (uc - 1) & 1, b, err)) break;
             for (int h = 0; h < 2; ++h) {
                 const int ntok = h ? pt.ntok1 : pt.ntok0;
-                for (int r = r0; r < kPreRows; r += kProducerThreads) {
+                int64_t oq[2];
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int r = row_of(lane + 32 * i);
                     const int t = r / G;
-                    if (t < ntok) {
-                        const int token = uv.casc ? groups[cmembers[pt.tok0 + h * TM + t]].tok0 : pt.tok0 + h * TM + t;
-                        const uint16_t* src = p.q + ((int64_t)token * Hq + pt.kvh * G + (r - t * G)) * D;
-                        copy_row(smem + L::kQ + h * L::kTile, r, src);
+                    oq[i] = -1;
+                    if (r < kPreRows && t < ntok) {
+                        const int token =
+                            uv.casc ? groups[cmembers[pt.tok0 + h * TM + t]].tok0 : pt.tok0 + h * TM + t;
+                        oq[i] = ((int64_t)token * Hq + pt.kvh * G + (r - t * G)) * D;
                     }
                 }
+                copy_tile(smem + L::kQ + h * L::kTile, oq[0], oq[1], p.q);
             }
             issue(&b->q_full);
             // ---- K and V tiles
             const int kv_end = uv.key_end;
             const int nkt = (kv_end - uv.key_base + kPreKeys - 1) / kPreKeys;
+            // page ids of this lane's two rows of tile j: read one tile ahead, so that the
+            // page-table round trip overlaps the copies and waits of the tile before
+            auto page_ids = [&](int j, int32_t (&pg)[2]) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int r = kv_row(i);
+                    const int key = uv.key_base + j * kPreKeys + r;
+                    pg[i] = (j < nkt && r < kPreRows && key < kv_end) ? prow[key >> p.page_shift] : 0;
+                }
+            };
+            // (with one thread per row the page ids are read just before use: reading them a
+            // tile ahead measured slower there)
+            int32_t pg_next[2] = {0, 0};
+            if (!row_per_thread) page_ids(0, pg_next);
             bool ok = true;
             for (int j = 0; j < nkt && ok; ++j, ++it) {
                 const int st = it & 1;
                 const uint32_t ph = (it >> 1) & 1;
-                // element offsets of this thread's (at most two) rows; -1: past kv_len
+                int32_t pg[2] = {pg_next[0], pg_next[1]};
+                if (row_per_thread) page_ids(j, pg);
+                else page_ids(j + 1, pg_next);
+                // element offsets of this lane's two rows; -1: past kv_len
                 int64_t off[2] = {-1, -1};
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
-                    const int r = r0 + i * kProducerThreads;
+                    const int r = kv_row(i);
                     const int key = uv.key_base + j * kPreKeys + r;
-                    if (r < kPreRows && key < kv_end) {
-                        int64_t page = prow[key >> p.page_shift];
-                        if (page < 0 || page >= p.num_pages) {
-                            dev::set_error(err, kErrPage);
-                            page = 0;
-                        }
-                        off[i] = (((page << p.page_shift) + (key & ps_mask)) * p.num_kv_heads + pt.kvh) * D;
+                    if (r >= kPreRows || key >= kv_end) continue;
+                    int64_t page = pg[i];
+                    if (page < 0 || page >= p.num_pages) {
+                        dev::set_error(err, kErrPage);
+                        page = 0;
                     }
+                    off[i] = (((page << p.page_shift) + (key & ps_mask)) * p.num_kv_heads + pt.kvh) * D;
                 }
                 if (!wait_or_abort(&b->k_empty[st], ph ^ 1, b, err)) {
                     ok = false;
                     break;
                 }
-#pragma unroll
-                for (int i = 0; i < 2; ++i)
-                    if (off[i] >= 0) copy_row(smem + L::kK + st * L::kTile, r0 + i * kProducerThreads, p.k_pool + off[i]);
+                copy_kv(smem + L::kK + st * L::kTile, off, p.k_pool);
                 issue(&b->k_full[st]);
                 if (!wait_or_abort(&b->v_empty[st], ph ^ 1, b, err)) {
                     ok = false;
                     break;
                 }
-#pragma unroll
-                for (int i = 0; i < 2; ++i)
-                    if (off[i] >= 0) copy_row(smem + L::kV + st * L::kTile, r0 + i * kProducerThreads, p.v_pool + off[i]);
+                copy_kv(smem + L::kV + st * L::kTile, off, p.v_pool);
                 issue(&b->v_full[st]);
             }
             if (!ok) break;
@@ -441,23 +519,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < kPreKeys / 32; ++c) tc::tmem_wait_ld_regs(s[c]);
                 const int key0 = uv.key_base + j * kPreKeys;
                 const bool need_mask = key0 + kPreKeys - 1 >= mask_from;
-                float mxa[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mxa[i] = -INFINITY;
                 if (need_mask) {  // a tile crossing the diagonal (or the end of the keys)
 #pragma unroll
-                    for (int c = 0; c < kPreKeys; ++c) {
-                        float x = s[c >> 5][c & 31];
-                        if (key0 + c > limit) x = -INFINITY;
-                        s[c >> 5][c & 31] = x;
-                        mxa[c & 7] = fmaxf(mxa[c & 7], x);
-                    }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < kPreKeys; ++c) mxa[c & 7] = fmaxf(mxa[c & 7], s[c >> 5][c & 31]);
+                    for (int c = 0; c < kPreKeys; ++c)
+                        if (key0 + c > limit) s[c >> 5][c & 31] = -INFINITY;
                 }
-                const float mx = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
-                                       fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
+                // row maximum: three-input max over 8 independent chains
+                float mxa[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mxa[i] = fmaxf(s[0][2 * i], s[0][2 * i + 1]);
+#pragma unroll
+                for (int c = 16; c < kPreKeys; c += 2) {
+                    const int i = (c >> 1) & 7;
+                    mxa[i] = dev::fmax3(mxa[i], s[c >> 5][c & 31], s[(c + 1) >> 5][(c + 1) & 31]);
+                }
+                const float mx = dev::fmax3(dev::fmax3(mxa[0], mxa[1], mxa[2]), dev::fmax3(mxa[3], mxa[4], mxa[5]),
+                                            fmaxf(mxa[6], mxa[7]));
                 const float m_new = fmaxf(m, mx * sl);  // log2 units (sl = scale * log2 e > 0)
                 if (j == 0) {
                     m = m_new;
@@ -486,16 +563,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float lsa[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) lsa[i] = 0.f;
-                // P = exp2(s * sl - m) as packed bf16 pairs, 32 columns (64 keys) per TMEM store
+                // P = exp2(s * sl - m) as packed bf16 pairs, 32 columns (64 keys) per TMEM store;
+                // the scale-and-shift and the row sum run as packed fp32 pairs
 #pragma unroll
                 for (int c2 = 0; c2 < kPreKeys / 64; ++c2) {
                     uint32_t pk[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int c = c2 * 64 + 2 * i;
-                        const float e0 = dev::fast_exp2(fmaf(s[c >> 5][c & 31], sl, nmu));
-                        const float e1 = dev::fast_exp2(fmaf(s[(c + 1) >> 5][(c + 1) & 31], sl, nmu));
-                        lsa[i & 7] += e0 + e1;
+                        float x0, x1;
+                        dev::ffma2(x0, x1, s[c >> 5][c & 31], s[(c + 1) >> 5][(c + 1) & 31], sl, sl, nmu, nmu);
+                        const float e0 = dev::fast_exp2(x0);
+                        const float e1 = dev::fast_exp2(x1);
+                        dev::fadd2(lsa[2 * (i & 3)], lsa[2 * (i & 3) + 1], e0, e1);
                         pk[i] = dev::pack_bf16x2(e0, e1);
                     }
                     tc::tmem_st32u(t_s + c2 * 32, pk);
