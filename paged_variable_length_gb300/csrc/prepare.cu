@@ -31,7 +31,7 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBuckets = 256;  // cost classes for the longest-first ordering of work items
-constexpr int kCmpPages = 8;   // page ids one thread compares per step of the shared-prefix search
+constexpr int kCmpPages = 8;   // page ids a lane compares per step of the shared-prefix search
 
 // Per-request shared-memory arrays (dynamic shared memory, batch <= smem_batch), followed
 // by the open-addressing table of the shared-prefix search when cascade detection runs.
@@ -153,10 +153,16 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         s_work = 0;
         s_casc_units = 0;
     }
+    const bool casc = p.use_cascade && small && B >= 2;
+    // One round trip for everything that depends on the request index alone: cu, the
+    // lengths and (for the shared-prefix search) each row's first page id.  Every later
+    // pass works from shared memory; the step runs with cold caches, so each dependent
+    // global round trip costs a DRAM latency.
     if (small) {
         for (int i = tid; i <= B; i += kThreads) {
             sa[kCu][i] = p.cu[i];
             if (i < B) sa[kLen][i] = p.seqlens[i];
+            if (casc && i < B) sa[kFirst][i] = p.page_table[(int64_t)i * p.ld];
             sa[kCgid][i] = -1;
         }
     }
@@ -167,20 +173,42 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     // each thread owns a contiguous run of requests for the counting passes
     const int chunk_req = (B + kThreads - 1) / kThreads;
     const int r0 = min(B, tid * chunk_req), r1 = min(B, r0 + chunk_req);
+    // derived slot of a single-token request (one request per thread): its page id is
+    // requested here and used only at the end, so the load overlaps the passes below
+    int32_t d_page = 0;
+    int d_tok = -1, d_pos = 0;
+    if (p.derived_slots != nullptr && chunk_req == 1 && tid < B) {
+        const int n = cu[tid + 1] - cu[tid], L = lens[tid];
+        if (n == 1 && valid_req(n, L)) {
+            d_pos = L - 1;
+            d_tok = cu[tid];
+            d_page = p.page_table[(int64_t)tid * p.ld + d_pos / ps];
+        }
+    }
+    // page-table rows the shared-prefix search may compare: pulled into L2 now
+    if (casc && chunk_req == 1 && tid < B) {
+        const int n = cu[tid + 1] - cu[tid], L = lens[tid];
+        const int pages = (n == 1 && valid_req(n, L)) ? (L - n) / ps : 0;
+        if (pages >= p.min_cascade_pages) {
+            const char* row = reinterpret_cast<const char*>(p.page_table + (int64_t)tid * p.ld);
+            for (int off = 0; off < pages * 4; off += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + off));
+        }
+    }
 
     // ---- pass 0: shared-prefix groups among single-token decodes.  Requests are keyed
     // by their first page; the lowest-numbered request with a key leads its group; the
     // group's prefix is the run of pages every member shares with the leader (whole pages
     // that lie strictly before each member's query, so no causal mask ever applies to it).
-    const bool casc = p.use_cascade && small && B >= 2;
     int n_cgroups = 0;
+    // shared-memory copy of the cascade group records (after the hash table)
+    CascGroup* scg = reinterpret_cast<CascGroup*>(dyn + kNumArrays * stride +
+                                                  2 * (casc ? (1 << casc_hash_bits(p.smem_batch)) : 0));
     if (casc) {
         int32_t* first = sa[kFirst];
         int32_t* leader = sa[kLeader];
         int32_t* lcp = sa[kLcp];
         int32_t* cnt = sa[kCnt];
         int32_t* lim = sa[kMpos];   // pages compared per member (until the groups are numbered)
-        int32_t* boff = sa[kToff];  // first compare block of each member (until pass 1)
         const int hbits = casc_hash_bits(p.smem_batch);
         const int HT = 1 << hbits;  // > 2 * batch: the probe below always meets a free entry
         int32_t* hkey = dyn + kNumArrays * stride;
@@ -193,79 +221,88 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
             const int n = cu[i + 1] - cu[i], L = lens[i];
             const bool ok = n == 1 && valid_req(n, L);
             const int pages = ok ? (L - n) / ps : 0;  // whole pages strictly before the query
-            const int f = (ok && pages >= p.min_cascade_pages) ? p.page_table[(int64_t)i * p.ld] : -1;
+            const int f = (ok && pages >= p.min_cascade_pages) ? first[i] : -1;
             first[i] = (f >= 0 && f < p.num_pages) ? f : -1;
             lcp[i] = pages;
             cnt[i] = 0;
             leader[i] = -1;
         }
         __syncthreads();
-        for (int i = tid; i < B; i += kThreads) {
-            const int f = first[i];
-            if (f < 0) continue;
-            uint32_t h = page_hash(f, hbits);
-            while (true) {
-                const int prev = atomicCAS(&hkey[h], -1, f);
-                if (prev == -1 || prev == f) break;
-                h = (h + 1) & (HT - 1);
-            }
-            atomicMin(&hval[h], i);
-            leader[i] = (int)h;
-        }
-        __syncthreads();
-        for (int i = tid; i < B; i += kThreads) {
-            if (first[i] < 0) continue;
-            const int ld = hval[leader[i]];
-            leader[i] = ld;
-            atomicAdd(&cnt[ld], 1);
-        }
-        __syncthreads();
-        // every member compares pages 1 .. lim-1 of its row with the leader's, in blocks
-        // of kCmpPages spread over the whole CTA; the group prefix is the smallest
-        // mismatch (or the smallest member's page count)
-        int nb[1] = {0};
-        for (int i = r0; i < r1; ++i) {
-            const int ld = leader[i];
-            int l = 0;
-            if (ld >= 0 && ld != i) {
-                l = min(lcp[i], lcp[ld]);
-                nb[0] += (l - 1 + kCmpPages - 1) / kCmpPages;
-            }
-            lim[i] = l;
-        }
-        int nbt[1];
-        block_scan<1>(nb, nbt, s_tmp1);
-        {
-            int off = nb[0];
-            for (int i = r0; i < r1; ++i) {
-                boff[i] = off;
-                const int l = lim[i];
-                if (l > 0) {
-                    off += (l - 1 + kCmpPages - 1) / kCmpPages;
-                    atomicMin(&lcp[leader[i]], l);
+        // Requests sharing a first page mostly sit in the same warps: the lanes of a warp
+        // with equal keys act once (lowest lane, which holds the lowest request index), so
+        // a group of many requests does not serialise on one shared-memory address.
+        const int lane = tid & 31;
+        for (int i0 = 0; i0 < B; i0 += kThreads) {  // uniform trip count: whole warps take part
+            const int i = i0 + tid;
+            const int f = i < B ? first[i] : -1;
+            const unsigned peers = __match_any_sync(0xffffffffu, f);
+            const int lead = __ffs(peers) - 1;
+            int h = 0;
+            if (f >= 0 && lane == lead) {
+                uint32_t hh = page_hash(f, hbits);
+                while (true) {
+                    const int prev = atomicCAS(&hkey[hh], -1, f);
+                    if (prev == -1 || prev == f) break;
+                    hh = (hh + 1) & (HT - 1);
                 }
+                atomicMin(&hval[hh], i);
+                h = (int)hh;
             }
+            h = __shfl_sync(0xffffffffu, h, lead);
+            if (f >= 0) leader[i] = h;
         }
         __syncthreads();
-        for (int x = tid; x < nbt[0]; x += kThreads) {
-            const int i = find_bucket(boff, B, x);
-            const int ld = leader[i];
-            const int k0 = 1 + (x - boff[i]) * kCmpPages;
-            const int k1 = min(lim[i], k0 + kCmpPages);
-            const int32_t* ri = p.page_table + (int64_t)i * p.ld;
-            const int32_t* rl = p.page_table + (int64_t)ld * p.ld;
-            int a[kCmpPages], b[kCmpPages];
-#pragma unroll
-            for (int k = 0; k < kCmpPages; ++k) {
-                const bool in = k0 + k < k1;
-                a[k] = in ? ri[k0 + k] : 0;
-                b[k] = in ? rl[k0 + k] : 0;
+        int has_member = 0;
+        for (int i0 = 0; i0 < B; i0 += kThreads) {
+            const int i = i0 + tid;
+            const int ld = (i < B && first[i] >= 0) ? hval[leader[i]] : -1;
+            const unsigned peers = __match_any_sync(0xffffffffu, ld);
+            if (ld >= 0) {
+                leader[i] = ld;
+                if (lane == __ffs(peers) - 1) atomicAdd(&cnt[ld], __popc(peers));
+                has_member |= ld != i;
             }
-            int mis = k1;
+        }
+        // no two candidates share a first page (the usual decode batch): no groups
+        if (__syncthreads_or(has_member)) {
+        // Every member compares pages 1 .. lim-1 of its row with the leader's (page 0
+        // matched by construction), one warp per member: lanes read consecutive page ids,
+        // so each load instruction is one line of each row, 256 ids per step.  The group
+        // prefix is the smallest mismatch, or the smallest member's page count.
+        for (int i = tid; i < B; i += kThreads) {
+            const int ld = leader[i];
+            lim[i] = (ld >= 0 && ld != i) ? min(lcp[i], lcp[ld]) : 0;
+        }
+        __syncthreads();
+        for (int i = tid; i < B; i += kThreads)
+            if (lim[i] > 0) atomicMin(&lcp[leader[i]], lim[i]);
+        {
+            constexpr int kU = kCmpPages;  // 8 ids per lane per step
+            const int warp = tid >> 5;
+            for (int i = warp; i < B; i += kWarps) {
+                const int l = lim[i];
+                if (l <= 1) continue;  // warp-uniform: i is the same for the whole warp
+                const int ld = leader[i];
+                const int32_t* ri = p.page_table + (int64_t)i * p.ld;
+                const int32_t* rl = p.page_table + (int64_t)ld * p.ld;
+                int mis = l;
+                for (int k0 = 1; k0 < l; k0 += 32 * kU) {
+                    int va[kU], vb[kU];
 #pragma unroll
-            for (int k = kCmpPages - 1; k >= 0; --k)
-                if (k0 + k < k1 && a[k] != b[k]) mis = k0 + k;
-            if (mis < k1) atomicMin(&lcp[ld], mis);
+                    for (int u = 0; u < kU; ++u) {
+                        const int k = k0 + u * 32 + lane;
+                        va[u] = k < l ? ri[k] : 0;
+                        vb[u] = k < l ? rl[k] : 0;
+                    }
+#pragma unroll
+                    for (int u = 0; u < kU; ++u) {
+                        const int k = k0 + u * 32 + lane;
+                        if (k < l && va[u] != vb[u]) mis = min(mis, k);
+                    }
+                }
+                mis = __reduce_min_sync(0xffffffffu, mis);
+                if (lane == 0 && mis < l) atomicMin(&lcp[ld], mis);
+            }
         }
         __syncthreads();
         // group ids in leader order (a deterministic plan) and member slot ranges
@@ -292,6 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
                 cg.unit_off = 0;
                 cg.n_units = 0;
                 store_record(&cgroups[gid], cg);
+                scg[gid] = cg;
                 sa[kMpos][i] = moff;  // next free member slot of the group
                 moff += cnt[i];
                 ++gid;
@@ -306,12 +344,13 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
                 sa[kCgid][i] = is_group_leader(leader, cnt, lcp, ld, p.min_cascade_pages) ? sa[kCgid][ld] : -1;
         }
         __syncthreads();
+        }  // some candidates share a first page
     }
     auto casc_of = [&](int i) { return casc ? sa[kCgid][i] : -1; };
     // prefix length (keys) of request i when it is a cascade member, else 0
     auto prefix_of = [&](int i) {
         const int g = casc_of(i);
-        return g >= 0 ? cgroups[g].prefix_len : 0;
+        return g >= 0 ? scg[g].prefix_len : 0;
     };
 
     // ---- pass 1: validate, count decode groups and prefill tiles, sum decode key extents
@@ -363,18 +402,18 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
 
     // ---- cascade groups: key chunks of each prefix (about casc_target prefix-pass units
     // in total, roughly one per SM), unit ranges, member lists
-    if (casc) {
+    if (casc && n_cgroups > 0) {
         const int ng = n_cgroups;
         const int gch = (ng + kThreads - 1) / kThreads;
         const int g0 = min(ng, tid * gch), g1 = min(ng, g0 + gch);
         int pv[1] = {0};
-        for (int g = g0; g < g1; ++g) pv[0] += casc_pair_units(cgroups[g].n_members, TM, Hkv);
+        for (int g = g0; g < g1; ++g) pv[0] += casc_pair_units(scg[g].n_members, TM, Hkv);
         int pt[1];
         block_scan<1>(pv, pt, s_tmp1);
         const int pair_units = max(pt[0], 1);
         int uv[1] = {0};
         for (int g = g0; g < g1; ++g) {
-            const CascGroup cg = cgroups[g];
+            const CascGroup cg = scg[g];
             int nc = (p.lay.casc_target + pair_units - 1) / pair_units;
             nc = max(1, min(nc, min(kMaxCascChunks, (cg.prefix_len + kPreKeys - 1) / kPreKeys)));
             const int ck = ((cg.prefix_len + nc - 1) / nc + kPreKeys - 1) / kPreKeys * kPreKeys;
@@ -384,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         block_scan<1>(uv, ut, s_tmp1);
         int uoff = uv[0];
         for (int g = g0; g < g1; ++g) {
-            CascGroup cg = cgroups[g];
+            CascGroup cg = scg[g];
             int nc = (p.lay.casc_target + pair_units - 1) / pair_units;
             nc = max(1, min(nc, min(kMaxCascChunks, (cg.prefix_len + kPreKeys - 1) / kPreKeys)));
             const int ck = ((cg.prefix_len + nc - 1) / nc + kPreKeys - 1) / kPreKeys * kPreKeys;
@@ -395,6 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
             sa[kCUoff][g] = uoff;
             uoff += cg.n_units;
             store_record(&cgroups[g], cg);
+            scg[g] = cg;
         }
         if (tid == 0) s_casc_units = ut[0];
         // members are listed by their decode group (a member has one new token, so exactly one)
@@ -439,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
                 const int ext = L - n + min((g + 1) * TB, n) - lp;
                 int per;
                 const int s = split_ranges(ext, chunk, &per);
-                const int nparts = s + (cg >= 0 ? cgroups[cg].n_chunks : 0);
+                const int nparts = s + (cg >= 0 ? scg[cg].n_chunks : 0);
                 cnt2[0] += s;
                 if (nparts > 1) cnt2[1] += nparts;
                 const int last = max(0, ext - (s - 1) * per);
@@ -478,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         // (cascade group, key chunk, pair of member tiles, kv head)
         const int y = x - tot3[1];
         const int g = find_bucket(sa[kCUoff], n_cgroups, y);
-        const CascGroup cgr = cgroups[g];
+        const CascGroup cgr = scg[g];
         const int ly = y - cgr.unit_off;
         const int pu = casc_pair_units(cgr.n_members, TM, Hkv);
         const int c = ly / pu, rest = ly % pu;
@@ -549,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
                 const int kv_end = L - n + a0 + na;
                 int per;
                 const int s = split_ranges(kv_end - lp, chunk, &per);
-                const int nparts = s + (cg >= 0 ? cgroups[cg].n_chunks : 0);
+                const int nparts = s + (cg >= 0 ? scg[cg].n_chunks : 0);
                 DecGroup dg;
                 dg.req = i;
                 dg.tok0 = c0 + a0;
@@ -595,9 +635,16 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     // ---- derived slot mapping: the new tokens are each request's last q_len positions
     if (run && p.derived_slots != nullptr) {
         uint32_t perr = 0;
+        if (d_tok >= 0) {  // single-token request, page id loaded at the start
+            int64_t slot = -1;
+            if (d_page < 0 || d_page >= p.num_pages) perr |= kErrPage;
+            else slot = (int64_t)d_page * ps + d_pos % ps;
+            p.derived_slots[d_tok] = slot;
+        }
         for (int t = tid; t < p.total_tokens; t += kThreads) {
             const int i = find_bucket(cu, B, t);  // request i with cu[i] <= t < cu[i+1]
             const int n = cu[i + 1] - cu[i], L = lens[i];
+            if (n == 1 && chunk_req == 1) continue;  // written above
             const int pos = L - n + (t - cu[i]);
             const int64_t page = p.page_table[(int64_t)i * p.ld + pos / ps];
             int64_t slot = -1;
@@ -626,7 +673,8 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
 
 size_t prepare_smem_bytes(int smem_batch, bool cascade) {
     size_t words = (size_t)kNumArrays * (smem_batch + 1);
-    if (cascade) words += 2 * ((size_t)1 << casc_hash_bits(smem_batch));
+    // hash table, then one group record per pair of requests
+    if (cascade) words += 2 * ((size_t)1 << casc_hash_bits(smem_batch)) + (smem_batch / 2 + 1) * (sizeof(CascGroup) / 4);
     return words * sizeof(int32_t);
 }
 
