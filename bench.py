@@ -48,11 +48,16 @@ def parse():
 # what they were at capture time; after any change the roofline reports null.
 NCU_TRAFFIC = {
     ("decode", "decode"): {
-        "bytes": 619.825152e6,
-        "sources": ["paged_variable_length_gb300/csrc/decode.cu", "paged_variable_length_gb300/csrc/device_utils.cuh",
-                    "paged_variable_length_gb300/csrc/pva_internal.h"],
-        "sha256_16": "117427c2844f34db",
+        "bytes": 619.82592e6,
+        "sources": ['paged_variable_length_gb300/csrc/decode.cu', 'paged_variable_length_gb300/csrc/device_utils.cuh', 'paged_variable_length_gb300/csrc/pva_internal.h'],
+        "sha256_16": "295c00393bba6fbd",
         "summary": "profiles/decode_kernel_decode_workload.md",
+    },
+    ("tensor_core", "prefill"): {
+        "bytes": 223.674112e6,
+        "sources": ['paged_variable_length_gb300/csrc/prefill_tc.cu', 'paged_variable_length_gb300/csrc/device_utils.cuh', 'paged_variable_length_gb300/csrc/tc_utils.cuh', 'paged_variable_length_gb300/csrc/pva_internal.h'],
+        "sha256_16": "740fc5b9e177d26a",
+        "summary": "profiles/prefill_kernel_prefill_workload.md",
     },
 }
 

@@ -438,14 +438,19 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(ForwardParams p) {
         dev::grid_dep_wait();
         return;
     }
-    dev::grid_dep_wait();
     const DecGroup* groups = reinterpret_cast<const DecGroup*>(p.ws + p.lay.dec_groups);
     const float* plse = reinterpret_cast<const float*>(p.ws + p.lay.partial_lse);
     const float* pout = reinterpret_cast<const float*>(p.ws + p.lay.partial_o);
     const int rps = p.lay.rows_per_slot, Hq = p.num_qo_heads;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // the group records come from the plan (complete before the forward began): the first
+    // one is read before the wait for the decode grid, only the partials after it
+    DecGroup dg_next{};
+    if ((int)blockIdx.x < n_groups) dg_next = groups[blockIdx.x];
+    dev::grid_dep_wait();
     for (int gi = blockIdx.x; gi < n_groups; gi += gridDim.x) {
-        const DecGroup dg = groups[gi];
+        const DecGroup dg = dg_next;
+        if (gi + (int)gridDim.x < n_groups) dg_next = groups[gi + gridDim.x];
         const int np = dg.nparts;
         if (np <= 1) continue;
         const int rows = dg.ntok * Hq;
