@@ -297,3 +297,28 @@ def test_cascade_group_size_and_tile_edges():
 def test_cascade_with_group_of_seven_heads():
     wl = _cascade_batch(4, Hq=28, Hkv=4, D=128, ps=16)
     _full_check(wl)
+
+
+# ------------------------------------------------------------------ head_dim 64 on the tensor-core path
+
+D64_CASES = [
+    # (Hq, Hkv, ps, q_lens, kv_lens): every batch has a request with q_len * G > 16 rows
+    (8, 8, 16, [40, 1, 300], [40, 700, 300]),          # MHA: prefills, a decode
+    (16, 8, 4, [100, 3, 17], [228, 3, 50]),            # G = 2: chunked prefill on a cached prefix
+    (32, 8, 1, [260, 1, 9], [260, 1500, 100]),         # G = 4, token slots
+    (28, 4, 16, [129, 255], [1000, 255]),              # G = 7, ragged tiles
+]
+
+
+@pytest.mark.parametrize("case", D64_CASES, ids=[f"d64-{c[0]}-{c[1]}-ps{c[2]}" for c in D64_CASES])
+def test_head_dim_64_tensor_core_path(case):
+    Hq, Hkv, ps, ql, kl = case
+    wl = W.custom(ql, kl, Hq, Hkv, 64, ps, seed=sum(ql))
+    _, eng = _full_check(wl)
+    assert pva.attn_debug_plan_counts(eng.meta)["pre_tiles"] > 0
+
+
+def test_head_dim_64_cascade():
+    wl = _cascade_batch(6, Hq=16, Hkv=4, D=64, ps=16)
+    _, eng = _full_check(wl)
+    assert pva.attn_debug_plan_counts(eng.meta)["casc_groups"] > 0
