@@ -218,23 +218,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         // data needs, and those bursts slowed the tensor core's operand reads).  Each lane
         // computes the source offsets of two of its warp's rows into the warp's own table in
         // shared memory, which the copy loop reads back (one broadcast load per copy).
-        // With pages of 16 or more slots, K and V rows are instead copied one thread per row
-        // (16 chunks each): there a copy instruction's 32 rows lie in two pages, so address
-        // translation stays local, and that mapping measured about 10 % faster; with small
-        // pages (a token-slot pool) 32 rows per instruction meant 32 random translations,
-        // and the two-rows-per-instruction mapping is 3.7 times faster.  A page of a few rows per kv head is too small a box for TMA
-        // to stream efficiently, and rows past kv_len are not copied.  The MMA thread orders
-        // these generic-proxy writes before its tensor-core reads with a proxy fence after it
-        // has waited on the tile's barrier.
+        // With pages of 16 or more slots, K and V rows are copied by 8 lanes per 128-byte
+        // half row instead (4 rows per instruction, the offsets of a lane's 11 rows kept in
+        // registers): that touches as few lines per instruction and issues faster there.
+        // With a token-slot pool the two-rows-per-instruction form is faster: fewer random
+        // address translations per instruction.  A page of a few rows per kv head is too
+        // small a box for TMA to stream efficiently (about 270 cycles per box measured), and
+        // rows past kv_len are not copied.  The MMA thread orders these generic-proxy writes
+        // before its tensor-core reads with a proxy fence after it has waited on the tile's
+        // barrier.
         constexpr int kChunks = D / 8;              // 16-byte chunks per row
         constexpr int kRowsPerCopy = 32 / kChunks;  // rows one copy instruction moves
         constexpr int kStride = 3 * kRowsPerCopy;   // rows the three warps move per step
         constexpr int kCopyIters = (kPreRows + kStride - 1) / kStride;
         static_assert(kCopyIters * kRowsPerCopy <= 64, "two row offsets per lane");
         const int pwarp = warp - kProducerWarp0;  // 0..2
-        const int pt_id = pwarp * 32 + lane;       // 0..95
         const int chunk = lane % kChunks, sub = lane / kChunks;
-        const bool row_per_thread = p.page_size >= 16;
+        const bool paged = p.page_size >= 16;  // K/V gather mapping, see above
         const int ps_mask = p.page_size - 1;
         // row of a tile held by this warp's row index k (k = copy step * kRowsPerCopy + sub)
         auto row_of = [&](int k) { return pwarp * kRowsPerCopy + (k % kRowsPerCopy) + (k / kRowsPerCopy) * kStride; };
@@ -271,28 +271,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         };
-        // one thread per row: a row -> its 16-byte chunks, swizzled
-        auto copy_row = [&](uint8_t* tile, int r, const uint16_t* src) {
-            const uint32_t d0 = dev::smem_u32(tile) + r * 128;
-#pragma unroll
-            for (int c = 0; c < D / 8; ++c) {
-                const uint32_t dst = d0 + (c >> 3) * kRegion + (((c & 7) ^ (r & 7)) << 4);
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + c * 8) : "memory");
-            }
-        };
-        // the K / V rows this lane computes offsets for (i = 0, 1)
-        auto kv_row = [&](int i) { return row_per_thread ? pt_id + i * kProducerThreads : row_of(lane + 32 * i); };
-        auto copy_kv = [&](uint8_t* tile, const int64_t (&off)[2], const uint16_t* base) {
-            if (row_per_thread) {
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const int r = pt_id + i * kProducerThreads;
-                    if (r < kPreRows && off[i] >= 0) copy_row(tile, r, base + off[i]);
-                }
-            } else {
-                copy_tile(tile, off[0], off[1], base);
-            }
-        };
         uint32_t it = 0;
         const bool fetcher = pwarp == 0 && lane == 0;
         if (fetcher) queue_push(b, 0, counter, n_units, err);
@@ -326,53 +304,100 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- K and V tiles
             const int kv_end = uv.key_end;
             const int nkt = (kv_end - uv.key_base + kPreKeys - 1) / kPreKeys;
-            // page ids of this lane's two rows of tile j: read one tile ahead, so that the
-            // page-table round trip overlaps the copies and waits of the tile before
-            auto page_ids = [&](int j, int32_t (&pg)[2]) {
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const int r = kv_row(i);
-                    const int key = uv.key_base + j * kPreKeys + r;
-                    pg[i] = (j < nkt && r < kPreRows && key < kv_end) ? prow[key >> p.page_shift] : 0;
-                }
-            };
-            // (with one thread per row the page ids are read just before use: reading them a
-            // tile ahead measured slower there)
-            int32_t pg_next[2] = {0, 0};
-            if (!row_per_thread) page_ids(0, pg_next);
             bool ok = true;
-            for (int j = 0; j < nkt && ok; ++j, ++it) {
-                const int st = it & 1;
-                const uint32_t ph = (it >> 1) & 1;
-                int32_t pg[2] = {pg_next[0], pg_next[1]};
-                if (row_per_thread) page_ids(j, pg);
-                else page_ids(j + 1, pg_next);
-                // element offsets of this lane's two rows; -1: past kv_len
-                int64_t off[2] = {-1, -1};
+            if (paged) {
+                // 8 lanes per 128-byte half row, 4 rows per copy instruction; each lane keeps
+                // the source offsets of its kG8 rows (pwarp * 4 + lane / 8 + 12 m) in registers
+                constexpr int kG8 = (kPreRows + 11) / 12;
+                const int grp = lane >> 3, c8 = lane & 7;
+                for (int j = 0; j < nkt && ok; ++j, ++it) {
+                    const int st = it & 1;
+                    const uint32_t ph = (it >> 1) & 1;
+                    int64_t off[kG8];
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const int r = kv_row(i);
-                    const int key = uv.key_base + j * kPreKeys + r;
-                    if (r >= kPreRows || key >= kv_end) continue;
-                    int64_t page = pg[i];
-                    if (page < 0 || page >= p.num_pages) {
-                        dev::set_error(err, kErrPage);
-                        page = 0;
+                    for (int m = 0; m < kG8; ++m) {
+                        const int r = pwarp * 4 + grp + 12 * m;
+                        const int key = uv.key_base + j * kPreKeys + r;
+                        off[m] = -1;
+                        if (r < kPreRows && key < kv_end) {
+                            int64_t page = prow[key >> p.page_shift];
+                            if (page < 0 || page >= p.num_pages) {
+                                dev::set_error(err, kErrPage);
+                                page = 0;
+                            }
+                            off[m] = (((page << p.page_shift) + (key & ps_mask)) * p.num_kv_heads + pt.kvh) * D + c8 * 8;
+                        }
                     }
-                    off[i] = (((page << p.page_shift) + (key & ps_mask)) * p.num_kv_heads + pt.kvh) * D;
+                    auto copy_g8 = [&](uint8_t* tile, const uint16_t* base) {
+                        const uint32_t t0 = dev::smem_u32(tile);
+#pragma unroll
+                        for (int m = 0; m < kG8; ++m) {
+                            const int r = pwarp * 4 + grp + 12 * m;
+                            if (off[m] < 0) continue;
+                            const uint32_t d = t0 + r * 128 + ((c8 ^ (r & 7)) << 4);
+                            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(base + off[m]));
+                            if (D == 128)
+                                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d + kRegion),
+                                             "l"(base + off[m] + 64));
+                        }
+                    };
+                    if (!wait_or_abort(&b->k_empty[st], ph ^ 1, b, err)) {
+                        ok = false;
+                        break;
+                    }
+                    copy_g8(smem + L::kK + st * L::kTile, p.k_pool);
+                    issue(&b->k_full[st]);
+                    if (!wait_or_abort(&b->v_empty[st], ph ^ 1, b, err)) {
+                        ok = false;
+                        break;
+                    }
+                    copy_g8(smem + L::kV + st * L::kTile, p.v_pool);
+                    issue(&b->v_full[st]);
                 }
-                if (!wait_or_abort(&b->k_empty[st], ph ^ 1, b, err)) {
-                    ok = false;
-                    break;
+            } else {
+                // token-slot pool: two rows per copy instruction through the offset table;
+                // page ids of this lane's two rows are read a tile ahead
+                auto page_ids = [&](int j, int32_t (&pg)[2]) {
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const int r = row_of(lane + 32 * i);
+                        const int key = uv.key_base + j * kPreKeys + r;
+                        pg[i] = (j < nkt && r < kPreRows && key < kv_end) ? prow[key >> p.page_shift] : 0;
+                    }
+                };
+                int32_t pg_next[2];
+                page_ids(0, pg_next);
+                for (int j = 0; j < nkt && ok; ++j, ++it) {
+                    const int st = it & 1;
+                    const uint32_t ph = (it >> 1) & 1;
+                    const int32_t pg[2] = {pg_next[0], pg_next[1]};
+                    page_ids(j + 1, pg_next);
+                    int64_t off[2] = {-1, -1};
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const int r = row_of(lane + 32 * i);
+                        const int key = uv.key_base + j * kPreKeys + r;
+                        if (r >= kPreRows || key >= kv_end) continue;
+                        int64_t page = pg[i];
+                        if (page < 0 || page >= p.num_pages) {
+                            dev::set_error(err, kErrPage);
+                            page = 0;
+                        }
+                        off[i] = (((page << p.page_shift) + (key & ps_mask)) * p.num_kv_heads + pt.kvh) * D;
+                    }
+                    if (!wait_or_abort(&b->k_empty[st], ph ^ 1, b, err)) {
+                        ok = false;
+                        break;
+                    }
+                    copy_tile(smem + L::kK + st * L::kTile, off[0], off[1], p.k_pool);
+                    issue(&b->k_full[st]);
+                    if (!wait_or_abort(&b->v_empty[st], ph ^ 1, b, err)) {
+                        ok = false;
+                        break;
+                    }
+                    copy_tile(smem + L::kV + st * L::kTile, off[0], off[1], p.v_pool);
+                    issue(&b->v_full[st]);
                 }
-                copy_kv(smem + L::kK + st * L::kTile, off, p.k_pool);
-                issue(&b->k_full[st]);
-                if (!wait_or_abort(&b->v_empty[st], ph ^ 1, b, err)) {
-                    ok = false;
-                    break;
-                }
-                copy_kv(smem + L::kV + st * L::kTile, off, p.v_pool);
-                issue(&b->v_full[st]);
             }
             if (!ok) break;
         }
