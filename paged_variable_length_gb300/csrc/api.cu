@@ -78,7 +78,7 @@ Layout make_layout(const pva_config* c, int sm_count, int target_units = 0) {
     L.partial_lse = take(sizeof(float) * (size_t)L.max_partial * L.rows_per_slot);
     L.req_scratch = take(sizeof(int32_t) * 4 * (size_t)(c->max_batch + 1));
     L.casc_groups = take(sizeof(CascGroup) * (size_t)L.max_casc_groups);
-    L.casc_members = take(sizeof(int32_t) * (size_t)c->max_batch);
+    L.casc_members = take(sizeof(int32_t) * 2 * (size_t)c->max_batch);
     L.total = off;
     return L;
 }

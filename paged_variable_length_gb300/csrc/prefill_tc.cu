@@ -162,9 +162,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const PreTile* units = reinterpret_cast<const PreTile*>(p.ws + p.lay.pre_tiles);
     int32_t* counter = &hdr->pad[1];  // zeroed by the store kernel of this forward
-    const DecGroup* groups = reinterpret_cast<const DecGroup*>(p.ws + p.lay.dec_groups);
     const CascGroup* cgroups = reinterpret_cast<const CascGroup*>(p.ws + p.lay.casc_groups);
-    const int32_t* cmembers = reinterpret_cast<const int32_t*>(p.ws + p.lay.casc_members);
+    const int2* cmembers = reinterpret_cast<const int2*>(p.ws + p.lay.casc_members);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.group, Hq = p.num_qo_heads;
@@ -294,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     oq[i] = -1;
                     if (r < kPreRows && t < ntok) {
                         const int token =
-                            uv.casc ? groups[cmembers[pt.tok0 + h * TM + t]].tok0 : pt.tok0 + h * TM + t;
+                            uv.casc ? cmembers[pt.tok0 + h * TM + t].x : pt.tok0 + h * TM + t;
                         oq[i] = ((int64_t)token * Hq + pt.kvh * G + (r - t * G)) * D;
                     }
                 }
@@ -631,9 +630,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++n_u;
             if (valid && uv.casc) {
                 // prefix-pass partial of a cascade member: normalised O and the log2-domain
-                // LSE into the member's slot for this key chunk (merged by the decode kernel)
-                const DecGroup dg = groups[cmembers[pt.tok0 + h * TM + row / G]];
-                const int slot = dg.pbase + dg.nsplit + pt.qpos0;
+                // LSE into the member's slot for this key chunk (combined by the merge kernel)
+                const int slot = cmembers[pt.tok0 + h * TM + row / G].y + pt.qpos0;
                 const int prow = pt.kvh * G + row % G;  // one new token: row = q head
                 float* po = reinterpret_cast<float*>(p.ws + p.lay.partial_o) +
                             ((int64_t)slot * p.lay.rows_per_slot + prow) * D;

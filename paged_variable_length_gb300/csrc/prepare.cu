@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     DecGroup* groups = reinterpret_cast<DecGroup*>(p.ws + p.lay.dec_groups);
     PreTile* tiles = reinterpret_cast<PreTile*>(p.ws + p.lay.pre_tiles);
     CascGroup* cgroups = reinterpret_cast<CascGroup*>(p.ws + p.lay.casc_groups);
-    int32_t* cmembers = reinterpret_cast<int32_t*>(p.ws + p.lay.casc_members);
+    int2* cmembers = reinterpret_cast<int2*>(p.ws + p.lay.casc_members);
 
     extern __shared__ int32_t dyn[];
     __shared__ uint32_t s_err;
@@ -437,11 +437,11 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
             scg[g] = cg;
         }
         if (tid == 0) s_casc_units = ut[0];
-        // members are listed by their decode group (a member has one new token, so exactly one)
+        // each member takes a slot of its group's member list (filled when its decode
+        // group is written below); the first-page array is free again
         for (int i = tid; i < B; i += kThreads) {
             if (sa[kCgid][i] < 0) continue;
-            const int slot = atomicAdd(&sa[kMpos][sa[kLeader][i]], 1);
-            cmembers[slot] = sa[kGoff][i];
+            sa[kFirst][i] = atomicAdd(&sa[kMpos][sa[kLeader][i]], 1);
         }
     }
     __syncthreads();
@@ -603,6 +603,9 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
                 dg.tail0 = lp;
                 dg.pad0 = dg.pad1 = dg.pad2 = dg.pad3 = dg.pad4 = dg.pad5 = 0;
                 store_record(&groups[gi], dg);
+                // member list entry of a shared-prefix member (one new token): its q row and
+                // the partial slot of prefix chunk 0
+                if (cg >= 0) cmembers[sa[kFirst][i]] = make_int2(dg.tok0, pi + s);
                 for (int u = 0; u < s; ++u) {
                     DecUnit du;
                     du.group = gi;

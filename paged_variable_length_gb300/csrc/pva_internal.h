@@ -93,7 +93,7 @@ struct CascGroup {
     int32_t leader;       // request whose page-table row addresses the prefix
     int32_t prefix_len;   // keys [0, prefix_len) are shared
     int32_t n_members;
-    int32_t member_off;   // members[member_off ..] hold the members' decode-group indices
+    int32_t member_off;   // members[member_off ..]: (token, first prefix partial slot) per member
     int32_t n_chunks;     // prefix pass key chunks
     int32_t chunk_keys;   // keys per chunk (multiple of kPreKeys)
     int32_t unit_off;     // first prefix-pass unit of the group (relative to the cascade units)
@@ -130,7 +130,7 @@ struct Layout {
     size_t partial_lse;  // fp32 [max_partial][rows_per_slot]
     size_t req_scratch;  // int32 [max_batch * 4] prepare scratch
     size_t casc_groups;  // CascGroup [max_casc_groups]
-    size_t casc_members; // int32 [max_batch]
+    size_t casc_members; // int2 [max_batch]: member's token, partial slot of its prefix chunk 0
     size_t total;
     int32_t max_dec_units;
     int32_t max_dec_groups;
