@@ -46,8 +46,8 @@ namespace {
 // for registers that are not there).
 constexpr int kThreads = 384;
 constexpr int kRegsLaunch = 168;
-constexpr int kRegsSoftmax = 208;
-constexpr int kRegsCtrl = 88;
+constexpr int kRegsSoftmax = 200;
+constexpr int kRegsCtrl = 104;
 static_assert(8 * kRegsSoftmax + 4 * kRegsCtrl == 12 * kRegsLaunch, "register split must balance");
 constexpr int kMmaWarp = 8;
 constexpr int kProducerWarp0 = 9;
@@ -560,41 +560,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float mx = dev::fmax3(dev::fmax3(mxa[0], mxa[1], mxa[2]), dev::fmax3(mxa[3], mxa[4], mxa[5]),
                                             fmaxf(mxa[6], mxa[7]));
                 const float m_new = fmaxf(m, mx * sl);  // log2 units (sl = scale * log2 e > 0)
+                // rescale decision: the row maximum grew by more than the threshold; O itself is
+                // rescaled after P is written (the S registers are dead by then), before P is
+                // signalled, so the PV product of this tile adds to the rescaled O
+                float alpha = 1.f;
+                bool resc = false;
                 if (j == 0) {
                     m = m_new;
                 } else {
-                    // O_h is stable here: P_h(j-1) V was issued before S_h(j), whose
-                    // completion this thread has just observed
-                    const bool resc = m_new > m + kRescaleThreshold;
-                    if (__any_sync(0xffffffffu, resc)) {
-                        const float alpha = resc ? dev::fast_exp2(m - m_new) : 1.f;
-#pragma unroll
-                        for (int c = 0; c < D / 32; ++c) {
-                            float v[32];
-                            tc::tmem_ld32_async(t_o + c * 32, v);
-                            tc::tmem_wait_ld_regs(v);
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] *= alpha;
-                            tc::tmem_st32(t_o + c * 32, v);
-                        }
-                        if (resc) {
-                            l *= alpha;
-                            m = m_new;
-                        }
+                    resc = m_new > m + kRescaleThreshold;
+                    if (resc) {
+                        alpha = dev::fast_exp2(m - m_new);
+                        l *= alpha;
+                        m = m_new;
                     }
                 }
                 const float nmu = m == -INFINITY ? 0.f : -m;
                 float lsa[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) lsa[i] = 0.f;
-                // P = exp2(s * sl - m) as packed bf16 pairs, 32 columns (64 keys) per TMEM store;
-                // the scale-and-shift and the row sum run as packed fp32 pairs
+                // P = exp2(s * sl - m) as packed bf16 pairs, 16 columns (32 keys) per TMEM store
+                // (a quarter of the row at a time keeps fewer registers live); the
+                // scale-and-shift and the row sum run as packed fp32 pairs
 #pragma unroll
-                for (int c2 = 0; c2 < kPreKeys / 64; ++c2) {
-                    uint32_t pk[32];
+                for (int c2 = 0; c2 < kPreKeys / 32; ++c2) {
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int c = c2 * 64 + 2 * i;
+                    for (int i = 0; i < 16; ++i) {
+                        const int c = c2 * 32 + 2 * i;
                         float x0, x1;
                         dev::ffma2(x0, x1, s[c >> 5][c & 31], s[(c + 1) >> 5][(c + 1) & 31], sl, sl, nmu, nmu);
                         const float e0 = dev::fast_exp2(x0);
@@ -602,9 +595,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         dev::fadd2(lsa[2 * (i & 3)], lsa[2 * (i & 3) + 1], e0, e1);
                         pk[i] = dev::pack_bf16x2(e0, e1);
                     }
-                    tc::tmem_st32u(t_s + c2 * 32, pk);
+                    tc::tmem_st16u(t_s + c2 * 16, pk);
                 }
                 l += ((lsa[0] + lsa[1]) + (lsa[2] + lsa[3])) + ((lsa[4] + lsa[5]) + (lsa[6] + lsa[7]));
+                if (__any_sync(0xffffffffu, resc)) {
+                    // O_h is stable here: P_h(j-1) V was issued before S_h(j), whose
+                    // completion this thread has observed
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        float v[32];
+                        tc::tmem_ld32_async(t_o + c * 32, v);
+                        tc::tmem_wait_ld_regs(v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] *= alpha;
+                        tc::tmem_st32(t_o + c * 32, v);
+                    }
+                }
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
                 __syncwarp();
