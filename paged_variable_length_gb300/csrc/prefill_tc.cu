@@ -312,21 +312,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < nkt && ok; ++j, ++it) {
                     const int st = it & 1;
                     const uint32_t ph = (it >> 1) & 1;
+                    // all page ids first (independent loads in flight together), then the checks:
+                    // an error report between the loads would order them one after another
+                    int32_t pg[kG8];
+#pragma unroll
+                    for (int m = 0; m < kG8; ++m) {
+                        const int r = pwarp * 4 + grp + 12 * m;
+                        const int key = uv.key_base + j * kPreKeys + r;
+                        pg[m] = (r < kPreRows && key < kv_end) ? prow[key >> p.page_shift] : 0;
+                    }
                     int64_t off[kG8];
+                    bool bad = false;
 #pragma unroll
                     for (int m = 0; m < kG8; ++m) {
                         const int r = pwarp * 4 + grp + 12 * m;
                         const int key = uv.key_base + j * kPreKeys + r;
                         off[m] = -1;
                         if (r < kPreRows && key < kv_end) {
-                            int64_t page = prow[key >> p.page_shift];
+                            int64_t page = pg[m];
                             if (page < 0 || page >= p.num_pages) {
-                                dev::set_error(err, kErrPage);
+                                bad = true;
                                 page = 0;
                             }
                             off[m] = (((page << p.page_shift) + (key & ps_mask)) * p.num_kv_heads + pt.kvh) * D + c8 * 8;
                         }
                     }
+                    if (bad) dev::set_error(err, kErrPage);
                     auto copy_g8 = [&](uint8_t* tile, const uint16_t* base) {
                         const uint32_t t0 = dev::smem_u32(tile);
 #pragma unroll
