@@ -17,7 +17,7 @@
 //   * warps 9-11 (producers) gather Q and K/V tiles row by row from the paged
 //     pool with 16-byte async copies into the 128-byte-swizzled layout of the
 //     MMA operands (rows past kv_len are not read); two K and two V stages;
-//   * warp 8 issues the MMAs from one thread, in the order
+//   * warp 8 issues the MMAs (one elected lane of the converged warp), in the order
 //     PV0(j), S0(j+1), PV1(j), S1(j+1): while one softmax warpgroup works on
 //     its S tile the tensor core runs the other tile's products;
 //   * warps 0-3 / 4-7 are the softmax warpgroups of Q tile 0 / 1, one row per
@@ -52,7 +52,7 @@ static_assert(8 * kRegsSoftmax + 4 * kRegsCtrl == 12 * kRegsLaunch, "register sp
 constexpr int kMmaWarp = 8;
 constexpr int kProducerWarp0 = 9;
 constexpr int kProducerThreads = 96;
-// Readers of every work-queue entry: 3 producer warps, the MMA thread, 8 softmax warps.
+// Readers of every work-queue entry: 3 producer warps, the MMA warp, 8 softmax warps.
 constexpr int kQueueReaders = 3 + 1 + 8;
 constexpr int kRegion = 128 * 128;  // one 128-row x 128-byte swizzled region (64 bf16 columns)
 constexpr uint32_t kTmemCols = 512;
@@ -414,103 +414,97 @@ __global__ void __launch_bounds__(kThreads, 1)
         // copies still in flight must land before the CTA may leave
         asm volatile("cp.async.wait_group 0;" ::: "memory");
     } else if (warp == kMmaWarp) {
-        // ============================================================== MMA issuer (one thread)
-        if (lane == 0) {
-            const uint32_t id_qk = tc::idesc_bf16_f32(128, 128, 0, 0);
-            const uint32_t id_pv = tc::idesc_bf16_f32(128, D, 0, 1);
-            uint32_t it = 0;                      // KV tiles across units
-            uint32_t n_p[2] = {0, 0};             // P tiles consumed per Q tile
-            uint32_t n_units_h[2] = {0, 0};       // units that had Q tile h
-            int uc = 0;
-            bool ok = true;
-            auto issue_s = [&](int h, int st) {
-                const uint32_t sq = dev::smem_u32(smem + L::kQ + h * L::kTile);
-                const uint32_t sk = dev::smem_u32(smem + L::kK + st * L::kTile);
+        // ============================================================== MMA issuer (one warp)
+        // The whole warp runs this role with warp-uniform control flow (every wait is voted
+        // across the warp); each MMA and commit is issued by one elected lane.
+        const uint32_t id_qk = tc::idesc_bf16_f32(128, 128, 0, 0);
+        const uint32_t id_pv = tc::idesc_bf16_f32(128, D, 0, 1);
+        constexpr uint32_t kDescHi = tc::smem_desc_hi(1024, tc::kSwizzle128B);
+        constexpr uint32_t kTileLo = L::kTile >> 4;  // one tile, in descriptor address units
+        // descriptor low words: Q tiles and K stages K-major, V stages MN-major (the leading
+        // byte offset of V steps from one 64-column region to the next)
+        const uint32_t q_lo = tc::smem_desc_lo(dev::smem_u32(smem + L::kQ), 16);
+        const uint32_t k_lo = tc::smem_desc_lo(dev::smem_u32(smem + L::kK), 16);
+        const uint32_t v_lo = tc::smem_desc_lo(dev::smem_u32(smem + L::kV), kRegion);
+        auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, wait_or_abort(bar, parity, b, err));
+        };
+        uint32_t it = 0;                      // KV tiles across units
+        uint32_t n_p[2] = {0, 0};             // P tiles consumed per Q tile
+        uint32_t n_units_h[2] = {0, 0};       // units that had Q tile h
+        bool ok = true;
+        // S_h = Q_h K(st)^T: K-steps of 16 columns inside a 128-byte swizzle row, then the
+        // next 64-column region
+        auto issue_s = [&](int h, int st) {
+            const uint32_t a0 = q_lo + h * kTileLo, b0 = k_lo + st * kTileLo;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t ad =
-                        tc::smem_desc(sq + (kk >> 2) * kRegion + (kk & 3) * 32, 16, 1024, tc::kSwizzle128B);
-                    const uint64_t bd =
-                        tc::smem_desc(sk + (kk >> 2) * kRegion + (kk & 3) * 32, 16, 1024, tc::kSwizzle128B);
-                    tc::mma_ss(tmem + 256 * h, ad, bd, id_qk, kk > 0 ? 1u : 0u);
-                }
-                tc::mma_commit(&b->s_full[h]);
-            };
-            // O_h += P_h V(st); P_h is read from TMEM (the first 64 columns of S_h)
-            auto issue_pv = [&](int h, int st, bool first) -> bool {
-                if (!wait_or_abort(&b->p_full[h], n_p[h] & 1, b, err)) return false;
-                ++n_p[h];
-                if (first && n_units_h[h] > 0 && !wait_or_abort(&b->o_free[h], (n_units_h[h] - 1) & 1, b, err))
-                    return false;
-                tc::fence_after_sync();
-                const uint32_t sv = dev::smem_u32(smem + L::kV + st * L::kTile);
-#pragma unroll
-                for (int kk = 0; kk < kPreKeys / 16; ++kk) {
-                    const uint64_t bd = tc::smem_desc(sv + kk * 2048, kRegion, 1024, tc::kSwizzle128B);
-                    tc::mma_ts(tmem + 256 * h + 128, tmem + 256 * h + kk * 8, bd, id_pv,
-                               (first && kk == 0) ? 0u : 1u);
-                }
-                return true;
-            };
-            for (uc = 0; ok; ++uc) {
-                const int u = queue_read(b, uc, lane, err, true);
-                if (u < 0) break;
-                const UnitView uv = unit_view(units[u]);
-                const int nkt0 = uv.nk[0];
-                const int nkt1 = uv.nk[1];
-                const int nkt = nkt1 > nkt0 ? nkt1 : nkt0;
-                if (!wait_or_abort(&b->q_full, uc & 1, b, err)) {
-                    ok = false;
-                    break;
-                }
-                // prologue: S_h(0) for both tiles
-                if (!wait_or_abort(&b->k_full[it & 1], (it >> 1) & 1, b, err)) {
-                    ok = false;
-                    break;
-                }
-                tc::fence_after_sync();
-                tc::fence_proxy_async_smem();  // the producers' generic-proxy copies -> MMA operand reads
-                if (nkt0 > 0) issue_s(0, it & 1);
-                if (nkt1 > 0) issue_s(1, it & 1);
-                tc::mma_commit(&b->k_empty[it & 1]);
-                if (nkt == 1) tc::mma_commit(&b->q_empty);
-                for (int j = 0; j < nkt && ok; ++j) {
-                    const uint32_t t = it + j;
-                    const int st = t & 1, st1 = (t + 1) & 1;
-                    if (!wait_or_abort(&b->v_full[st], (t >> 1) & 1, b, err)) {
-                        ok = false;
-                        break;
-                    }
-                    const bool next = j + 1 < nkt;
-                    if (next && !wait_or_abort(&b->k_full[st1], ((t + 1) >> 1) & 1, b, err)) {
-                        ok = false;
-                        break;
-                    }
-                    tc::fence_after_sync();
-                    tc::fence_proxy_async_smem();
-                    for (int h = 0; h < 2 && ok; ++h) {
-                        const int nk = h ? nkt1 : nkt0;
-                        if (j >= nk) continue;
-                        ok = issue_pv(h, st, j == 0);
-                        if (!ok) break;
-                        if (j == nk - 1) tc::mma_commit(&b->o_ready[h]);
-                        if (j + 1 < nk) issue_s(h, st1);
-                    }
-                    if (!ok) break;
-                    tc::mma_commit(&b->v_empty[st]);
-                    if (next) {
-                        tc::mma_commit(&b->k_empty[st1]);
-                        if (j + 1 == nkt - 1) tc::mma_commit(&b->q_empty);
-                    }
-                }
-                if (nkt0 > 0) ++n_units_h[0];
-                if (nkt1 > 0) ++n_units_h[1];
-                it += nkt;
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (uint32_t)((kk >> 2) * kRegion + (kk & 3) * 32) >> 4;
+                tc::mma_ss_warp(tmem + 256 * h, a0 + off, b0 + off, kDescHi, id_qk, kk > 0 ? 1u : 0u);
             }
-            // every MMA issued must complete before TMEM is released
-            tc::mma_commit(&b->drain);
-            (void)dev::mbar_wait(&b->drain, 0);
+            tc::mma_commit_warp(&b->s_full[h]);
+        };
+        // O_h += P_h V(st); P_h is read from TMEM (the first 64 columns of S_h), V in K-steps
+        // of 16 rows (2048 bytes)
+        auto issue_pv = [&](int h, int st, bool first) -> bool {
+            if (!wait(&b->p_full[h], n_p[h] & 1)) return false;
+            ++n_p[h];
+            if (first && n_units_h[h] > 0 && !wait(&b->o_free[h], (n_units_h[h] - 1) & 1)) return false;
+            tc::fence_after_sync();
+            const uint32_t b0 = v_lo + st * kTileLo;
+#pragma unroll
+            for (int kk = 0; kk < kPreKeys / 16; ++kk)
+                tc::mma_ts_warp(tmem + 256 * h + 128, tmem + 256 * h + kk * 8, b0 + kk * (2048 >> 4), kDescHi, id_pv,
+                                (first && kk == 0) ? 0u : 1u);
+            return true;
+        };
+        for (int uc = 0; ok; ++uc) {
+            const int u = __shfl_sync(0xffffffffu, queue_read(b, uc, lane, err), 0);
+            if (u < 0) break;
+            const UnitView uv = unit_view(units[u]);
+            const int nkt0 = uv.nk[0];
+            const int nkt1 = uv.nk[1];
+            const int nkt = nkt1 > nkt0 ? nkt1 : nkt0;
+            if (!wait(&b->q_full, uc & 1)) break;
+            // prologue: S_h(0) for both tiles
+            if (!wait(&b->k_full[it & 1], (it >> 1) & 1)) break;
+            tc::fence_after_sync();
+            tc::fence_proxy_async_smem();  // the producers' generic-proxy copies -> MMA operand reads
+            if (nkt0 > 0) issue_s(0, it & 1);
+            if (nkt1 > 0) issue_s(1, it & 1);
+            tc::mma_commit_warp(&b->k_empty[it & 1]);
+            if (nkt == 1) tc::mma_commit_warp(&b->q_empty);
+            for (int j = 0; j < nkt && ok; ++j) {
+                const uint32_t t = it + j;
+                const int st = t & 1, st1 = (t + 1) & 1;
+                const bool next = j + 1 < nkt;
+                ok = wait(&b->v_full[st], (t >> 1) & 1) &&
+                     (!next || wait(&b->k_full[st1], ((t + 1) >> 1) & 1));
+                if (!ok) break;
+                tc::fence_after_sync();
+                tc::fence_proxy_async_smem();
+                for (int h = 0; h < 2 && ok; ++h) {
+                    const int nk = h ? nkt1 : nkt0;
+                    if (j >= nk) continue;
+                    ok = issue_pv(h, st, j == 0);
+                    if (!ok) break;
+                    if (j == nk - 1) tc::mma_commit_warp(&b->o_ready[h]);
+                    if (j + 1 < nk) issue_s(h, st1);
+                }
+                if (!ok) break;
+                tc::mma_commit_warp(&b->v_empty[st]);
+                if (next) {
+                    tc::mma_commit_warp(&b->k_empty[st1]);
+                    if (j + 1 == nkt - 1) tc::mma_commit_warp(&b->q_empty);
+                }
+            }
+            if (nkt0 > 0) ++n_units_h[0];
+            if (nkt1 > 0) ++n_units_h[1];
+            it += nkt;
         }
+        // every MMA issued must complete before TMEM is released
+        tc::mma_commit_warp(&b->drain);
+        (void)dev::mbar_wait(&b->drain, 0);
         __syncwarp();
     }  // warps 10-11: idle
     } else {
