@@ -29,7 +29,11 @@
 // 64 columns) and O_h at 256h+128 .. 256h+255.
 // Every wait is bounded; a timeout sets PVA_DEVERR_TIMEOUT and the CTA winds
 // down (outstanding copies and MMAs waited for, TMEM freed) without trapping.
+#include <cuda.h>  // CUtensorMap and the tensor-map encoder's types (resolved through the runtime)
 #include <cuda_runtime.h>
+
+#include <cstring>
+#include <mutex>
 
 #include "device_utils.cuh"
 #include "pva_internal.h"
@@ -140,9 +144,11 @@ __device__ __forceinline__ UnitView unit_view(const PreTile& pt) {
     return v;
 }
 
+// q_map: Q as a 3-D tensor (D, Hq, T) whose box is one 64-column half of a Q tile (64
+// columns x G heads x TM tokens, rows in tile order); used when q_tma is nonzero.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_kernel(const ForwardParams p) {
+    prefill_kernel(const ForwardParams p, const __grid_constant__ CUtensorMap q_map, const int q_tma) {
     using L = SmemMap<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -283,6 +289,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 p.page_table + (int64_t)(uv.casc ? cgroups[-1 - pt.req].leader : pt.req) * p.ld;
             // ---- Q: row r = token (or cascade member) r / G, head r % G of each tile
             if (uc > 0 && !wait_or_abort(&b->q_empty, (uc - 1) & 1, b, err)) break;
+            if (q_tma && !uv.casc) {
+                // consecutive tokens: the G heads of a kv head are adjacent rows of q, so a tile
+                // half is one tensor box (tokens past the batch read as zeros; rows of tokens
+                // past the unit's are never used).  The producers' arrivals below still count,
+                // and the phase also waits for the boxes' bytes.
+                if (pwarp == 0 && lane == 0) {
+                    tc::fence_proxy_async_smem();  // earlier gathers into these tiles -> async-proxy writes
+                    const uint32_t box = 128u * (uint32_t)(G * TM);
+                    dev::mbar_expect_tx(&b->q_full, box * (D / 64) * ((pt.ntok0 > 0) + (pt.ntok1 > 0)));
+                    for (int h = 0; h < 2; ++h) {
+                        if ((h ? pt.ntok1 : pt.ntok0) <= 0) continue;
+                        for (int x = 0; x < D / 64; ++x)
+                            tc::tma_load_3d(smem + L::kQ + h * L::kTile + x * kRegion, &q_map, x * 64, pt.kvh * G,
+                                            pt.tok0 + h * TM, &b->q_full);
+                    }
+                }
+            } else
             for (int h = 0; h < 2; ++h) {
                 const int ntok = h ? pt.ntok1 : pt.ntok0;
                 int64_t oq[2];
@@ -682,6 +705,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn tensor_map_encoder() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+// The Q tensor map of the kernel; false when it cannot be built (the kernel then gathers
+// Q rows with async copies, as it does for cascade members).
+bool encode_q_map(const ForwardParams& p, int D, CUtensorMap* m) {
+    const EncodeTiledFn enc = tensor_map_encoder();
+    if (enc == nullptr || p.total_tokens <= 0 || (reinterpret_cast<uintptr_t>(p.q) & 15) != 0) return false;
+    const int G = p.group, TM = kPreRows / G;
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.num_qo_heads, (cuuint64_t)p.total_tokens};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)p.num_qo_heads * D * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)TM};
+    const cuuint32_t elem_strides[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(p.q), dims, strides, box, elem_strides,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D>
 cudaError_t launch_p(const ForwardParams& p, int ctas, cudaStream_t s) {
     const size_t smem = SmemMap<D>::kBytes + 1024;
@@ -698,7 +754,10 @@ cudaError_t launch_p(const ForwardParams& p, int ctas, cudaStream_t s) {
         launch_regs = attr.numRegs;
     }
     if (launch_regs != kRegsLaunch) return cudaErrorInvalidConfiguration;
-    return launch_programmatic(prefill_kernel<D>, (unsigned)ctas, (unsigned)kThreads, smem, s, p);
+    CUtensorMap q_map;
+    memset(&q_map, 0, sizeof(q_map));
+    const int q_tma = encode_q_map(p, D, &q_map) ? 1 : 0;
+    return launch_programmatic(prefill_kernel<D>, (unsigned)ctas, (unsigned)kThreads, smem, s, p, q_map, q_tma);
 }
 
 }  // namespace
