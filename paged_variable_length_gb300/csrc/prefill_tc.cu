@@ -458,15 +458,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         // S_h = Q_h K(st)^T: K-steps of 16 columns inside a 128-byte swizzle row, then the
         // next 64-column region
-        auto issue_s = [&](int h, int st) {
+        // `mid` runs after the first half of the MMAs, when the tensor core's queue is full:
+        // work placed there overlaps the queued products instead of leaving the queue empty
+        auto issue_s = [&](int h, int st, auto&& mid) {
             const uint32_t a0 = q_lo + h * kTileLo, b0 = k_lo + st * kTileLo;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
+                if (kk == D / 32) mid();
                 const uint32_t off = (uint32_t)((kk >> 2) * kRegion + (kk & 3) * 32) >> 4;
                 tc::mma_ss_warp(tmem + 256 * h, a0 + off, b0 + off, kDescHi, id_qk, kk > 0 ? 1u : 0u);
             }
             tc::mma_commit_warp(&b->s_full[h]);
         };
+        auto nothing = [] {};
         // O_h += P_h V(st); P_h is read from TMEM (the first 64 columns of S_h), V in K-steps
         // of 16 rows (2048 bytes)
         auto issue_pv = [&](int h, int st, bool first) -> bool {
@@ -493,29 +497,48 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!wait(&b->k_full[it & 1], (it >> 1) & 1)) break;
             tc::fence_after_sync();
             tc::fence_proxy_async_smem();  // the producers' generic-proxy copies -> MMA operand reads
-            if (nkt0 > 0) issue_s(0, it & 1);
-            if (nkt1 > 0) issue_s(1, it & 1);
+            if (nkt0 > 0) issue_s(0, it & 1, nothing);
+            if (nkt1 > 0) issue_s(1, it & 1, nothing);
             tc::mma_commit_warp(&b->k_empty[it & 1]);
             if (nkt == 1) tc::mma_commit_warp(&b->q_empty);
+            // inputs of the coming step (V(t), K(t + 1)) already seen complete
+            bool inputs_seen = false;
             for (int j = 0; j < nkt && ok; ++j) {
                 const uint32_t t = it + j;
                 const int st = t & 1, st1 = (t + 1) & 1;
                 const bool next = j + 1 < nkt;
-                ok = wait(&b->v_full[st], (t >> 1) & 1) &&
-                     (!next || wait(&b->k_full[st1], ((t + 1) >> 1) & 1));
-                if (!ok) break;
+                if (!inputs_seen &&
+                    !(ok = wait(&b->v_full[st], (t >> 1) & 1) && (!next || wait(&b->k_full[st1], ((t + 1) >> 1) & 1))))
+                    break;
+                inputs_seen = false;
                 tc::fence_after_sync();
                 tc::fence_proxy_async_smem();
-                for (int h = 0; h < 2 && ok; ++h) {
+                // the last product of this step that reads V(t), and the last S
+                const int last_pv = j < nkt1 ? 1 : 0;
+                const int last_s = j + 1 < nkt1 ? 1 : 0;
+                // in the middle of the last S: a look (no wait) at the next step's inputs, and the
+                // release of V(t)'s stage
+                auto probe = [&] {
+                    if (j + 1 < nkt) {
+                        const uint32_t t1 = t + 1;
+                        inputs_seen = __all_sync(0xffffffffu, dev::mbar_test_wait(&b->v_full[st1], (t1 >> 1) & 1) &&
+                                                                  (j + 2 >= nkt || dev::mbar_test_wait(&b->k_full[st],
+                                                                                                       ((t1 + 1) >> 1) & 1)));
+                    }
+                };
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
                     const int nk = h ? nkt1 : nkt0;
                     if (j >= nk) continue;
-                    ok = issue_pv(h, st, j == 0);
-                    if (!ok) break;
+                    if (!(ok = issue_pv(h, st, j == 0))) break;
                     if (j == nk - 1) tc::mma_commit_warp(&b->o_ready[h]);
-                    if (j + 1 < nk) issue_s(h, st1);
+                    if (h == last_pv) tc::mma_commit_warp(&b->v_empty[st]);
+                    if (j + 1 < nk) {
+                        if (h == last_s) issue_s(h, st1, probe);
+                        else issue_s(h, st1, nothing);
+                    }
                 }
                 if (!ok) break;
-                tc::mma_commit_warp(&b->v_empty[st]);
                 if (next) {
                     tc::mma_commit_warp(&b->k_empty[st1]);
                     if (j + 1 == nkt - 1) tc::mma_commit_warp(&b->q_empty);
