@@ -48,15 +48,15 @@ def parse():
 # what they were at capture time; after any change the roofline reports null.
 NCU_TRAFFIC = {
     ("decode", "decode"): {
-        "bytes": 619.82592e6,
+        "bytes": 620.137728e6,
         "sources": ['paged_variable_length_gb300/csrc/decode.cu', 'paged_variable_length_gb300/csrc/device_utils.cuh', 'paged_variable_length_gb300/csrc/pva_internal.h'],
-        "sha256_16": "295c00393bba6fbd",
+        "sha256_16": "0f902f1ff81ecbae",
         "summary": "profiles/decode_kernel_decode_workload.md",
     },
     ("tensor_core", "prefill"): {
-        "bytes": 223.674112e6,
+        "bytes": 220.103424e6,
         "sources": ['paged_variable_length_gb300/csrc/prefill_tc.cu', 'paged_variable_length_gb300/csrc/device_utils.cuh', 'paged_variable_length_gb300/csrc/tc_utils.cuh', 'paged_variable_length_gb300/csrc/pva_internal.h'],
-        "sha256_16": "740fc5b9e177d26a",
+        "sha256_16": "808e72d60924057d",
         "summary": "profiles/prefill_kernel_prefill_workload.md",
     },
 }
