@@ -15,6 +15,10 @@ it, and adds the host-side metadata helpers the pages define:
 * ``last_indices`` -- "The attention backend and a reference implementation",
   section "The interface" (``get_last_indices``: each request's last query
   index in the flat q).
+* ``e4m3_encode`` / ``e4m3_decode`` and the ``*_fp8`` functions -- an FP8 (E4M3,
+  OCP 8-bit floating-point format) KV pool with a per-kv-head scale, the
+  KV-cache dtype choice of "Attention backends: ..." (the backend interface's
+  kv_cache_dtype): stored e4m3(x / scale), read back as e4m3 * scale.
 
 Parity pins for everything here are in ``tests/test_oracle_pins.py``.
 """
@@ -66,6 +70,15 @@ def _load():
         lib.oracle_attention.argtypes = [i32, P, P, P, i64, i32, i64, i32, i32, i32, f32,
                                          P, P, P, P, P, P]
         lib.oracle_attention.restype = i32
+        lib.oracle_attention_fp8.argtypes = [i32, P, P, P, i64, i32, i64, i32, i32, i32, f32,
+                                             P, P, P, P, P, P, P, P]
+        lib.oracle_attention_fp8.restype = i32
+        lib.oracle_store_kvcache_fp8.argtypes = [i64, i32, i32, P, P, P, i64, P, P, P, P]
+        lib.oracle_store_kvcache_fp8.restype = i32
+        lib.oracle_e4m3_encode_array.argtypes = [i64, P, P]
+        lib.oracle_e4m3_encode_array.restype = None
+        lib.oracle_e4m3_decode_array.argtypes = [i64, P, P]
+        lib.oracle_e4m3_decode_array.restype = None
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = i32
         lib.oracle_set_num_threads.argtypes = [i32]
@@ -218,3 +231,99 @@ def forward(q, k, v, k_pool, v_pool, cu_seqlens_q, cache_seqlens, page_table, pa
     kp, vp = store_kvcache(k, v, slots, k_pool, v_pool)
     out, lse = attention(q, kp, vp, cu_seqlens_q, cache_seqlens, page_table, page_size, scale, row_select)
     return out, lse, kp, vp
+
+
+# --------------------------------------------------------------------------- FP8 (E4M3) KV pool
+
+def e4m3_encode(x) -> np.ndarray:
+    """Nearest E4M3 codes (ties to even, |x| > 448 saturates, NaN -> NaN code) of fp32 values."""
+    a = _c(np.asarray(x, dtype=np.float32), np.float32)
+    out = np.empty(a.shape, dtype=np.uint8)
+    _load().oracle_e4m3_encode_array(a.size, _ptr(a), _ptr(out))
+    return out
+
+
+def e4m3_decode(b) -> np.ndarray:
+    """fp32 values of E4M3 codes."""
+    a = _c(np.asarray(b, dtype=np.uint8), np.uint8)
+    out = np.empty(a.shape, dtype=np.float32)
+    _load().oracle_e4m3_decode_array(a.size, _ptr(a), _ptr(out))
+    return out
+
+
+def _u8(a) -> np.ndarray:
+    if isinstance(a, np.ndarray):
+        if a.dtype != np.uint8:
+            raise TypeError("expected an FP8 pool as uint8 codes")
+        return np.ascontiguousarray(a)
+    import torch
+
+    if a.dtype not in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)):
+        raise TypeError("expected a torch uint8 (or float8_e4m3fn) tensor")
+    return np.ascontiguousarray(a.detach().cpu().contiguous().view(torch.uint8).numpy())
+
+
+def _scales(x, Hkv: int) -> np.ndarray:
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().numpy()
+    a = _c(np.asarray(x, dtype=np.float32).reshape(-1), np.float32)
+    if a.shape[0] != Hkv:
+        raise OracleError("one scale per kv head expected")
+    return a
+
+
+def store_kvcache_fp8(k, v, slots, k_pool, v_pool, k_scale, v_scale) -> tuple[np.ndarray, np.ndarray]:
+    """Copies of the FP8 pools with this step's K/V quantised into their slots."""
+    kb, vb = _bits(k), _bits(v)
+    kp, vp = _u8(k_pool).copy(), _u8(v_pool).copy()
+    T, Hkv, D = kb.shape
+    s = _c(slots, np.int64)
+    ks, vs = _scales(k_scale, Hkv), _scales(v_scale, Hkv)
+    rc = _load().oracle_store_kvcache_fp8(T, Hkv, D, _ptr(kb), _ptr(vb), _ptr(s), kp.shape[0], _ptr(ks), _ptr(vs),
+                                         _ptr(kp), _ptr(vp))
+    if rc != 0:
+        raise OracleError(f"token {-rc - 1}: slot out of range")
+    return kp, vp
+
+
+def attention_fp8(q, k_pool, v_pool, k_scale, v_scale, cu_seqlens_q, cache_seqlens, page_table, page_size: int,
+                  scale: float | None = None, row_select: np.ndarray | None = None):
+    """``attention`` over FP8 pools ([slots, Hkv, D] uint8 codes, one scale per kv head)."""
+    qb, kp, vp = _bits(q), _u8(k_pool), _u8(v_pool)
+    T, Hq, D = qb.shape
+    Hkv = kp.shape[1]
+    if Hq % Hkv != 0:
+        raise OracleError("Hq must be a multiple of Hkv")
+    ks, vs = _scales(k_scale, Hkv), _scales(v_scale, Hkv)
+    cu = _c(cu_seqlens_q, np.int32)
+    lens = _c(cache_seqlens, np.int32)
+    pt = _c(page_table, np.int32)
+    B = lens.shape[0]
+    num_pages = kp.shape[0] // page_size
+    if scale is None:
+        scale = float(D) ** -0.5
+    out = np.full((T, Hq, D), np.nan, dtype=np.float32)
+    lse = np.full((T, Hq), np.nan, dtype=np.float32)
+    sel = None if row_select is None else _c(row_select, np.uint8)
+    rc = _load().oracle_attention_fp8(B, _ptr(cu), _ptr(lens), _ptr(pt), pt.shape[1], page_size, num_pages,
+                                      Hq, Hkv, D, float(scale), _ptr(qb), _ptr(kp), _ptr(vp), _ptr(ks), _ptr(vs),
+                                      _ptr(sel), _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise OracleError(f"request {-rc - 1}: q_len > kv_len or page id out of range" if rc > -1000000
+                          else "out of host memory")
+    return out, lse
+
+
+def forward_fp8(q, k, v, k_pool, v_pool, k_scale, v_scale, cu_seqlens_q, cache_seqlens, page_table,
+                page_size: int, slots=None, scale: float | None = None, row_select: np.ndarray | None = None):
+    """The whole step over FP8 pools: quantised store first, then attention.
+
+    Returns (out fp32 [T,Hq,D], lse fp32 [T,Hq], k_pool codes, v_pool codes).
+    """
+    if slots is None:
+        slots = slot_mapping(cu_seqlens_q, cache_seqlens, page_table, page_size)
+    kp, vp = store_kvcache_fp8(k, v, slots, k_pool, v_pool, k_scale, v_scale)
+    out, lse = attention_fp8(q, kp, vp, k_scale, v_scale, cu_seqlens_q, cache_seqlens, page_table, page_size,
+                             scale, row_select)
+    return out, lse, kp, vp
+

@@ -33,6 +33,14 @@
  *
  * Storage types: bf16 values are passed as their raw 16-bit patterns
  * (uint16_t); bf16 -> fp32 is exact (the pattern becomes the high half).
+ *
+ * FP8 KV pool (a pool element type the pages name only as a KV-cache dtype
+ * choice, "Attention backends: ...", the kv_cache_dtype of the backend
+ * interface): one byte per element in the E4M3 format of the OCP 8-bit
+ * floating-point specification, with one fp32 scale per kv head for K and
+ * one for V.  Readings: a stored element is e4m3(x / scale[g]) (fp32 division,
+ * round to nearest even, values beyond the largest finite 448 saturate); the
+ * attention reads e4m3 * scale[g] (fp32 product) and is otherwise unchanged.
  */
 #include <math.h>
 #include <stdint.h>
@@ -48,6 +56,56 @@ static float bf16_bits_to_float(uint16_t b) {
     float f;
     memcpy(&f, &u, sizeof f);
     return f;
+}
+
+/*
+ * E4M3: sign bit, 4 exponent bits (bias 7), 3 mantissa bits.  Exponent field 0
+ * holds the subnormals m * 2^-9; fields 1..15 the normals 2^(e-7) * (1 + m/8),
+ * except S.1111.111, the only NaN.  There are no infinities; the largest finite
+ * value is 2^8 * 1.75 = 448.
+ */
+float oracle_e4m3_decode(uint8_t b) {
+    const int e = (b >> 3) & 15, m = b & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double v = e == 0 ? ldexp((double)m, -9) : ldexp((double)(8 + m), e - 10);
+    return (float)((b & 0x80) ? -v : v);
+}
+
+/*
+ * Nearest E4M3 value of x, ties to the even mantissa; |x| above 448 (also
+ * infinities) gives +-448; NaN gives the NaN code with x's sign.  The rounding
+ * is done in double on the magnitude divided by the quantum of its binade (an
+ * exact power-of-two division), so rint() sees the exact quotient.
+ */
+uint8_t oracle_e4m3_encode(float x) {
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    if (isnan(x)) return (uint8_t)(sign | 0x7F);
+    const double a = fabs((double)x);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+    double quantum;
+    if (a < ldexp(1.0, -6)) {
+        quantum = ldexp(1.0, -9);  /* subnormal spacing */
+    } else {
+        int e2;
+        frexp(a, &e2);  /* a = f * 2^e2, f in [0.5, 1): a in [2^(e2-1), 2^e2) */
+        quantum = ldexp(1.0, e2 - 1 - 3);
+    }
+    const double v = rint(a / quantum) * quantum; /* default rounding mode: to nearest, ties to even */
+    if (v == 0.0) return sign;
+    if (v < ldexp(1.0, -6)) return (uint8_t)(sign | (int)(v / ldexp(1.0, -9)));
+    int e2;
+    frexp(v, &e2);
+    const int e = e2 - 1;                                   /* v in [2^e, 2^(e+1)) */
+    const int m = (int)((v / ldexp(1.0, e) - 1.0) * 8.0);  /* exact: v has 3 fraction bits */
+    return (uint8_t)(sign | ((e + 7) << 3) | m);
+}
+
+void oracle_e4m3_encode_array(int64_t n, const float *x, uint8_t *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_encode(x[i]);
+}
+
+void oracle_e4m3_decode_array(int64_t n, const uint8_t *b, float *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_decode(b[i]);
 }
 
 /* Number of OpenMP threads the attention loop will use (1 without OpenMP). */
@@ -122,6 +180,34 @@ int oracle_store_kvcache(int64_t T, int Hkv, int D, const uint16_t *k, const uin
 }
 
 /*
+ * store_kvcache into an FP8 pool: pool[slot[t]][h][d] = e4m3(float(new[t][h][d])
+ * / scale[h]) for K and V.  Same slot rules and return value as above.
+ */
+int oracle_store_kvcache_fp8(int64_t T, int Hkv, int D, const uint16_t *k, const uint16_t *v,
+                             const int64_t *slots, int64_t num_slots, const float *k_scale,
+                             const float *v_scale, uint8_t *k_pool, uint8_t *v_pool) {
+    int rc = 0;
+    const int64_t row = (int64_t)Hkv * D;
+    for (int64_t t = 0; t < T; ++t) {
+        int64_t s = slots[t];
+        if (s == -1) continue;
+        if (s < 0 || s >= num_slots) {
+            if (rc == 0) rc = (int)-(t + 1);
+            continue;
+        }
+        for (int h = 0; h < Hkv; ++h)
+            for (int d = 0; d < D; ++d) {
+                const int64_t src = t * row + (int64_t)h * D + d, dst = s * row + (int64_t)h * D + d;
+                const float kx = bf16_bits_to_float(k[src]) / k_scale[h];
+                const float vx = bf16_bits_to_float(v[src]) / v_scale[h];
+                k_pool[dst] = oracle_e4m3_encode(kx);
+                v_pool[dst] = oracle_e4m3_encode(vx);
+            }
+    }
+    return rc;
+}
+
+/*
  * The bottom-right causal mask of one request: M[r][j] = (j <= L - n + r),
  * for r < n and j < L ("The attention backend and a reference
  * implementation", the mask figure and "query r sits at absolute position
@@ -152,11 +238,17 @@ void oracle_causal_mask(int n, int L, uint8_t *mask_out) {
  * Returns 0, or -(i+1) when request i violates n <= L or reads a page id
  * outside [0, num_pages).
  */
-int oracle_attention(int B, const int32_t *cu_seqlens_q, const int32_t *cache_seqlens,
-                     const int32_t *page_table, int64_t ld, int page_size, int64_t num_pages,
-                     int Hq, int Hkv, int D, float scale,
-                     const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
-                     const uint8_t *row_select, float *out, float *lse) {
+/* One pool element as fp32: a bf16 pattern, or an E4M3 byte times its head's scale. */
+static float pool_value(const void *pool, int fp8, int64_t idx, float scale) {
+    if (fp8) return oracle_e4m3_decode(((const uint8_t *)pool)[idx]) * scale;
+    return bf16_bits_to_float(((const uint16_t *)pool)[idx]);
+}
+
+static int attention_core(int B, const int32_t *cu_seqlens_q, const int32_t *cache_seqlens,
+                          const int32_t *page_table, int64_t ld, int page_size, int64_t num_pages,
+                          int Hq, int Hkv, int D, float scale, const uint16_t *q,
+                          const void *k_pool, const void *v_pool, int fp8, const float *k_scale,
+                          const float *v_scale, const uint8_t *row_select, float *out, float *lse) {
     const int group = Hq / Hkv;
     const int64_t kv_row = (int64_t)Hkv * D;
 
@@ -205,13 +297,12 @@ int oracle_attention(int B, const int32_t *cu_seqlens_q, const int32_t *cache_se
             rc = -1000000;
             continue;
         }
+        const float ks = fp8 ? k_scale[g] : 1.0f, vs = fp8 ? v_scale[g] : 1.0f;
         for (int64_t j = 0; j < L; ++j) {
-            int64_t s = slot_of(page_table, ld, page_size, i, j);
-            const uint16_t *kr = k_pool + s * kv_row + (int64_t)g * D;
-            const uint16_t *vr = v_pool + s * kv_row + (int64_t)g * D;
+            const int64_t row0 = slot_of(page_table, ld, page_size, i, j) * kv_row + (int64_t)g * D;
             for (int d = 0; d < D; ++d) {
-                Ki[j * D + d] = bf16_bits_to_float(kr[d]);
-                Vi[j * D + d] = bf16_bits_to_float(vr[d]);
+                Ki[j * D + d] = pool_value(k_pool, fp8, row0 + d, ks);
+                Vi[j * D + d] = pool_value(v_pool, fp8, row0 + d, vs);
             }
         }
         oracle_causal_mask(n, L, M);
@@ -248,4 +339,24 @@ int oracle_attention(int B, const int32_t *cu_seqlens_q, const int32_t *cache_se
         free(Ki); free(Vi); free(M); free(S); free(qf);
     }
     return rc;
+}
+
+int oracle_attention(int B, const int32_t *cu_seqlens_q, const int32_t *cache_seqlens,
+                     const int32_t *page_table, int64_t ld, int page_size, int64_t num_pages,
+                     int Hq, int Hkv, int D, float scale,
+                     const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
+                     const uint8_t *row_select, float *out, float *lse) {
+    return attention_core(B, cu_seqlens_q, cache_seqlens, page_table, ld, page_size, num_pages, Hq, Hkv, D,
+                          scale, q, k_pool, v_pool, 0, NULL, NULL, row_select, out, lse);
+}
+
+/* The same attention over an FP8 pool (elements read as e4m3 * scale of their kv head). */
+int oracle_attention_fp8(int B, const int32_t *cu_seqlens_q, const int32_t *cache_seqlens,
+                         const int32_t *page_table, int64_t ld, int page_size, int64_t num_pages,
+                         int Hq, int Hkv, int D, float scale,
+                         const uint16_t *q, const uint8_t *k_pool, const uint8_t *v_pool,
+                         const float *k_scale, const float *v_scale,
+                         const uint8_t *row_select, float *out, float *lse) {
+    return attention_core(B, cu_seqlens_q, cache_seqlens, page_table, ld, page_size, num_pages, Hq, Hkv, D,
+                          scale, q, k_pool, v_pool, 1, k_scale, v_scale, row_select, out, lse);
 }

@@ -417,3 +417,137 @@ def test_padding_waste_example():
     padded, real = len(ql) * max(ql), sum(ql)
     assert (padded, real) == (gold["padded"], gold["real"])
     assert round(100 * (1 - real / padded)) == gold["waste_percent"]
+
+
+# --------------------------------------------------------------------------- FP8 (E4M3) pool
+
+E4M3_POINTS = [
+    # (code, value) straight from the format definition: bias 7, 3 mantissa bits,
+    # subnormals m * 2^-9, S.1111.111 the only NaN, largest finite 1.75 * 2^8
+    (0x00, 0.0), (0x01, 2.0 ** -9), (0x07, 7 * 2.0 ** -9), (0x08, 2.0 ** -6), (0x0F, 1.875 * 2.0 ** -6),
+    (0x38, 1.0), (0x39, 1.125), (0x3F, 1.875), (0x40, 2.0), (0x77, 1.875 * 2.0 ** 7), (0x7E, 448.0),
+    (0x80, -0.0), (0xB8, -1.0), (0xFE, -448.0),
+]
+
+
+def test_e4m3_decode_format_points():
+    codes = np.array([c for c, _ in E4M3_POINTS], np.uint8)
+    got = oracle.e4m3_decode(codes)
+    for (c, v), g in zip(E4M3_POINTS, got):
+        assert g == v and math.copysign(1.0, g) == math.copysign(1.0, v), hex(c)
+    assert np.isnan(oracle.e4m3_decode(np.array([0x7F, 0xFF], np.uint8))).all()
+
+
+def test_e4m3_encode_rounding_and_saturation():
+    cases = [
+        (1.0, 0x38), (448.0, 0x7E), (449.0, 0x7E), (1e6, 0x7E), (np.inf, 0x7E), (-np.inf, 0xFE),
+        (2.0 ** -10, 0x00),          # half the smallest subnormal: tie, to the even code 0
+        (3 * 2.0 ** -10, 0x02),      # 1.5 quanta: tie between codes 1 and 2, to the even 2
+        (2.0 ** -10 * 1.01, 0x01),   # just above the tie
+        (1.0625, 0x38),              # halfway 1.0 / 1.125: even mantissa 0
+        (1.1875, 0x3A),              # halfway 1.125 / 1.25: even mantissa 2
+        (-0.0, 0x80), (-1e-30, 0x80),
+        (15.5, 0x58),                # quantum 1 in [8, 16): a tie between 15 (0x57) and 16 (0x58), even 16
+    ]
+    got = oracle.e4m3_encode(np.array([x for x, _ in cases], np.float32))
+    for (x, c), g in zip(cases, got):
+        assert g == c, (x, hex(c), hex(g))
+    assert oracle.e4m3_encode(np.array([np.nan], np.float32))[0] & 0x7F == 0x7F
+
+
+def test_e4m3_round_trip_every_code():
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], np.uint8)
+    assert np.array_equal(oracle.e4m3_encode(oracle.e4m3_decode(codes)), codes)
+
+
+def test_e4m3_encode_is_nearest_by_brute_force():
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.uniform(-460, 460, 3000), rng.normal(0, 1, 3000), rng.normal(0, 0.01, 3000)])
+    x = x.astype(np.float32)
+    finite = np.array([c for c in range(256) if c & 0x7F != 0x7F], np.uint8)
+    vals = oracle.e4m3_decode(finite).astype(np.float64)
+    got = oracle.e4m3_decode(oracle.e4m3_encode(x)).astype(np.float64)
+    clipped = np.clip(x.astype(np.float64), -448, 448)
+    best = np.min(np.abs(vals[None, :] - clipped[:, None]), axis=1)
+    assert np.array_equal(np.abs(got - clipped), best)
+
+
+def test_e4m3_encode_matches_torch_in_range():
+    """torch's float8_e4m3fn conversion (round to nearest even) is an independent
+    implementation for values inside the finite range."""
+    f8 = getattr(torch, "float8_e4m3fn", None)
+    if f8 is None:
+        pytest.skip("torch without float8_e4m3fn")
+    rng = np.random.default_rng(4)
+    x = np.concatenate([rng.uniform(-440, 440, 5000), rng.normal(0, 1, 5000), rng.normal(0, 0.003, 5000)])
+    x = x.astype(np.float32)
+    ref = torch.from_numpy(x).to(f8).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3_encode(x), ref)
+
+
+def test_fp8_store_quantises_each_head_with_its_scale():
+    rng = np.random.default_rng(5)
+    T, Hkv, D = 3, 2, 8
+    k = torch.from_numpy(rng.normal(0, 3, (T, Hkv, D)).astype(np.float32)).to(torch.bfloat16)
+    v = torch.from_numpy(rng.normal(0, 3, (T, Hkv, D)).astype(np.float32)).to(torch.bfloat16)
+    ks, vs = np.array([0.5, 2.0], np.float32), np.array([4.0, 0.25], np.float32)
+    kp = np.full((10, Hkv, D), 0x7F, np.uint8)
+    vp = np.full((10, Hkv, D), 0x7F, np.uint8)
+    slots = np.array([7, -1, 2], np.int64)
+    kq, vq = oracle.store_kvcache_fp8(k, v, slots, kp, vp, ks, vs)
+    # untouched slots keep their bytes; slot -1 writes nothing
+    untouched = [s for s in range(10) if s not in (7, 2)]
+    assert (kq[untouched] == 0x7F).all() and (vq[untouched] == 0x7F).all()
+    # the written rows decode to the inputs within half a quantum (scales are powers of
+    # two, so the quotient is exact), and each head uses its own scale
+    for t, s in ((0, 7), (2, 2)):
+        for h in range(Hkv):
+            kx = k[t, h].float().numpy() / ks[h]
+            back = oracle.e4m3_decode(kq[s, h])
+            q = np.where(np.abs(kx) < 2.0 ** -6, 2.0 ** -9, 2.0 ** (np.floor(np.log2(np.maximum(np.abs(kx), 1e-30))) - 3))
+            assert (np.abs(back - kx) <= q / 2 + 1e-12).all()
+            assert (np.abs(oracle.e4m3_decode(vq[s, h]) * vs[h] - v[t, h].float().numpy()) <=
+                    np.abs(v[t, h].float().numpy()) * 2.0 ** -4 + 2.0 ** -9 * vs[h]).all()
+
+
+def test_fp8_attention_reduces_to_bf16_attention_on_exact_values():
+    """K/V values that are E4M3 values times power-of-two scales are stored exactly, so
+    the FP8 step must equal the (pinned) bf16 step on the same values."""
+    rng = np.random.default_rng(6)
+    B, Hq, Hkv, D, ps = 3, 4, 2, 16, 4
+    q_lens, kv_lens = [3, 1, 5], [9, 13, 5]
+    pages = [math.ceil(L / ps) for L in kv_lens]
+    P = sum(pages) + 2
+    pt = np.zeros((B, max(pages)), np.int32)
+    perm = rng.permutation(P)
+    off = 0
+    for i, n in enumerate(pages):
+        pt[i, :n] = perm[off:off + n]
+        off += n
+    cu = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    lens = np.array(kv_lens, np.int32)
+    T = int(cu[-1])
+    ks, vs = np.array([0.5, 4.0], np.float32), np.array([2.0, 0.125], np.float32)
+    finite = np.array([c for c in range(256) if c & 0x7F != 0x7F], np.uint8)
+
+    def exact(shape, scale_per_head):
+        codes = rng.choice(finite, size=shape)
+        return oracle.e4m3_decode(codes) * scale_per_head[None, :, None]
+
+    q = torch.from_numpy(rng.normal(0, 1, (T, Hq, D)).astype(np.float32)).to(torch.bfloat16)
+    # e4m3 values times a power-of-two scale: exact in bf16 and exact after division by the scale
+    k = exact((T, Hkv, D), ks)
+    v = exact((T, Hkv, D), vs)
+    kp0, vp0 = exact((P * ps, Hkv, D), ks), exact((P * ps, Hkv, D), vs)
+    kb, vb = (torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16) for a in (k, v))
+    kpb, vpb = (torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16) for a in (kp0, vp0))
+    # the same values as bf16 (exact: e4m3 has 3 mantissa bits) and as FP8 codes
+    assert np.array_equal(kb.float().numpy(), k) and np.array_equal(kpb.float().numpy(), kp0)
+    kp8 = oracle.e4m3_encode(kp0 / ks[None, :, None])
+    vp8 = oracle.e4m3_encode(vp0 / vs[None, :, None])
+    o8, l8, kq, vq = oracle.forward_fp8(q, kb, vb, kp8, vp8, ks, vs, cu, lens, pt, ps)
+    o16, l16, kq16, vq16 = oracle.forward(q, kb, vb, kpb, vpb, cu, lens, pt, ps)
+    assert np.array_equal(oracle.e4m3_decode(kq) * ks[None, :, None],
+                          torch.from_numpy(kq16.view(np.int16)).view(torch.bfloat16).float().numpy())
+    np.testing.assert_allclose(o8, o16, rtol=1e-6, atol=1e-6)
+    np.testing.assert_allclose(l8, l16, rtol=1e-6, atol=1e-6)
