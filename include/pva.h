@@ -67,7 +67,7 @@
 extern "C" {
 #endif
 
-#define PVA_ABI_VERSION 1
+#define PVA_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define PVA_API __attribute__((visibility("default")))
@@ -94,6 +94,17 @@ typedef enum pva_status {
 #define PVA_DEVERR_TIMEOUT    0x20u  /* a bounded wait inside a kernel gave up (internal error) */
 
 /*
+ * Element type of the paged KV pool (pva_config.kv_dtype).  The pages name the
+ * pool's dtype as a backend choice ("Attention backends: backend, metadata builder
+ * and implementation", the kv_cache_dtype of the backend interface) without fixing
+ * a format; the 8-bit one here is E4M3 of the OCP 8-bit floating-point
+ * specification (bias 7, 3 mantissa bits, no infinities, largest finite 448) with
+ * one fp32 scale per kv head for K and one for V.
+ */
+#define PVA_KV_BF16 0
+#define PVA_KV_E4M3 1
+
+/*
  * Static description of the model's attention layer and of the largest batch
  * the workspace is planned for.  Plain data; the caller fills every field.
  */
@@ -110,6 +121,7 @@ typedef struct pva_config {
     int32_t enable_split_kv;    /* nonzero: split long KV ranges over several CTAs (LSE combine) */
     int32_t enable_cascade;     /* nonzero: read prefixes shared by several decodes once */
     int32_t min_cascade_pages;  /* shortest shared prefix (in pages) worth a cascade pass; <= 0 -> 8 */
+    int32_t kv_dtype;           /* PVA_KV_BF16 (0) or PVA_KV_E4M3: the pool element type */
 } pva_config;
 
 /*
@@ -220,6 +232,29 @@ PVA_API pva_status attn_forward(const pva_meta* meta, const void* q, const void*
  */
 PVA_API pva_status attn_store_kvcache(const pva_meta* meta, const void* k, const void* v, void* k_pool,
                               void* v_pool, void* stream);
+
+/*
+ * attn_forward for a pool of E4M3 bytes (the meta must come from a config with
+ * kv_dtype = PVA_KV_E4M3; attn_forward refuses such a meta and this call refuses a
+ * bf16 one, with PVA_ERR_INVALID_ARG).
+ *   k_pool, v_pool  uint8 [num_pages * page_size, Hkv, D], updated in place, 16-byte aligned
+ *   k_scale, v_scale  DEVICE fp32 [Hkv], the scale of each kv head
+ *   q, k, v, out, lse as for attn_forward (bf16 activations)
+ * The store writes e4m3(k[t, h, d] / k_scale[h]) (IEEE fp32 division, round to
+ * nearest even, magnitudes beyond 448 saturate to 448, NaN stays NaN), likewise for
+ * v; attention reads each element as e4m3 * scale of its head, otherwise exactly as
+ * attn_forward.  Every request runs on the decode kernel (tensor-core and
+ * shared-prefix passes are off for this pool type), whose warp MMAs take f16
+ * operands: q enters as f16, exact for 2^-17 <= |q| <= 65504, and q outside f16's
+ * range gives undefined results.  Scales must be finite and nonzero.
+ */
+PVA_API pva_status attn_forward_fp8kv(const pva_meta* meta, const void* q, const void* k, const void* v,
+                              void* k_pool, void* v_pool, const float* k_scale, const float* v_scale,
+                              void* out, float* lse, void* stream);
+
+/* store_kvcache alone into an E4M3 pool (the quantisation of attn_forward_fp8kv). */
+PVA_API pva_status attn_store_kvcache_fp8kv(const pva_meta* meta, const void* k, const void* v, void* k_pool,
+                                    void* v_pool, const float* k_scale, const float* v_scale, void* stream);
 
 /*
  * Debug/test helper: synchronises the stream of the last prepare/forward on

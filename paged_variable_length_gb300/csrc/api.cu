@@ -37,6 +37,7 @@ pva_status check_config(const pva_config* c) {
     if (!is_pow2(c->page_size) || c->page_size > 128) return PVA_ERR_UNSUPPORTED;
     if (!decode_supported(c->num_qo_heads, c->num_kv_heads, c->head_dim)) return PVA_ERR_UNSUPPORTED;
     if ((int64_t)c->num_pages * c->page_size > ((int64_t)1 << 40)) return PVA_ERR_UNSUPPORTED;
+    if (c->kv_dtype != PVA_KV_BF16 && c->kv_dtype != PVA_KV_E4M3) return PVA_ERR_UNSUPPORTED;
     return PVA_OK;
 }
 
@@ -192,7 +193,9 @@ pva_status prepare_in_workspace(const pva_config* cfg, const int32_t* cu_seqlens
     h.sm_count = sms;
     // requests with more than TB new tokens run on the tensor-core prefill kernel, which
     // also runs the prefix pass of shared-prefix groups
-    const bool tc_ok = prefill_supported(cfg->num_qo_heads, cfg->num_kv_heads, cfg->head_dim);
+    // (an E4M3 pool is read by the decode kernel only: every request becomes decode groups)
+    const bool tc_ok =
+        cfg->kv_dtype == PVA_KV_BF16 && prefill_supported(cfg->num_qo_heads, cfg->num_kv_heads, cfg->head_dim);
     h.use_prefill = (mq > TB && tc_ok) ? 1 : 0;
     h.use_cascade = (cfg->enable_cascade && tc_ok && batch >= 2 && batch <= kCascadeMaxBatch) ? 1 : 0;
     h.dec_ctas = sms * decode_ctas_per_sm(cfg->num_kv_heads, cfg->head_dim);
@@ -268,16 +271,39 @@ pva_status attn_prepare_metadata(const pva_config* cfg, const int32_t* cu_seqlen
                                 total_tokens, max_q_len, workspace, lay, sms, stream, meta);
 }
 
-pva_status attn_store_kvcache(const pva_meta* meta, const void* k, const void* v, void* k_pool, void* v_pool,
-                              void* stream) {
-    const MetaHost* h = meta_of(meta);
-    if (h == nullptr) return PVA_ERR_NOT_PREPARED;
+namespace pva {
+namespace {
+
+pva_status store_impl(const MetaHost* h, const void* k, const void* v, void* k_pool, void* v_pool,
+                      const float* k_scale, const float* v_scale, void* stream) {
     if (h->total_tokens > 0 && (k == nullptr || v == nullptr)) return PVA_ERR_INVALID_ARG;
     if (k_pool == nullptr || v_pool == nullptr) return PVA_ERR_INVALID_ARG;
     if (!aligned16(k) || !aligned16(v) || !aligned16(k_pool) || !aligned16(v_pool)) return PVA_ERR_INVALID_ARG;
     ForwardParams fp = forward_params(h, nullptr, k, v, k_pool, v_pool, nullptr, nullptr);
+    fp.kv_fp8 = h->cfg.kv_dtype == PVA_KV_E4M3 ? 1 : 0;
+    fp.k_scale = k_scale;
+    fp.v_scale = v_scale;
     if (launch_store(fp, h->cfg.head_dim, static_cast<cudaStream_t>(stream)) != cudaSuccess) return PVA_ERR_CUDA;
     return PVA_OK;
+}
+
+}  // namespace
+}  // namespace pva
+
+pva_status attn_store_kvcache(const pva_meta* meta, const void* k, const void* v, void* k_pool, void* v_pool,
+                              void* stream) {
+    const MetaHost* h = meta_of(meta);
+    if (h == nullptr) return PVA_ERR_NOT_PREPARED;
+    if (h->cfg.kv_dtype != PVA_KV_BF16) return PVA_ERR_INVALID_ARG;
+    return store_impl(h, k, v, k_pool, v_pool, nullptr, nullptr, stream);
+}
+
+pva_status attn_store_kvcache_fp8kv(const pva_meta* meta, const void* k, const void* v, void* k_pool,
+                                    void* v_pool, const float* k_scale, const float* v_scale, void* stream) {
+    const MetaHost* h = meta_of(meta);
+    if (h == nullptr) return PVA_ERR_NOT_PREPARED;
+    if (h->cfg.kv_dtype != PVA_KV_E4M3 || k_scale == nullptr || v_scale == nullptr) return PVA_ERR_INVALID_ARG;
+    return store_impl(h, k, v, k_pool, v_pool, k_scale, v_scale, stream);
 }
 
 pva_status attn_prepare_metadata_static(const pva_config* cfg, const int32_t* cu_seqlens_q,
@@ -313,10 +339,11 @@ pva_status attn_prepare_metadata_static(const pva_config* cfg, const int32_t* cu
                                 total_tokens, max_q_len, ws, lay, sms, stream, meta);
 }
 
-pva_status attn_forward(const pva_meta* meta, const void* q, const void* k, const void* v, void* k_pool,
-                        void* v_pool, void* out, float* lse, void* stream) {
-    const MetaHost* h = meta_of(meta);
-    if (h == nullptr) return PVA_ERR_NOT_PREPARED;
+namespace pva {
+namespace {
+
+pva_status forward_impl(const MetaHost* h, const void* q, const void* k, const void* v, void* k_pool, void* v_pool,
+                        const float* k_scale, const float* v_scale, void* out, float* lse, void* stream) {
     if (h->total_tokens > 0 && (q == nullptr || k == nullptr || v == nullptr || out == nullptr))
         return PVA_ERR_INVALID_ARG;
     if (k_pool == nullptr || v_pool == nullptr) return PVA_ERR_INVALID_ARG;
@@ -326,6 +353,9 @@ pva_status attn_forward(const pva_meta* meta, const void* q, const void* k, cons
     if (h->total_tokens == 0) return PVA_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     ForwardParams fp = forward_params(h, q, k, v, k_pool, v_pool, out, lse);
+    fp.kv_fp8 = h->cfg.kv_dtype == PVA_KV_E4M3 ? 1 : 0;
+    fp.k_scale = k_scale;
+    fp.v_scale = v_scale;
     // inside a stream capture the events become graph nodes that still time the replay
     cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
     if (h->n_events == 5 && cudaStreamIsCapturing(s, &capture) != cudaSuccess) return PVA_ERR_CUDA;
@@ -346,6 +376,26 @@ pva_status attn_forward(const pva_meta* meta, const void* q, const void* k, cons
     if (h->use_merge && launch_merge(fp, h->cfg.head_dim, h->sm_count, s) != cudaSuccess) return PVA_ERR_CUDA;
     if (mark(4) != cudaSuccess) return PVA_ERR_CUDA;
     return PVA_OK;
+}
+
+}  // namespace
+}  // namespace pva
+
+pva_status attn_forward(const pva_meta* meta, const void* q, const void* k, const void* v, void* k_pool,
+                        void* v_pool, void* out, float* lse, void* stream) {
+    const MetaHost* h = meta_of(meta);
+    if (h == nullptr) return PVA_ERR_NOT_PREPARED;
+    if (h->cfg.kv_dtype != PVA_KV_BF16) return PVA_ERR_INVALID_ARG;
+    return forward_impl(h, q, k, v, k_pool, v_pool, nullptr, nullptr, out, lse, stream);
+}
+
+pva_status attn_forward_fp8kv(const pva_meta* meta, const void* q, const void* k, const void* v, void* k_pool,
+                              void* v_pool, const float* k_scale, const float* v_scale, void* out, float* lse,
+                              void* stream) {
+    const MetaHost* h = meta_of(meta);
+    if (h == nullptr) return PVA_ERR_NOT_PREPARED;
+    if (h->cfg.kv_dtype != PVA_KV_E4M3 || k_scale == nullptr || v_scale == nullptr) return PVA_ERR_INVALID_ARG;
+    return forward_impl(h, q, k, v, k_pool, v_pool, k_scale, v_scale, out, lse, stream);
 }
 
 pva_status attn_get_device_status(const pva_meta* meta, uint32_t* error_bits) {

@@ -34,6 +34,15 @@
 //     decode kernel (by the CTA finishing a group last) kept that CTA's
 //     consumers from the ring for the whole combine, and the arrival protocol
 //     stalled every split unit on a fence and an atomic round trip.
+// FP8 pools (F8): the staged rows are E4M3 bytes (half the bytes per key), and the warp
+// MMAs take f16 operands: an E4M3 pair becomes an f16 pair with one exact conversion,
+// where bf16 would need several instructions per pair.  Q is converted to f16 once per
+// unit (exact for 2^-17 <= |q| <= 65504), P is packed as f16.  The dot products may run
+// over the head dimension in any order, so each lane reads its K fragments from one
+// contiguous run of its key's row (Q uses the same order); for P V each lane owns a
+// run of output columns of its four key rows, and the epilogue writes the columns back
+// in place.  The per-head scales: k_scale folds into the softmax scale, v_scale into
+// the final 1/l.
 // Every wait is bounded (PVA_DEVERR_TIMEOUT, then the CTA drains its copies
 // and leaves); nothing traps.
 #include <cuda_runtime.h>
@@ -71,9 +80,10 @@ __device__ __forceinline__ void abort_cta(DecSmemHead* sh, uint32_t* err) {
     dev::set_error(err, kErrTimeout);
 }
 
-template <int D>
+template <int D, bool F8>
 __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
     decode_kernel(ForwardParams p, int stages, int row_stride) {
+    constexpr int ES = F8 ? 1 : 2;  // bytes per pool element
     extern __shared__ __align__(128) uint8_t smem[];
     DecSmemHead* sh = reinterpret_cast<DecSmemHead*>(smem);
     uint8_t* ring = smem + ((sizeof(DecSmemHead) + 127) / 128) * 128;
@@ -85,7 +95,7 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
     const int HB = Hkv < kMaxKvHeads ? Hkv : kMaxKvHeads;
     const int n_hb = Hkv / HB;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row_bytes = HB * D * 2;
+    const int row_bytes = HB * D * ES;
     const int stage_bytes = 2 * kStageKeys * row_stride;
     // Plan from the prepare kernel (finished before the store kernel began); pool rows,
     // the work counter and the prefix-pass partials only after grid_dep_wait.
@@ -209,8 +219,8 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
                 __syncwarp();
                 if (r < nk) {
                     const int64_t slot = (page << p.page_shift) + ((k + r) & ps_mask);
-                    const uint16_t* src =
-                        (lane < 16 ? p.k_pool : p.v_pool) + slot * (int64_t)(Hkv * D) + hb * HB * D;
+                    const uint8_t* src = reinterpret_cast<const uint8_t*>(lane < 16 ? p.k_pool : p.v_pool) +
+                                         (slot * (int64_t)(Hkv * D) + hb * HB * D) * ES;
                     uint8_t* dst = ring + stage * stage_bytes + (lane < 16 ? 0 : kStageKeys * row_stride) +
                                    r * row_stride;
                     dev::bulk_g2s_hint(dst, src, (uint32_t)row_bytes, &sh->full[stage], policy);
@@ -242,8 +252,8 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
     float o[NT][4];
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     int lim0 = 0, lim1 = 0;
+    float ks = 1.f, vs = 1.f;  // per-head scales of an FP8 pool
     const int r0 = gq, r1 = gq + 8;
-    const int consumer_threads = HB * 32;
     int stage = 0;
     uint32_t phase = 0;
 
@@ -261,13 +271,31 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
             const uint32_t* q32 = reinterpret_cast<const uint32_t*>(p.q);
             const int64_t qrow0 = r0 < rows ? ((int64_t)(si.tok0 + r0 / G) * Hq + g * G + r0 % G) * D : -1;
             const int64_t qrow1 = r1 < rows ? ((int64_t)(si.tok0 + r1 / G) * Hq + g * G + r1 % G) * D : -1;
+            if constexpr (F8) {
+                // k-step kk, fragment columns (2cq, 2cq+1 | 2cq+8, 2cq+9) <- head dims
+                // cq*D/4 + 4kk + (0, 1 | 2, 3): the order the K fragments use below
+                auto f16pair = [](uint32_t bf2) {
+                    return dev::pack_f16x2(__uint_as_float(bf2 << 16), __uint_as_float(bf2 & 0xFFFF0000u));
+                };
 #pragma unroll
-            for (int kk = 0; kk < KS; ++kk) {
-                const int c = kk * 16 + 2 * cq;
-                qa[kk][0] = qrow0 >= 0 ? q32[(qrow0 + c) >> 1] : 0u;
-                qa[kk][1] = qrow1 >= 0 ? q32[(qrow1 + c) >> 1] : 0u;
-                qa[kk][2] = qrow0 >= 0 ? q32[(qrow0 + c + 8) >> 1] : 0u;
-                qa[kk][3] = qrow1 >= 0 ? q32[(qrow1 + c + 8) >> 1] : 0u;
+                for (int kk = 0; kk < KS; ++kk) {
+                    const int c = cq * (D / 4) + 4 * kk;
+                    qa[kk][0] = qrow0 >= 0 ? f16pair(q32[(qrow0 + c) >> 1]) : 0u;
+                    qa[kk][1] = qrow1 >= 0 ? f16pair(q32[(qrow1 + c) >> 1]) : 0u;
+                    qa[kk][2] = qrow0 >= 0 ? f16pair(q32[(qrow0 + c + 2) >> 1]) : 0u;
+                    qa[kk][3] = qrow1 >= 0 ? f16pair(q32[(qrow1 + c + 2) >> 1]) : 0u;
+                }
+                ks = p.k_scale[g];
+                vs = p.v_scale[g];
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < KS; ++kk) {
+                    const int c = kk * 16 + 2 * cq;
+                    qa[kk][0] = qrow0 >= 0 ? q32[(qrow0 + c) >> 1] : 0u;
+                    qa[kk][1] = qrow1 >= 0 ? q32[(qrow1 + c) >> 1] : 0u;
+                    qa[kk][2] = qrow0 >= 0 ? q32[(qrow0 + c + 8) >> 1] : 0u;
+                    qa[kk][3] = qrow1 >= 0 ? q32[(qrow1 + c + 8) >> 1] : 0u;
+                }
             }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
@@ -278,7 +306,7 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
             lim1 = r1 < rows ? si.qpos0 + r1 / G : -1;
         }
 
-        const uint8_t* Ks = ring + stage * stage_bytes + gl * D * 2;
+        const uint8_t* Ks = ring + stage * stage_bytes + gl * D * ES;
         const uint8_t* Vs = Ks + kStageKeys * row_stride;
         const uint32_t ks_base = dev::smem_u32(Ks);
         const uint32_t vs_base = dev::smem_u32(Vs);
@@ -287,21 +315,41 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
         float s[2][4];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-#pragma unroll
-        for (int kk2 = 0; kk2 < KS / 2; ++kk2) {
+        if constexpr (F8) {
+            // key nt*8 + gq: the lane's D/4 bytes of the row, four per k-step
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
-                const uint32_t addr =
-                    ks_base + (nt * 8 + (lane & 7)) * row_stride + (kk2 * 32 + (lane >> 3) * 8) * 2;
-                uint32_t b0, b1, b2, b3;
-                dev::ldsm_x4(addr, b0, b1, b2, b3);
-                dev::mma_bf16_16816(s[nt], qa[2 * kk2], b0, b1);
-                dev::mma_bf16_16816(s[nt], qa[2 * kk2 + 1], b2, b3);
+                const uint8_t* krow = Ks + (nt * 8 + gq) * row_stride + cq * (D / 4);
+                uint32_t kw[KS];
+#pragma unroll
+                for (int i = 0; i < KS / 4; ++i) {
+                    const int4 w = *reinterpret_cast<const int4*>(krow + 16 * i);
+                    kw[4 * i] = (uint32_t)w.x;
+                    kw[4 * i + 1] = (uint32_t)w.y;
+                    kw[4 * i + 2] = (uint32_t)w.z;
+                    kw[4 * i + 3] = (uint32_t)w.w;
+                }
+#pragma unroll
+                for (int kk = 0; kk < KS; ++kk)
+                    dev::mma_f16_16816(s[nt], qa[kk], dev::e4m3x2_to_f16x2(kw[kk]), dev::e4m3x2_to_f16x2(kw[kk] >> 16));
+            }
+        } else {
+#pragma unroll
+            for (int kk2 = 0; kk2 < KS / 2; ++kk2) {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const uint32_t addr =
+                        ks_base + (nt * 8 + (lane & 7)) * row_stride + (kk2 * 32 + (lane >> 3) * 8) * 2;
+                    uint32_t b0, b1, b2, b3;
+                    dev::ldsm_x4(addr, b0, b1, b2, b3);
+                    dev::mma_bf16_16816(s[nt], qa[2 * kk2], b0, b1);
+                    dev::mma_bf16_16816(s[nt], qa[2 * kk2 + 1], b2, b3);
+                }
             }
         }
 
         // ---- scale, mask (range end and causal diagonal), online softmax
-        const float sl = p.scale_log2;
+        const float sl = p.scale_log2 * ks;
         float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
@@ -347,20 +395,55 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
             o[nt][3] *= al1;
         }
         uint32_t pa[4];
-        pa[0] = dev::pack_bf16x2(s[0][0], s[0][1]);
-        pa[1] = dev::pack_bf16x2(s[0][2], s[0][3]);
-        pa[2] = dev::pack_bf16x2(s[1][0], s[1][1]);
-        pa[3] = dev::pack_bf16x2(s[1][2], s[1][3]);
-
-        // ---- O += P V (V rows are the k dimension: transposed fragment loads)
+        if constexpr (F8) {
+            pa[0] = dev::pack_f16x2(s[0][0], s[0][1]);
+            pa[1] = dev::pack_f16x2(s[0][2], s[0][3]);
+            pa[2] = dev::pack_f16x2(s[1][0], s[1][1]);
+            pa[3] = dev::pack_f16x2(s[1][2], s[1][3]);
+            // ---- O += P V: the lane's keys 2cq, 2cq+1 | 2cq+8, 2cq+9 (its k rows), its run of
+            // D/8 output columns gq*D/8 .. (gq+1)*D/8 - 1; output tile nt, column n holds head
+            // dim n*D/8 + nt.  A byte permute pairs the two keys of a column for the conversion.
+            constexpr int VW = D / 32;  // words of a lane's run
+            uint32_t vw[4][VW];
 #pragma unroll
-        for (int dt = 0; dt < D / 16; ++dt) {
-            const uint32_t addr =
-                vs_base + ((lane & 7) + ((lane >> 3) & 1) * 8) * row_stride + (dt * 16 + (lane >> 4) * 8) * 2;
-            uint32_t v0, v1, v2, v3;
-            dev::ldsm_x4_t(addr, v0, v1, v2, v3);
-            dev::mma_bf16_16816(o[2 * dt], pa, v0, v1);
-            dev::mma_bf16_16816(o[2 * dt + 1], pa, v2, v3);
+            for (int i = 0; i < 4; ++i) {
+                const uint8_t* vrow = Vs + (2 * cq + (i & 1) + (i >> 1) * 8) * row_stride + gq * (D / 8);
+                if constexpr (VW == 4) {
+                    const int4 w = *reinterpret_cast<const int4*>(vrow);
+                    vw[i][0] = (uint32_t)w.x;
+                    vw[i][1] = (uint32_t)w.y;
+                    vw[i][2] = (uint32_t)w.z;
+                    vw[i][3] = (uint32_t)w.w;
+                } else {
+                    const uint2 w = *reinterpret_cast<const uint2*>(vrow);
+                    vw[i][0] = w.x;
+                    vw[i][1] = w.y;
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; nt += 2) {
+                const int wi = nt >> 2, j = nt & 3;  // word and byte of columns nt, nt + 1
+                const uint32_t sel = (uint32_t)(j | ((4 + j) << 4) | ((j + 1) << 8) | ((5 + j) << 12));
+                const uint32_t x01 = dev::prmt(vw[0][wi], vw[1][wi], sel);  // k rows 2cq, 2cq+1
+                const uint32_t x89 = dev::prmt(vw[2][wi], vw[3][wi], sel);  // k rows 2cq+8, 2cq+9
+                dev::mma_f16_16816(o[nt], pa, dev::e4m3x2_to_f16x2(x01), dev::e4m3x2_to_f16x2(x89));
+                dev::mma_f16_16816(o[nt + 1], pa, dev::e4m3x2_to_f16x2(x01 >> 16), dev::e4m3x2_to_f16x2(x89 >> 16));
+            }
+        } else {
+            pa[0] = dev::pack_bf16x2(s[0][0], s[0][1]);
+            pa[1] = dev::pack_bf16x2(s[0][2], s[0][3]);
+            pa[2] = dev::pack_bf16x2(s[1][0], s[1][1]);
+            pa[3] = dev::pack_bf16x2(s[1][2], s[1][3]);
+            // ---- O += P V (V rows are the k dimension: transposed fragment loads)
+#pragma unroll
+            for (int dt = 0; dt < D / 16; ++dt) {
+                const uint32_t addr =
+                    vs_base + ((lane & 7) + ((lane >> 3) & 1) * 8) * row_stride + (dt * 16 + (lane >> 4) * 8) * 2;
+                uint32_t v0, v1, v2, v3;
+                dev::ldsm_x4_t(addr, v0, v1, v2, v3);
+                dev::mma_bf16_16816(o[2 * dt], pa, v0, v1);
+                dev::mma_bf16_16816(o[2 * dt + 1], pa, v2, v3);
+            }
         }
 
         __syncwarp();
@@ -376,8 +459,8 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
         lt0 += __shfl_xor_sync(0xffffffffu, lt0, 2);
         float lt1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
         lt1 += __shfl_xor_sync(0xffffffffu, lt1, 2);
-        const float inv0 = lt0 > 0.f ? 1.f / lt0 : 0.f;
-        const float inv1 = lt1 > 0.f ? 1.f / lt1 : 0.f;
+        const float inv0 = lt0 > 0.f ? vs / lt0 : 0.f;
+        const float inv1 = lt1 > 0.f ? vs / lt1 : 0.f;
         const float lse0 = lt0 > 0.f ? m0 + __log2f(lt0) : -INFINITY;  // log2 domain
         const float lse1 = lt1 > 0.f ? m1 + __log2f(lt1) : -INFINITY;
 
@@ -389,9 +472,24 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
                 const int64_t orow = (int64_t)(si.tok0 + r / G) * Hq + g * G + r % G;
                 uint32_t* dst = reinterpret_cast<uint32_t*>(p.out + orow * D);
                 const float inv = half ? inv1 : inv0;
+                if constexpr (F8) {
+                    // columns (2cq + e) * D/8 + nt of o[nt][2 half + e]: two runs of D/8
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-                    dst[(nt * 8 + 2 * cq) >> 1] = dev::pack_bf16x2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
+                    for (int e = 0; e < 2; ++e) {
+                        uint32_t w[NT / 2];
+#pragma unroll
+                        for (int nt = 0; nt < NT; nt += 2)
+                            w[nt / 2] = dev::pack_bf16x2(o[nt][2 * half + e] * inv, o[nt + 1][2 * half + e] * inv);
+                        uint4* d4 = reinterpret_cast<uint4*>(dst + (2 * cq + e) * (D / 16));
+#pragma unroll
+                        for (int i = 0; i < NT / 8; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        dst[(nt * 8 + 2 * cq) >> 1] =
+                            dev::pack_bf16x2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
+                }
                 if (p.lse != nullptr && cq == 0) p.lse[orow] = (half ? lse1 : lse0) * kLn2;
             }
             continue;
@@ -409,10 +507,21 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
             if (r >= rows) continue;
             const int prow = (r / G) * Hq + g * G + r % G;  // (token, q head) within the group
             const float inv = half ? inv1 : inv0;
+            if constexpr (F8) {
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-                *reinterpret_cast<float2*>(po + (int64_t)prow * D + nt * 8 + 2 * cq) =
-                    make_float2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
+                for (int e = 0; e < 2; ++e) {
+                    float4* d4 = reinterpret_cast<float4*>(po + (int64_t)prow * D + (2 * cq + e) * (D / 8));
+#pragma unroll
+                    for (int i = 0; i < NT / 4; ++i)
+                        d4[i] = make_float4(o[4 * i][2 * half + e] * inv, o[4 * i + 1][2 * half + e] * inv,
+                                            o[4 * i + 2][2 * half + e] * inv, o[4 * i + 3][2 * half + e] * inv);
+                }
+            } else {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    *reinterpret_cast<float2*>(po + (int64_t)prow * D + nt * 8 + 2 * cq) =
+                        make_float2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
+            }
             if (cq == 0) pl[prow] = half ? lse1 : lse0;
         }
     }
@@ -511,9 +620,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(ForwardParams p) {
 }
 
 template <int D>
-int stage_count(int num_kv_heads, int ctas_per_sm) {
+int stage_count(int num_kv_heads, int ctas_per_sm, int es) {
     const int hb = num_kv_heads < kMaxKvHeads ? num_kv_heads : kMaxKvHeads;
-    const int row_stride = hb * D * 2 + kRowPad;
+    const int row_stride = hb * D * es + kRowPad;
     const int stage_bytes = 2 * kStageKeys * row_stride;
     const int budget = 220 * 1024 / ctas_per_sm - 1024;
     int st = budget / stage_bytes;
@@ -521,22 +630,25 @@ int stage_count(int num_kv_heads, int ctas_per_sm) {
 }
 
 template <int D>
-size_t smem_bytes(int num_kv_heads, int stages) {
+size_t smem_bytes(int num_kv_heads, int stages, int es) {
     const int hb = num_kv_heads < kMaxKvHeads ? num_kv_heads : kMaxKvHeads;
-    const int row_stride = hb * D * 2 + kRowPad;
+    const int row_stride = hb * D * es + kRowPad;
     return ((sizeof(DecSmemHead) + 127) / 128) * 128 + (size_t)stages * 2 * kStageKeys * row_stride;
 }
 
-template <int D>
+template <int D, bool F8>
 cudaError_t launch_d(const ForwardParams& p, int ctas, cudaStream_t s) {
+    constexpr int es = F8 ? 1 : 2;
     const int cps = decode_ctas_per_sm(p.num_kv_heads, D);
-    const int stages = stage_count<D>(p.num_kv_heads, cps);
-    const size_t smem = smem_bytes<D>(p.num_kv_heads, stages);
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const int stages = stage_count<D>(p.num_kv_heads, cps, es);
+    const size_t smem = smem_bytes<D>(p.num_kv_heads, stages, es);
+    cudaError_t e =
+        cudaFuncSetAttribute(decode_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int hb = p.num_kv_heads < kMaxKvHeads ? p.num_kv_heads : kMaxKvHeads;
-    const int row_stride = hb * D * 2 + kRowPad;
-    return launch_programmatic(decode_kernel<D>, (unsigned)ctas, 32u * (hb + 1), smem, s, p, stages, row_stride);
+    const int row_stride = hb * D * es + kRowPad;
+    return launch_programmatic(decode_kernel<D, F8>, (unsigned)ctas, 32u * (hb + 1), smem, s, p, stages,
+                               row_stride);
 }
 
 template <int D>
@@ -562,8 +674,8 @@ bool decode_supported(int num_qo_heads, int num_kv_heads, int head_dim) {
 }
 
 cudaError_t launch_decode(const ForwardParams& p, int head_dim, int ctas, cudaStream_t s) {
-    if (head_dim == 128) return launch_d<128>(p, ctas, s);
-    if (head_dim == 64) return launch_d<64>(p, ctas, s);
+    if (head_dim == 128) return p.kv_fp8 ? launch_d<128, true>(p, ctas, s) : launch_d<128, false>(p, ctas, s);
+    if (head_dim == 64) return p.kv_fp8 ? launch_d<64, true>(p, ctas, s) : launch_d<64, false>(p, ctas, s);
     return cudaErrorInvalidValue;
 }
 

@@ -197,6 +197,11 @@ struct ForwardParams {
     float scale_log2;            // sm_scale * log2(e)
     uint8_t* ws;
     Layout lay;
+    // FP8 (E4M3) pools: k_pool / v_pool hold one byte per element and each kv head h
+    // has the scales k_scale[h], v_scale[h] (device fp32); zero for bf16 pools
+    int32_t kv_fp8;
+    const float* k_scale;
+    const float* v_scale;
 };
 
 // Host view of a prepared batch, stored inside pva_meta::opaque.

@@ -7,7 +7,8 @@
 // update as a scatter by slot.  A slot row holds all kv heads of one token,
 // Hkv * D bf16 = 1-2 KiB contiguous in both the source and the pool, so one
 // warp moves one token's K row (or V row) with 16-byte vector accesses: reads
-// stream past L1, writes stay in L2 for the attention kernels that follow.
+// stream past L1, writes stay in L2 for the attention kernels that follow.  Into an
+// FP8 pool each element is quantised on the way (x / scale of its kv head, to E4M3).
 #include <cuda_runtime.h>
 
 #include "device_utils.cuh"
@@ -41,8 +42,33 @@ __global__ void __launch_bounds__(kThreads) store_kernel(ForwardParams p, int ro
         return;
     }
     const int4* src = reinterpret_cast<const int4*>(is_v ? p.v : p.k) + t * row_vecs;
-    int4* dst = reinterpret_cast<int4*>(is_v ? p.v_pool : p.k_pool) + slot * row_vecs;
-    for (int i = lane; i < row_vecs; i += 32) dst[i] = dev::ld_stream_v4(src + i);
+    if (!p.kv_fp8) {
+        int4* dst = reinterpret_cast<int4*>(is_v ? p.v_pool : p.k_pool) + slot * row_vecs;
+        for (int i = lane; i < row_vecs; i += 32) dst[i] = dev::ld_stream_v4(src + i);
+        return;
+    }
+    // FP8 pool: element (h, d) becomes e4m3(x / scale[h]) (IEEE division, nearest even,
+    // saturating); a lane turns 16 elements (two source vectors, one head) into one
+    // 16-byte pool vector
+    const float* scale = is_v ? p.v_scale : p.k_scale;
+    int4* dst = reinterpret_cast<int4*>(is_v ? p.v_pool : p.k_pool) + slot * (row_vecs / 2);
+    const int D = row_vecs * 8 / p.num_kv_heads;
+    for (int i = lane; i < row_vecs / 2; i += 32) {
+        const float sc = scale[(16 * i) / D];
+        const int4 a = dev::ld_stream_v4(src + 2 * i), b = dev::ld_stream_v4(src + 2 * i + 1);
+        const uint32_t w[8] = {(uint32_t)a.x, (uint32_t)a.y, (uint32_t)a.z, (uint32_t)a.w,
+                               (uint32_t)b.x, (uint32_t)b.y, (uint32_t)b.z, (uint32_t)b.w};
+        uint32_t q[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float x0 = __fdiv_rn(__uint_as_float(w[2 * j] << 16), sc);
+            const float x1 = __fdiv_rn(__uint_as_float(w[2 * j] & 0xFFFF0000u), sc);
+            const float x2 = __fdiv_rn(__uint_as_float(w[2 * j + 1] << 16), sc);
+            const float x3 = __fdiv_rn(__uint_as_float(w[2 * j + 1] & 0xFFFF0000u), sc);
+            q[j] = dev::f32x2_to_e4m3x2(x0, x1) | (dev::f32x2_to_e4m3x2(x2, x3) << 16);
+        }
+        dst[i] = make_int4((int)q[0], (int)q[1], (int)q[2], (int)q[3]);
+    }
 }
 
 }  // namespace

@@ -26,7 +26,7 @@ DEVERR = {
 # Every function include/pva.h declares; the CPU tests check the library exports each one.
 EXPORTS = ("attn_abi_version", "attn_status_string", "attn_workspace_size", "attn_prepare_metadata",
            "attn_forward", "attn_store_kvcache", "attn_get_device_status", "attn_debug_plan_counts",
-           "attn_set_timing_events", "attn_prepare_metadata_static")
+           "attn_set_timing_events", "attn_prepare_metadata_static", "attn_forward_fp8kv", "attn_store_kvcache_fp8kv")
 
 
 class PvaError(RuntimeError):
@@ -42,7 +42,7 @@ class Config(ctypes.Structure):
         ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int64), ("sm_scale", ctypes.c_float),
         ("max_batch", ctypes.c_int32), ("max_tokens", ctypes.c_int32), ("max_kv_len", ctypes.c_int32),
         ("enable_split_kv", ctypes.c_int32), ("enable_cascade", ctypes.c_int32),
-        ("min_cascade_pages", ctypes.c_int32),
+        ("min_cascade_pages", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
     ]
 
 
@@ -78,6 +78,10 @@ def load(path: str | None = None):
         lib.attn_forward.restype = ctypes.c_int
         lib.attn_store_kvcache.argtypes = [MP, P, P, P, P, P]
         lib.attn_store_kvcache.restype = ctypes.c_int
+        lib.attn_forward_fp8kv.argtypes = [MP, P, P, P, P, P, P, P, P, P, P]
+        lib.attn_forward_fp8kv.restype = ctypes.c_int
+        lib.attn_store_kvcache_fp8kv.argtypes = [MP, P, P, P, P, P, P, P]
+        lib.attn_store_kvcache_fp8kv.restype = ctypes.c_int
         lib.attn_get_device_status.argtypes = [MP, ctypes.POINTER(ctypes.c_uint32)]
         lib.attn_get_device_status.restype = ctypes.c_int
         lib.attn_set_timing_events.argtypes = [MP, ctypes.POINTER(ctypes.c_void_p), i32]
@@ -115,11 +119,14 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+KV_BF16, KV_E4M3 = 0, 1
+
+
 def make_config(num_qo_heads, num_kv_heads, head_dim, page_size, num_pages, max_batch, max_tokens, max_kv_len,
                 sm_scale: float = 0.0, enable_split_kv: bool = True, enable_cascade: bool = True,
-                min_cascade_pages: int = 8) -> Config:
+                min_cascade_pages: int = 8, kv_dtype: int = KV_BF16) -> Config:
     return Config(num_qo_heads, num_kv_heads, head_dim, page_size, num_pages, sm_scale, max_batch, max_tokens,
-                  max_kv_len, int(enable_split_kv), int(enable_cascade), int(min_cascade_pages))
+                  max_kv_len, int(enable_split_kv), int(enable_cascade), int(min_cascade_pages), int(kv_dtype))
 
 
 def attn_workspace_size(cfg: Config) -> int:
@@ -160,6 +167,19 @@ def attn_store_kvcache(meta: Meta, k, v, k_pool, v_pool, stream=None) -> None:
     _check(st, "attn_store_kvcache")
 
 
+def attn_forward_fp8kv(meta: Meta, q, k, v, k_pool, v_pool, k_scale, v_scale, out, lse=None, stream=None) -> None:
+    """attn_forward over E4M3 pools (uint8 tensors) with per-kv-head fp32 scales (device tensors)."""
+    st = load().attn_forward_fp8kv(ctypes.byref(meta), _ptr(q), _ptr(k), _ptr(v), _ptr(k_pool), _ptr(v_pool),
+                                   _ptr(k_scale), _ptr(v_scale), _ptr(out), _ptr(lse), _stream(stream))
+    _check(st, "attn_forward_fp8kv")
+
+
+def attn_store_kvcache_fp8kv(meta: Meta, k, v, k_pool, v_pool, k_scale, v_scale, stream=None) -> None:
+    st = load().attn_store_kvcache_fp8kv(ctypes.byref(meta), _ptr(k), _ptr(v), _ptr(k_pool), _ptr(v_pool),
+                                         _ptr(k_scale), _ptr(v_scale), _stream(stream))
+    _check(st, "attn_store_kvcache_fp8kv")
+
+
 def attn_get_device_status(meta: Meta) -> int:
     """Synchronises; returns the device error word (0 = clean)."""
     bits = ctypes.c_uint32(0)
@@ -195,11 +215,11 @@ class PagedAttention:
 
     def __init__(self, num_qo_heads, num_kv_heads, head_dim, page_size, num_pages, max_batch, max_tokens,
                  max_kv_len, sm_scale: float = 0.0, enable_split_kv: bool = True, enable_cascade: bool = True,
-                 min_cascade_pages: int = 8, device="cuda"):
+                 min_cascade_pages: int = 8, device="cuda", kv_dtype: int = KV_BF16):
         import torch
 
         self.cfg = make_config(num_qo_heads, num_kv_heads, head_dim, page_size, num_pages, max_batch, max_tokens,
-                               max_kv_len, sm_scale, enable_split_kv, enable_cascade, min_cascade_pages)
+                               max_kv_len, sm_scale, enable_split_kv, enable_cascade, min_cascade_pages, kv_dtype)
         nbytes = attn_workspace_size(self.cfg)
         if nbytes == 0:
             raise PvaError(2, "attn_workspace_size")
@@ -216,10 +236,15 @@ class PagedAttention:
                                           total_tokens, max_q_len, self.workspace, stream)
         return self.meta
 
-    def forward(self, q, k, v, k_pool, v_pool, out=None, lse=None, stream=None):
+    def forward(self, q, k, v, k_pool, v_pool, out=None, lse=None, stream=None, k_scale=None, v_scale=None):
+        """One layer.  With an E4M3 config the pools are uint8 and k_scale / v_scale (fp32 [Hkv],
+        on the device) are required."""
         import torch
 
         if out is None:
             out = torch.empty_like(q)
-        attn_forward(self.meta, q, k, v, k_pool, v_pool, out, lse, stream)
+        if self.cfg.kv_dtype == KV_E4M3:
+            attn_forward_fp8kv(self.meta, q, k, v, k_pool, v_pool, k_scale, v_scale, out, lse, stream)
+        else:
+            attn_forward(self.meta, q, k, v, k_pool, v_pool, out, lse, stream)
         return out

@@ -235,6 +235,44 @@ def make_tensors(wl: Workload, device="cpu", poison_unused: bool = False, fill_a
     }
 
 
+def make_fp8_pools(wl: Workload, device="cpu", poison_unused: bool = False):
+    """E4M3 pools (uint8 codes) and one fp32 scale per kv head for K and for V.
+
+    Codes are drawn directly (random sign, exponent field 0..10, random mantissa:
+    magnitudes up to ~15 times the scale), so no conversion arithmetic is involved.
+    Pages no request uses, and with ``poison_unused`` the slots of a request's last page
+    past its kv_len, hold the NaN code 0x7F instead (zero codes without poisoning).
+    Scales are drawn in [0.02, 0.1) (not powers of two, so quantising divides inexactly).
+    Returns (k_pool, v_pool, k_scale, v_scale), torch tensors on ``device``.
+    """
+    import torch
+
+    rng = np.random.default_rng(int(wl.seed) * 104729 + 3)
+    Hkv, D, ps, P = wl.num_kv_heads, wl.head_dim, wl.page_size, wl.num_pages
+
+    def codes(n_pages):
+        sign = rng.integers(0, 2, size=(n_pages, ps, Hkv, D), dtype=np.uint8) << 7
+        expo = rng.integers(0, 11, size=(n_pages, ps, Hkv, D), dtype=np.uint8) << 3
+        mant = rng.integers(0, 8, size=(n_pages, ps, Hkv, D), dtype=np.uint8)
+        return sign | expo | mant
+
+    fill = 0x7F if poison_unused else 0x00
+    pools = []
+    used = np.asarray(wl.used_pages(), dtype=np.int64)
+    for _ in range(2):
+        pool = np.full((P, ps, Hkv, D), fill, dtype=np.uint8)
+        if used.size:
+            pool[used] = codes(used.size)
+        if poison_unused:
+            for i, L in enumerate(wl.kv_lens):
+                if L % ps:
+                    pool[int(wl.page_table[i, L // ps]), L % ps:] = 0x7F
+        pools.append(torch.from_numpy(pool.reshape(P * ps, Hkv, D)).to(device))
+    k_scale = torch.from_numpy(rng.uniform(0.02, 0.1, Hkv).astype(np.float32)).to(device)
+    v_scale = torch.from_numpy(rng.uniform(0.02, 0.1, Hkv).astype(np.float32)).to(device)
+    return pools[0], pools[1], k_scale, v_scale
+
+
 def set_junk_columns(wl: Workload, page_id: int) -> None:
     """Point every page-table column past a request's last page at ``page_id``."""
     for i, L in enumerate(wl.kv_lens):

@@ -20,12 +20,13 @@ LSE_ATOL = 1e-3
 
 
 def make_engine(wl: W.Workload, enable_split_kv=True, enable_cascade=True, min_cascade_pages=8, sm_scale=0.0,
-                max_tokens=None, max_batch=None, max_kv_len=None):
+                max_tokens=None, max_batch=None, max_kv_len=None, kv_dtype=pva.KV_BF16):
     return pva.PagedAttention(
         wl.num_qo_heads, wl.num_kv_heads, wl.head_dim, wl.page_size, wl.num_pages,
         max_batch=max_batch or max(wl.batch, 1), max_tokens=max_tokens or max(wl.total_tokens, 1),
         max_kv_len=max_kv_len or max(max(wl.kv_lens) if wl.kv_lens else 1, 1), sm_scale=sm_scale,
-        enable_split_kv=enable_split_kv, enable_cascade=enable_cascade, min_cascade_pages=min_cascade_pages)
+        enable_split_kv=enable_split_kv, enable_cascade=enable_cascade, min_cascade_pages=min_cascade_pages,
+        kv_dtype=kv_dtype)
 
 
 def run_cuda(wl: W.Workload, t: dict, engine=None, slot_mapping=None, max_q_len=0, with_lse=True):

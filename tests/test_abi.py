@@ -42,7 +42,7 @@ def test_only_the_abi_is_exported():
 
 
 def test_version_and_status_strings(lib):
-    assert pva.abi_version() == 1
+    assert pva.abi_version() == 2
     for s in range(7):
         assert pva.status_string(s).startswith(pva.STATUS_NAMES[s])
     assert "unknown" in pva.status_string(99)
@@ -119,3 +119,4 @@ def test_forward_requires_a_prepared_meta(lib):
     assert lib.attn_forward(ctypes.byref(meta), dummy, dummy, dummy, dummy, dummy, dummy, None, None) == 6
     assert lib.attn_store_kvcache(ctypes.byref(meta), dummy, dummy, dummy, dummy, None) == 6
     assert lib.attn_forward(None, dummy, dummy, dummy, dummy, dummy, dummy, None, None) == 6
+
