@@ -38,6 +38,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "e4m3"],
+                    help="pool element type (e4m3: one byte per element, a scale per kv head)")
     return ap.parse_args()
 
 
@@ -96,6 +98,7 @@ def job_tokens_per_s(tokens_per_rank: int, world: int, ms: float) -> float:
 def job_config(wl, args, world: int) -> dict:
     return {
         "workload": wl.description, "seed": args.seed, "batch": wl.batch, "new_tokens": wl.total_tokens,
+        "kv_dtype": args.kv_dtype,
         "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write, outside the timed events)",
         "step": "attn_prepare_metadata + attn_forward (store_kvcache + attention), one layer",
         "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
@@ -104,17 +107,17 @@ def job_config(wl, args, world: int) -> dict:
 
 # ------------------------------------------------------------------------------ algorithmic work
 
-def algorithmic_work(wl):
+def algorithmic_work(wl, kv_elem_bytes: int = 2):
     """Bytes and FLOPs the step must move / compute, independent of the kernels.
 
     bytes: every visible KV row once (unique pages), this step's Q read and O
-    write, the new K/V read and their pool write.  FLOPs: 4*D per visible
-    (query, key) pair per q head (QK^T and PV), causal pairs only.
+    write, the new K/V read (bf16) and their pool write (kv_elem_bytes per element).
+    FLOPs: 4*D per visible (query, key) pair per q head (QK^T and PV), causal pairs only.
     """
     import numpy as np
 
     Hq, Hkv, D, ps = wl.num_qo_heads, wl.num_kv_heads, wl.head_dim, wl.page_size
-    row_kv = Hkv * D * 2  # bytes of one slot's K (or V) row, all kv heads
+    row_kv = Hkv * D * kv_elem_bytes  # bytes of one slot's K (or V) row in the pool, all kv heads
     # unique KV rows read: positions < kv_len of each request, shared prefix pages counted once
     seen = set()
     kv_rows = 0
@@ -134,8 +137,8 @@ def algorithmic_work(wl):
     kv_bytes = 2 * kv_rows * row_kv
     q_bytes = T * Hq * D * 2
     o_bytes = T * Hq * D * 2
-    new_kv_bytes = 2 * T * row_kv
-    store_bytes = 2 * new_kv_bytes  # read k,v + write pool
+    new_kv_bytes = 2 * T * Hkv * D * 2
+    store_bytes = new_kv_bytes + 2 * T * row_kv  # read k,v (bf16) + write the pool rows
     pairs = 0
     for n, L in zip(wl.q_lens, wl.kv_lens):
         # query r sees L - n + r + 1 keys
@@ -250,8 +253,12 @@ def cpu_baseline(wl, tensors_cpu, budget_s: float):
     k = tensors_cpu["k"][rows]
     v = tensors_cpu["v"][rows]
     t0 = time.perf_counter()
-    oracle.forward(q, k, v, tensors_cpu["k_pool"], tensors_cpu["v_pool"], sub_cu, sub_lens, sub_table,
-                   wl.page_size)
+    if "k_scale" in tensors_cpu:
+        oracle.forward_fp8(q, k, v, tensors_cpu["k_pool"], tensors_cpu["v_pool"], tensors_cpu["k_scale"],
+                           tensors_cpu["v_scale"], sub_cu, sub_lens, sub_table, wl.page_size)
+    else:
+        oracle.forward(q, k, v, tensors_cpu["k_pool"], tensors_cpu["v_pool"], sub_cu, sub_lens, sub_table,
+                       wl.page_size)
     dt = time.perf_counter() - t0
     tokens = int(sub_cu[-1])
     return {"value": tokens / dt if dt > 0 else None, "unit": "tokens/s", "cores": threads, "kind": "oracle",
@@ -269,6 +276,8 @@ def run_reference(args):
 
     wl = W.WORKLOADS[args.workload](args.seed)
     t = W.make_tensors(wl, "cpu")
+    if args.kv_dtype == "e4m3":
+        t["k_pool"], t["v_pool"], t["k_scale"], t["v_scale"] = W.make_fp8_pools(wl, "cpu")
     vals = []
     base = None
     budget = min(args.cpu_budget_s, 150.0 / max(args.steps + args.warmup, 1))
@@ -313,13 +322,18 @@ def run_ours(args):
     pva.load()
 
     wl = W.WORKLOADS[args.workload](args.seed + rank)
-    work = algorithmic_work(wl)
+    fp8 = args.kv_dtype == "e4m3"
+    work = algorithmic_work(wl, 1 if fp8 else 2)
     dev = torch.device("cuda", local)
     t = W.make_tensors(wl, dev)
+    scales = {}
+    if fp8:
+        t["k_pool"], t["v_pool"], ks, vs = W.make_fp8_pools(wl, dev)
+        scales = {"k_scale": ks, "v_scale": vs}
     max_q = max(wl.q_lens)
     eng = pva.PagedAttention(wl.num_qo_heads, wl.num_kv_heads, wl.head_dim, wl.page_size, wl.num_pages,
                              max_batch=wl.batch, max_tokens=wl.total_tokens, max_kv_len=max(wl.kv_lens),
-                             device=dev)
+                             device=dev, kv_dtype=pva.KV_E4M3 if fp8 else pva.KV_BF16)
     out = torch.empty_like(t["q"])
     lse = torch.empty(t["q"].shape[:2], dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -327,7 +341,7 @@ def run_ours(args):
 
     def step():
         eng.prepare(t["cu_seqlens_q"], t["cache_seqlens"], t["page_table"], wl.total_tokens, None, max_q)
-        eng.forward(t["q"], t["k"], t["v"], t["k_pool"], t["v_pool"], out, lse)
+        eng.forward(t["q"], t["k"], t["v"], t["k_pool"], t["v_pool"], out, lse, **scales)
 
     for _ in range(args.warmup):
         flush.fill_(1.0)
@@ -389,7 +403,7 @@ def run_ours(args):
         eng.prepare(t["cu_seqlens_q"], t["cache_seqlens"], t["page_table"], wl.total_tokens, None, max_q)
         pev[1].record()
         pva.attn_set_timing_events(eng.meta, kev)
-        eng.forward(t["q"], t["k"], t["v"], t["k_pool"], t["v_pool"], out, lse)
+        eng.forward(t["q"], t["k"], t["v"], t["k_pool"], t["v_pool"], out, lse, **scales)
     pva.attn_set_timing_events(eng.meta, None)
     for i in range(args.steps):
         flush.fill_(float(i))
@@ -410,7 +424,7 @@ def run_ours(args):
         roof = {"bound": "hbm", "achieved": work["attn_bytes"] / (phase_ms[dom] / 1e3) / 1e9,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = ncu_traffic(dom, args.workload)
+    roof["traffic"] = ncu_traffic(dom, args.workload if not fp8 else args.workload + "-e4m3")
     roof["kernel"] = dom
     roof["peak_source"] = peaks["source"]
     roof_time_s = max(work["flops"] / (peaks["bf16_tflops"] * 1e12), work["step_bytes"] / (peaks["hbm_gbs"] * 1e9))
@@ -427,7 +441,7 @@ def run_ours(args):
             dev_in[k2].copy_(v2, non_blocking=True)
         eng.prepare(dev_in["cu_seqlens_q"], dev_in["cache_seqlens"], dev_in["page_table"], wl.total_tokens, None,
                     max_q)
-        eng.forward(dev_in["q"], dev_in["k"], dev_in["v"], t["k_pool"], t["v_pool"], out, None)
+        eng.forward(dev_in["q"], dev_in["k"], dev_in["v"], t["k_pool"], t["v_pool"], out, None, **scales)
         host_out.copy_(out, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
@@ -446,13 +460,13 @@ def run_ours(args):
 
     base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        base = cpu_baseline(wl, {k: v.cpu() for k, v in t.items()}, args.cpu_budget_s)
+        base = cpu_baseline(wl, {k: v.cpu() for k, v in dict(t, **scales).items()}, args.cpu_budget_s)
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "vs_baseline": None, "dtype": "f16 MMA on e4m3 KV" if fp8 else "bf16", "data": "synthetic",
             "config": job_config(wl, args, world),
             "roofline": roof,
             "step_roofline": {"roofline_time_us": roof_time_s * 1e6, "frac_of_step": roof_time_s / (ms / 1e3),

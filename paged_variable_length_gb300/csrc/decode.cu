@@ -96,6 +96,8 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
     const int n_hb = Hkv / HB;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row_bytes = HB * D * ES;
+    // rows staged back to back (no padding): one copy per stage and pool (see launch_d)
+    const bool runs = row_stride == row_bytes;
     const int stage_bytes = 2 * kStageKeys * row_stride;
     // Plan from the prepare kernel (finished before the store kernel began); pool rows,
     // the work counter and the prefix-pass partials only after grid_dep_wait.
@@ -217,7 +219,17 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
                 armed |= 1u << stage;
                 armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
                 __syncwarp();
-                if (r < nk) {
+                if (runs && (k & (kStageKeys - 1)) == 0) {
+                    // the stage's rows are consecutive slots of one page (a 16-aligned run of
+                    // keys inside a page of >= 16 slots): one copy for K, one for V
+                    if (r == 0) {
+                        const int64_t slot = (page << p.page_shift) + (k & ps_mask);
+                        const uint8_t* src = reinterpret_cast<const uint8_t*>(lane < 16 ? p.k_pool : p.v_pool) +
+                                             slot * (int64_t)(Hkv * D) * ES;
+                        uint8_t* dst = ring + stage * stage_bytes + (lane < 16 ? 0 : kStageKeys * row_stride);
+                        dev::bulk_g2s_hint(dst, src, (uint32_t)(nk * row_bytes), &sh->full[stage], policy);
+                    }
+                } else if (r < nk) {
                     const int64_t slot = (page << p.page_shift) + ((k + r) & ps_mask);
                     const uint8_t* src = reinterpret_cast<const uint8_t*>(lane < 16 ? p.k_pool : p.v_pool) +
                                          (slot * (int64_t)(Hkv * D) + hb * HB * D) * ES;
@@ -620,9 +632,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(ForwardParams p) {
 }
 
 template <int D>
-int stage_count(int num_kv_heads, int ctas_per_sm, int es) {
+int stage_count(int num_kv_heads, int ctas_per_sm, int es, int pad) {
     const int hb = num_kv_heads < kMaxKvHeads ? num_kv_heads : kMaxKvHeads;
-    const int row_stride = hb * D * es + kRowPad;
+    const int row_stride = hb * D * es + pad;
     const int stage_bytes = 2 * kStageKeys * row_stride;
     const int budget = 220 * 1024 / ctas_per_sm - 1024;
     int st = budget / stage_bytes;
@@ -630,23 +642,31 @@ int stage_count(int num_kv_heads, int ctas_per_sm, int es) {
 }
 
 template <int D>
-size_t smem_bytes(int num_kv_heads, int stages, int es) {
+size_t smem_bytes(int num_kv_heads, int stages, int es, int pad) {
     const int hb = num_kv_heads < kMaxKvHeads ? num_kv_heads : kMaxKvHeads;
-    const int row_stride = hb * D * es + kRowPad;
+    const int row_stride = hb * D * es + pad;
     return ((sizeof(DecSmemHead) + 127) / 128) * 128 + (size_t)stages * 2 * kStageKeys * row_stride;
 }
 
+// FP8 rows are half as long as bf16 ones, and one bulk copy per 1 KiB row left the copy
+// engine, not HBM, the limit (ncu: DRAM at a third of its peak, consumers waiting on the
+// stages).  So with pages of at least a stage (16 slots) and every kv head in the CTA, a
+// stage's rows -- consecutive slots of one page, contiguous in the pool -- come as one
+// copy per pool and sit back to back.  The K fragment reads then meet 2-way shared-memory
+// bank conflicts (a lane's run sits at the same bank offset in every row); the padded
+// per-row layout stays for the other cases and for bf16, whose ldmatrix reads need it.
 template <int D, bool F8>
 cudaError_t launch_d(const ForwardParams& p, int ctas, cudaStream_t s) {
     constexpr int es = F8 ? 1 : 2;
     const int cps = decode_ctas_per_sm(p.num_kv_heads, D);
-    const int stages = stage_count<D>(p.num_kv_heads, cps, es);
-    const size_t smem = smem_bytes<D>(p.num_kv_heads, stages, es);
+    const bool runs = F8 && p.page_size >= kStageKeys && p.num_kv_heads <= kMaxKvHeads;
+    const int stages = stage_count<D>(p.num_kv_heads, cps, es, runs ? 0 : kRowPad);
+    const size_t smem = smem_bytes<D>(p.num_kv_heads, stages, es, runs ? 0 : kRowPad);
     cudaError_t e =
         cudaFuncSetAttribute(decode_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int hb = p.num_kv_heads < kMaxKvHeads ? p.num_kv_heads : kMaxKvHeads;
-    const int row_stride = hb * D * es + kRowPad;
+    const int row_stride = hb * D * es + (runs ? 0 : kRowPad);
     return launch_programmatic(decode_kernel<D, F8>, (unsigned)ctas, 32u * (hb + 1), smem, s, p, stages,
                                row_stride);
 }
