@@ -32,7 +32,8 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="decode", choices=["worked", "decode", "prefill", "mixed", "cascade"])
+    ap.add_argument("--workload", default="decode",
+                    choices=["worked", "decode", "prefill", "mixed", "cascade", "specdec"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -54,6 +55,12 @@ NCU_TRAFFIC = {
         "sources": ['paged_variable_length_gb300/csrc/decode.cu', 'paged_variable_length_gb300/csrc/device_utils.cuh', 'paged_variable_length_gb300/csrc/pva_internal.h'],
         "sha256_16": "0f902f1ff81ecbae",
         "summary": "profiles/decode_kernel_decode_workload.md",
+    },
+    ("decode", "decode-e4m3"): {
+        "bytes": 312.932096e6,
+        "sources": ['paged_variable_length_gb300/csrc/decode.cu', 'paged_variable_length_gb300/csrc/device_utils.cuh', 'paged_variable_length_gb300/csrc/pva_internal.h'],
+        "sha256_16": "d5d81c69c42037e9",
+        "summary": "profiles/decode_kernel_fp8_decode_workload.md",
     },
     ("tensor_core", "prefill"): {
         "bytes": 220.103424e6,

@@ -158,6 +158,19 @@ def cascade(seed: int = 0, batch: int = 128, prefix: int = 4096, lo: int = 16, h
                                 f"U[{lo},{hi}], Hq32/Hkv8/D128, ps16, 20000-page pool")
 
 
+def spec_decode(seed: int = 0, batch: int = 64, draft: int = 3, lo: int = 512, hi: int = 4096) -> Workload:
+    """A uniform speculative-decoding verify step: every request appends 1 + draft tokens
+    (the last accepted token and the drafted ones), causally masked among themselves;
+    kv_len ~ U[lo, hi] including them; Hq 32, Hkv 8, D 128; page_size 16 over a 20000-page pool."""
+    rng = np.random.default_rng(seed)
+    n = 1 + draft
+    kv_lens = [int(x) for x in rng.integers(max(lo, n), hi + 1, size=batch)]
+    table = _allocate_rows(rng, kv_lens, 16, 20000)
+    return Workload("specdec", [n] * batch, kv_lens, 32, 8, 128, 16, 20000, table, 1.0, seed,
+                    description=f"speculative verify: {batch} requests x {n} queries (1 + {draft} drafted), "
+                                f"kv_len U[{lo},{hi}], Hq32/Hkv8/D128, ps16, 20000-page pool")
+
+
 def custom(q_lens, kv_lens, num_qo_heads, num_kv_heads, head_dim, page_size, num_pages=None,
            seed: int = 0, value_scale: float = 1.0, shared_prefix_pages: int = 0, slack_pages: int = 8,
            name: str = "custom") -> Workload:
@@ -177,6 +190,7 @@ WORKLOADS = {
     "prefill": prefill_only,
     "mixed": mixed,
     "cascade": cascade,
+    "specdec": spec_decode,
 }
 
 

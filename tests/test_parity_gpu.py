@@ -322,3 +322,22 @@ def test_head_dim_64_cascade():
     wl = _cascade_batch(6, Hq=16, Hkv=4, D=64, ps=16)
     _, eng = _full_check(wl)
     assert pva.attn_debug_plan_counts(eng.meta)["casc_groups"] > 0
+
+
+# ------------------------------------------------------------------ speculative-decoding verify batches
+
+
+@pytest.mark.parametrize("draft,Hq,Hkv", [(1, 32, 8), (3, 32, 8), (7, 32, 8), (3, 28, 4), (3, 64, 8)])
+def test_spec_decode_uniform_batches(draft, Hq, Hkv):
+    """Every request appends 1 + draft tokens that see the cache and each other causally
+    (the decode kernel's groups hold up to 16 / G of them; larger groups split)."""
+    rng = np.random.default_rng(draft * 100 + Hq)
+    n = 1 + draft
+    kl = [int(x) for x in rng.integers(n, 1500, size=12)] + [n, n + 1]  # two with (almost) no cache
+    wl = W.custom([n] * len(kl), kl, Hq, Hkv, 128, 16, seed=draft + Hq)
+    _full_check(wl, max_q_len=n)
+    _full_check(wl)  # without the max_q_len hint
+
+
+def test_spec_decode_full_size_workload():
+    _sampled_check(W.WORKLOADS["specdec"](0))
