@@ -243,10 +243,10 @@ PVA_API pva_status attn_store_kvcache(const pva_meta* meta, const void* k, const
  * The store writes e4m3(k[t, h, d] / k_scale[h]) (IEEE fp32 division, round to
  * nearest even, magnitudes beyond 448 saturate to 448, NaN stays NaN), likewise for
  * v; attention reads each element as e4m3 * scale of its head, otherwise exactly as
- * attn_forward.  Every request runs on the decode kernel (tensor-core and
- * shared-prefix passes are off for this pool type), whose warp MMAs take f16
- * operands: q enters as f16, exact for 2^-17 <= |q| <= 65504, and q outside f16's
- * range gives undefined results.  Scales must be finite and nonzero.
+ * attn_forward (same kernels and plan: the tensor cores and the warp MMAs then take
+ * f16 operands, every E4M3 value being an f16 value).  q enters as f16, exact for
+ * 2^-17 <= |q| <= 65504; q outside f16's range gives undefined results.  Scales must
+ * be finite and nonzero.
  */
 PVA_API pva_status attn_forward_fp8kv(const pva_meta* meta, const void* q, const void* k, const void* v,
                               void* k_pool, void* v_pool, const float* k_scale, const float* v_scale,

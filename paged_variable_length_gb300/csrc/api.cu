@@ -193,9 +193,7 @@ pva_status prepare_in_workspace(const pva_config* cfg, const int32_t* cu_seqlens
     h.sm_count = sms;
     // requests with more than TB new tokens run on the tensor-core prefill kernel, which
     // also runs the prefix pass of shared-prefix groups
-    // (an E4M3 pool is read by the decode kernel only: every request becomes decode groups)
-    const bool tc_ok =
-        cfg->kv_dtype == PVA_KV_BF16 && prefill_supported(cfg->num_qo_heads, cfg->num_kv_heads, cfg->head_dim);
+    const bool tc_ok = prefill_supported(cfg->num_qo_heads, cfg->num_kv_heads, cfg->head_dim);
     h.use_prefill = (mq > TB && tc_ok) ? 1 : 0;
     h.use_cascade = (cfg->enable_cascade && tc_ok && batch >= 2 && batch <= kCascadeMaxBatch) ? 1 : 0;
     h.dec_ctas = sms * decode_ctas_per_sm(cfg->num_kv_heads, cfg->head_dim);

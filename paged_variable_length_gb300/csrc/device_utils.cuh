@@ -179,6 +179,15 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
     return r;
 }
 
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// A bf16 pair -> the same values as an f16 pair (round to nearest even; exact inside f16's range).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x) {
+    return pack_f16x2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
+}
+
 // Byte permute: bytes of {b, a} (a = bytes 0-3, b = bytes 4-7) picked by the four selector nibbles.
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t r;

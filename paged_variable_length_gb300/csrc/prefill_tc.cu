@@ -27,6 +27,11 @@
 //     a row's max grows by more than 2^8, and normalised once at the end.
 // TMEM: per Q tile h, S_h at columns 256h .. 256h+127 (P_h aliases its first
 // 64 columns) and O_h at 256h+128 .. 256h+255.
+// FP8 pools (F8): the MMAs take f16 operands (kind::f16 needs one type for both): the
+// producers load E4M3 K/V rows into registers, convert them (exactly) to f16 and store
+// the operand tiles; Q lands as bf16 and each softmax thread converts its own row in
+// place at the start of a unit (exact inside f16's range); P is packed as f16.
+// k_scale of the unit's kv head folds into the softmax scale, v_scale into 1/l.
 // Every wait is bounded; a timeout sets PVA_DEVERR_TIMEOUT and the CTA winds
 // down (outstanding copies and MMAs waited for, TMEM freed) without trapping.
 #include <cuda.h>  // CUtensorMap and the tensor-map encoder's types (resolved through the runtime)
@@ -63,7 +68,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-template <int D>
+template <int D, bool F8 = false>
 struct SmemMap {
     static constexpr int kHalves = D / 64;
     static constexpr int kTile = kRegion * kHalves;
@@ -71,11 +76,15 @@ struct SmemMap {
     static constexpr int kK = kQ + 2 * kTile;    // two K stages
     static constexpr int kV = kK + 2 * kTile;    // two V stages
     static constexpr int kOff = kV + 2 * kTile;  // per producer warp: source offsets of its rows (64 x int64)
-    static constexpr int kBytes = kOff + 3 * 64 * 8;
+    // FP8: the raw E4M3 rows of one K tile and one V tile (row r at r * D)
+    static constexpr int kStage8 = kOff + 3 * 64 * 8;
+    static constexpr int kBytes = kStage8 + (F8 ? 2 * kPreRows * D : 0);
 };
 
 struct Bars {
-    uint64_t q_full, q_empty;
+    // q_full: both Q tiles in operand form (F8: q_raw when the bf16 rows have landed,
+    // q_full once the softmax warps have converted them)
+    uint64_t q_full, q_empty, q_raw;
     uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
     uint64_t s_full[2], p_full[2], o_ready[2], o_free[2];
     uint64_t drain;
@@ -146,10 +155,10 @@ __device__ __forceinline__ UnitView unit_view(const PreTile& pt) {
 
 // q_map: Q as a 3-D tensor (D, Hq, T) whose box is one 64-column half of a Q tile (64
 // columns x G heads x TM tokens, rows in tile order); used when q_tma is nonzero.
-template <int D>
+template <int D, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const ForwardParams p, const __grid_constant__ CUtensorMap q_map, const int q_tma) {
-    using L = SmemMap<D>;
+    using L = SmemMap<D, F8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ Bars bars;
@@ -179,7 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<int4*>(smem + i) = make_int4(0, 0, 0, 0);
     tc::fence_proxy_async_smem();
     if (threadIdx.x == 0) {
-        dev::mbar_init(&b->q_full, kProducerThreads);
+        dev::mbar_init(&b->q_full, F8 ? 8 : kProducerThreads);
+        dev::mbar_init(&b->q_raw, kProducerThreads);
         dev::mbar_init(&b->q_empty, 1);
         for (int s = 0; s < 2; ++s) {
             dev::mbar_init(&b->k_full[s], kProducerThreads);
@@ -289,6 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 p.page_table + (int64_t)(uv.casc ? cgroups[-1 - pt.req].leader : pt.req) * p.ld;
             // ---- Q: row r = token (or cascade member) r / G, head r % G of each tile
             if (uc > 0 && !wait_or_abort(&b->q_empty, (uc - 1) & 1, b, err)) break;
+            uint64_t* q_land = F8 ? &b->q_raw : &b->q_full;
             if (q_tma && !uv.casc) {
                 // consecutive tokens: the G heads of a kv head are adjacent rows of q, so a tile
                 // half is one tensor box (tokens past the batch read as zeros; rows of tokens
@@ -297,12 +308,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (pwarp == 0 && lane == 0) {
                     tc::fence_proxy_async_smem();  // earlier gathers into these tiles -> async-proxy writes
                     const uint32_t box = 128u * (uint32_t)(G * TM);
-                    dev::mbar_expect_tx(&b->q_full, box * (D / 64) * ((pt.ntok0 > 0) + (pt.ntok1 > 0)));
+                    dev::mbar_expect_tx(q_land, box * (D / 64) * ((pt.ntok0 > 0) + (pt.ntok1 > 0)));
                     for (int h = 0; h < 2; ++h) {
                         if ((h ? pt.ntok1 : pt.ntok0) <= 0) continue;
                         for (int x = 0; x < D / 64; ++x)
                             tc::tma_load_3d(smem + L::kQ + h * L::kTile + x * kRegion, &q_map, x * 64, pt.kvh * G,
-                                            pt.tok0 + h * TM, &b->q_full);
+                                            pt.tok0 + h * TM, q_land);
                     }
                 }
             } else
@@ -322,12 +333,98 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 copy_tile(smem + L::kQ + h * L::kTile, oq[0], oq[1], p.q);
             }
-            issue(&b->q_full);
+            issue(q_land);
             // ---- K and V tiles
             const int kv_end = uv.key_end;
             const int nkt = (kv_end - uv.key_base + kPreKeys - 1) / kPreKeys;
             bool ok = true;
-            if (paged) {
+            if constexpr (F8) {
+                // E4M3 rows: each lane async-copies 16 bytes (16 elements) of its rows of a tile's
+                // K and V into a staging area, and once its own copies have landed converts
+                // exactly those bytes to f16 (exact) into the swizzled operand tiles -- no
+                // registers hold rows in flight, and the copies of a tile go out together (one
+                // round trip per tile).  LPR lanes cover a row, so one copy instruction takes RPI
+                // whole rows.  The next tile's page ids are read while this one is converted.
+                constexpr int LPR = D / 16, RPI = 32 / LPR, RPS = 3 * RPI;
+                constexpr int NS = (kPreRows + RPS - 1) / RPS;
+                static_assert(NS <= 32, "one validity bit per row");
+                const int sub = lane / LPR, e0 = (lane % LPR) * 16;
+                const int c0 = (e0 % 64) / 8;  // first chunk of the lane's pair in its region
+                const uint32_t region = (uint32_t)(e0 / 64) * kRegion;
+                const int64_t ld_row = (int64_t)p.num_kv_heads * D;  // pool bytes per slot
+                const uint32_t stage8 = dev::smem_u32(smem + L::kStage8);
+                auto row_of8 = [&](int m) { return pwarp * RPI + sub + RPS * m; };
+                auto tile_pages = [&](int j, int32_t (&pg)[NS]) {
+#pragma unroll
+                    for (int m = 0; m < NS; ++m) {
+                        const int key = uv.key_base + j * kPreKeys + row_of8(m);
+                        pg[m] = (j < nkt && row_of8(m) < kPreRows && key < kv_end) ? prow[key >> p.page_shift] : 0;
+                    }
+                };
+                // the copies of tile j (page ids pg); returns the rows this lane copied
+                auto load_tile = [&](int j, int32_t (&pg)[NS]) -> uint32_t {
+                    uint32_t valid = 0;
+                    bool bad = false;
+#pragma unroll
+                    for (int m = 0; m < NS; ++m) {
+                        const int r = row_of8(m);
+                        const int key = uv.key_base + j * kPreKeys + r;
+                        if (r >= kPreRows || key >= kv_end) continue;
+                        valid |= 1u << m;
+                        int64_t page = pg[m];
+                        if (page < 0 || page >= p.num_pages) {
+                            bad = true;
+                            page = 0;
+                        }
+                        const int64_t off = ((page << p.page_shift) + (key & ps_mask)) * ld_row + (int64_t)pt.kvh * D + e0;
+                        const uint32_t dk = stage8 + r * D + e0, dv = dk + kPreRows * D;
+                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dk),
+                                     "l"(reinterpret_cast<const uint8_t*>(p.k_pool) + off));
+                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dv),
+                                     "l"(reinterpret_cast<const uint8_t*>(p.v_pool) + off));
+                    }
+                    asm volatile("cp.async.commit_group;" ::: "memory");
+                    if (bad) dev::set_error(err, kErrPage);
+                    return valid;
+                };
+                // staged rows (K at 0, V at kPreRows * D) -> f16 tile, then the tile's barrier
+                auto convert = [&](uint32_t valid, uint32_t src0, uint8_t* tile, uint64_t* full) {
+                    const uint32_t t0 = dev::smem_u32(tile) + region;
+#pragma unroll
+                    for (int m = 0; m < NS; ++m) {
+                        if (!(valid >> m & 1)) continue;
+                        const int r = row_of8(m);
+                        uint32_t x, y, z, q;
+                        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(x), "=r"(y), "=r"(z), "=r"(q)
+                                     : "r"(src0 + r * D + e0));
+                        const uint32_t row = t0 + r * 128;
+                        dev::st_shared_v4(row + ((c0 ^ (r & 7)) << 4), dev::e4m3x2_to_f16x2(x),
+                                          dev::e4m3x2_to_f16x2(x >> 16), dev::e4m3x2_to_f16x2(y),
+                                          dev::e4m3x2_to_f16x2(y >> 16));
+                        dev::st_shared_v4(row + (((c0 + 1) ^ (r & 7)) << 4), dev::e4m3x2_to_f16x2(z),
+                                          dev::e4m3x2_to_f16x2(z >> 16), dev::e4m3x2_to_f16x2(q),
+                                          dev::e4m3x2_to_f16x2(q >> 16));
+                    }
+                    // these generic-proxy stores -> the tensor core's operand reads
+                    tc::fence_proxy_async_smem();
+                    dev::mbar_arrive(full);
+                };
+                int32_t pg[NS];
+                tile_pages(0, pg);
+                uint32_t valid = nkt > 0 ? load_tile(0, pg) : 0u;
+                for (int j = 0; j < nkt && ok; ++j, ++it) {
+                    const int st = it & 1;
+                    const uint32_t ph = (it >> 1) & 1;
+                    tile_pages(j + 1, pg);
+                    asm volatile("cp.async.wait_group 0;" ::: "memory");  // this lane's copies of tile j
+                    if (!(ok = wait_or_abort(&b->k_empty[st], ph ^ 1, b, err))) break;
+                    convert(valid, stage8, smem + L::kK + st * L::kTile, &b->k_full[st]);
+                    if (!(ok = wait_or_abort(&b->v_empty[st], ph ^ 1, b, err))) break;
+                    convert(valid, stage8 + kPreRows * D, smem + L::kV + st * L::kTile, &b->v_full[st]);
+                    if (j + 1 < nkt) valid = load_tile(j + 1, pg);
+                }
+            } else if (paged) {
                 // 8 lanes per 128-byte half row, 4 rows per copy instruction; each lane keeps
                 // the source offsets of its kG8 rows (pwarp * 4 + lane / 8 + 12 m) in registers
                 constexpr int kG8 = (kPreRows + 11) / 12;
@@ -440,8 +537,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ============================================================== MMA issuer (one warp)
         // The whole warp runs this role with warp-uniform control flow (every wait is voted
         // across the warp); each MMA and commit is issued by one elected lane.
-        const uint32_t id_qk = tc::idesc_bf16_f32(128, 128, 0, 0);
-        const uint32_t id_pv = tc::idesc_bf16_f32(128, D, 0, 1);
+        const uint32_t id_qk = F8 ? tc::idesc_f16_f32(128, 128, 0, 0) : tc::idesc_bf16_f32(128, 128, 0, 0);
+        const uint32_t id_pv = F8 ? tc::idesc_f16_f32(128, D, 0, 1) : tc::idesc_bf16_f32(128, D, 0, 1);
         constexpr uint32_t kDescHi = tc::smem_desc_hi(1024, tc::kSwizzle128B);
         constexpr uint32_t kTileLo = L::kTile >> 4;  // one tile, in descriptor address units
         // descriptor low words: Q tiles and K stages K-major, V stages MN-major (the leading
@@ -562,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         const uint32_t t_s = tmem + 256 * h + lane_base;
         const uint32_t t_o = t_s + 128;
-        const float sl = p.scale_log2;
+        const float sl_base = p.scale_log2;
         uint32_t n_s = 0;   // S tiles seen by this warpgroup
         uint32_t n_u = 0;   // units with this Q tile
         for (int k = 0;; ++k) {
@@ -572,7 +669,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             const UnitView uv = unit_view(pt);
             const int ntok = h ? pt.ntok1 : pt.ntok0;
             const int nk = uv.nk[h];
+            if constexpr (F8) {
+                // this thread's row of Q tile h, bf16 -> f16 in place (both regions; every
+                // warp takes part in every unit: q_full counts the eight softmax warps)
+                if (!wait_or_abort(&b->q_raw, k & 1, b, err)) break;
+#pragma unroll
+                for (int x = 0; x < D / 64; ++x) {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        uint4* q16 = reinterpret_cast<uint4*>(smem + L::kQ + h * L::kTile + x * kRegion + row * 128 +
+                                                              c * 16);
+                        const uint4 v = *q16;
+                        *q16 = make_uint4(dev::bf16x2_to_f16x2(v.x), dev::bf16x2_to_f16x2(v.y),
+                                          dev::bf16x2_to_f16x2(v.z), dev::bf16x2_to_f16x2(v.w));
+                    }
+                }
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) dev::mbar_arrive(&b->q_full);
+            }
             if (nk == 0) continue;
+            const float sl = F8 ? sl_base * p.k_scale[pt.kvh] : sl_base;
             const bool valid = row < ntok * G;
             // last visible key of this row, and the first key some row may not see
             const int qpos = pt.qpos0 + h * TM;
@@ -644,7 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float e0 = dev::fast_exp2(x0);
                         const float e1 = dev::fast_exp2(x1);
                         dev::fadd2(lsa[2 * (i & 3)], lsa[2 * (i & 3) + 1], e0, e1);
-                        pk[i] = dev::pack_bf16x2(e0, e1);
+                        pk[i] = F8 ? dev::pack_f16x2(e0, e1) : dev::pack_bf16x2(e0, e1);
                     }
                     tc::tmem_st16u(t_s + c2 * 16, pk);
                 }
@@ -671,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- epilogue: O / l -> bf16 rows of out, LSE
             if (!wait_or_abort(&b->o_ready[h], n_u & 1, b, err)) break;
             tc::fence_after_sync();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float inv = l > 0.f ? (F8 ? p.v_scale[pt.kvh] : 1.f) / l : 0.f;
             const int64_t orow = (valid && !uv.casc)
                                      ? ((int64_t)(pt.tok0 + h * TM + row / G) * Hq + pt.kvh * G + row % G)
                                      : 0;
@@ -761,10 +878,12 @@ bool encode_q_map(const ForwardParams& p, int D, CUtensorMap* m) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, bool F8>
 cudaError_t launch_p(const ForwardParams& p, int ctas, cudaStream_t s) {
-    const size_t smem = SmemMap<D>::kBytes + 1024;
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const size_t smem = SmemMap<D, F8>::kBytes + 1024;
+    static_assert(SmemMap<D, F8>::kBytes + 1024 + 512 <= 227 * 1024, "shared memory per block");
+    cudaError_t e =
+        cudaFuncSetAttribute(prefill_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     // The register split inside the kernel assumes the launch allocates exactly
     // kRegsLaunch registers per thread; with fewer, the softmax warps' increase
@@ -772,7 +891,7 @@ cudaError_t launch_p(const ForwardParams& p, int ctas, cudaStream_t s) {
     static int launch_regs = -1;
     if (launch_regs < 0) {
         cudaFuncAttributes attr{};
-        e = cudaFuncGetAttributes(&attr, prefill_kernel<D>);
+        e = cudaFuncGetAttributes(&attr, prefill_kernel<D, F8>);
         if (e != cudaSuccess) return e;
         launch_regs = attr.numRegs;
     }
@@ -780,7 +899,8 @@ cudaError_t launch_p(const ForwardParams& p, int ctas, cudaStream_t s) {
     CUtensorMap q_map;
     memset(&q_map, 0, sizeof(q_map));
     const int q_tma = encode_q_map(p, D, &q_map) ? 1 : 0;
-    return launch_programmatic(prefill_kernel<D>, (unsigned)ctas, (unsigned)kThreads, smem, s, p, q_map, q_tma);
+    return launch_programmatic(prefill_kernel<D, F8>, (unsigned)ctas, (unsigned)kThreads, smem, s, p, q_map,
+                               q_tma);
 }
 
 }  // namespace
@@ -793,8 +913,8 @@ bool prefill_supported(int num_qo_heads, int num_kv_heads, int head_dim) {
 
 cudaError_t launch_prefill(const ForwardParams& p, int head_dim, int ctas, cudaStream_t s) {
     if (ctas <= 0) return cudaSuccess;
-    if (head_dim == 128) return launch_p<128>(p, ctas, s);
-    if (head_dim == 64) return launch_p<64>(p, ctas, s);
+    if (head_dim == 128) return p.kv_fp8 ? launch_p<128, true>(p, ctas, s) : launch_p<128, false>(p, ctas, s);
+    if (head_dim == 64) return p.kv_fp8 ? launch_p<64, true>(p, ctas, s) : launch_p<64, false>(p, ctas, s);
     return cudaErrorInvalidValue;
 }
 

@@ -69,6 +69,14 @@ __host__ __device__ constexpr uint32_t smem_desc_hi(uint32_t sbo_bytes, uint32_t
     return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | ((layout & 7u) << 29);
 }
 
+// Instruction descriptor, kind::f16 with f16 A/B and fp32 accumulate (A/B format fields 0).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn, int b_mn) {
+    return (1u << 4)                      // D format: f32
+           | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16)
+           | ((uint32_t)(N >> 3) << 17)   // N / 8
+           | ((uint32_t)(M >> 4) << 24);  // M / 16
+}
+
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 accumulate.
 // a_mn / b_mn: operand stored MN-major (1) instead of K-major (0).
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn) {
