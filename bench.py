@@ -51,21 +51,21 @@ def parse():
 # what they were at capture time; after any change the roofline reports null.
 NCU_TRAFFIC = {
     ("decode", "decode"): {
-        "bytes": 620.137728e6,
+        "bytes": 619.810048e6,
         "sources": ['paged_variable_length_gb300/csrc/decode.cu', 'paged_variable_length_gb300/csrc/device_utils.cuh', 'paged_variable_length_gb300/csrc/pva_internal.h'],
-        "sha256_16": "0f902f1ff81ecbae",
+        "sha256_16": "7a5cc1b333d7c6d5",
         "summary": "profiles/decode_kernel_decode_workload.md",
     },
     ("decode", "decode-e4m3"): {
-        "bytes": 312.932096e6,
+        "bytes": 312.963584e6,
         "sources": ['paged_variable_length_gb300/csrc/decode.cu', 'paged_variable_length_gb300/csrc/device_utils.cuh', 'paged_variable_length_gb300/csrc/pva_internal.h'],
-        "sha256_16": "d5d81c69c42037e9",
+        "sha256_16": "7a5cc1b333d7c6d5",
         "summary": "profiles/decode_kernel_fp8_decode_workload.md",
     },
     ("tensor_core", "prefill"): {
-        "bytes": 220.103424e6,
+        "bytes": 220.759808e6,
         "sources": ['paged_variable_length_gb300/csrc/prefill_tc.cu', 'paged_variable_length_gb300/csrc/device_utils.cuh', 'paged_variable_length_gb300/csrc/tc_utils.cuh', 'paged_variable_length_gb300/csrc/pva_internal.h'],
-        "sha256_16": "808e72d60924057d",
+        "sha256_16": "b064b09b12e35c18",
         "summary": "profiles/prefill_kernel_prefill_workload.md",
     },
 }

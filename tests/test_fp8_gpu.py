@@ -51,7 +51,7 @@ CASES = [
     (32, 8, 128, 16, [1, 1, 1, 1, 3], [1, 16, 17, 700, 33]),
     (28, 4, 128, 1, [1, 2, 1, 1], [5, 2, 1000, 257]),
     (8, 8, 64, 4, [1, 9, 0, 16, 1], [3, 20, 5, 16, 77]),
-    (32, 8, 128, 16, [40, 1, 130], [40, 2000, 300]),      # prefills and a chunk: decode-kernel groups
+    (32, 8, 128, 16, [40, 1, 130], [40, 2000, 300]),      # prefills and a chunk (tensor-core kernel)
     (16, 1, 128, 32, [1, 5, 1], [4096, 5, 31]),            # MQA
     (16, 16, 64, 2, [1, 1, 7], [9, 1, 7]),                 # MHA
     (32, 2, 128, 8, [1, 1], [3000, 5]),                    # group 16
@@ -118,3 +118,50 @@ def test_fp8_full_size_decode_workload_sampled_rows():
     ref_o, ref_l = oracle.attention_fp8(t["q"].cpu(), kp.cpu(), vp.cpu(), ks.cpu(), vs.cpu(), wl.cu_seqlens_q,
                                         wl.cache_seqlens, wl.page_table, wl.page_size, row_select=sel)
     assert_close(out, lse, ref_o, ref_l, mask=sel)
+
+
+def _fp8_sampled(wl, n_rows=1500, seed=0):
+    """Full-size FP8 workload: written slots byte-exact, sampled rows (and every request's
+    last token) against the oracle over the written pool."""
+    t = W.make_tensors(wl, DEV)
+    kp, vp, ks, vs = W.make_fp8_pools(wl, DEV)
+    slots = oracle.slot_mapping(wl.cu_seqlens_q, wl.cache_seqlens, wl.page_table, wl.page_size)
+    eng = make_engine(wl, kv_dtype=pva.KV_E4M3)
+    eng.prepare(t["cu_seqlens_q"], t["cache_seqlens"], t["page_table"], wl.total_tokens, None, max(wl.q_lens))
+    out = torch.empty_like(t["q"])
+    lse = torch.empty(wl.total_tokens, wl.num_qo_heads, dtype=torch.float32, device=DEV)
+    eng.forward(t["q"], t["k"], t["v"], kp, vp, out, lse, k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    assert pva.attn_get_device_status(eng.meta) == 0
+    sl = torch.as_tensor(slots, device=DEV)
+    ref_k = oracle.e4m3_encode(t["k"].float().cpu().numpy() / ks.cpu().numpy()[None, :, None])
+    ref_v = oracle.e4m3_encode(t["v"].float().cpu().numpy() / vs.cpu().numpy()[None, :, None])
+    assert np.array_equal(kp[sl].cpu().numpy(), ref_k) and np.array_equal(vp[sl].cpu().numpy(), ref_v)
+    rng = np.random.default_rng(seed)
+    T, Hq = wl.total_tokens, wl.num_qo_heads
+    sel = np.zeros((T, Hq), bool)
+    sel.reshape(-1)[rng.choice(T * Hq, size=min(n_rows, T * Hq), replace=False)] = True
+    sel[np.asarray(wl.cu_seqlens_q[1:]) - 1, :] = True
+    ref_o, ref_l = oracle.attention_fp8(t["q"].cpu(), kp.cpu(), vp.cpu(), ks.cpu(), vs.cpu(), wl.cu_seqlens_q,
+                                        wl.cache_seqlens, wl.page_table, wl.page_size, row_select=sel)
+    assert_close(out, lse, ref_o, ref_l, mask=sel)
+    return pva.attn_debug_plan_counts(eng.meta)
+
+
+@pytest.mark.parametrize("name", ["prefill", "mixed", "cascade", "specdec"])
+def test_fp8_full_size_workloads(name):
+    counts = _fp8_sampled(W.WORKLOADS[name](0))
+    if name == "cascade":
+        assert counts["casc_groups"] >= 1, "the shared prefix should run as a prefix pass"
+    if name in ("prefill", "mixed"):
+        assert counts["pre_tiles"] > 0, "prefills should run on the tensor-core kernel"
+
+
+def test_fp8_shared_prefix_groups():
+    """Two prefix groups, a member sharing only part of its group's prefix, an unrelated
+    decode, a too-short request and a prefill in one FP8 batch (prefix pass + merge)."""
+    from test_parity_gpu import _cascade_batch
+
+    wl = _cascade_batch(seed=4)
+    _fp8_case(wl)
+    _fp8_case(wl, enable_cascade=False)
