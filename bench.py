@@ -33,7 +33,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="decode",
-                    choices=["worked", "decode", "prefill", "mixed", "cascade", "specdec"])
+                    choices=["worked", "decode", "prefill", "mixed", "cascade", "specdec", "ragged"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -146,6 +146,8 @@ def algorithmic_work(wl, kv_elem_bytes: int = 2):
     o_bytes = T * Hq * D * 2
     new_kv_bytes = 2 * T * Hkv * D * 2
     store_bytes = new_kv_bytes + 2 * T * row_kv  # read k,v (bf16) + write the pool rows
+    if wl.name == "ragged":
+        store_bytes = 0  # contiguous K/V: nothing is stored
     pairs = 0
     for n, L in zip(wl.q_lens, wl.kv_lens):
         # query r sees L - n + r + 1 keys
@@ -337,6 +339,11 @@ def run_ours(args):
     if fp8:
         t["k_pool"], t["v_pool"], ks, vs = W.make_fp8_pools(wl, dev)
         scales = {"k_scale": ks, "v_scale": vs}
+    slots = None
+    if wl.name == "ragged":
+        # contiguous K/V: the batch's own k / v rows are the keys, nothing is stored
+        t["k_pool"], t["v_pool"] = t["k"], t["v"]
+        slots = torch.full((wl.total_tokens,), -1, dtype=torch.int64, device=dev)
     max_q = max(wl.q_lens)
     eng = pva.PagedAttention(wl.num_qo_heads, wl.num_kv_heads, wl.head_dim, wl.page_size, wl.num_pages,
                              max_batch=wl.batch, max_tokens=wl.total_tokens, max_kv_len=max(wl.kv_lens),
@@ -347,7 +354,7 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
 
     def step():
-        eng.prepare(t["cu_seqlens_q"], t["cache_seqlens"], t["page_table"], wl.total_tokens, None, max_q)
+        eng.prepare(t["cu_seqlens_q"], t["cache_seqlens"], t["page_table"], wl.total_tokens, slots, max_q)
         eng.forward(t["q"], t["k"], t["v"], t["k_pool"], t["v_pool"], out, lse, **scales)
 
     for _ in range(args.warmup):
@@ -407,7 +414,7 @@ def run_ours(args):
     pgraph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(pgraph):
         pev[0].record()
-        eng.prepare(t["cu_seqlens_q"], t["cache_seqlens"], t["page_table"], wl.total_tokens, None, max_q)
+        eng.prepare(t["cu_seqlens_q"], t["cache_seqlens"], t["page_table"], wl.total_tokens, slots, max_q)
         pev[1].record()
         pva.attn_set_timing_events(eng.meta, kev)
         eng.forward(t["q"], t["k"], t["v"], t["k_pool"], t["v_pool"], out, lse, **scales)
@@ -446,9 +453,10 @@ def run_ours(args):
     def e2e_step():
         for k2, v2 in host_in.items():
             dev_in[k2].copy_(v2, non_blocking=True)
-        eng.prepare(dev_in["cu_seqlens_q"], dev_in["cache_seqlens"], dev_in["page_table"], wl.total_tokens, None,
+        eng.prepare(dev_in["cu_seqlens_q"], dev_in["cache_seqlens"], dev_in["page_table"], wl.total_tokens, slots,
                     max_q)
-        eng.forward(dev_in["q"], dev_in["k"], dev_in["v"], t["k_pool"], t["v_pool"], out, None, **scales)
+        kp_e, vp_e = (dev_in["k"], dev_in["v"]) if wl.name == "ragged" else (t["k_pool"], t["v_pool"])
+        eng.forward(dev_in["q"], dev_in["k"], dev_in["v"], kp_e, vp_e, out, None, **scales)
         host_out.copy_(out, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):

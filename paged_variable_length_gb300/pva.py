@@ -210,6 +210,31 @@ def deverr_names(bits: int) -> list[str]:
     return [name for b, name in DEVERR.items() if bits & b]
 
 
+def ragged_layout(cu_seqlens_q, cu_seqlens_kv, device=None):
+    """Page table and slot mapping that make contiguous (ragged) K/V an ordinary batch.
+
+    With K/V given as [total_kv, Hkv, D] tensors whose rows cu_seqlens_kv[i] ..
+    cu_seqlens_kv[i+1]-1 are request i's keys (its cached part, if any, followed by its
+    new tokens), a config with page_size 1 and num_pages >= total_kv, and
+    page_table[i][j] = cu_seqlens_kv[i] + j address them in place: pass k / v themselves
+    as the pools, kv lengths cu_seqlens_kv[i+1] - cu_seqlens_kv[i] as cache_seqlens, and
+    this slot mapping (-1 for every new token: nothing is stored, the keys already sit
+    where the table points).  Returns (page_table int32 [B, max_kv], slot_mapping int64
+    [total_q]) on ``device``.  Host-side arithmetic, once per batch.
+    """
+    import torch
+
+    cu = torch.as_tensor(cu_seqlens_kv, dtype=torch.int64).cpu()
+    lens = cu[1:] - cu[:-1]
+    B = int(lens.numel())
+    width = max(int(lens.max()) if B else 1, 1)
+    j = torch.arange(width, dtype=torch.int64)
+    table = torch.where(j[None, :] < lens[:, None], cu[:-1, None] + j[None, :], torch.zeros(1, dtype=torch.int64))
+    total_q = int(torch.as_tensor(cu_seqlens_q)[-1])
+    dev = device if device is not None else "cpu"
+    return table.to(torch.int32).to(dev), torch.full((total_q,), -1, dtype=torch.int64, device=dev)
+
+
 class PagedAttention:
     """Owns a config and a torch-allocated workspace; one prepare per batch, one forward per layer."""
 

@@ -158,6 +158,21 @@ def cascade(seed: int = 0, batch: int = 128, prefix: int = 4096, lo: int = 16, h
                                 f"U[{lo},{hi}], Hq32/Hkv8/D128, ps16, 20000-page pool")
 
 
+def ragged_prefill(seed: int = 0, batch: int = 8, lo: int = 256, hi: int = 4096) -> Workload:
+    """The prefill workload's requests (8 fresh prefills, len U[256,4096], Hq 32, Hkv 8,
+    D 128) over contiguous K/V: page_size 1, the "pool" is the batch's own k / v rows and
+    page_table[i][j] = cu_seqlens[i] + j (request i's keys are its new tokens)."""
+    rng = np.random.default_rng(seed)
+    lens = [int(x) for x in rng.integers(lo, hi + 1, size=batch)]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    table = np.zeros((batch, max(lens)), np.int32)
+    for i, L in enumerate(lens):
+        table[i, :L] = np.arange(cu[i], cu[i] + L)
+    return Workload("ragged", list(lens), list(lens), 32, 8, 128, 1, int(cu[-1]), table, 0.5, seed,
+                    description=f"ragged prefill: {batch} fresh prefills, len U[{lo},{hi}], Hq32/Hkv8/D128, "
+                                "contiguous K/V (no pool, no store)")
+
+
 def spec_decode(seed: int = 0, batch: int = 64, draft: int = 3, lo: int = 512, hi: int = 4096) -> Workload:
     """A uniform speculative-decoding verify step: every request appends 1 + draft tokens
     (the last accepted token and the drafted ones), causally masked among themselves;
@@ -191,6 +206,7 @@ WORKLOADS = {
     "mixed": mixed,
     "cascade": cascade,
     "specdec": spec_decode,
+    "ragged": ragged_prefill,
 }
 
 

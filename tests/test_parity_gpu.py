@@ -341,3 +341,61 @@ def test_spec_decode_uniform_batches(draft, Hq, Hkv):
 
 def test_spec_decode_full_size_workload():
     _sampled_check(W.WORKLOADS["specdec"](0))
+
+
+# ------------------------------------------------------------------ ragged (contiguous) K/V
+
+
+@pytest.mark.parametrize("case", [
+    # (Hq, Hkv, D, q_lens, kv_lens): keys of request i are rows cu_kv[i] .. of k / v
+    (32, 8, 128, [300, 1, 77, 1000], [300, 40, 77, 1500]),   # fresh prefills, a decode, a chunk on cache
+    (8, 2, 64, [5, 1, 16], [9, 1, 16]),
+    (28, 4, 128, [2000, 512], [2000, 512]),
+])
+def test_ragged_kv_through_the_identity_table(case):
+    """FlashInfer's ragged layout: K/V contiguous per request, no pool.  The identity page
+    table (page_size 1) and slot -1 for every token address them in place."""
+    Hq, Hkv, D, ql, kl = case
+    rng = np.random.default_rng(len(ql) + D)
+    cu_q = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
+    cu_kv = np.concatenate([[0], np.cumsum(kl)]).astype(np.int64)
+    T, TK = int(cu_q[-1]), int(cu_kv[-1])
+    g = torch.Generator(device="cpu").manual_seed(11)
+    q = torch.randn(T, Hq, D, generator=g).to(torch.bfloat16)
+    k = torch.randn(TK, Hkv, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(TK, Hkv, D, generator=g).to(torch.bfloat16)
+    table, slots = pva.ragged_layout(cu_q, cu_kv, DEV)
+    eng = pva.PagedAttention(Hq, Hkv, D, 1, TK, len(ql), T, max(kl))
+    dq, dk, dv = q.to(DEV), k.to(DEV), v.to(DEV)
+    lens = torch.as_tensor(kl, dtype=torch.int32, device=DEV)
+    eng.prepare(torch.as_tensor(cu_q, device=DEV), lens, table, T, slots, max(ql))
+    out = torch.empty_like(dq)
+    lse = torch.empty(T, Hq, dtype=torch.float32, device=DEV)
+    eng.forward(dq, dk, dv, dk, dv, out, lse)
+    torch.cuda.synchronize()
+    assert pva.attn_get_device_status(eng.meta) == 0
+    assert torch.equal(dk.cpu(), k) and torch.equal(dv.cpu(), v), "nothing may be stored"
+    ref_o, ref_l = oracle.attention(q, k, v, cu_q, np.asarray(kl, np.int32), table.cpu().numpy(), 1)
+    assert_close(out, lse, ref_o, ref_l)
+
+
+def test_ragged_full_size_workload():
+    wl = W.WORKLOADS["ragged"](0)
+    t = W.make_tensors(wl, DEV)
+    t["k_pool"], t["v_pool"] = t["k"], t["v"]
+    eng = make_engine(wl)
+    slots = torch.full((wl.total_tokens,), -1, dtype=torch.int64, device=DEV)
+    eng.prepare(t["cu_seqlens_q"], t["cache_seqlens"], t["page_table"], wl.total_tokens, slots, max(wl.q_lens))
+    out = torch.empty_like(t["q"])
+    lse = torch.empty(wl.total_tokens, wl.num_qo_heads, dtype=torch.float32, device=DEV)
+    eng.forward(t["q"], t["k"], t["v"], t["k_pool"], t["v_pool"], out, lse)
+    torch.cuda.synchronize()
+    assert pva.attn_get_device_status(eng.meta) == 0
+    rng = np.random.default_rng(0)
+    T, Hq = wl.total_tokens, wl.num_qo_heads
+    sel = np.zeros((T, Hq), bool)
+    sel.reshape(-1)[rng.choice(T * Hq, size=2000, replace=False)] = True
+    sel[np.asarray(wl.cu_seqlens_q[1:]) - 1, :] = True
+    ref_o, ref_l = oracle.attention(t["q"].cpu(), t["k"].cpu(), t["v"].cpu(), wl.cu_seqlens_q, wl.cache_seqlens,
+                                    wl.page_table, 1, row_select=sel)
+    assert_close(out, lse, ref_o, ref_l, mask=sel)
