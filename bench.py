@@ -33,7 +33,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="decode",
-                    choices=["worked", "decode", "prefill", "mixed", "cascade", "specdec", "ragged"])
+                    choices=["worked", "decode", "prefill", "mixed", "cascade", "cascade_tree", "specdec", "ragged"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -25,7 +25,7 @@ bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 // memory; shared-prefix detection needs them there, with its hash table beside them,
 // which bounds it to smaller batches.
 constexpr int kPrepareSmemBatch = 4096;
-constexpr int kCascadeMaxBatch = 2048;
+constexpr int kCascadeMaxBatch = 1536;
 
 // Host-side validation of the static configuration.
 pva_status check_config(const pva_config* c) {
@@ -54,14 +54,17 @@ Layout make_layout(const pva_config* c, int sm_count, int target_units = 0) {
     L.max_dec_units = L.max_dec_groups + L.target_units + 1;
     L.max_partial = 2 * L.target_units + 2;
     L.max_pre_tiles = (int32_t)((c->max_tokens / TM + c->max_batch + 1) * (int64_t)c->num_kv_heads);
-    L.max_casc_groups = c->enable_cascade ? c->max_batch / 2 + 1 : 1;
+    // two levels of groups (top level and sub-groups), each at most one per two requests
+    L.max_casc_groups = c->enable_cascade ? c->max_batch + 1 : 1;
     L.casc_target = sm_count;
     if (c->enable_cascade) {
-        // every member of a group takes one partial slot per prefix chunk; the prefix pass
-        // has at most (member tiles / 2 + groups) x kv heads x chunks units
+        // every member of a group takes one partial slot per prefix chunk of each of its
+        // (up to two) groups, at most kMaxCascChunks in all (with sub-groups in a batch each
+        // level takes at most half); the prefix pass has at most (member tiles / 2 +
+        // groups) x kv heads x chunks units per level
         L.max_partial += c->max_batch * kMaxCascChunks;
-        L.max_pre_tiles += (int32_t)((c->max_batch / (2 * TM) + L.max_casc_groups + 1) * (int64_t)c->num_kv_heads *
-                                     kMaxCascChunks);
+        L.max_pre_tiles += (int32_t)((2 * (c->max_batch / (2 * TM)) + L.max_casc_groups + 2) *
+                                     (int64_t)c->num_kv_heads * kMaxCascChunks);
     }
     L.rows_per_slot = kDecRows * c->num_kv_heads;
     size_t off = 0;
@@ -79,7 +82,7 @@ Layout make_layout(const pva_config* c, int sm_count, int target_units = 0) {
     L.partial_lse = take(sizeof(float) * (size_t)L.max_partial * L.rows_per_slot);
     L.req_scratch = take(sizeof(int32_t) * 4 * (size_t)(c->max_batch + 1));
     L.casc_groups = take(sizeof(CascGroup) * (size_t)L.max_casc_groups);
-    L.casc_members = take(sizeof(int32_t) * 2 * (size_t)c->max_batch);
+    L.casc_members = take(sizeof(int32_t) * 2 * 2 * (size_t)c->max_batch);  // (token, slot) per member per level
     L.total = off;
     return L;
 }

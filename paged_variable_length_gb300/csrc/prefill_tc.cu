@@ -135,7 +135,7 @@ __device__ __forceinline__ int queue_read(Bars* b, int k, int lane, uint32_t* er
 // both member tiles, no causal mask).
 struct UnitView {
     bool casc;
-    int key_base;   // first key of the unit (a multiple of kPreKeys)
+    int key_base;   // first key of the unit (on a page boundary)
     int key_end;    // keys [key_base, key_end) are loaded
     int end[2];     // keys visible to tile h end here
     int nk[2];      // 128-key tiles tile h walks (0: tile absent)

@@ -10,7 +10,9 @@
 //
 //   0. shared-prefix (cascade) groups: single-token decodes whose page tables start
 //      with the same run of pages ("Source walkthrough: Attention backends",
-//      section 3.3: the shared part is computed once and merged by log-sum-exp);
+//      section 3.3: the shared part is computed once and merged by log-sum-exp), and
+//      inside each group sub-groups whose rows continue with a further shared run (two
+//      levels of the prefix tree the page describes its multi-level form over);
 //   1. validate cu_seqlens_q / cache_seqlens (error word, never a trap) and
 //      classify each request: q_len * G <= 16 rows -> decode groups (the
 //      warp-MMA streaming kernel), otherwise -> 128-row tensor-core tiles;
@@ -35,7 +37,9 @@ constexpr int kCmpPages = 8;   // page ids a lane compares per step of the share
 
 // Per-request shared-memory arrays (dynamic shared memory, batch <= smem_batch), followed
 // by the open-addressing table of the shared-prefix search when cascade detection runs.
-enum SmemArray { kCu = 0, kLen, kToff, kFirst, kLeader, kLcp, kCnt, kCgid, kGoff, kMpos, kCUoff, kNumArrays };
+enum SmemArray {
+    kCu = 0, kLen, kToff, kFirst, kLeader, kLcp, kCnt, kCgid, kGoff, kMpos, kCUoff, kLeader2, kCgid2, kNumArrays
+};
 
 // Write a plan record as whole 16-byte words (a record is 32, 48 or 64 bytes, and the
 // record arrays start on 256-byte boundaries): one 16-byte store per word instead of
@@ -200,6 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     // group's prefix is the run of pages every member shares with the leader (whole pages
     // that lie strictly before each member's query, so no causal mask ever applies to it).
     int n_cgroups = 0;
+    int n_sub = 0;  // sub-groups among them
     // shared-memory copy of the cascade group records (after the hash table)
     CascGroup* scg = reinterpret_cast<CascGroup*>(dyn + kNumArrays * stride +
                                                   2 * (casc ? (1 << casc_hash_bits(p.smem_batch)) : 0));
@@ -328,6 +333,9 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
                 cg.chunk_keys = 0;
                 cg.unit_off = 0;
                 cg.n_units = 0;
+                cg.key_base = 0;
+                cg.level = 0;
+                cg.pad0 = cg.pad1 = 0;
                 store_record(&cgroups[gid], cg);
                 scg[gid] = cg;
                 sa[kMpos][i] = moff;  // next free member slot of the group
@@ -343,14 +351,183 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
             if (ld >= 0 && ld != i)
                 sa[kCgid][i] = is_group_leader(leader, cnt, lcp, ld, p.min_cascade_pages) ? sa[kCgid][ld] : -1;
         }
+        const int members1 = gt[1];  // member-list entries of the top-level groups
         __syncthreads();
+        // ---- level 2: inside a group, members keyed by the page right after the group's
+        // prefix; the lowest-numbered one leads its sub-group, whose prefix extends the
+        // group's by the run of pages every sub-member shares with it (again at least
+        // min_cascade_pages, again whole pages before each member's query).  Its prefix
+        // pass covers keys [group prefix, sub-group prefix) only.  The arrays of level 1
+        // that are no longer needed hold level 2's: the page after the prefix (kFirst),
+        // pages before the query then the sub-prefix (kLcp), counts then next free member
+        // slots (kCnt); the hash table is reused.
+        if (n_cgroups > 0) {
+            int32_t* page2 = first;
+            int32_t* pg2 = lcp;
+            int32_t* cnt2 = cnt;
+            int32_t* lead2 = sa[kLeader2];
+            int32_t* cgid2 = sa[kCgid2];  // pages compared per member until the sub-groups are numbered
+            for (int h = tid; h < HT; h += kThreads) {
+                hkey[h] = -1;
+                hval[h] = 0x7fffffff;
+            }
+            for (int i = tid; i < B; i += kThreads) {
+                const int g = sa[kCgid][i];
+                int pg = -1, pages = 0;
+                if (g >= 0) {
+                    const int n = cu[i + 1] - cu[i], L = lens[i];
+                    pages = (L - n) / ps;
+                    const int P1 = scg[g].prefix_len / ps;
+                    if (pages - P1 >= p.min_cascade_pages) {
+                        const int32_t x = p.page_table[(int64_t)i * p.ld + P1];
+                        pg = (x >= 0 && x < p.num_pages) ? x : -1;
+                    }
+                }
+                page2[i] = pg;
+                pg2[i] = pages;
+                cnt2[i] = 0;
+                lead2[i] = -1;
+                cgid2[i] = 0;
+            }
+            __syncthreads();
+            // hash key: the page mixed with the group id (two different pairs meeting on one
+            // key would only lose sharing: a member whose pair differs from its sub-leader's
+            // is dropped below)
+            auto key2 = [&](int i) -> int {
+                return page2[i] < 0 ? -1
+                                    : (int)(((uint32_t)page2[i] * 2654435761u ^ (uint32_t)sa[kCgid][i] * 0x9E3779B9u) &
+                                            0x7fffffffu);
+            };
+            for (int i0 = 0; i0 < B; i0 += kThreads) {
+                const int i = i0 + tid;
+                const int f = i < B ? key2(i) : -1;
+                const unsigned peers = __match_any_sync(0xffffffffu, f);
+                const int lead = __ffs(peers) - 1;
+                int h = 0;
+                if (f >= 0 && lane == lead) {
+                    uint32_t hh = page_hash(f, hbits);
+                    while (true) {
+                        const int prev = atomicCAS(&hkey[hh], -1, f);
+                        if (prev == -1 || prev == f) break;
+                        hh = (hh + 1) & (HT - 1);
+                    }
+                    atomicMin(&hval[hh], i);
+                    h = (int)hh;
+                }
+                h = __shfl_sync(0xffffffffu, h, lead);
+                if (f >= 0) lead2[i] = h;
+            }
+            __syncthreads();
+            for (int i0 = 0; i0 < B; i0 += kThreads) {
+                const int i = i0 + tid;
+                int ld = (i < B && page2[i] >= 0) ? hval[lead2[i]] : -1;
+                if (ld >= 0 && (sa[kCgid][ld] != sa[kCgid][i] || page2[ld] != page2[i])) ld = -1;
+                const unsigned peers = __match_any_sync(0xffffffffu, ld);
+                if (i < B) lead2[i] = ld;
+                if (ld >= 0 && lane == __ffs(peers) - 1) atomicAdd(&cnt2[ld], __popc(peers));
+            }
+            __syncthreads();
+            for (int i = tid; i < B; i += kThreads) {
+                const int ld = lead2[i];
+                cgid2[i] = (ld >= 0 && ld != i) ? min(pg2[i], pg2[ld]) : 0;
+            }
+            __syncthreads();
+            for (int i = tid; i < B; i += kThreads)
+                if (cgid2[i] > 0) atomicMin(&pg2[lead2[i]], cgid2[i]);
+            {
+                constexpr int kU = kCmpPages;
+                const int warp = tid >> 5;
+                for (int i = warp; i < B; i += kWarps) {
+                    const int l = cgid2[i];
+                    const int g = sa[kCgid][i];
+                    if (l <= 0 || g < 0) continue;  // warp-uniform
+                    const int start = scg[g].prefix_len / ps + 1;  // page start - 1 matched by the key
+                    if (l <= start) continue;
+                    const int ld = lead2[i];
+                    const int32_t* ri = p.page_table + (int64_t)i * p.ld;
+                    const int32_t* rl = p.page_table + (int64_t)ld * p.ld;
+                    int mis = l;
+                    for (int k0 = start; k0 < l; k0 += 32 * kU) {
+                        int va[kU], vb[kU];
+#pragma unroll
+                        for (int u = 0; u < kU; ++u) {
+                            const int k = k0 + u * 32 + lane;
+                            va[u] = k < l ? ri[k] : 0;
+                            vb[u] = k < l ? rl[k] : 0;
+                        }
+#pragma unroll
+                        for (int u = 0; u < kU; ++u) {
+                            const int k = k0 + u * 32 + lane;
+                            if (k < l && va[u] != vb[u]) mis = min(mis, k);
+                        }
+                    }
+                    mis = __reduce_min_sync(0xffffffffu, mis);
+                    if (lane == 0 && mis < l) atomicMin(&pg2[ld], mis);
+                }
+            }
+            __syncthreads();
+            for (int i = tid; i < B; i += kThreads) cgid2[i] = -1;
+            __syncthreads();
+            auto is_sub_leader = [&](int i) {
+                if (lead2[i] != i || cnt2[i] < 2) return false;
+                return pg2[i] - scg[sa[kCgid][i]].prefix_len / ps >= p.min_cascade_pages;
+            };
+            int hv[2] = {0, 0};
+            for (int i = r0; i < r1; ++i)
+                if (is_sub_leader(i)) {
+                    hv[0] += 1;
+                    hv[1] += cnt2[i];
+                }
+            int ht[2];
+            block_scan<2>(hv, ht, s_tmp2);
+            {
+                int gid = n_cgroups + hv[0], moff = members1 + hv[1];
+                for (int i = r0; i < r1; ++i) {
+                    if (!is_sub_leader(i)) continue;
+                    CascGroup cg;
+                    cg.leader = i;
+                    cg.key_base = scg[sa[kCgid][i]].prefix_len;
+                    cg.prefix_len = pg2[i] * ps;
+                    cg.n_members = cnt2[i];
+                    cg.member_off = moff;
+                    cg.n_chunks = 0;
+                    cg.chunk_keys = 0;
+                    cg.unit_off = 0;
+                    cg.n_units = 0;
+                    cg.level = 1;
+                    cg.pad0 = cg.pad1 = 0;
+                    store_record(&cgroups[gid], cg);
+                    scg[gid] = cg;
+                    cgid2[i] = gid;
+                    cnt2[i] = moff;  // next free member slot of the sub-group
+                    moff += cg.n_members;
+                    ++gid;
+                }
+            }
+            n_cgroups += ht[0];
+            n_sub = ht[0];
+            __syncthreads();
+            for (int i = tid; i < B; i += kThreads) {
+                const int ld = lead2[i];
+                if (ld >= 0 && ld != i) cgid2[i] = cgid2[ld];
+            }
+            __syncthreads();
+        }
         }  // some candidates share a first page
     }
-    auto casc_of = [&](int i) { return casc ? sa[kCgid][i] : -1; };
-    // prefix length (keys) of request i when it is a cascade member, else 0
+    auto casc_of = [&](int i) { return casc && n_cgroups > 0 ? sa[kCgid][i] : -1; };
+    auto casc2_of = [&](int i) { return casc && n_cgroups > 0 ? sa[kCgid2][i] : -1; };
+    // keys before request i's decode tail: its deepest shared prefix (0 for no group)
     auto prefix_of = [&](int i) {
+        const int g2 = casc2_of(i);
+        if (g2 >= 0) return scg[g2].prefix_len;
         const int g = casc_of(i);
         return g >= 0 ? scg[g].prefix_len : 0;
+    };
+    // prefix partial slots of request i (its groups' chunks)
+    auto prefix_parts = [&](int i) {
+        const int g = casc_of(i), g2 = casc2_of(i);
+        return (g >= 0 ? scg[g].n_chunks : 0) + (g2 >= 0 ? scg[g2].n_chunks : 0);
     };
 
     // ---- pass 1: validate, count decode groups and prefill tiles, sum decode key extents
@@ -401,9 +578,12 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     }
 
     // ---- cascade groups: key chunks of each prefix (about casc_target prefix-pass units
-    // in total, roughly one per SM), unit ranges, member lists
+    // in total, roughly one per SM), unit ranges, member lists.  A member takes one
+    // partial slot per chunk of each of its groups; with sub-groups in the batch each
+    // level gets at most half the chunks, so no member needs more than kMaxCascChunks.
     if (casc && n_cgroups > 0) {
         const int ng = n_cgroups;
+        const int nc_cap = n_sub > 0 ? kMaxCascChunks / 2 : kMaxCascChunks;
         const int gch = (ng + kThreads - 1) / kThreads;
         const int g0 = min(ng, tid * gch), g1 = min(ng, g0 + gch);
         int pv[1] = {0};
@@ -414,21 +594,23 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         int uv[1] = {0};
         for (int g = g0; g < g1; ++g) {
             const CascGroup cg = scg[g];
+            const int span = cg.prefix_len - cg.key_base;
             int nc = (p.lay.casc_target + pair_units - 1) / pair_units;
-            nc = max(1, min(nc, min(kMaxCascChunks, (cg.prefix_len + kPreKeys - 1) / kPreKeys)));
-            const int ck = ((cg.prefix_len + nc - 1) / nc + kPreKeys - 1) / kPreKeys * kPreKeys;
-            uv[0] += (cg.prefix_len + ck - 1) / ck * casc_pair_units(cg.n_members, TM, Hkv);
+            nc = max(1, min(nc, min(nc_cap, (span + kPreKeys - 1) / kPreKeys)));
+            const int ck = ((span + nc - 1) / nc + kPreKeys - 1) / kPreKeys * kPreKeys;
+            uv[0] += (span + ck - 1) / ck * casc_pair_units(cg.n_members, TM, Hkv);
         }
         int ut[1];
         block_scan<1>(uv, ut, s_tmp1);
         int uoff = uv[0];
         for (int g = g0; g < g1; ++g) {
             CascGroup cg = scg[g];
+            const int span = cg.prefix_len - cg.key_base;
             int nc = (p.lay.casc_target + pair_units - 1) / pair_units;
-            nc = max(1, min(nc, min(kMaxCascChunks, (cg.prefix_len + kPreKeys - 1) / kPreKeys)));
-            const int ck = ((cg.prefix_len + nc - 1) / nc + kPreKeys - 1) / kPreKeys * kPreKeys;
+            nc = max(1, min(nc, min(nc_cap, (span + kPreKeys - 1) / kPreKeys)));
+            const int ck = ((span + nc - 1) / nc + kPreKeys - 1) / kPreKeys * kPreKeys;
             cg.chunk_keys = ck;
-            cg.n_chunks = (cg.prefix_len + ck - 1) / ck;
+            cg.n_chunks = (span + ck - 1) / ck;
             cg.unit_off = uoff;
             cg.n_units = cg.n_chunks * casc_pair_units(cg.n_members, TM, Hkv);
             sa[kCUoff][g] = uoff;
@@ -439,9 +621,11 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         if (tid == 0) s_casc_units = ut[0];
         // each member takes a slot of its group's member list (filled when its decode
         // group is written below); the first-page array is free again
+        // (and of its sub-group's: the slot goes to kLcp, free since level 2 was numbered)
         for (int i = tid; i < B; i += kThreads) {
             if (sa[kCgid][i] < 0) continue;
             sa[kFirst][i] = atomicAdd(&sa[kMpos][sa[kLeader][i]], 1);
+            if (sa[kCgid2][i] >= 0) sa[kLcp][i] = atomicAdd(&sa[kCnt][sa[kLeader2][i]], 1);
         }
     }
     __syncthreads();
@@ -474,12 +658,12 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
             if (n <= 0 || (p.use_prefill && n > TB)) continue;
             const int ng = (n + TB - 1) / TB;
             const int lp = prefix_of(i);
-            const int cg = casc_of(i);
+            const int npre = prefix_parts(i);
             for (int g = 0; g < ng; ++g) {
                 const int ext = L - n + min((g + 1) * TB, n) - lp;
                 int per;
                 const int s = split_ranges(ext, chunk, &per);
-                const int nparts = s + (cg >= 0 ? scg[cg].n_chunks : 0);
+                const int nparts = s + npre;
                 cnt2[0] += s;
                 if (nparts > 1) cnt2[1] += nparts;
                 const int last = max(0, ext - (s - 1) * per);
@@ -530,8 +714,8 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         pt.ntok0 = min(TM, cgr.n_members - m0);
         pt.ntok1 = max(0, min(TM, cgr.n_members - m0 - TM));
         pt.qpos0 = c;
-        pt.kv_end0 = c * cgr.chunk_keys;
-        pt.kv_end1 = min(cgr.prefix_len, (c + 1) * cgr.chunk_keys);
+        pt.kv_end0 = cgr.key_base + c * cgr.chunk_keys;
+        pt.kv_end1 = min(cgr.prefix_len, cgr.key_base + (c + 1) * cgr.chunk_keys);
         return (pt.kv_end1 - pt.kv_end0 + kPreKeys - 1) / kPreKeys;
     };
     if (run) {
@@ -583,13 +767,14 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
             if (p.use_prefill && n > TB) continue;  // prefill units: emitted below
             const int ng = (n + TB - 1) / TB;
             const int lp = prefix_of(i);
-            const int cg = casc_of(i);
+            const int cg = casc_of(i), cg2 = casc2_of(i);
+            const int npre = prefix_parts(i);
             for (int g = 0; g < ng; ++g) {
                 const int a0 = g * TB, na = min(TB, n - a0);
                 const int kv_end = L - n + a0 + na;
                 int per;
                 const int s = split_ranges(kv_end - lp, chunk, &per);
-                const int nparts = s + (cg >= 0 ? scg[cg].n_chunks : 0);
+                const int nparts = s + npre;
                 DecGroup dg;
                 dg.req = i;
                 dg.tok0 = c0 + a0;
@@ -603,9 +788,11 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
                 dg.tail0 = lp;
                 dg.pad0 = dg.pad1 = dg.pad2 = dg.pad3 = dg.pad4 = dg.pad5 = 0;
                 store_record(&groups[gi], dg);
-                // member list entry of a shared-prefix member (one new token): its q row and
-                // the partial slot of prefix chunk 0
+                // member list entries of a shared-prefix member (one new token): its q row and
+                // the partial slot of chunk 0 of each of its groups (the group's chunks first,
+                // then the sub-group's)
                 if (cg >= 0) cmembers[sa[kFirst][i]] = make_int2(dg.tok0, pi + s);
+                if (cg2 >= 0) cmembers[sa[kLcp][i]] = make_int2(dg.tok0, pi + s + scg[cg].n_chunks);
                 for (int u = 0; u < s; ++u) {
                     DecUnit du;
                     du.group = gi;
@@ -676,8 +863,8 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
 
 size_t prepare_smem_bytes(int smem_batch, bool cascade) {
     size_t words = (size_t)kNumArrays * (smem_batch + 1);
-    // hash table, then one group record per pair of requests
-    if (cascade) words += 2 * ((size_t)1 << casc_hash_bits(smem_batch)) + (smem_batch / 2 + 1) * (sizeof(CascGroup) / 4);
+    // hash table, then group records (top level and sub-groups: one per pair of requests each)
+    if (cascade) words += 2 * ((size_t)1 << casc_hash_bits(smem_batch)) + (smem_batch + 1) * (sizeof(CascGroup) / 4);
     return words * sizeof(int32_t);
 }
 

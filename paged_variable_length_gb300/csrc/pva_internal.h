@@ -91,14 +91,18 @@ struct DecUnit {
 // the keys after the prefix, and the merge combines both by log-sum-exp.
 struct CascGroup {
     int32_t leader;       // request whose page-table row addresses the prefix
-    int32_t prefix_len;   // keys [0, prefix_len) are shared
+    int32_t prefix_len;   // keys [key_base, prefix_len) are shared by the members
     int32_t n_members;
     int32_t member_off;   // members[member_off ..]: (token, first prefix partial slot) per member
     int32_t n_chunks;     // prefix pass key chunks
     int32_t chunk_keys;   // keys per chunk (multiple of kPreKeys)
     int32_t unit_off;     // first prefix-pass unit of the group (relative to the cascade units)
     int32_t n_units;
+    int32_t key_base;     // 0 for a top-level group; a sub-group's: its parent's prefix_len
+    int32_t level;        // 0 top level, 1 sub-group
+    int32_t pad0, pad1;
 };
+static_assert(sizeof(CascGroup) % 16 == 0, "CascGroup is whole 16-byte words");
 
 // One work unit of the tensor-core prefill kernel: two consecutive Q tiles of one
 // request and kv head.  A Q tile is kPreRows rows = floor(kPreRows / G) tokens x the

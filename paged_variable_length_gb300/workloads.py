@@ -158,6 +158,37 @@ def cascade(seed: int = 0, batch: int = 128, prefix: int = 4096, lo: int = 16, h
                                 f"U[{lo},{hi}], Hq32/Hkv8/D128, ps16, 20000-page pool")
 
 
+def cascade_tree(seed: int = 0, branches: int = 8, per_branch: int = 16, root: int = 2048, branch: int = 1024,
+                 lo: int = 16, hi: int = 512, page_size: int = 16, num_pages: int = 20000) -> Workload:
+    """A two-level prefix tree of single-token decodes: every row starts with the same
+    ``root``-token run of pages, each of ``branches`` groups of ``per_branch`` rows then
+    shares a further ``branch``-token run of its own, and each row ends in a private tail
+    of U[lo, hi] tokens; Hq 32, Hkv 8, D 128; page_size 16 over a 20000-page pool."""
+    rng = np.random.default_rng(seed)
+    if root % page_size or branch % page_size:
+        raise ValueError("the shared runs are whole pages")
+    perm = [int(x) for x in rng.permutation(num_pages)]
+    take = lambda k: [perm.pop() for _ in range(k)]
+    root_pages = take(root // page_size)
+    rows, kv_lens = [], []
+    for _ in range(branches):
+        branch_pages = take(branch // page_size)
+        for _ in range(per_branch):
+            tail = int(rng.integers(lo, hi + 1))
+            L = root + branch + tail
+            rows.append(root_pages + branch_pages + take(math.ceil(L / page_size) - len(root_pages) - len(branch_pages)))
+            kv_lens.append(L)
+    table = np.zeros((len(rows), max(len(r) for r in rows)), np.int32)
+    for i, r in enumerate(rows):
+        table[i, :len(r)] = r
+    return Workload("cascade_tree", [1] * len(rows), kv_lens, 32, 8, 128, page_size, num_pages, table, 1.0, seed,
+                    shared_prefix_pages=root // page_size,
+                    extra={"branch_pages": branch // page_size, "per_branch": per_branch},
+                    description=f"cascade tree: {branches}x{per_branch} decodes, a {root}-token root prefix, "
+                                f"{branch}-token branch prefixes, tails U[{lo},{hi}], Hq32/Hkv8/D128, "
+                                f"ps{page_size}, {num_pages}-page pool")
+
+
 def ragged_prefill(seed: int = 0, batch: int = 8, lo: int = 256, hi: int = 4096) -> Workload:
     """The prefill workload's requests (8 fresh prefills, len U[256,4096], Hq 32, Hkv 8,
     D 128) over contiguous K/V: page_size 1, the "pool" is the batch's own k / v rows and
@@ -205,6 +236,7 @@ WORKLOADS = {
     "prefill": prefill_only,
     "mixed": mixed,
     "cascade": cascade,
+    "cascade_tree": cascade_tree,
     "specdec": spec_decode,
     "ragged": ragged_prefill,
 }

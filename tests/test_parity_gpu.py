@@ -222,6 +222,16 @@ def test_full_size_workload(name):
     _sampled_check(W.WORKLOADS[name](0))
 
 
+def test_full_size_prefix_tree():
+    """128 decodes: a 2048-token root, 8 branches of 16 sharing 1024 more tokens each."""
+    wl = W.cascade_tree(0)
+    t = W.make_tensors(wl, DEV)
+    eng = make_engine(wl)
+    eng.prepare(t["cu_seqlens_q"], t["cache_seqlens"], t["page_table"], wl.total_tokens)
+    assert pva.attn_debug_plan_counts(eng.meta)["casc_groups"] == 9
+    _sampled_check(wl)
+
+
 # ------------------------------------------------------------------ shared-prefix (cascade) path
 
 
@@ -297,6 +307,82 @@ def test_cascade_group_size_and_tile_edges():
 def test_cascade_with_group_of_seven_heads():
     wl = _cascade_batch(4, Hq=28, Hkv=4, D=128, ps=16)
     _full_check(wl)
+
+
+def _tree_batch(seed=0, Hq=32, Hkv=8, D=128, ps=16):
+    """Two levels of shared prefixes.  Group A (10 root pages) holds sub-group A1 (9 more
+    shared pages; one member's query sits right after them), sub-group A2 (12 more pages,
+    one member sharing only 8 of them), three members with private pages after the root
+    and two sharing only 5 more pages (too short for a sub-group).  Group B (8 root pages)
+    holds sub-group B1 (10 more) and one private member.  Plus an unrelated decode and a
+    prefill: 2 groups and 3 sub-groups."""
+    rng = np.random.default_rng(seed)
+    P = 900
+    perm = list(rng.permutation(P))
+    take = lambda k: [int(perm.pop()) for _ in range(k)]
+    rows, q_lens, kv_lens = [], [], []
+
+    def add(shared, tail):
+        L = len(shared) * ps + tail
+        rows.append(shared + take((L + ps - 1) // ps - len(shared)))
+        q_lens.append(1)
+        kv_lens.append(L)
+
+    root_a, a1, a2, a5 = take(10), take(9), take(12), take(5)
+    for tail in (1, 7, 16, 40, 23):
+        add(root_a + a1, tail)
+    for tail in (3, 30, 64):
+        add(root_a + a2, tail)
+    add(root_a + a2[:8], 17)
+    for tail in (5, 90, 33):
+        add(root_a, tail)
+    for tail in (2, 19):
+        add(root_a + a5, tail)
+    root_b, b1 = take(8), take(10)
+    for tail in (11, 48, 1):
+        add(root_b + b1, tail)
+    add(root_b, 70)
+    add([], 300)                                # unrelated decode
+    L = 200                                     # a prefill in the same batch
+    rows.append(take((L + ps - 1) // ps)); q_lens.append(L); kv_lens.append(L)
+    return _table_workload(q_lens, kv_lens, rows, Hq, Hkv, D, ps, P, seed)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_two_level_prefix_tree_matches_the_oracle(seed):
+    wl = _tree_batch(seed)
+    _, eng = _full_check(wl)
+    counts = pva.attn_debug_plan_counts(eng.meta)
+    assert counts["casc_groups"] == 5, counts
+    _, eng_off = _full_check(wl, enable_cascade=False)
+    assert pva.attn_debug_plan_counts(eng_off.meta)["casc_groups"] == 0
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(28, 4, 128), (16, 4, 64), (32, 32, 128)])
+def test_two_level_prefix_tree_head_layouts(Hq, Hkv, D):
+    wl = _tree_batch(5, Hq=Hq, Hkv=Hkv, D=D)
+    _, eng = _full_check(wl)
+    assert pva.attn_debug_plan_counts(eng.meta)["casc_groups"] == 5
+
+
+def test_sub_group_larger_than_a_tile_pair():
+    """A sub-group of 70 members (G 4: 32 member rows per tile) under a 27-page root
+    (432 keys: the sub-group's keys start off a 128-key boundary), a second sub-group of
+    3, and root members without one."""
+    ps = 16
+    rng = np.random.default_rng(8)
+    P = 4000
+    perm = list(rng.permutation(P))
+    take = lambda k: [int(perm.pop()) for _ in range(k)]
+    root, s1, s2 = take(27), take(13), take(20)
+    rows, ql, kl = [], [], []
+    for shared, count in ((root + s1, 70), (root + s2, 3), (root, 4)):
+        for _ in range(count):
+            L = len(shared) * ps + int(rng.integers(1, 80))
+            rows.append(shared + take((L + ps - 1) // ps - len(shared))); ql.append(1); kl.append(L)
+    wl = _table_workload(ql, kl, rows, 32, 8, 128, ps, P, 8)
+    _, eng = _full_check(wl)
+    assert pva.attn_debug_plan_counts(eng.meta)["casc_groups"] == 3
 
 
 # ------------------------------------------------------------------ head_dim 64 on the tensor-core path
