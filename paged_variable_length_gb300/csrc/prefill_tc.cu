@@ -130,6 +130,11 @@ __device__ __forceinline__ int queue_read(Bars* b, int k, int lane, uint32_t* er
     return v;
 }
 
+template <bool B>
+struct BoolTag {
+    static constexpr bool value = B;
+};
+
 // What a unit asks for, for either kind: a prefill tile pair (keys [0, kv_end_h) of Q
 // tile h, causal) or a cascade prefix-pass unit (keys [k0, k1) of the shared prefix for
 // both member tiles, no causal mask).
@@ -226,18 +231,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ============================================================== producer (cp.async gathers)
         // The three producer warps move the rows of every Q / K / V tile: a row is one kv
         // head of one slot (or one q head of one token), D*2 bytes, copied as 16-byte async
-        // copies into the 128-byte-swizzled layout the MMA descriptors expect.  The lanes of
-        // a copy instruction take consecutive 16-byte chunks of kRowsPerCopy whole rows, so
+        // copies into the 128-byte-swizzled layout the MMA descriptors expect.  Q rows that
+        // are gathered (shared-prefix members, or Q without a tensor map): the lanes of a
+        // copy instruction take consecutive 16-byte chunks of kRowsPerCopy whole rows, so
         // every instruction touches whole 128-byte lines on both sides (one lane per row
         // made each instruction touch 32 lines, eight times the shared-memory wavefronts the
         // data needs, and those bursts slowed the tensor core's operand reads).  Each lane
         // computes the source offsets of two of its warp's rows into the warp's own table in
         // shared memory, which the copy loop reads back (one broadcast load per copy).
-        // With pages of 16 or more slots, K and V rows are copied by 8 lanes per 128-byte
-        // half row instead (4 rows per instruction, the offsets of a lane's 11 rows kept in
-        // registers): that touches as few lines per instruction and issues faster there.
-        // With a token-slot pool the two-rows-per-instruction form is faster: fewer random
-        // address translations per instruction.  A page of a few rows per kv head is too
+        // K and V rows (any page size) are copied by 8 lanes per 128-byte half row instead:
+        // 4 rows per instruction, the offsets of a lane's 11 rows kept in registers, no
+        // table round trip.  With a token-slot pool (page size 1) this form also beat the
+        // table form: 255 against 327 us for the tensor-core pass of 8 contiguous prefills,
+        // 108 against 142 us for the mixed batch.  A page of a few rows per kv head is too
         // small a box for TMA to stream efficiently (about 270 cycles per box measured), and
         // rows past kv_len are not copied.  The MMA thread orders these generic-proxy writes
         // before its tensor-core reads with a proxy fence after it has waited on the tile's
@@ -249,7 +255,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         static_assert(kCopyIters * kRowsPerCopy <= 64, "two row offsets per lane");
         const int pwarp = warp - kProducerWarp0;  // 0..2
         const int chunk = lane % kChunks, sub = lane / kChunks;
-        const bool paged = p.page_size >= 16;  // K/V gather mapping, see above
         const int ps_mask = p.page_size - 1;
         // row of a tile held by this warp's row index k (k = copy step * kRowsPerCopy + sub)
         auto row_of = [&](int k) { return pwarp * kRowsPerCopy + (k % kRowsPerCopy) + (k / kRowsPerCopy) * kStride; };
@@ -424,110 +429,76 @@ __global__ void __launch_bounds__(kThreads, 1)
                     convert(valid, stage8 + kPreRows * D, smem + L::kV + st * L::kTile, &b->v_full[st]);
                     if (j + 1 < nkt) valid = load_tile(j + 1, pg);
                 }
-            } else if (paged) {
+            } else {
                 // 8 lanes per 128-byte half row, 4 rows per copy instruction; each lane keeps
                 // the source offsets of its kG8 rows (pwarp * 4 + lane / 8 + 12 m) in registers
                 constexpr int kG8 = (kPreRows + 11) / 12;
                 const int grp = lane >> 3, c8 = lane & 7;
-                for (int j = 0; j < nkt && ok; ++j, ++it) {
-                    const int st = it & 1;
-                    const uint32_t ph = (it >> 1) & 1;
-                    // all page ids first (independent loads in flight together), then the checks:
-                    // an error report between the loads would order them one after another
-                    int32_t pg[kG8];
-#pragma unroll
-                    for (int m = 0; m < kG8; ++m) {
-                        const int r = pwarp * 4 + grp + 12 * m;
-                        const int key = uv.key_base + j * kPreKeys + r;
-                        pg[m] = (r < kPreRows && key < kv_end) ? prow[key >> p.page_shift] : 0;
-                    }
-                    int64_t off[kG8];
-                    bool bad = false;
-#pragma unroll
-                    for (int m = 0; m < kG8; ++m) {
-                        const int r = pwarp * 4 + grp + 12 * m;
-                        const int key = uv.key_base + j * kPreKeys + r;
-                        off[m] = -1;
-                        if (r < kPreRows && key < kv_end) {
-                            int64_t page = pg[m];
-                            if (page < 0 || page >= p.num_pages) {
-                                bad = true;
-                                page = 0;
-                            }
-                            off[m] = (((page << p.page_shift) + (key & ps_mask)) * p.num_kv_heads + pt.kvh) * D + c8 * 8;
-                        }
-                    }
-                    if (bad) dev::set_error(err, kErrPage);
-                    auto copy_g8 = [&](uint8_t* tile, const uint16_t* base) {
-                        const uint32_t t0 = dev::smem_u32(tile);
+                // specialised for token slots (page size 1: the page id is the slot) and for
+                // pages of several slots
+                auto gather = [&](auto token_slots) {
+                    constexpr bool kTok = decltype(token_slots)::value;
+                    for (int j = 0; j < nkt && ok; ++j, ++it) {
+                        const int st = it & 1;
+                        const uint32_t ph = (it >> 1) & 1;
+                        // all page ids first (independent loads in flight together), then the checks:
+                        // an error report between the loads would order them one after another
+                        int32_t pg[kG8];
 #pragma unroll
                         for (int m = 0; m < kG8; ++m) {
                             const int r = pwarp * 4 + grp + 12 * m;
-                            if (off[m] < 0) continue;
-                            const uint32_t d = t0 + r * 128 + ((c8 ^ (r & 7)) << 4);
-                            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(base + off[m]));
-                            if (D == 128)
-                                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d + kRegion),
-                                             "l"(base + off[m] + 64));
+                            const int key = uv.key_base + j * kPreKeys + r;
+                            pg[m] = (r < kPreRows && key < kv_end) ? prow[kTok ? key : key >> p.page_shift] : 0;
                         }
-                    };
-                    if (!wait_or_abort(&b->k_empty[st], ph ^ 1, b, err)) {
-                        ok = false;
-                        break;
-                    }
-                    copy_g8(smem + L::kK + st * L::kTile, p.k_pool);
-                    issue(&b->k_full[st]);
-                    if (!wait_or_abort(&b->v_empty[st], ph ^ 1, b, err)) {
-                        ok = false;
-                        break;
-                    }
-                    copy_g8(smem + L::kV + st * L::kTile, p.v_pool);
-                    issue(&b->v_full[st]);
-                }
-            } else {
-                // token-slot pool: two rows per copy instruction through the offset table;
-                // page ids of this lane's two rows are read a tile ahead
-                auto page_ids = [&](int j, int32_t (&pg)[2]) {
+                        int64_t off[kG8];
+                        bool bad = false;
 #pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        const int r = row_of(lane + 32 * i);
-                        const int key = uv.key_base + j * kPreKeys + r;
-                        pg[i] = (j < nkt && r < kPreRows && key < kv_end) ? prow[key >> p.page_shift] : 0;
+                        for (int m = 0; m < kG8; ++m) {
+                            const int r = pwarp * 4 + grp + 12 * m;
+                            const int key = uv.key_base + j * kPreKeys + r;
+                            off[m] = -1;
+                            if (r < kPreRows && key < kv_end) {
+                                int64_t page = pg[m];
+                                if (page < 0 || page >= p.num_pages) {
+                                    bad = true;
+                                    page = 0;
+                                }
+                                const int64_t slot = kTok ? page : (page << p.page_shift) + (key & ps_mask);
+                                off[m] = (slot * p.num_kv_heads + pt.kvh) * D + c8 * 8;
+                            }
+                        }
+                        if (bad) dev::set_error(err, kErrPage);
+                        auto copy_g8 = [&](uint8_t* tile, const uint16_t* base) {
+                            const uint32_t t0 = dev::smem_u32(tile);
+#pragma unroll
+                            for (int m = 0; m < kG8; ++m) {
+                                const int r = pwarp * 4 + grp + 12 * m;
+                                if (off[m] < 0) continue;
+                                const uint32_t d = t0 + r * 128 + ((c8 ^ (r & 7)) << 4);
+                                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(base + off[m]));
+                                if (D == 128)
+                                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d + kRegion),
+                                                 "l"(base + off[m] + 64));
+                            }
+                        };
+                        if (!wait_or_abort(&b->k_empty[st], ph ^ 1, b, err)) {
+                            ok = false;
+                            break;
+                        }
+                        copy_g8(smem + L::kK + st * L::kTile, p.k_pool);
+                        issue(&b->k_full[st]);
+                        if (!wait_or_abort(&b->v_empty[st], ph ^ 1, b, err)) {
+                            ok = false;
+                            break;
+                        }
+                        copy_g8(smem + L::kV + st * L::kTile, p.v_pool);
+                        issue(&b->v_full[st]);
                     }
                 };
-                int32_t pg_next[2];
-                page_ids(0, pg_next);
-                for (int j = 0; j < nkt && ok; ++j, ++it) {
-                    const int st = it & 1;
-                    const uint32_t ph = (it >> 1) & 1;
-                    const int32_t pg[2] = {pg_next[0], pg_next[1]};
-                    page_ids(j + 1, pg_next);
-                    int64_t off[2] = {-1, -1};
-#pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        const int r = row_of(lane + 32 * i);
-                        const int key = uv.key_base + j * kPreKeys + r;
-                        if (r >= kPreRows || key >= kv_end) continue;
-                        int64_t page = pg[i];
-                        if (page < 0 || page >= p.num_pages) {
-                            dev::set_error(err, kErrPage);
-                            page = 0;
-                        }
-                        off[i] = (((page << p.page_shift) + (key & ps_mask)) * p.num_kv_heads + pt.kvh) * D;
-                    }
-                    if (!wait_or_abort(&b->k_empty[st], ph ^ 1, b, err)) {
-                        ok = false;
-                        break;
-                    }
-                    copy_tile(smem + L::kK + st * L::kTile, off[0], off[1], p.k_pool);
-                    issue(&b->k_full[st]);
-                    if (!wait_or_abort(&b->v_empty[st], ph ^ 1, b, err)) {
-                        ok = false;
-                        break;
-                    }
-                    copy_tile(smem + L::kV + st * L::kTile, off[0], off[1], p.v_pool);
-                    issue(&b->v_full[st]);
-                }
+                if (p.page_size == 1)
+                    gather(BoolTag<true>{});
+                else
+                    gather(BoolTag<false>{});
             }
             if (!ok) break;
         }
