@@ -357,6 +357,7 @@ pva_status forward_impl(const MetaHost* h, const void* q, const void* k, const v
     fp.kv_fp8 = h->cfg.kv_dtype == PVA_KV_E4M3 ? 1 : 0;
     fp.k_scale = k_scale;
     fp.v_scale = v_scale;
+    fp.dec_wait_late = (h->use_prefill || h->use_cascade) ? 1 : 0;
     // inside a stream capture the events become graph nodes that still time the replay
     cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
     if (h->n_events == 5 && cudaStreamIsCapturing(s, &capture) != cudaSuccess) return PVA_ERR_CUDA;

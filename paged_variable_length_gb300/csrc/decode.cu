@@ -122,7 +122,13 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
-    dev::grid_dep_wait();
+    // after the tensor-core kernel the store kernel has already finished (see
+    // ForwardParams::dec_wait_late); that grid is waited for at every exit below, so
+    // that this grid (and the merge after it) completes after it
+    if (!p.dec_wait_late) dev::grid_dep_wait();
+    auto finish = [&]() {
+        if (p.dec_wait_late) dev::grid_dep_wait();
+    };
 
     const DecUnit* units = reinterpret_cast<const DecUnit*>(p.ws + p.lay.dec_units);
     int32_t* sched = &hdr->pad[0];
@@ -251,6 +257,7 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
             for (int s = 0; s < stages; ++s)
                 if (armed & (1u << s)) (void)dev::mbar_wait(&sh->full[s], (armed_par >> s) & 1u);
         }
+        finish();
         return;
     }
 
@@ -272,6 +279,7 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
     while (true) {
         if (!dev::mbar_wait(&sh->full[stage], phase)) {
             abort_cta(sh, err);
+            finish();
             return;
         }
         const StageInfo si = sh->info[stage];
@@ -537,6 +545,7 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
             if (cq == 0) pl[prow] = half ? lse1 : lse0;
         }
     }
+    finish();
 }
 
 // K4: log-sum-exp combine of the split groups (and of the prefix-pass partials of

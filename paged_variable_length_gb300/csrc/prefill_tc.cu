@@ -173,8 +173,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The plan was written by the prepare kernel, which finished before the store
     // kernel began; the pool rows and the work counter come from the store kernel, which
     // may still run (programmatic launch): they are read only after grid_dep_wait.  An
-    // idle CTA waits too, so that this grid never completes before its predecessor.
-    dev::grid_dep_launch();
+    // idle CTA waits too, so that this grid never completes before its predecessor.  The
+    // dependents (the decode kernel) are released only after that wait, so that when
+    // they start the store kernel has finished: decode does not wait for this grid
+    // before its own work, only before it exits.
     const int n_units = hdr->n_pre_tiles;
     if ((hdr->error_bits & kErrFatal) || n_units == 0 || (int)blockIdx.x >= n_units) {
         dev::grid_dep_wait();
@@ -223,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after_sync();
     const uint32_t tmem = b->tmem_base;
     dev::grid_dep_wait();
+    dev::grid_dep_launch();
 
     if (warp >= 8) {
         // control warpgroups: give registers to the softmax warpgroups

@@ -206,6 +206,10 @@ struct ForwardParams {
     int32_t kv_fp8;
     const float* k_scale;
     const float* v_scale;
+    // the decode kernel follows the tensor-core kernel, which signals its dependents only
+    // after its own wait for the store kernel: decode then starts on SMs the tensor-core
+    // kernel has left and waits for that grid only before it exits
+    int32_t dec_wait_late;
 };
 
 // Host view of a prepared batch, stored inside pva_meta::opaque.
