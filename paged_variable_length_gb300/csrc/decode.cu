@@ -122,12 +122,14 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
-    // after the tensor-core kernel the store kernel has already finished (see
+    // after a tensor-core kernel with units the store kernel has already finished (see
     // ForwardParams::dec_wait_late); that grid is waited for at every exit below, so
-    // that this grid (and the merge after it) completes after it
-    if (!p.dec_wait_late) dev::grid_dep_wait();
+    // that this grid (and the merge after it) completes after it.  With no unit the
+    // tensor-core kernel released this grid at once, and it waits here as usual.
+    const bool wait_late = p.dec_wait_late && hdr->n_pre_tiles > 0;
+    if (!wait_late) dev::grid_dep_wait();
     auto finish = [&]() {
-        if (p.dec_wait_late) dev::grid_dep_wait();
+        if (wait_late) dev::grid_dep_wait();
     };
 
     const DecUnit* units = reinterpret_cast<const DecUnit*>(p.ws + p.lay.dec_units);
@@ -554,13 +556,21 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
 // pbase .. pbase + nparts - 1, in slot order (deterministic).  One warp per row: lane s
 // holds part s's LSE, so the maximum and the normaliser are two warp reductions, and
 // lane c accumulates columns [c * D/32, (c+1) * D/32) of every part with independent
-// loads (the partials are L2-resident: written by the kernels just before).  Launched
-// programmatically after the decode kernel, whose grid it waits for.
+// loads (the partials are L2-resident: written by the kernels just before).  A work
+// item is one group's rows [32c, 32c + 32) (c < rows_per_slot / 32), one row per warp,
+// items numbered chunk-major (chunk 0 of every group first, so single-token groups,
+// whose rows are all in chunk 0, each go to their own CTA), so the rows of a group
+// with several tokens spread over several SMs (a CTA per group
+// left each warp four rows in sequence in a speculative-verify batch: merge 23.6 ->
+// 14 us there).  Smaller CTAs with fewer rows each cost more in launch and record
+// reads than they saved (merge of the cascade batch 10.2 -> 16.4 us at 8 warps).
+// Launched programmatically after the decode kernel, whose grid it waits for.
 constexpr int kMergeThreads = 1024;
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(ForwardParams p) {
     constexpr int kPer = D / 32;  // output columns per lane
+    constexpr int kWarps = kMergeThreads / 32;
     dev::grid_dep_launch();
     PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws + p.lay.header);
     const int n_groups = hdr->n_dec_groups;
@@ -573,20 +583,25 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(ForwardParams p) {
     const float* pout = reinterpret_cast<const float*>(p.ws + p.lay.partial_o);
     const int rps = p.lay.rows_per_slot, Hq = p.num_qo_heads;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // row chunks of a group: its rows are at most max_group_tokens * Hq (<= rps)
+    const int chunks = (min(rps, max(hdr->max_group_tokens, 1) * Hq) + kWarps - 1) / kWarps;
+    const int n_items = n_groups * chunks;
     // the group records come from the plan (complete before the forward began): the first
     // one is read before the wait for the decode grid, only the partials after it
     DecGroup dg_next{};
-    if ((int)blockIdx.x < n_groups) dg_next = groups[blockIdx.x];
+    if ((int)blockIdx.x < n_items) dg_next = groups[blockIdx.x % n_groups];
     dev::grid_dep_wait();
-    for (int gi = blockIdx.x; gi < n_groups; gi += gridDim.x) {
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
         const DecGroup dg = dg_next;
-        if (gi + (int)gridDim.x < n_groups) dg_next = groups[gi + gridDim.x];
+        if (it + (int)gridDim.x < n_items) dg_next = groups[(it + gridDim.x) % n_groups];
         const int np = dg.nparts;
         if (np <= 1) continue;
         const int rows = dg.ntok * Hq;
         const float* plb = plse + (int64_t)dg.pbase * rps;
         const float* pob = pout + (int64_t)dg.pbase * rps * D;
-        for (int row = warp; row < rows; row += kMergeThreads / 32) {
+        {
+            const int row = (it / n_groups) * kWarps + warp;
+            if (row >= rows) continue;
             const float lfirst = lane < np ? __ldcg(plb + (int64_t)lane * rps + row) : -INFINITY;
             float mx = lfirst;
             for (int s0 = 32; s0 < np; s0 += 32)

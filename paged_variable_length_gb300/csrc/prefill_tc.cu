@@ -179,6 +179,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // before its own work, only before it exits.
     const int n_units = hdr->n_pre_tiles;
     if ((hdr->error_bits & kErrFatal) || n_units == 0 || (int)blockIdx.x >= n_units) {
+        // an idle CTA releases the dependents at once: with no unit at all the decode
+        // kernel then waits for this grid at its start (see ForwardParams::dec_wait_late)
+        dev::grid_dep_launch();
         dev::grid_dep_wait();
         return;
     }

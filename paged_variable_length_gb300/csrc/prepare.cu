@@ -143,6 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     __shared__ int s_hist_u[kBuckets];
     __shared__ int s_hist_t[kBuckets];
     __shared__ int s_casc_units;
+    __shared__ int s_max_ntok;
 
     const int tid = threadIdx.x;
     const int B = p.batch;
@@ -156,6 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         s_err = 0;
         s_work = 0;
         s_casc_units = 0;
+        s_max_ntok = 0;
     }
     const bool casc = p.use_cascade && small && B >= 2;
     // One round trip for everything that depends on the request index alone: cu, the
@@ -534,6 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     uint32_t err = 0;
     int cnt[3] = {0, 0, 0};  // decode groups, prefill tile pairs x kv heads, (unused)
     unsigned long long work = 0;
+    int max_ntok = 0;
     if (tid == 0 && p.cu[0] != 0) err |= kErrCu;
     if (tid == 0 && B > p.max_batch) err |= kErrLimits;
     if (tid == 0 && p.total_tokens > p.max_tokens) err |= kErrLimits;
@@ -550,6 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         } else {
             const int ng = (n + TB - 1) / TB;
             cnt[0] += ng;
+            max_ntok = max(max_ntok, min(n, TB));
             const int lp = prefix_of(i);
             for (int g = 0; g < ng; ++g) work += (unsigned long long)(L - n + min((g + 1) * TB, n) - lp);
         }
@@ -558,6 +562,8 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) work += __shfl_xor_sync(0xffffffffu, work, o);
     if ((tid & 31) == 0 && work) atomicAdd(&s_work, work);
+    max_ntok = __reduce_max_sync(0xffffffffu, max_ntok);
+    if ((tid & 31) == 0 && max_ntok) atomicMax(&s_max_ntok, max_ntok);
     int tot3[3];
     block_scan<3>(cnt, tot3, s_tmp3);  // cnt now holds this thread's exclusive offsets
     // first prefill unit and first decode group of each request: the emission below runs
@@ -856,6 +862,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         hdr->n_casc_groups = ok ? n_cgroups : 0;
         hdr->n_casc_tiles = ok ? s_casc_units : 0;
         hdr->n_casc_units = ok ? s_casc_units : 0;
+        hdr->max_group_tokens = ok ? s_max_ntok : 0;
     }
 }
 

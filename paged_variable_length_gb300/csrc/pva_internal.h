@@ -47,7 +47,8 @@ struct PlanHeader {
     int32_t split_chunk;
     int32_t n_partial_slots;
     int32_t n_casc_units;
-    int32_t pad[55];
+    int32_t max_group_tokens;  // most tokens in one decode group (bounds the merge's rows)
+    int32_t pad[54];           // pad[0] / pad[1]: decode / tensor-core work counters
 };
 static_assert(sizeof(PlanHeader) == 256, "header is one 256-byte line");
 
@@ -206,9 +207,10 @@ struct ForwardParams {
     int32_t kv_fp8;
     const float* k_scale;
     const float* v_scale;
-    // the decode kernel follows the tensor-core kernel, which signals its dependents only
-    // after its own wait for the store kernel: decode then starts on SMs the tensor-core
-    // kernel has left and waits for that grid only before it exits
+    // the decode kernel follows the tensor-core kernel; when that kernel has units it
+    // signals its dependents only after its own wait for the store kernel, and decode
+    // then starts on SMs the tensor-core kernel has left and waits for that grid only
+    // before it exits
     int32_t dec_wait_late;
 };
 
