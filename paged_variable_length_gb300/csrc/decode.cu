@@ -103,6 +103,12 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
     // the work counter and the prefix-pass partials only after grid_dep_wait.
     dev::grid_dep_launch();
     const int n_units = hdr->n_dec_units * n_hb;
+    // after a tensor-core kernel with units the store kernel has already finished (see
+    // ForwardParams::dec_wait_late); the producer warp waits for that grid before it
+    // returns (a CTA cannot exit before it), so this grid (and the merge after it)
+    // completes after it.  With no unit the tensor-core kernel released this grid at
+    // once, and it waits before its work.
+    const bool wait_late = p.dec_wait_late && hdr->n_pre_tiles > 0;
     if ((hdr->error_bits & kErrFatal) || n_units == 0) {
         dev::grid_dep_wait();
         return;
@@ -122,15 +128,7 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
-    // after a tensor-core kernel with units the store kernel has already finished (see
-    // ForwardParams::dec_wait_late); that grid is waited for at every exit below, so
-    // that this grid (and the merge after it) completes after it.  With no unit the
-    // tensor-core kernel released this grid at once, and it waits here as usual.
-    const bool wait_late = p.dec_wait_late && hdr->n_pre_tiles > 0;
     if (!wait_late) dev::grid_dep_wait();
-    auto finish = [&]() {
-        if (wait_late) dev::grid_dep_wait();
-    };
 
     const DecUnit* units = reinterpret_cast<const DecUnit*>(p.ws + p.lay.dec_units);
     int32_t* sched = &hdr->pad[0];
@@ -259,7 +257,7 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
             for (int s = 0; s < stages; ++s)
                 if (armed & (1u << s)) (void)dev::mbar_wait(&sh->full[s], (armed_par >> s) & 1u);
         }
-        finish();
+        if (wait_late) dev::grid_dep_wait();
         return;
     }
 
@@ -281,7 +279,6 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
     while (true) {
         if (!dev::mbar_wait(&sh->full[stage], phase)) {
             abort_cta(sh, err);
-            finish();
             return;
         }
         const StageInfo si = sh->info[stage];
@@ -547,7 +544,6 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
             if (cq == 0) pl[prow] = half ? lse1 : lse0;
         }
     }
-    finish();
 }
 
 // K4: log-sum-exp combine of the split groups (and of the prefix-pass partials of

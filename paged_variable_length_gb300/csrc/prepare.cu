@@ -126,6 +126,190 @@ __device__ __forceinline__ int casc_pair_units(int members, int TM, int Hkv) {
     return (((members + TM - 1) / TM) + 1) / 2 * Hkv;
 }
 
+// Level 2 of the shared-prefix search (pass 0 of the kernel below): inside a group,
+// members keyed by the page right after the group's prefix; the lowest-numbered one
+// leads its sub-group, whose prefix extends the group's by the run of pages every
+// sub-member shares with it (again at least min_pages, again whole pages before each
+// member's query).  Its prefix pass covers keys [group prefix, sub-group prefix) only.
+// The arrays of level 1 that are no longer needed hold level 2's: the page after the
+// prefix (kFirst), pages before the query then the sub-prefix (kLcp), counts then next
+// free member slots (kCnt); the hash table is reused.  Sub-group records are numbered
+// after the n_groups top-level ones; returns how many there are.  A function of its
+// own (not inlined), so that its registers do not weigh on the rest of the kernel,
+// which runs 1024 threads and so has 64 registers each.
+__device__ __noinline__ int find_sub_groups(int32_t* dyn, int stride, int32_t* hkey, int32_t* hval, int hbits,
+                                            CascGroup* scg, CascGroup* cgroups, const int32_t* page_table,
+                                            int64_t ld_table, int64_t num_pages, int min_pages, int B, int ps,
+                                            int r0, int r1, int n_groups, int members1, int (*s_tmp2)[2]) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int HT = 1 << hbits;
+    auto sa = [&](int a) { return dyn + a * stride; };
+    const int32_t* cu = sa(kCu);
+    const int32_t* lens = sa(kLen);
+    int32_t* first = sa(kFirst);
+    int32_t* lcp = sa(kLcp);
+    int32_t* cnt = sa(kCnt);
+    int32_t* page2 = first;
+    int32_t* pg2 = lcp;
+    int32_t* cnt2 = cnt;
+    int32_t* lead2 = sa(kLeader2);
+    int32_t* cgid2 = sa(kCgid2);  // pages compared per member until the sub-groups are numbered
+    for (int h = tid; h < HT; h += kThreads) {
+        hkey[h] = -1;
+        hval[h] = 0x7fffffff;
+    }
+    for (int i = tid; i < B; i += kThreads) {
+        const int g = sa(kCgid)[i];
+        int pg = -1, pages = 0;
+        if (g >= 0) {
+            const int n = cu[i + 1] - cu[i], L = lens[i];
+            pages = (L - n) / ps;
+            const int P1 = scg[g].prefix_len / ps;
+            if (pages - P1 >= min_pages) {
+                const int32_t x = page_table[(int64_t)i * ld_table + P1];
+                pg = (x >= 0 && x < num_pages) ? x : -1;
+            }
+        }
+        page2[i] = pg;
+        pg2[i] = pages;
+        cnt2[i] = 0;
+        lead2[i] = -1;
+        cgid2[i] = 0;
+    }
+    __syncthreads();
+    // hash key: the page mixed with the group id (two different pairs meeting on one
+    // key would only lose sharing: a member whose pair differs from its sub-leader's
+    // is dropped below)
+    auto key2 = [&](int i) -> int {
+        return page2[i] < 0 ? -1
+                            : (int)(((uint32_t)page2[i] * 2654435761u ^ (uint32_t)sa(kCgid)[i] * 0x9E3779B9u) &
+                                    0x7fffffffu);
+    };
+    int dup = 0;  // some key met twice (in a warp, or already in the table)
+    for (int i0 = 0; i0 < B; i0 += kThreads) {
+        const int i = i0 + tid;
+        const int f = i < B ? key2(i) : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, f);
+        const int lead = __ffs(peers) - 1;
+        int h = 0;
+        if (f >= 0 && __popc(peers) > 1) dup = 1;
+        if (f >= 0 && lane == lead) {
+            uint32_t hh = page_hash(f, hbits);
+            while (true) {
+                const int prev = atomicCAS(&hkey[hh], -1, f);
+                if (prev == f) dup = 1;
+                if (prev == -1 || prev == f) break;
+                hh = (hh + 1) & (HT - 1);
+            }
+            atomicMin(&hval[hh], i);
+            h = (int)hh;
+        }
+        h = __shfl_sync(0xffffffffu, h, lead);
+        if (f >= 0) lead2[i] = h;
+    }
+    // no two members of a group continue with the same page: no sub-group (the usual
+    // case; the rest of the search is skipped)
+    if (!__syncthreads_or(dup)) {
+        for (int i = tid; i < B; i += kThreads) cgid2[i] = -1;
+        __syncthreads();
+        return 0;
+    }
+    for (int i0 = 0; i0 < B; i0 += kThreads) {
+        const int i = i0 + tid;
+        int ld = (i < B && page2[i] >= 0) ? hval[lead2[i]] : -1;
+        if (ld >= 0 && (sa(kCgid)[ld] != sa(kCgid)[i] || page2[ld] != page2[i])) ld = -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, ld);
+        if (i < B) lead2[i] = ld;
+        if (ld >= 0 && lane == __ffs(peers) - 1) atomicAdd(&cnt2[ld], __popc(peers));
+    }
+    __syncthreads();
+    for (int i = tid; i < B; i += kThreads) {
+        const int ld = lead2[i];
+        cgid2[i] = (ld >= 0 && ld != i) ? min(pg2[i], pg2[ld]) : 0;
+    }
+    __syncthreads();
+    for (int i = tid; i < B; i += kThreads)
+        if (cgid2[i] > 0) atomicMin(&pg2[lead2[i]], cgid2[i]);
+    {
+        constexpr int kU = kCmpPages;
+        const int warp = tid >> 5;
+        for (int i = warp; i < B; i += kWarps) {
+            const int l = cgid2[i];
+            const int g = sa(kCgid)[i];
+            if (l <= 0 || g < 0) continue;  // warp-uniform
+            const int start = scg[g].prefix_len / ps + 1;  // page start - 1 matched by the key
+            if (l <= start) continue;
+            const int ld = lead2[i];
+            const int32_t* ri = page_table + (int64_t)i * ld_table;
+            const int32_t* rl = page_table + (int64_t)ld * ld_table;
+            int mis = l;
+            for (int k0 = start; k0 < l; k0 += 32 * kU) {
+                int va[kU], vb[kU];
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int k = k0 + u * 32 + lane;
+                    va[u] = k < l ? ri[k] : 0;
+                    vb[u] = k < l ? rl[k] : 0;
+                }
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int k = k0 + u * 32 + lane;
+                    if (k < l && va[u] != vb[u]) mis = min(mis, k);
+                }
+            }
+            mis = __reduce_min_sync(0xffffffffu, mis);
+            if (lane == 0 && mis < l) atomicMin(&pg2[ld], mis);
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < B; i += kThreads) cgid2[i] = -1;
+    __syncthreads();
+    auto is_sub_leader = [&](int i) {
+        if (lead2[i] != i || cnt2[i] < 2) return false;
+        return pg2[i] - scg[sa(kCgid)[i]].prefix_len / ps >= min_pages;
+    };
+    int hv[2] = {0, 0};
+    for (int i = r0; i < r1; ++i)
+        if (is_sub_leader(i)) {
+            hv[0] += 1;
+            hv[1] += cnt2[i];
+        }
+    int ht[2];
+    block_scan<2>(hv, ht, s_tmp2);
+    {
+        int gid = n_groups + hv[0], moff = members1 + hv[1];
+        for (int i = r0; i < r1; ++i) {
+            if (!is_sub_leader(i)) continue;
+            CascGroup cg;
+            cg.leader = i;
+            cg.key_base = scg[sa(kCgid)[i]].prefix_len;
+            cg.prefix_len = pg2[i] * ps;
+            cg.n_members = cnt2[i];
+            cg.member_off = moff;
+            cg.n_chunks = 0;
+            cg.chunk_keys = 0;
+            cg.unit_off = 0;
+            cg.n_units = 0;
+            cg.level = 1;
+            cg.pad0 = cg.pad1 = 0;
+            store_record(&cgroups[gid], cg);
+            scg[gid] = cg;
+            cgid2[i] = gid;
+            cnt2[i] = moff;  // next free member slot of the sub-group
+            moff += cg.n_members;
+            ++gid;
+        }
+    }
+    const int n_new = ht[0];
+    __syncthreads();
+    for (int i = tid; i < B; i += kThreads) {
+        const int ld = lead2[i];
+        if (ld >= 0 && ld != i) cgid2[i] = cgid2[ld];
+    }
+    __syncthreads();
+    return n_new;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws + p.lay.header);
     DecUnit* units = reinterpret_cast<DecUnit*>(p.ws + p.lay.dec_units);
@@ -150,9 +334,9 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     const int TB = p.dec_tokens, TM = p.pre_tokens, Hkv = p.num_kv_heads, ps = p.page_size;
     const bool small = p.smem_batch >= B;  // per-request arrays fit in shared memory
     const int stride = p.smem_batch + 1;
-    int32_t* sa[kNumArrays];
-#pragma unroll
-    for (int a = 0; a < kNumArrays; ++a) sa[a] = dyn + a * stride;
+    // per-request array a (computed where used: a table of 13 pointers would hold 26 of
+    // the kernel's 64 registers)
+    auto sa = [&](int a) { return dyn + a * stride; };
     if (tid == 0) {
         s_err = 0;
         s_work = 0;
@@ -166,15 +350,15 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     // global round trip costs a DRAM latency.
     if (small) {
         for (int i = tid; i <= B; i += kThreads) {
-            sa[kCu][i] = p.cu[i];
-            if (i < B) sa[kLen][i] = p.seqlens[i];
-            if (casc && i < B) sa[kFirst][i] = p.page_table[(int64_t)i * p.ld];
-            sa[kCgid][i] = -1;
+            sa(kCu)[i] = p.cu[i];
+            if (i < B) sa(kLen)[i] = p.seqlens[i];
+            if (casc && i < B) sa(kFirst)[i] = p.page_table[(int64_t)i * p.ld];
+            sa(kCgid)[i] = -1;
         }
     }
     __syncthreads();
-    const int32_t* cu = small ? sa[kCu] : p.cu;
-    const int32_t* lens = small ? sa[kLen] : p.seqlens;
+    const int32_t* cu = small ? sa(kCu) : p.cu;
+    const int32_t* lens = small ? sa(kLen) : p.seqlens;
     auto valid_req = [&](int n, int L) { return n >= 0 && n <= L && L <= p.max_kv_len && n <= p.max_q_len; };
     // each thread owns a contiguous run of requests for the counting passes
     const int chunk_req = (B + kThreads - 1) / kThreads;
@@ -211,11 +395,11 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     CascGroup* scg = reinterpret_cast<CascGroup*>(dyn + kNumArrays * stride +
                                                   2 * (casc ? (1 << casc_hash_bits(p.smem_batch)) : 0));
     if (casc) {
-        int32_t* first = sa[kFirst];
-        int32_t* leader = sa[kLeader];
-        int32_t* lcp = sa[kLcp];
-        int32_t* cnt = sa[kCnt];
-        int32_t* lim = sa[kMpos];   // pages compared per member (until the groups are numbered)
+        int32_t* first = sa(kFirst);
+        int32_t* leader = sa(kLeader);
+        int32_t* lcp = sa(kLcp);
+        int32_t* cnt = sa(kCnt);
+        int32_t* lim = sa(kMpos);   // pages compared per member (until the groups are numbered)
         const int hbits = casc_hash_bits(p.smem_batch);
         const int HT = 1 << hbits;  // > 2 * batch: the probe below always meets a free entry
         int32_t* hkey = dyn + kNumArrays * stride;
@@ -325,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
             int gid = gv[0], moff = gv[1];
             for (int i = r0; i < r1; ++i) {
                 if (!is_group_leader(leader, cnt, lcp, i, p.min_cascade_pages)) continue;
-                sa[kCgid][i] = gid;
+                sa(kCgid)[i] = gid;
                 CascGroup cg;
                 cg.leader = i;
                 cg.prefix_len = lcp[i] * ps;
@@ -340,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
                 cg.pad0 = cg.pad1 = 0;
                 store_record(&cgroups[gid], cg);
                 scg[gid] = cg;
-                sa[kMpos][i] = moff;  // next free member slot of the group
+                sa(kMpos)[i] = moff;  // next free member slot of the group
                 moff += cnt[i];
                 ++gid;
             }
@@ -351,174 +535,20 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         for (int i = tid; i < B; i += kThreads) {
             const int ld = leader[i];
             if (ld >= 0 && ld != i)
-                sa[kCgid][i] = is_group_leader(leader, cnt, lcp, ld, p.min_cascade_pages) ? sa[kCgid][ld] : -1;
+                sa(kCgid)[i] = is_group_leader(leader, cnt, lcp, ld, p.min_cascade_pages) ? sa(kCgid)[ld] : -1;
         }
         const int members1 = gt[1];  // member-list entries of the top-level groups
         __syncthreads();
-        // ---- level 2: inside a group, members keyed by the page right after the group's
-        // prefix; the lowest-numbered one leads its sub-group, whose prefix extends the
-        // group's by the run of pages every sub-member shares with it (again at least
-        // min_cascade_pages, again whole pages before each member's query).  Its prefix
-        // pass covers keys [group prefix, sub-group prefix) only.  The arrays of level 1
-        // that are no longer needed hold level 2's: the page after the prefix (kFirst),
-        // pages before the query then the sub-prefix (kLcp), counts then next free member
-        // slots (kCnt); the hash table is reused.
+        // ---- level 2: sub-groups inside each group (find_sub_groups)
         if (n_cgroups > 0) {
-            int32_t* page2 = first;
-            int32_t* pg2 = lcp;
-            int32_t* cnt2 = cnt;
-            int32_t* lead2 = sa[kLeader2];
-            int32_t* cgid2 = sa[kCgid2];  // pages compared per member until the sub-groups are numbered
-            for (int h = tid; h < HT; h += kThreads) {
-                hkey[h] = -1;
-                hval[h] = 0x7fffffff;
-            }
-            for (int i = tid; i < B; i += kThreads) {
-                const int g = sa[kCgid][i];
-                int pg = -1, pages = 0;
-                if (g >= 0) {
-                    const int n = cu[i + 1] - cu[i], L = lens[i];
-                    pages = (L - n) / ps;
-                    const int P1 = scg[g].prefix_len / ps;
-                    if (pages - P1 >= p.min_cascade_pages) {
-                        const int32_t x = p.page_table[(int64_t)i * p.ld + P1];
-                        pg = (x >= 0 && x < p.num_pages) ? x : -1;
-                    }
-                }
-                page2[i] = pg;
-                pg2[i] = pages;
-                cnt2[i] = 0;
-                lead2[i] = -1;
-                cgid2[i] = 0;
-            }
-            __syncthreads();
-            // hash key: the page mixed with the group id (two different pairs meeting on one
-            // key would only lose sharing: a member whose pair differs from its sub-leader's
-            // is dropped below)
-            auto key2 = [&](int i) -> int {
-                return page2[i] < 0 ? -1
-                                    : (int)(((uint32_t)page2[i] * 2654435761u ^ (uint32_t)sa[kCgid][i] * 0x9E3779B9u) &
-                                            0x7fffffffu);
-            };
-            for (int i0 = 0; i0 < B; i0 += kThreads) {
-                const int i = i0 + tid;
-                const int f = i < B ? key2(i) : -1;
-                const unsigned peers = __match_any_sync(0xffffffffu, f);
-                const int lead = __ffs(peers) - 1;
-                int h = 0;
-                if (f >= 0 && lane == lead) {
-                    uint32_t hh = page_hash(f, hbits);
-                    while (true) {
-                        const int prev = atomicCAS(&hkey[hh], -1, f);
-                        if (prev == -1 || prev == f) break;
-                        hh = (hh + 1) & (HT - 1);
-                    }
-                    atomicMin(&hval[hh], i);
-                    h = (int)hh;
-                }
-                h = __shfl_sync(0xffffffffu, h, lead);
-                if (f >= 0) lead2[i] = h;
-            }
-            __syncthreads();
-            for (int i0 = 0; i0 < B; i0 += kThreads) {
-                const int i = i0 + tid;
-                int ld = (i < B && page2[i] >= 0) ? hval[lead2[i]] : -1;
-                if (ld >= 0 && (sa[kCgid][ld] != sa[kCgid][i] || page2[ld] != page2[i])) ld = -1;
-                const unsigned peers = __match_any_sync(0xffffffffu, ld);
-                if (i < B) lead2[i] = ld;
-                if (ld >= 0 && lane == __ffs(peers) - 1) atomicAdd(&cnt2[ld], __popc(peers));
-            }
-            __syncthreads();
-            for (int i = tid; i < B; i += kThreads) {
-                const int ld = lead2[i];
-                cgid2[i] = (ld >= 0 && ld != i) ? min(pg2[i], pg2[ld]) : 0;
-            }
-            __syncthreads();
-            for (int i = tid; i < B; i += kThreads)
-                if (cgid2[i] > 0) atomicMin(&pg2[lead2[i]], cgid2[i]);
-            {
-                constexpr int kU = kCmpPages;
-                const int warp = tid >> 5;
-                for (int i = warp; i < B; i += kWarps) {
-                    const int l = cgid2[i];
-                    const int g = sa[kCgid][i];
-                    if (l <= 0 || g < 0) continue;  // warp-uniform
-                    const int start = scg[g].prefix_len / ps + 1;  // page start - 1 matched by the key
-                    if (l <= start) continue;
-                    const int ld = lead2[i];
-                    const int32_t* ri = p.page_table + (int64_t)i * p.ld;
-                    const int32_t* rl = p.page_table + (int64_t)ld * p.ld;
-                    int mis = l;
-                    for (int k0 = start; k0 < l; k0 += 32 * kU) {
-                        int va[kU], vb[kU];
-#pragma unroll
-                        for (int u = 0; u < kU; ++u) {
-                            const int k = k0 + u * 32 + lane;
-                            va[u] = k < l ? ri[k] : 0;
-                            vb[u] = k < l ? rl[k] : 0;
-                        }
-#pragma unroll
-                        for (int u = 0; u < kU; ++u) {
-                            const int k = k0 + u * 32 + lane;
-                            if (k < l && va[u] != vb[u]) mis = min(mis, k);
-                        }
-                    }
-                    mis = __reduce_min_sync(0xffffffffu, mis);
-                    if (lane == 0 && mis < l) atomicMin(&pg2[ld], mis);
-                }
-            }
-            __syncthreads();
-            for (int i = tid; i < B; i += kThreads) cgid2[i] = -1;
-            __syncthreads();
-            auto is_sub_leader = [&](int i) {
-                if (lead2[i] != i || cnt2[i] < 2) return false;
-                return pg2[i] - scg[sa[kCgid][i]].prefix_len / ps >= p.min_cascade_pages;
-            };
-            int hv[2] = {0, 0};
-            for (int i = r0; i < r1; ++i)
-                if (is_sub_leader(i)) {
-                    hv[0] += 1;
-                    hv[1] += cnt2[i];
-                }
-            int ht[2];
-            block_scan<2>(hv, ht, s_tmp2);
-            {
-                int gid = n_cgroups + hv[0], moff = members1 + hv[1];
-                for (int i = r0; i < r1; ++i) {
-                    if (!is_sub_leader(i)) continue;
-                    CascGroup cg;
-                    cg.leader = i;
-                    cg.key_base = scg[sa[kCgid][i]].prefix_len;
-                    cg.prefix_len = pg2[i] * ps;
-                    cg.n_members = cnt2[i];
-                    cg.member_off = moff;
-                    cg.n_chunks = 0;
-                    cg.chunk_keys = 0;
-                    cg.unit_off = 0;
-                    cg.n_units = 0;
-                    cg.level = 1;
-                    cg.pad0 = cg.pad1 = 0;
-                    store_record(&cgroups[gid], cg);
-                    scg[gid] = cg;
-                    cgid2[i] = gid;
-                    cnt2[i] = moff;  // next free member slot of the sub-group
-                    moff += cg.n_members;
-                    ++gid;
-                }
-            }
-            n_cgroups += ht[0];
-            n_sub = ht[0];
-            __syncthreads();
-            for (int i = tid; i < B; i += kThreads) {
-                const int ld = lead2[i];
-                if (ld >= 0 && ld != i) cgid2[i] = cgid2[ld];
-            }
-            __syncthreads();
+            n_sub = find_sub_groups(dyn, stride, hkey, hval, hbits, scg, cgroups, p.page_table, p.ld, p.num_pages,
+                                    p.min_cascade_pages, B, ps, r0, r1, n_cgroups, members1, s_tmp2);
+            n_cgroups += n_sub;
         }
         }  // some candidates share a first page
     }
-    auto casc_of = [&](int i) { return casc && n_cgroups > 0 ? sa[kCgid][i] : -1; };
-    auto casc2_of = [&](int i) { return casc && n_cgroups > 0 ? sa[kCgid2][i] : -1; };
+    auto casc_of = [&](int i) { return casc && n_cgroups > 0 ? sa(kCgid)[i] : -1; };
+    auto casc2_of = [&](int i) { return casc && n_cgroups > 0 ? sa(kCgid2)[i] : -1; };
     // keys before request i's decode tail: its deepest shared prefix (0 for no group)
     auto prefix_of = [&](int i) {
         const int g2 = casc2_of(i);
@@ -568,12 +598,12 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     block_scan<3>(cnt, tot3, s_tmp3);  // cnt now holds this thread's exclusive offsets
     // first prefill unit and first decode group of each request: the emission below runs
     // in parallel over units and finds a unit's request by binary search
-    int32_t* tile_off = small ? sa[kToff] : reinterpret_cast<int32_t*>(p.ws + p.lay.req_scratch);
+    int32_t* tile_off = small ? sa(kToff) : reinterpret_cast<int32_t*>(p.ws + p.lay.req_scratch);
     {
         int toff = cnt[1], goff = cnt[0];
         for (int i = r0; i < r1; ++i) {
             tile_off[i] = toff;
-            if (small) sa[kGoff][i] = goff;
+            if (small) sa(kGoff)[i] = goff;
             const int n = cu[i + 1] - cu[i], L = lens[i];
             if (n > 0 && valid_req(n, L)) {
                 if (p.use_prefill && n > TB) toff += (int)((((n + TM - 1) / TM) + 1) / 2) * Hkv;
@@ -619,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
             cg.n_chunks = (span + ck - 1) / ck;
             cg.unit_off = uoff;
             cg.n_units = cg.n_chunks * casc_pair_units(cg.n_members, TM, Hkv);
-            sa[kCUoff][g] = uoff;
+            sa(kCUoff)[g] = uoff;
             uoff += cg.n_units;
             store_record(&cgroups[g], cg);
             scg[g] = cg;
@@ -629,9 +659,9 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         // group is written below); the first-page array is free again
         // (and of its sub-group's: the slot goes to kLcp, free since level 2 was numbered)
         for (int i = tid; i < B; i += kThreads) {
-            if (sa[kCgid][i] < 0) continue;
-            sa[kFirst][i] = atomicAdd(&sa[kMpos][sa[kLeader][i]], 1);
-            if (sa[kCgid2][i] >= 0) sa[kLcp][i] = atomicAdd(&sa[kCnt][sa[kLeader2][i]], 1);
+            if (sa(kCgid)[i] < 0) continue;
+            sa(kFirst)[i] = atomicAdd(&sa(kMpos)[sa(kLeader)[i]], 1);
+            if (sa(kCgid2)[i] >= 0) sa(kLcp)[i] = atomicAdd(&sa(kCnt)[sa(kLeader2)[i]], 1);
         }
     }
     __syncthreads();
@@ -707,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         }
         // (cascade group, key chunk, pair of member tiles, kv head)
         const int y = x - tot3[1];
-        const int g = find_bucket(sa[kCUoff], n_cgroups, y);
+        const int g = find_bucket(sa(kCUoff), n_cgroups, y);
         const CascGroup cgr = scg[g];
         const int ly = y - cgr.unit_off;
         const int pu = casc_pair_units(cgr.n_members, TM, Hkv);
@@ -797,8 +827,8 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
                 // member list entries of a shared-prefix member (one new token): its q row and
                 // the partial slot of chunk 0 of each of its groups (the group's chunks first,
                 // then the sub-group's)
-                if (cg >= 0) cmembers[sa[kFirst][i]] = make_int2(dg.tok0, pi + s);
-                if (cg2 >= 0) cmembers[sa[kLcp][i]] = make_int2(dg.tok0, pi + s + scg[cg].n_chunks);
+                if (cg >= 0) cmembers[sa(kFirst)[i]] = make_int2(dg.tok0, pi + s);
+                if (cg2 >= 0) cmembers[sa(kLcp)[i]] = make_int2(dg.tok0, pi + s + scg[cg].n_chunks);
                 for (int u = 0; u < s; ++u) {
                     DecUnit du;
                     du.group = gi;
