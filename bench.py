@@ -51,21 +51,21 @@ def parse():
 # what they were at capture time; after any change the roofline reports null.
 NCU_TRAFFIC = {
     ("decode", "decode"): {
-        "bytes": 619.810048e6,
+        "bytes": 619.878144e6,
         "sources": ['paged_variable_length_gb300/csrc/decode.cu', 'paged_variable_length_gb300/csrc/device_utils.cuh', 'paged_variable_length_gb300/csrc/pva_internal.h'],
-        "sha256_16": "7a5cc1b333d7c6d5",
+        "sha256_16": "62d4e0d437e852f8",
         "summary": "profiles/decode_kernel_decode_workload.md",
     },
     ("decode", "decode-e4m3"): {
-        "bytes": 312.963584e6,
+        "bytes": 312.797952e6,
         "sources": ['paged_variable_length_gb300/csrc/decode.cu', 'paged_variable_length_gb300/csrc/device_utils.cuh', 'paged_variable_length_gb300/csrc/pva_internal.h'],
-        "sha256_16": "7a5cc1b333d7c6d5",
+        "sha256_16": "62d4e0d437e852f8",
         "summary": "profiles/decode_kernel_fp8_decode_workload.md",
     },
     ("tensor_core", "prefill"): {
-        "bytes": 220.759808e6,
+        "bytes": 220.406016e6,
         "sources": ['paged_variable_length_gb300/csrc/prefill_tc.cu', 'paged_variable_length_gb300/csrc/device_utils.cuh', 'paged_variable_length_gb300/csrc/tc_utils.cuh', 'paged_variable_length_gb300/csrc/pva_internal.h'],
-        "sha256_16": "b064b09b12e35c18",
+        "sha256_16": "987fc1f12d9ec8e5",
         "summary": "profiles/prefill_kernel_prefill_workload.md",
     },
 }
