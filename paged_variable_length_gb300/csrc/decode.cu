@@ -114,6 +114,22 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
         return;
     }
 
+    const DecUnit* units = reinterpret_cast<const DecUnit*>(p.ws + p.lay.dec_units);
+    // When every CTA of the grid starts at once (not after a tensor-core kernel, whose
+    // CTAs release SMs one by one), CTA b's first unit is unit b: its record and its
+    // first page ids (plan and page table, complete before this grid) are requested
+    // now, before the set-up and the wait below, and the work counter serves the units
+    // after the first gridDim.x.  After a tensor-core kernel the first unit comes from the
+    // counter too, so the longest units go to the CTAs that start first.
+    const bool static_first = !wait_late;
+    DecUnit du_first{};
+    int32_t page_first_raw = 0;
+    if (static_first && warp == HB && (int)blockIdx.x < n_units) {
+        du_first = units[blockIdx.x / n_hb];
+        const int key = du_first.k0 + (lane & 15);
+        if (key < du_first.k1) page_first_raw = p.page_table[(int64_t)du_first.req * p.ld + (key >> p.page_shift)];
+    }
+
     // zero the ring once so rows past a range's end are finite (they are masked,
     // and 0 * finite stays 0 in the P V product)
     for (int i = threadIdx.x * 16; i < stages * stage_bytes; i += blockDim.x * 16)
@@ -130,8 +146,8 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
     __syncthreads();
     if (!wait_late) dev::grid_dep_wait();
 
-    const DecUnit* units = reinterpret_cast<const DecUnit*>(p.ws + p.lay.dec_units);
     int32_t* sched = &hdr->pad[0];
+    const int sched_base = static_first ? (int)gridDim.x : 0;  // units taken statically
 
     if (warp == HB) {
         // ================================================================ producer
@@ -155,10 +171,25 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
             return page;
         };
         const int r = lane & 15;
-        int u = __shfl_sync(0xffffffffu, lane == 0 ? atomicAdd(sched, 1) : 0, 0);
+        int u;
         DecUnit du{};
-        if (u < n_units) du = units[u / n_hb];
         int64_t page_first = -1;  // page of the unit's first stage, when already fetched
+        if (static_first) {
+            u = min((int)blockIdx.x, n_units);
+            if (u < n_units) {
+                du = du_first;
+                if (du.k0 + r < du.k1) {
+                    page_first = page_first_raw;
+                    if (page_first < 0 || page_first >= p.num_pages) {
+                        dev::set_error(err, kErrPage);
+                        page_first = 0;  // keep the transaction count; the result is flagged
+                    }
+                }
+            }
+        } else {
+            u = __shfl_sync(0xffffffffu, lane == 0 ? atomicAdd(sched, 1) : 0, 0);
+            if (u < n_units) du = units[u / n_hb];
+        }
         while (true) {
             if (!dev::mbar_wait(&sh->empty[stage], phase ^ 1)) {
                 abort_cta(sh, err);
@@ -187,7 +218,7 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
             DecUnit du_next{};
             for (int si_ = 0; si_ < nst; ++si_) {
                 const int k = du.k0 + si_ * kStageKeys;
-                if (si_ == max(nst - 4, 0) && lane == 0) ticket = atomicAdd(sched, 1);
+                if (si_ == max(nst - 4, 0) && lane == 0) ticket = sched_base + atomicAdd(sched, 1);
                 if (si_ == max(nst - 2, 0)) {
                     u_next = __shfl_sync(0xffffffffu, ticket, 0);
                     if (u_next < n_units) du_next = units[u_next / n_hb];
