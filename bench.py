@@ -51,15 +51,15 @@ def parse():
 # what they were at capture time; after any change the roofline reports null.
 NCU_TRAFFIC = {
     ("decode", "decode"): {
-        "bytes": 619.878144e6,
+        "bytes": 620.172544e6,
         "sources": ['paged_variable_length_gb300/csrc/decode.cu', 'paged_variable_length_gb300/csrc/device_utils.cuh', 'paged_variable_length_gb300/csrc/pva_internal.h'],
-        "sha256_16": "62d4e0d437e852f8",
+        "sha256_16": "f90b197f7fbf69d0",
         "summary": "profiles/decode_kernel_decode_workload.md",
     },
     ("decode", "decode-e4m3"): {
-        "bytes": 312.797952e6,
+        "bytes": 312.732928e6,
         "sources": ['paged_variable_length_gb300/csrc/decode.cu', 'paged_variable_length_gb300/csrc/device_utils.cuh', 'paged_variable_length_gb300/csrc/pva_internal.h'],
-        "sha256_16": "62d4e0d437e852f8",
+        "sha256_16": "f90b197f7fbf69d0",
         "summary": "profiles/decode_kernel_fp8_decode_workload.md",
     },
     ("tensor_core", "prefill"): {
