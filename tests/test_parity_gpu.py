@@ -485,3 +485,53 @@ def test_ragged_full_size_workload():
     ref_o, ref_l = oracle.attention(t["q"].cpu(), t["k"].cpu(), t["v"].cpu(), wl.cu_seqlens_q, wl.cache_seqlens,
                                     wl.page_table, 1, row_select=sel)
     assert_close(out, lse, ref_o, ref_l, mask=sel)
+
+
+def _random_forest(seed, Hq=32, Hkv=8, D=128, ps=16, min_pages=8):
+    """Random shared-prefix forests: 1-3 roots of min_pages-1 .. min_pages+5 pages (some too
+    short for a group), each with 1-3 branches of min_pages-1 .. min_pages+3 further
+    pages, leaves that sometimes share a third run (a level below the second: it must run
+    as part of their tails), leaves cut short inside a shared run, multi-token decodes
+    (never prefix members), unrelated decodes and a prefill."""
+    rng = np.random.default_rng(1000 + seed)
+    P = 4000
+    perm = [int(x) for x in rng.permutation(P)]
+    take = lambda k: [perm.pop() for _ in range(int(k))]
+    rows, ql, kl = [], [], []
+
+    def add(shared, tail, n=1):
+        L = len(shared) * ps + tail
+        rows.append(shared + take((L + ps - 1) // ps - len(shared)))
+        ql.append(n)
+        kl.append(L)
+
+    for _ in range(int(rng.integers(1, 4))):
+        root = take(rng.integers(min_pages - 1, min_pages + 6))
+        for _ in range(int(rng.integers(1, 5))):
+            branch = root + take(rng.integers(min_pages - 1, min_pages + 4))
+            third = branch + take(rng.integers(1, 12)) if rng.random() < 0.4 else None
+            for _ in range(int(rng.integers(2, 7))):
+                shared = third if third is not None and rng.random() < 0.6 else branch
+                if rng.random() < 0.2:  # shares only part of the run
+                    shared = shared[:int(rng.integers(1, len(shared) + 1))]
+                n = 1 if rng.random() < 0.85 else int(rng.integers(2, 4))
+                add(shared, int(rng.integers(n, 60)), n)
+    for _ in range(int(rng.integers(0, 4))):  # unrelated decodes
+        add([], int(rng.integers(1, 700)))
+    L = int(rng.integers(20, 300))             # a prefill
+    rows.append(take((L + ps - 1) // ps)); ql.append(L); kl.append(L)
+    order = rng.permutation(len(rows))          # requests in any order
+    rows = [rows[i] for i in order]
+    ql = [ql[i] for i in order]
+    kl = [kl[i] for i in order]
+    return _table_workload(ql, kl, rows, Hq, Hkv, D, ps, P, seed)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_prefix_forests(seed):
+    layouts = [(32, 8, 128), (28, 4, 128), (16, 4, 64), (32, 32, 128)]
+    Hq, Hkv, D = layouts[seed % len(layouts)]
+    wl = _random_forest(seed, Hq=Hq, Hkv=Hkv, D=D)
+    _, eng = _full_check(wl)
+    assert pva.attn_debug_plan_counts(eng.meta)["casc_groups"] >= 1
+    _full_check(wl, enable_cascade=False)
