@@ -83,6 +83,8 @@ Layout make_layout(const pva_config* c, int sm_count, int target_units = 0) {
     L.req_scratch = take(sizeof(int32_t) * 4 * (size_t)(c->max_batch + 1));
     L.casc_groups = take(sizeof(CascGroup) * (size_t)L.max_casc_groups);
     L.casc_members = take(sizeof(int32_t) * 2 * 2 * (size_t)c->max_batch);  // (token, slot) per member per level
+    L.dec_ctas = sm_count * cps;
+    L.dec_first = take(sizeof(int32_t) * ((size_t)L.dec_ctas + 1));
     L.total = off;
     return L;
 }
@@ -199,7 +201,7 @@ pva_status prepare_in_workspace(const pva_config* cfg, const int32_t* cu_seqlens
     const bool tc_ok = prefill_supported(cfg->num_qo_heads, cfg->num_kv_heads, cfg->head_dim);
     h.use_prefill = (mq > TB && tc_ok) ? 1 : 0;
     h.use_cascade = (cfg->enable_cascade && tc_ok && batch >= 2 && batch <= kCascadeMaxBatch) ? 1 : 0;
-    h.dec_ctas = sms * decode_ctas_per_sm(cfg->num_kv_heads, cfg->head_dim);
+    h.dec_ctas = lay.dec_ctas;  // sms x decode CTAs per SM; the plan's balanced split assumes it
     {
         const int64_t TM = kPreRows / G;
         const int64_t bound = ((int64_t)total_tokens / TM + batch + 1) * cfg->num_kv_heads;

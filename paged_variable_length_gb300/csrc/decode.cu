@@ -55,7 +55,7 @@
 namespace pva {
 namespace {
 
-constexpr int kMaxKvHeads = 8;
+constexpr int kMaxKvHeads = kDecHeadBlock;
 constexpr int kStageKeys = kDecKeysPerStage;  // 16
 constexpr int kRowPad = 16;                    // bytes between consecutive staged rows beyond Hkv*D*2
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -115,19 +115,61 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
     }
 
     const DecUnit* units = reinterpret_cast<const DecUnit*>(p.ws + p.lay.dec_units);
+    const DecGroup* dgroups = reinterpret_cast<const DecGroup*>(p.ws + p.lay.dec_groups);
+    // Balanced split (share > 0, planned only when no tensor-core unit precedes this grid):
+    // the decode groups' keys lie end to end on one line, each group padded to whole
+    // stages, and this CTA takes the line's keys [line_lo, line_hi).  Its pieces are cut
+    // from the group records; a piece that starts at a share boundary inside a group is
+    // that group's split (boundary index - index of the boundary before the group).
+    const int share = hdr->dec_share;
+    const int n_groups = hdr->n_dec_groups;
+    const int line_lo = (int)blockIdx.x * share, line_hi = line_lo + share;
+    auto piece = [&](int g, const DecGroup& dg, DecUnit& du) -> bool {
+        const int ext = dg.kv_end - dg.tail0;
+        const int a = max(dg.g0, line_lo), e = min(dg.g0 + ext, line_hi);
+        if (a >= e) return false;
+        du.group = g;
+        du.k0 = dg.tail0 + (a - dg.g0);
+        du.k1 = dg.tail0 + (e - dg.g0);
+        du.split = a == dg.g0 ? 0 : (int)blockIdx.x - dg.g0 / share;
+        du.req = dg.req;
+        du.tok0 = dg.tok0;
+        du.ntok = dg.ntok;
+        du.qpos0 = dg.qpos0;
+        du.nsplit = dg.nsplit;
+        du.pbase = dg.pbase;
+        du.nparts = dg.nparts;
+        du.pad1 = 0;
+        return true;
+    };
     // When every CTA of the grid starts at once (not after a tensor-core kernel, whose
-    // CTAs release SMs one by one), CTA b's first unit is unit b: its record and its
-    // first page ids (plan and page table, complete before this grid) are requested
-    // now, before the set-up and the wait below, and the work counter serves the units
-    // after the first gridDim.x.  After a tensor-core kernel the first unit comes from the
-    // counter too, so the longest units go to the CTAs that start first.
-    const bool static_first = !wait_late;
+    // CTAs release SMs one by one), this CTA's first piece -- unit b of the queue, or the
+    // start of its share of the line -- and its first page ids (plan and page table,
+    // complete before this grid) are requested now, before the set-up and the wait below;
+    // the work counter serves the queue's units after the first gridDim.x.  After a
+    // tensor-core kernel the first unit comes from the counter too, so the longest units
+    // go to the CTAs that start first.
+    const bool static_first = !wait_late || share > 0;  // (a balanced plan has no tensor-core unit)
     DecUnit du_first{};
+    bool have_first = false;
+    int g_first = -1;
     int32_t page_first_raw = 0;
-    if (static_first && warp == HB && (int)blockIdx.x < n_units) {
-        du_first = units[blockIdx.x / n_hb];
+    if (static_first && warp == HB) {
+        if (share > 0) {
+            int g = reinterpret_cast<const int32_t*>(p.ws + p.lay.dec_first)[blockIdx.x];
+            if (g < n_groups) {
+                have_first = piece(g, dgroups[g], du_first);
+                // the share starts in the group's padding: the next group
+                if (!have_first && ++g < n_groups) have_first = piece(g, dgroups[g], du_first);
+            }
+            g_first = g;
+        } else if ((int)blockIdx.x < n_units) {
+            du_first = units[blockIdx.x / n_hb];
+            have_first = true;
+        }
         const int key = du_first.k0 + (lane & 15);
-        if (key < du_first.k1) page_first_raw = p.page_table[(int64_t)du_first.req * p.ld + (key >> p.page_shift)];
+        if (have_first && key < du_first.k1)
+            page_first_raw = p.page_table[(int64_t)du_first.req * p.ld + (key >> p.page_shift)];
     }
 
     // zero the ring once so rows past a range's end are finite (they are masked,
@@ -174,8 +216,9 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
         int u;
         DecUnit du{};
         int64_t page_first = -1;  // page of the unit's first stage, when already fetched
+        int g_cur = g_first;  // balanced split: the group of the current piece
         if (static_first) {
-            u = min((int)blockIdx.x, n_units);
+            u = have_first ? (share > 0 ? 0 : (int)blockIdx.x) : n_units;
             if (u < n_units) {
                 du = du_first;
                 if (du.k0 + r < du.k1) {
@@ -214,14 +257,22 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
             int64_t page_next = page_first >= 0 ? page_first : ((du.k0 + r < du.k1) ? page_of(prow, du.k0 + r) : 0);
             page_first = -1;
             const int nst = (du.k1 - du.k0 + kStageKeys - 1) / kStageKeys;
-            int ticket = 0, u_next = n_units;
+            int ticket = 0, u_next = n_units, g_next = g_cur;
             DecUnit du_next{};
             for (int si_ = 0; si_ < nst; ++si_) {
                 const int k = du.k0 + si_ * kStageKeys;
-                if (si_ == max(nst - 4, 0) && lane == 0) ticket = sched_base + atomicAdd(sched, 1);
+                if (share == 0 && si_ == max(nst - 4, 0) && lane == 0) ticket = sched_base + atomicAdd(sched, 1);
                 if (si_ == max(nst - 2, 0)) {
-                    u_next = __shfl_sync(0xffffffffu, ticket, 0);
-                    if (u_next < n_units) du_next = units[u_next / n_hb];
+                    if (share > 0) {  // the next group's piece of this CTA's share, if any
+                        const int gn = g_cur + 1;
+                        if (gn < n_groups && piece(gn, dgroups[gn], du_next)) {
+                            u_next = 0;
+                            g_next = gn;
+                        }
+                    } else {
+                        u_next = __shfl_sync(0xffffffffu, ticket, 0);
+                        if (u_next < n_units) du_next = units[u_next / n_hb];
+                    }
                 }
                 const int64_t page = page_next;
                 if (k + kStageKeys + r < du.k1) {
@@ -281,6 +332,7 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
             }
             u = u_next;
             du = du_next;
+            g_cur = g_next;
         }
     producer_done:
         // drain: every copy this warp issued must land before the CTA may exit

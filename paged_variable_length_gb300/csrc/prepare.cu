@@ -33,7 +33,8 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBuckets = 256;  // cost classes for the longest-first ordering of work items
-constexpr int kCmpPages = 8;   // page ids a lane compares per step of the shared-prefix search
+constexpr int kCmpPages = 8;
+constexpr int kLineLimit = 1 << 29;  // the balanced decode split is used below this many keys   // page ids a lane compares per step of the shared-prefix search
 
 // Per-request shared-memory arrays (dynamic shared memory, batch <= smem_batch), followed
 // by the open-addressing table of the shared-prefix search when cascade detection runs.
@@ -564,8 +565,8 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
 
     // ---- pass 1: validate, count decode groups and prefill tiles, sum decode key extents
     uint32_t err = 0;
-    int cnt[3] = {0, 0, 0};  // decode groups, prefill tile pairs x kv heads, (unused)
-    unsigned long long work = 0;
+    int cnt[3] = {0, 0, 0};  // decode groups, prefill tile pairs x kv heads, decode key line
+    unsigned long long work = 0, line = 0;
     int max_ntok = 0;
     if (tid == 0 && p.cu[0] != 0) err |= kErrCu;
     if (tid == 0 && B > p.max_batch) err |= kErrLimits;
@@ -585,9 +586,14 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
             cnt[0] += ng;
             max_ntok = max(max_ntok, min(n, TB));
             const int lp = prefix_of(i);
-            for (int g = 0; g < ng; ++g) work += (unsigned long long)(L - n + min((g + 1) * TB, n) - lp);
+            for (int g = 0; g < ng; ++g) {
+                const int ext = L - n + min((g + 1) * TB, n) - lp;
+                work += (unsigned long long)ext;
+                line += (unsigned long long)((ext + kDecKeysPerStage - 1) / kDecKeysPerStage * kDecKeysPerStage);
+            }
         }
     }
+    cnt[2] = (int)min(line, (unsigned long long)kLineLimit);
     if (err) atomicOr(&s_err, err);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) work += __shfl_xor_sync(0xffffffffu, work, o);
@@ -679,6 +685,18 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         c = (c + kDecKeysPerStage - 1) / kDecKeysPerStage * kDecKeysPerStage;
         chunk = (int)(c > (unsigned long long)kMinSplitChunk ? c : (unsigned long long)kMinSplitChunk);
     }
+    // ---- balanced split: with no tensor-core unit every decode CTA starts at once, so the
+    // decode groups' keys (each group padded to whole 16-key stages) are laid end to end on
+    // one line and CTA c takes the line's keys [c * share, (c + 1) * share): equal work per
+    // CTA, and a group is cut only where a CTA's share ends (fewer partials than queued
+    // units of one chunk each, which also left the grid's last units as a tail).  The
+    // decode kernel cuts its pieces from the group records (g0: the group's start on the
+    // line) and dec_first (the group the CTA's share starts in).
+    int share = 0;
+    if (p.split_kv && tiles_total == 0 && Hkv <= kDecHeadBlock && s_work > 0 && s_work < kLineLimit / 2) {
+        const int per_cta = (tot3[2] + p.lay.dec_ctas - 1) / p.lay.dec_ctas;
+        share = max(kMinDecShare, (per_cta + kDecKeysPerStage - 1) / kDecKeysPerStage * kDecKeysPerStage);
+    }
 
     // ---- pass 2: units and partial slots per thread's requests, and the unit cost
     // histogram (a group's units all have length `per` but the last)
@@ -689,6 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     __syncthreads();
     int cnt2[2] = {0, 0};  // units, partial slots
     if (!fatal) {
+        int g0 = cnt[2];  // balanced split: this thread's first group's start on the line
         for (int i = r0; i < r1; ++i) {
             const int n = cu[i + 1] - cu[i], L = lens[i];
             if (n <= 0 || (p.use_prefill && n > TB)) continue;
@@ -697,6 +716,13 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
             const int npre = prefix_parts(i);
             for (int g = 0; g < ng; ++g) {
                 const int ext = L - n + min((g + 1) * TB, n) - lp;
+                if (share > 0) {  // pieces: one, plus one per CTA share boundary inside the group
+                    const int pieces = 1 + (g0 + ext - 1) / share - g0 / share;
+                    cnt2[0] += pieces;
+                    if (pieces > 1) cnt2[1] += pieces;
+                    g0 += (ext + kDecKeysPerStage - 1) / kDecKeysPerStage * kDecKeysPerStage;
+                    continue;
+                }
                 int per;
                 const int s = split_ranges(ext, chunk, &per);
                 const int nparts = s + npre;
@@ -797,6 +823,11 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     __syncthreads();
     if (run) {
         int gi = cnt[0], pi = cnt2[1];
+        int g0 = cnt[2];  // balanced split: start of this thread's first group on the line
+        int32_t* dec_first = reinterpret_cast<int32_t*>(p.ws + p.lay.dec_first);
+        if (share > 0 && tid == 0) {  // CTAs whose share starts past the line: no group
+            for (int c = (tot3[2] + share - 1) / share; c <= p.lay.dec_ctas; ++c) dec_first[c] = tot3[0];
+        }
         for (int i = r0; i < r1; ++i) {
             const int c0 = cu[i], n = cu[i + 1] - c0, L = lens[i];
             if (n <= 0) continue;
@@ -808,8 +839,11 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
             for (int g = 0; g < ng; ++g) {
                 const int a0 = g * TB, na = min(TB, n - a0);
                 const int kv_end = L - n + a0 + na;
-                int per;
-                const int s = split_ranges(kv_end - lp, chunk, &per);
+                int per = 0;
+                const int ext = kv_end - lp;
+                // balanced split: pieces cut where a CTA's share ends (no unit records: the
+                // decode kernel cuts them); otherwise units of `per` keys
+                const int s = share > 0 ? 1 + (g0 + ext - 1) / share - g0 / share : split_ranges(ext, chunk, &per);
                 const int nparts = s + npre;
                 DecGroup dg;
                 dg.req = i;
@@ -822,8 +856,19 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
                 dg.casc = cg;
                 dg.nparts = nparts;
                 dg.tail0 = lp;
-                dg.pad0 = dg.pad1 = dg.pad2 = dg.pad3 = dg.pad4 = dg.pad5 = 0;
+                dg.g0 = share > 0 ? g0 : 0;
+                dg.pad1 = dg.pad2 = dg.pad3 = dg.pad4 = dg.pad5 = 0;
                 store_record(&groups[gi], dg);
+                if (share > 0) {
+                    // the CTAs whose share starts inside this group's stretch of the line
+                    const int e16 = g0 + (ext + kDecKeysPerStage - 1) / kDecKeysPerStage * kDecKeysPerStage;
+                    for (int c = (g0 + share - 1) / share; c * share < e16 && c <= p.lay.dec_ctas; ++c)
+                        dec_first[c] = gi;
+                    g0 = e16;
+                    if (nparts > 1) pi += nparts;
+                    ++gi;
+                    continue;
+                }
                 // member list entries of a shared-prefix member (one new token): its q row and
                 // the partial slot of chunk 0 of each of its groups (the group's chunks first,
                 // then the sub-group's)
@@ -893,6 +938,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         hdr->n_casc_tiles = ok ? s_casc_units : 0;
         hdr->n_casc_units = ok ? s_casc_units : 0;
         hdr->max_group_tokens = ok ? s_max_ntok : 0;
+        hdr->dec_share = ok ? share : 0;
     }
 }
 

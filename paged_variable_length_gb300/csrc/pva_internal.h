@@ -23,6 +23,8 @@ constexpr int kPreKeys = 128;
 constexpr int kMinSplitChunk = 256;
 // Most key chunks one shared prefix is cut into for the cascade prefix pass.
 constexpr int kMaxCascChunks = 8;
+constexpr int kDecHeadBlock = 8;     // kv heads one decode CTA serves (more: several CTAs per unit)
+constexpr int kMinDecShare = 128;    // fewest keys a decode CTA gets in the balanced split
 
 // Error bits the kernels OR into the plan's error word (same values as pva.h).
 constexpr uint32_t kErrCu = PVA_DEVERR_CU_SEQLENS;
@@ -48,7 +50,8 @@ struct PlanHeader {
     int32_t n_partial_slots;
     int32_t n_casc_units;
     int32_t max_group_tokens;  // most tokens in one decode group (bounds the merge's rows)
-    int32_t pad[54];           // pad[0] / pad[1]: decode / tensor-core work counters
+    int32_t dec_share;         // keys per decode CTA of the balanced split; 0: the work queue
+    int32_t pad[53];           // pad[0] / pad[1]: decode / tensor-core work counters
 };
 static_assert(sizeof(PlanHeader) == 256, "header is one 256-byte line");
 
@@ -65,7 +68,8 @@ struct DecGroup {
     int32_t casc;        // cascade group id feeding prefix partials, or -1
     int32_t nparts;      // partial slots of the group (see DecUnit::nparts)
     int32_t tail0;       // first key the decode units cover (the prefix length of a cascade member)
-    int32_t pad0, pad1, pad2, pad3, pad4, pad5;
+    int32_t g0;          // balanced split: first key of the group in the batch's key line
+    int32_t pad1, pad2, pad3, pad4, pad5;
 };
 static_assert(sizeof(DecGroup) == 64, "DecGroup is one 64-byte record");
 
@@ -136,6 +140,7 @@ struct Layout {
     size_t req_scratch;  // int32 [max_batch * 4] prepare scratch
     size_t casc_groups;  // CascGroup [max_casc_groups]
     size_t casc_members; // int2 [max_batch]: member's token, partial slot of its prefix chunk 0
+    size_t dec_first;    // int32 [dec_ctas + 1]: balanced split, first group of each CTA's keys
     size_t total;
     int32_t max_dec_units;
     int32_t max_dec_groups;
@@ -145,6 +150,7 @@ struct Layout {
     int32_t target_units;
     int32_t max_casc_groups;
     int32_t casc_target;  // prefix-pass units aimed for (about one per SM)
+    int32_t dec_ctas;     // CTAs of the decode grid
 };
 
 // Parameters of the prepare kernel (by value).
