@@ -311,6 +311,49 @@ __device__ __noinline__ int find_sub_groups(int32_t* dyn, int stride, int32_t* h
     return n_new;
 }
 
+// Pass 3 of the balanced decode split (see the kernel below): the decode groups of this
+// thread's requests with their start on the key line (g0) and their pieces (one, plus one
+// per CTA share boundary inside the group), and dec_first: for every CTA whose share
+// starts inside a group's stretch of the line, that group.  No unit records: the decode
+// kernel cuts the pieces.  Not inlined, so that its registers do not weigh on the rest of
+// the kernel.  (A balanced plan has no tensor-core unit, hence no shared-prefix group.)
+__device__ __noinline__ void emit_balanced_groups(const PrepareParams& p, const int32_t* cu, const int32_t* lens,
+                                                  int r0, int r1, int TB, int gi, int pi, int g0, int share,
+                                                  int line, int n_groups, DecGroup* groups) {
+    int32_t* dec_first = reinterpret_cast<int32_t*>(p.ws + p.lay.dec_first);
+    if (threadIdx.x == 0)  // CTAs whose share starts past the line: no group
+        for (int c = (line + share - 1) / share; c <= p.lay.dec_ctas; ++c) dec_first[c] = n_groups;
+    for (int i = r0; i < r1; ++i) {
+        const int c0 = cu[i], n = cu[i + 1] - c0, L = lens[i];
+        if (n <= 0 || (p.use_prefill && n > TB)) continue;
+        const int ng = (n + TB - 1) / TB;
+        for (int g = 0; g < ng; ++g) {
+            const int a0 = g * TB, na = min(TB, n - a0);
+            const int kv_end = L - n + a0 + na;
+            const int pieces = 1 + (g0 + kv_end - 1) / share - g0 / share;
+            DecGroup dg;
+            dg.req = i;
+            dg.tok0 = c0 + a0;
+            dg.ntok = na;
+            dg.qpos0 = L - n + a0;
+            dg.nsplit = pieces;
+            dg.pbase = pieces > 1 ? pi : -1;
+            dg.kv_end = kv_end;
+            dg.casc = -1;
+            dg.nparts = pieces;
+            dg.tail0 = 0;
+            dg.g0 = g0;
+            dg.pad1 = dg.pad2 = dg.pad3 = dg.pad4 = dg.pad5 = 0;
+            store_record(&groups[gi], dg);
+            const int e16 = g0 + (kv_end + kDecKeysPerStage - 1) / kDecKeysPerStage * kDecKeysPerStage;
+            for (int c = (g0 + share - 1) / share; c * share < e16 && c <= p.lay.dec_ctas; ++c) dec_first[c] = gi;
+            g0 = e16;
+            if (pieces > 1) pi += pieces;
+            ++gi;
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws + p.lay.header);
     DecUnit* units = reinterpret_cast<DecUnit*>(p.ws + p.lay.dec_units);
@@ -329,6 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     __shared__ int s_hist_t[kBuckets];
     __shared__ int s_casc_units;
     __shared__ int s_max_ntok;
+    __shared__ int s_share;  // balanced decode split: keys per CTA (0: the unit queue)
+    __shared__ int s_line;   // balanced decode split: length of the key line
 
     const int tid = threadIdx.x;
     const int B = p.batch;
@@ -692,10 +737,15 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     // units of one chunk each, which also left the grid's last units as a tail).  The
     // decode kernel cuts its pieces from the group records (g0: the group's start on the
     // line) and dec_first (the group the CTA's share starts in).
-    int share = 0;
-    if (p.split_kv && tiles_total == 0 && Hkv <= kDecHeadBlock && s_work > 0 && s_work < kLineLimit / 2) {
-        const int per_cta = (tot3[2] + p.lay.dec_ctas - 1) / p.lay.dec_ctas;
-        share = max(kMinDecShare, (per_cta + kDecKeysPerStage - 1) / kDecKeysPerStage * kDecKeysPerStage);
+    // (kept in shared memory and read where used: this kernel has 64 registers a thread)
+    if (tid == 0) {
+        int share = 0;
+        if (p.split_kv && tiles_total == 0 && Hkv <= kDecHeadBlock && s_work > 0 && s_work < kLineLimit / 2) {
+            const int per_cta = (tot3[2] + p.lay.dec_ctas - 1) / p.lay.dec_ctas;
+            share = max(kMinDecShare, (per_cta + kDecKeysPerStage - 1) / kDecKeysPerStage * kDecKeysPerStage);
+        }
+        s_share = share;
+        s_line = tot3[2];
     }
 
     // ---- pass 2: units and partial slots per thread's requests, and the unit cost
@@ -707,6 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     __syncthreads();
     int cnt2[2] = {0, 0};  // units, partial slots
     if (!fatal) {
+        const int share = s_share;
         int g0 = cnt[2];  // balanced split: this thread's first group's start on the line
         for (int i = r0; i < r1; ++i) {
             const int n = cu[i + 1] - cu[i], L = lens[i];
@@ -821,13 +872,10 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         }
     }
     __syncthreads();
-    if (run) {
+    if (run && s_share > 0) {
+        emit_balanced_groups(p, cu, lens, r0, r1, TB, cnt[0], cnt2[1], cnt[2], s_share, s_line, tot3[0], groups);
+    } else if (run) {
         int gi = cnt[0], pi = cnt2[1];
-        int g0 = cnt[2];  // balanced split: start of this thread's first group on the line
-        int32_t* dec_first = reinterpret_cast<int32_t*>(p.ws + p.lay.dec_first);
-        if (share > 0 && tid == 0) {  // CTAs whose share starts past the line: no group
-            for (int c = (tot3[2] + share - 1) / share; c <= p.lay.dec_ctas; ++c) dec_first[c] = tot3[0];
-        }
         for (int i = r0; i < r1; ++i) {
             const int c0 = cu[i], n = cu[i + 1] - c0, L = lens[i];
             if (n <= 0) continue;
@@ -839,11 +887,8 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
             for (int g = 0; g < ng; ++g) {
                 const int a0 = g * TB, na = min(TB, n - a0);
                 const int kv_end = L - n + a0 + na;
-                int per = 0;
-                const int ext = kv_end - lp;
-                // balanced split: pieces cut where a CTA's share ends (no unit records: the
-                // decode kernel cuts them); otherwise units of `per` keys
-                const int s = share > 0 ? 1 + (g0 + ext - 1) / share - g0 / share : split_ranges(ext, chunk, &per);
+                int per;
+                const int s = split_ranges(kv_end - lp, chunk, &per);
                 const int nparts = s + npre;
                 DecGroup dg;
                 dg.req = i;
@@ -856,19 +901,9 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
                 dg.casc = cg;
                 dg.nparts = nparts;
                 dg.tail0 = lp;
-                dg.g0 = share > 0 ? g0 : 0;
+                dg.g0 = 0;
                 dg.pad1 = dg.pad2 = dg.pad3 = dg.pad4 = dg.pad5 = 0;
                 store_record(&groups[gi], dg);
-                if (share > 0) {
-                    // the CTAs whose share starts inside this group's stretch of the line
-                    const int e16 = g0 + (ext + kDecKeysPerStage - 1) / kDecKeysPerStage * kDecKeysPerStage;
-                    for (int c = (g0 + share - 1) / share; c * share < e16 && c <= p.lay.dec_ctas; ++c)
-                        dec_first[c] = gi;
-                    g0 = e16;
-                    if (nparts > 1) pi += nparts;
-                    ++gi;
-                    continue;
-                }
                 // member list entries of a shared-prefix member (one new token): its q row and
                 // the partial slot of chunk 0 of each of its groups (the group's chunks first,
                 // then the sub-group's)
@@ -938,7 +973,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         hdr->n_casc_tiles = ok ? s_casc_units : 0;
         hdr->n_casc_units = ok ? s_casc_units : 0;
         hdr->max_group_tokens = ok ? s_max_ntok : 0;
-        hdr->dec_share = ok ? share : 0;
+        hdr->dec_share = ok ? s_share : 0;
     }
 }
 
