@@ -51,21 +51,21 @@ def parse():
 # what they were at capture time; after any change the roofline reports null.
 NCU_TRAFFIC = {
     ("decode", "decode"): {
-        "bytes": 620.172544e6,
+        "bytes": 617.566208e6,
         "sources": ['paged_variable_length_gb300/csrc/decode.cu', 'paged_variable_length_gb300/csrc/device_utils.cuh', 'paged_variable_length_gb300/csrc/pva_internal.h'],
-        "sha256_16": "f90b197f7fbf69d0",
+        "sha256_16": "504bbaf9b8038139",
         "summary": "profiles/decode_kernel_decode_workload.md",
     },
     ("decode", "decode-e4m3"): {
-        "bytes": 312.732928e6,
+        "bytes": 310.656512e6,
         "sources": ['paged_variable_length_gb300/csrc/decode.cu', 'paged_variable_length_gb300/csrc/device_utils.cuh', 'paged_variable_length_gb300/csrc/pva_internal.h'],
-        "sha256_16": "f90b197f7fbf69d0",
+        "sha256_16": "504bbaf9b8038139",
         "summary": "profiles/decode_kernel_fp8_decode_workload.md",
     },
     ("tensor_core", "prefill"): {
-        "bytes": 220.406016e6,
+        "bytes": 220.372992e6,
         "sources": ['paged_variable_length_gb300/csrc/prefill_tc.cu', 'paged_variable_length_gb300/csrc/device_utils.cuh', 'paged_variable_length_gb300/csrc/tc_utils.cuh', 'paged_variable_length_gb300/csrc/pva_internal.h'],
-        "sha256_16": "987fc1f12d9ec8e5",
+        "sha256_16": "2c8ba785af2836db",
         "summary": "profiles/prefill_kernel_prefill_workload.md",
     },
 }
