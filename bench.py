@@ -53,13 +53,13 @@ NCU_TRAFFIC = {
     ("decode", "decode"): {
         "bytes": 617.566208e6,
         "sources": ['paged_variable_length_gb300/csrc/decode.cu', 'paged_variable_length_gb300/csrc/device_utils.cuh', 'paged_variable_length_gb300/csrc/pva_internal.h'],
-        "sha256_16": "504bbaf9b8038139",
+        "sha256_16": "833ec089899ee64a",
         "summary": "profiles/decode_kernel_decode_workload.md",
     },
     ("decode", "decode-e4m3"): {
         "bytes": 310.656512e6,
         "sources": ['paged_variable_length_gb300/csrc/decode.cu', 'paged_variable_length_gb300/csrc/device_utils.cuh', 'paged_variable_length_gb300/csrc/pva_internal.h'],
-        "sha256_16": "504bbaf9b8038139",
+        "sha256_16": "833ec089899ee64a",
         "summary": "profiles/decode_kernel_fp8_decode_workload.md",
     },
     ("tensor_core", "prefill"): {

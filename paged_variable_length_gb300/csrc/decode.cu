@@ -10,10 +10,14 @@
 // scheme "Variable-length batching and one mixed forward pass" (Exercises,
 // answer 2) names for decode batches.
 //
-// GB300 design (one CTA per SM-slot, persistent, dynamic work fetch):
+// GB300 design (one CTA per SM-slot, persistent):
 //   * a work unit is (decode group, key range); a group is up to floor(16/G)
 //     consecutive new tokens of one request, all q heads;
-//   * producer warp: fetches units with an atomic counter, and for every
+//   * work distribution: when no tensor-core pass precedes the grid (every CTA starts
+//     at once), a balanced split -- the groups' keys on one line, each CTA an equal
+//     share, the pieces cut from the group records; otherwise a queue of split-KV
+//     chunks, longest first, taken with an atomic counter by CTAs as they start;
+//   * producer warp: takes its pieces or units, and for every
 //     16-key stage issues one bulk async copy (TMA, 1-D) per key row --
 //     Hkv*D bf16 = all kv heads of one slot, 1-2 KiB contiguous in the pool --
 //     for K and for V into a ring of shared-memory stages (mbarrier
