@@ -56,7 +56,11 @@ Layout make_layout(const pva_config* c, int sm_count, int target_units = 0) {
     L.max_pre_tiles = (int32_t)((c->max_tokens / TM + c->max_batch + 1) * (int64_t)c->num_kv_heads);
     // two levels of groups (top level and sub-groups), each at most one per two requests
     L.max_casc_groups = c->enable_cascade ? c->max_batch + 1 : 1;
-    L.casc_target = sm_count;
+    // prefix-pass units aimed for: about one per two SMs.  The decode kernel's tails start
+    // on the SMs the prefix pass leaves free, so fewer, longer prefix units (their fixed
+    // costs spread over more key tiles) overlap with the tails: cascade step 101 -> 93 us,
+    // FP8 99 -> 87 us, against one unit per SM (one per four: 86 / 97 us)
+    L.casc_target = sm_count / 2;
     if (c->enable_cascade) {
         // every member of a group takes one partial slot per prefix chunk of each of its
         // (up to two) groups, at most kMaxCascChunks in all (with sub-groups in a batch each

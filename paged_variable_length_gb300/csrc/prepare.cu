@@ -665,7 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     }
 
     // ---- cascade groups: key chunks of each prefix (about casc_target prefix-pass units
-    // in total, roughly one per SM), unit ranges, member lists.  A member takes one
+    // in total, roughly one per two SMs), unit ranges, member lists.  A member takes one
     // partial slot per chunk of each of its groups; with sub-groups in the batch each
     // level gets at most half the chunks, so no member needs more than kMaxCascChunks.
     if (casc && n_cgroups > 0) {

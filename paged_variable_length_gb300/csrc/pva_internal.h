@@ -149,7 +149,7 @@ struct Layout {
     int32_t rows_per_slot;
     int32_t target_units;
     int32_t max_casc_groups;
-    int32_t casc_target;  // prefix-pass units aimed for (about one per SM)
+    int32_t casc_target;  // prefix-pass units aimed for (about one per two SMs)
     int32_t dec_ctas;     // CTAs of the decode grid
 };
 
