@@ -93,3 +93,20 @@ def test_work_model_counts_a_shared_prefix_once():
     tails = [L - 256 for L in wl.kv_lens]
     assert work["kv_bytes"] == 2 * (256 + sum(tails)) * row
     assert work["kv_bytes_without_sharing"] == 2 * sum(wl.kv_lens) * row
+
+
+def test_work_model_counts_a_prefix_tree_once():
+    """Two levels: the root run once, each branch run once, every private tail once."""
+    root, branch, branches, per = 256, 128, 3, 4
+    wl = W.cascade_tree(0, branches=branches, per_branch=per, root=root, branch=branch, lo=16, hi=40,
+                        num_pages=400)
+    work = bench.algorithmic_work(wl)
+    row = wl.num_kv_heads * wl.head_dim * 2
+    tails = [L - root - branch for L in wl.kv_lens]
+    assert len(tails) == branches * per and min(tails) >= 16
+    assert work["kv_bytes"] == 2 * (root + branches * branch + sum(tails)) * row
+    assert work["kv_bytes_without_sharing"] == 2 * sum(wl.kv_lens) * row
+    # the page table has the tree's structure: one root run, `branches` distinct branch runs
+    rp, bp = root // wl.page_size, branch // wl.page_size
+    assert len({tuple(r[:rp]) for r in wl.page_table}) == 1
+    assert len({tuple(r[rp:rp + bp]) for r in wl.page_table}) == branches
