@@ -53,19 +53,19 @@ NCU_TRAFFIC = {
     ("decode", "decode"): {
         "bytes": 617.566208e6,
         "sources": ['paged_variable_length_gb300/csrc/decode.cu', 'paged_variable_length_gb300/csrc/device_utils.cuh', 'paged_variable_length_gb300/csrc/pva_internal.h'],
-        "sha256_16": "d1099403fe8194e9",
+        "sha256_16": "d22e27864064e1e0",
         "summary": "profiles/decode_kernel_decode_workload.md",
     },
     ("decode", "decode-e4m3"): {
         "bytes": 310.656512e6,
         "sources": ['paged_variable_length_gb300/csrc/decode.cu', 'paged_variable_length_gb300/csrc/device_utils.cuh', 'paged_variable_length_gb300/csrc/pva_internal.h'],
-        "sha256_16": "d1099403fe8194e9",
+        "sha256_16": "d22e27864064e1e0",
         "summary": "profiles/decode_kernel_fp8_decode_workload.md",
     },
     ("tensor_core", "prefill"): {
         "bytes": 220.372992e6,
         "sources": ['paged_variable_length_gb300/csrc/prefill_tc.cu', 'paged_variable_length_gb300/csrc/device_utils.cuh', 'paged_variable_length_gb300/csrc/tc_utils.cuh', 'paged_variable_length_gb300/csrc/pva_internal.h'],
-        "sha256_16": "5391211db47036e4",
+        "sha256_16": "d7afb9e03a9ef989",
         "summary": "profiles/prefill_kernel_prefill_workload.md",
     },
 }

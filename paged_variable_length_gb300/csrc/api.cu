@@ -56,11 +56,9 @@ Layout make_layout(const pva_config* c, int sm_count, int target_units = 0) {
     L.max_pre_tiles = (int32_t)((c->max_tokens / TM + c->max_batch + 1) * (int64_t)c->num_kv_heads);
     // two levels of groups (top level and sub-groups), each at most one per two requests
     L.max_casc_groups = c->enable_cascade ? c->max_batch + 1 : 1;
-    // prefix-pass units aimed for: about one per two SMs.  The decode kernel's tails start
-    // on the SMs the prefix pass leaves free, so fewer, longer prefix units (their fixed
-    // costs spread over more key tiles) overlap with the tails: cascade step 101 -> 93 us,
-    // FP8 99 -> 87 us, against one unit per SM (one per four: 86 / 97 us)
-    L.casc_target = sm_count / 2;
+    // at most one prefix-pass unit per SM; the prepare kernel aims for fewer, weighing the
+    // prefix pass against the decode tails that run beside it
+    L.casc_target = sm_count;
     if (c->enable_cascade) {
         // every member of a group takes one partial slot per prefix chunk of each of its
         // (up to two) groups, at most kMaxCascChunks in all (with sub-groups in a batch each
@@ -245,6 +243,7 @@ pva_status prepare_in_workspace(const pva_config* cfg, const int32_t* cu_seqlens
     pp.pre_tokens = kPreRows / G;
     pp.use_prefill = h.use_prefill;
     pp.use_cascade = h.use_cascade;
+    pp.kv_fp8 = cfg->kv_dtype == PVA_KV_E4M3 ? 1 : 0;
     pp.min_cascade_pages = h.cfg.min_cascade_pages;
     pp.smem_batch = batch <= kPrepareSmemBatch ? batch : 0;
     pp.split_kv = cfg->enable_split_kv ? 1 : 0;

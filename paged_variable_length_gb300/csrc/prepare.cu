@@ -664,8 +664,8 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         if (tid == 0) tile_off[B] = tot3[1];
     }
 
-    // ---- cascade groups: key chunks of each prefix (about casc_target prefix-pass units
-    // in total, roughly one per two SMs), unit ranges, member lists.  A member takes one
+    // ---- cascade groups: key chunks of each prefix (about `target` prefix-pass units in
+    // total, see below), unit ranges, member lists.  A member takes one
     // partial slot per chunk of each of its groups; with sub-groups in the batch each
     // level gets at most half the chunks, so no member needs more than kMaxCascChunks.
     if (casc && n_cgroups > 0) {
@@ -673,16 +673,34 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         const int nc_cap = n_sub > 0 ? kMaxCascChunks / 2 : kMaxCascChunks;
         const int gch = (ng + kThreads - 1) / kThreads;
         const int g0 = min(ng, tid * gch), g1 = min(ng, g0 + gch);
-        int pv[1] = {0};
-        for (int g = g0; g < g1; ++g) pv[0] += casc_pair_units(scg[g].n_members, TM, Hkv);
-        int pt[1];
-        block_scan<1>(pv, pt, s_tmp1);
+        int pv[2] = {0, 0};  // pair units; (member, 16 prefix keys) pairs
+        for (int g = g0; g < g1; ++g) {
+            pv[0] += casc_pair_units(scg[g].n_members, TM, Hkv);
+            pv[1] += scg[g].n_members * ((scg[g].prefix_len - scg[g].key_base) / 16);
+        }
+        int pt[2];
+        block_scan<2>(pv, pt, s_tmp2);
         const int pair_units = max(pt[0], 1);
+        // Units aimed for: the decode tails start on the SMs the prefix pass leaves free, so
+        // the pass gets about the share of the SMs its tensor-core time takes beside the
+        // tails' HBM time.  Per-SM rates measured on GB300: ~6.9 TFLOP/s in the tensor-core
+        // kernel (1/1.6 of that with FP8 pools) and ~36 GB/s of decode streaming; with
+        // 4 D Hq FLOPs per (member, key) and 2 Hkv D es bytes per tail key the time ratio is
+        // pairs * G * 72 / (tail keys * es * 6900).  Measured on the cascade batch: 38 units
+        // for bf16 (step 86 us) and 76 for FP8 (87 us) were the best targets tried, and this
+        // gives 37 and 77; one per SM took 101 / 99 us.
+        int target = p.lay.casc_target;
+        if (s_work > 0) {
+            const float pre = (float)pt[1] * 16.f * (float)p.group * 72.f * (p.kv_fp8 ? 1.6f : 1.f);
+            const float tail = (float)s_work * (p.kv_fp8 ? 1.f : 2.f) * 6900.f;
+            const float r = pre / tail;
+            target = max(1, min(target, (int)((float)p.lay.casc_target * r / (1.f + r))));
+        }
         int uv[1] = {0};
         for (int g = g0; g < g1; ++g) {
             const CascGroup cg = scg[g];
             const int span = cg.prefix_len - cg.key_base;
-            int nc = (p.lay.casc_target + pair_units - 1) / pair_units;
+            int nc = (target + pair_units - 1) / pair_units;
             nc = max(1, min(nc, min(nc_cap, (span + kPreKeys - 1) / kPreKeys)));
             const int ck = ((span + nc - 1) / nc + kPreKeys - 1) / kPreKeys * kPreKeys;
             uv[0] += (span + ck - 1) / ck * casc_pair_units(cg.n_members, TM, Hkv);
@@ -693,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         for (int g = g0; g < g1; ++g) {
             CascGroup cg = scg[g];
             const int span = cg.prefix_len - cg.key_base;
-            int nc = (p.lay.casc_target + pair_units - 1) / pair_units;
+            int nc = (target + pair_units - 1) / pair_units;
             nc = max(1, min(nc, min(nc_cap, (span + kPreKeys - 1) / kPreKeys)));
             const int ck = ((span + nc - 1) / nc + kPreKeys - 1) / kPreKeys * kPreKeys;
             cg.chunk_keys = ck;

@@ -149,7 +149,7 @@ struct Layout {
     int32_t rows_per_slot;
     int32_t target_units;
     int32_t max_casc_groups;
-    int32_t casc_target;  // prefix-pass units aimed for (about one per two SMs)
+    int32_t casc_target;  // most prefix-pass units aimed for (one per SM; prepare aims lower)
     int32_t dec_ctas;     // CTAs of the decode grid
 };
 
@@ -176,6 +176,7 @@ struct PrepareParams {
     int32_t min_cascade_pages;
     int32_t smem_batch;          // per-request arrays live in shared memory when batch <= this
     int32_t split_kv;
+    int32_t kv_fp8;              // 1: E4M3 pools (weighs the prefix pass against the tails)
     int32_t max_kv_len;
     int32_t max_tokens;
     int32_t max_batch;
