@@ -1,10 +1,12 @@
 """Benchmark: one step = prepare_metadata + one attn_forward (store + attention)
 over one synthetic batch, through the C ABI of libpva.so.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|mixed|cascade|worked]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|mixed|cascade|worked|...]
     python bench.py --impl reference ...     # the CPU oracle on a bounded sample
 
-Prints ONE JSON line.  Multi-GPU (torchrun, one process per GPU): every rank
+Prints ONE JSON line: the headline workload (decode by default) and, at N = 1, under
+"configs" the other workloads (worked example, prefill, mixed, shared-prefix cascade
+with and without the prefix pass, decode on an E4M3 pool) timed the same way.  Multi-GPU (torchrun, one process per GPU): every rank
 runs an independent replica of the workload (requests are independent; no
 collective in the data path), timing is max over ranks, `value` is the
 whole-job tokens/s (weak scaling).
@@ -39,6 +41,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--clocks-dir", default=None,
+                    help="where the nvidia-smi clock samples are written (default: a temporary directory)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="time only --workload (skip the other workloads' entries under 'configs')")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "e4m3"],
                     help="pool element type (e4m3: one byte per element, a scale per kv head)")
     return ap.parse_args()
@@ -178,14 +184,17 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, enabled: bool = True):
+    def __init__(self, gpu_index: int, enabled: bool = True, directory: str | None = None):
         self.proc = None
         self.path = None
         if not enabled:
             return
         try:
-            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+            import tempfile
+
+            directory = directory or tempfile.mkdtemp(prefix="pva_clocks_")
+            os.makedirs(directory, exist_ok=True)
+            self.path = os.path.join(directory, f"clocks_rank{gpu_index}.csv")
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "50"],
@@ -234,45 +243,87 @@ class ClockSampler:
 
 # ------------------------------------------------------------------------------ CPU oracle baseline
 
-def cpu_baseline(wl, tensors_cpu, budget_s: float):
-    """The oracle as it stands, timed on this host over a bounded sample of the
-    workload's requests (in order, until the estimated work reaches the budget)."""
+def _oracle_sample(wl, tensors_cpu, chosen):
+    """The sampled requests' inputs in the oracle's form."""
     import numpy as np
 
-    import oracle
-    from paged_variable_length_gb300 import workloads as W
-
-    oracle.build()
-    threads = oracle.num_threads()
-    # estimated oracle rate: ~0.5 GFLOP/s per thread on the plain loops (used only to size the sample)
-    rate = 0.5e9 * max(threads, 1)
-    chosen, est = [], 0.0
-    for i, (n, L) in enumerate(zip(wl.q_lens, wl.kv_lens)):
-        cost = 4.0 * wl.head_dim * wl.num_qo_heads * (n * L) + 1e6
-        if chosen and est + cost / rate > budget_s:
-            break
-        chosen.append(i)
-        est += cost / rate
     cu = wl.cu_seqlens_q
     rows = np.concatenate([np.arange(cu[i], cu[i + 1]) for i in chosen]) if chosen else np.zeros(0, np.int64)
     sub_cu = np.concatenate([[0], np.cumsum([wl.q_lens[i] for i in chosen])]).astype(np.int32)
-    sub_lens = np.asarray([wl.kv_lens[i] for i in chosen], np.int32)
-    sub_table = wl.page_table[chosen]
-    q = tensors_cpu["q"][rows]
-    k = tensors_cpu["k"][rows]
-    v = tensors_cpu["v"][rows]
+    return {"q": tensors_cpu["q"][rows], "k": tensors_cpu["k"][rows], "v": tensors_cpu["v"][rows], "cu": sub_cu,
+            "lens": np.asarray([wl.kv_lens[i] for i in chosen], np.int32), "table": wl.page_table[chosen]}
+
+
+def _oracle_pass(wl, tensors_cpu, s) -> float:
+    """One store + attention pass of the oracle over a sample; returns its seconds."""
+    import oracle
+
     t0 = time.perf_counter()
     if "k_scale" in tensors_cpu:
-        oracle.forward_fp8(q, k, v, tensors_cpu["k_pool"], tensors_cpu["v_pool"], tensors_cpu["k_scale"],
-                           tensors_cpu["v_scale"], sub_cu, sub_lens, sub_table, wl.page_size)
+        oracle.forward_fp8(s["q"], s["k"], s["v"], tensors_cpu["k_pool"], tensors_cpu["v_pool"],
+                           tensors_cpu["k_scale"], tensors_cpu["v_scale"], s["cu"], s["lens"], s["table"],
+                           wl.page_size)
     else:
-        oracle.forward(q, k, v, tensors_cpu["k_pool"], tensors_cpu["v_pool"], sub_cu, sub_lens, sub_table,
-                       wl.page_size)
-    dt = time.perf_counter() - t0
-    tokens = int(sub_cu[-1])
-    return {"value": tokens / dt if dt > 0 else None, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"{len(chosen)} of {wl.batch} requests ({tokens} of {wl.total_tokens} new tokens), "
-                      f"one store+attention pass, {dt:.2f} s"}
+        oracle.forward(s["q"], s["k"], s["v"], tensors_cpu["k_pool"], tensors_cpu["v_pool"], s["cu"], s["lens"],
+                       s["table"], wl.page_size)
+    return time.perf_counter() - t0
+
+
+def _sample_by_rate(wl, rate_flops: float, budget_s: float):
+    """Requests in order until the estimated oracle time reaches the budget (at least one)."""
+    chosen, est = [], 0.0
+    for i, (n, L) in enumerate(zip(wl.q_lens, wl.kv_lens)):
+        cost = 4.0 * wl.head_dim * wl.num_qo_heads * (n * L) + 1e6
+        if chosen and est + cost / rate_flops > budget_s:
+            break
+        chosen.append(i)
+        est += cost / rate_flops
+    return chosen
+
+
+def cpu_baseline(wl, tensors_cpu, budget_s: float, single_thread: bool = True):
+    """The oracle as it stands, timed on this host over bounded samples of the workload's
+    requests (in order): with OpenMP on all the cores it gets (passes repeated for about
+    half the budget), and single-threaded on a sample sized from the first leg's rate for
+    the other half.  When even one request would take the single-threaded leg past its
+    budget, its rate is that of the OpenMP leg divided by the thread count, labelled as
+    extrapolated."""
+    import oracle
+
+    oracle.build()
+    threads = oracle.num_threads()
+    half = budget_s / 2 if single_thread else budget_s
+    # ~0.5 GFLOP/s per thread on the plain loops: only sizes the first sample
+    chosen = _sample_by_rate(wl, 0.5e9 * max(threads, 1), half)
+    s = _oracle_sample(wl, tensors_cpu, chosen)
+    tokens = int(s["cu"][-1])
+    flops = sum(4.0 * wl.head_dim * wl.num_qo_heads * wl.q_lens[i] * wl.kv_lens[i] for i in chosen)
+    secs, passes = 0.0, 0
+    while passes < 1 or (secs < half and passes < 50):
+        secs += _oracle_pass(wl, tensors_cpu, s)
+        passes += 1
+    value = tokens * passes / secs if secs > 0 else None
+    out = {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+           "sample": f"{len(chosen)} of {wl.batch} requests ({tokens} of {wl.total_tokens} new tokens), "
+                     f"{passes} store+attention passes with {threads} OpenMP threads, {secs:.2f} s"}
+    if not single_thread:
+        return out
+    rate1 = flops * passes / secs / max(threads, 1)  # FLOP/s of one thread, from the first leg
+    chosen1 = _sample_by_rate(wl, rate1, half)
+    first_cost = 4.0 * wl.head_dim * wl.num_qo_heads * wl.q_lens[0] * wl.kv_lens[0] / rate1
+    try:
+        oracle.set_num_threads(1)
+        if first_cost > 2 * half:
+            v1, how = value / max(threads, 1), "extrapolated: the OpenMP rate / thread count (one request exceeds the budget)"
+        else:
+            s1 = _oracle_sample(wl, tensors_cpu, chosen1)
+            dt = _oracle_pass(wl, tensors_cpu, s1)
+            v1 = int(s1["cu"][-1]) / dt if dt > 0 else None
+            how = f"{len(chosen1)} of {wl.batch} requests, one pass, {dt:.2f} s"
+    finally:
+        oracle.set_num_threads(threads)
+    out["single_thread"] = {"value": v1, "unit": "tokens/s", "cores": 1, "sample": how}
+    return out
 
 
 # ------------------------------------------------------------------------------ reference arm
@@ -289,9 +340,11 @@ def run_reference(args):
         t["k_pool"], t["v_pool"], t["k_scale"], t["v_scale"] = W.make_fp8_pools(wl, "cpu")
     vals = []
     base = None
-    budget = min(args.cpu_budget_s, 150.0 / max(args.steps + args.warmup, 1))
+    # each step a bounded sample (about a minute in all); the single-threaded leg on the last
+    budget = min(args.cpu_budget_s, 60.0 / max(args.steps + args.warmup, 1))
     for i in range(args.warmup + args.steps):
-        base = cpu_baseline(wl, t, budget_s=budget)
+        last = i == args.warmup + args.steps - 1
+        base = cpu_baseline(wl, t, budget_s=2 * budget if last else budget, single_thread=last)
         if i >= args.warmup:
             vals.append(base["value"])
     value = statistics.median(vals)
@@ -308,12 +361,214 @@ def run_reference(args):
 
 # ------------------------------------------------------------------------------ our arm
 
+class Bench:
+    """One workload on the GPU: its tensors, an engine, and the timed graph-replayed step."""
+
+    def __init__(self, name, args, dev, rank=0, fp8=False, enable_cascade=True):
+        import torch
+
+        from paged_variable_length_gb300 import pva
+        from paged_variable_length_gb300 import workloads as W
+
+        self.pva, self.torch = pva, torch
+        self.name, self.args, self.dev, self.fp8 = name, args, dev, fp8
+        self.wl = wl = W.WORKLOADS[name](args.seed + rank)
+        self.work = algorithmic_work(wl, 1 if fp8 else 2)
+        self.t = t = W.make_tensors(wl, dev)
+        self.scales = {}
+        if fp8:
+            t["k_pool"], t["v_pool"], ks, vs = W.make_fp8_pools(wl, dev)
+            self.scales = {"k_scale": ks, "v_scale": vs}
+        self.slots = None
+        if wl.name == "ragged":
+            # contiguous K/V: the batch's own k / v rows are the keys, nothing is stored
+            t["k_pool"], t["v_pool"] = t["k"], t["v"]
+            self.slots = torch.full((wl.total_tokens,), -1, dtype=torch.int64, device=dev)
+        self.max_q = max(wl.q_lens)
+        self.eng = pva.PagedAttention(wl.num_qo_heads, wl.num_kv_heads, wl.head_dim, wl.page_size, wl.num_pages,
+                                      max_batch=wl.batch, max_tokens=wl.total_tokens, max_kv_len=max(wl.kv_lens),
+                                      device=dev, kv_dtype=pva.KV_E4M3 if fp8 else pva.KV_BF16,
+                                      enable_cascade=enable_cascade)
+        self.out = torch.empty_like(t["q"])
+        self.lse = torch.empty(t["q"].shape[:2], dtype=torch.float32, device=dev)
+
+    def step(self):
+        t = self.t
+        self.eng.prepare(t["cu_seqlens_q"], t["cache_seqlens"], t["page_table"], self.wl.total_tokens, self.slots,
+                         self.max_q)
+        self.eng.forward(t["q"], t["k"], t["v"], t["k_pool"], t["v_pool"], self.out, self.lse, **self.scales)
+
+    def warm_and_capture(self, flush):
+        """Warm-up steps, the device status check, and the step captured as a CUDA graph
+        (the library makes no host-device synchronisation and allocates nothing, so the
+        whole prepare + forward is capturable and the timed replays carry no Python gaps)."""
+        torch, pva = self.torch, self.pva
+        for _ in range(self.args.warmup):
+            flush.fill_(1.0)
+            self.step()
+        torch.cuda.synchronize()
+        bits = pva.attn_get_device_status(self.eng.meta)
+        if bits:
+            raise RuntimeError(f"{self.name}: device error bits: {pva.deverr_names(bits)}")
+        self.plan = pva.attn_debug_plan_counts(self.eng.meta)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.step()
+        self.graph.replay()
+        torch.cuda.synchronize()
+
+    def time_steps(self, flush, stream):
+        """K graph replays, L2 flushed before each (outside the events); mean ms per step."""
+        torch = self.torch
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(self.args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(self.args.steps)]
+        for i in range(self.args.steps):
+            flush.fill_(float(i))
+            starts[i].record(stream)
+            self.graph.replay()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        times = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+        return sum(times) / len(times)
+
+    def phases(self, flush, stream):
+        """Per-kernel durations: the same step replayed from a second graph with the
+        library's timing events between its kernels (they break the kernels' launch
+        overlap, so the phases add up to more than the step)."""
+        torch, pva, t = self.torch, self.pva, self.t
+        kev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
+        pev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+        for e in kev + pev:
+            e.record(stream)
+        phase = {"prepare": [], "store": [], "tensor_core": [], "decode": [], "merge": []}
+        pgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(pgraph):
+            pev[0].record()
+            self.eng.prepare(t["cu_seqlens_q"], t["cache_seqlens"], t["page_table"], self.wl.total_tokens,
+                             self.slots, self.max_q)
+            pev[1].record()
+            pva.attn_set_timing_events(self.eng.meta, kev)
+            self.eng.forward(t["q"], t["k"], t["v"], t["k_pool"], t["v_pool"], self.out, self.lse, **self.scales)
+        pva.attn_set_timing_events(self.eng.meta, None)
+        for i in range(self.args.steps):
+            flush.fill_(float(i))
+            pgraph.replay()
+            torch.cuda.synchronize()
+            phase["prepare"].append(pev[0].elapsed_time(pev[1]))
+            for j, nm in enumerate(["store", "tensor_core", "decode", "merge"]):
+                phase[nm].append(kev[j].elapsed_time(kev[j + 1]))
+        return {k: (sum(v) / len(v) if v else 0.0) for k, v in phase.items()}
+
+    def rooflines(self, ms, phase_ms, peaks):
+        """The dominant kernel's roofline and the whole step's."""
+        work = self.work
+        dom = max(("tensor_core", "decode"), key=lambda k: phase_ms[k])
+        if dom == "tensor_core" and work["flops"] > 0:
+            roof = {"bound": "tensor", "achieved": work["flops"] / (phase_ms[dom] / 1e3) / 1e12,
+                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+        else:
+            roof = {"bound": "hbm", "achieved": work["attn_bytes"] / (phase_ms[dom] / 1e3) / 1e9,
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+        roof["frac"] = roof["achieved"] / roof["peak"]
+        roof["traffic"] = ncu_traffic(dom, self.name if not self.fp8 else self.name + "-e4m3")
+        roof["kernel"] = dom
+        roof["peak_source"] = peaks["source"]
+        roof_time_s = max(work["flops"] / (peaks["bf16_tflops"] * 1e12),
+                          work["step_bytes"] / (peaks["hbm_gbs"] * 1e9))
+        step = {"roofline_time_us": roof_time_s * 1e6, "frac_of_step": roof_time_s / (ms / 1e3),
+                "bytes": work["step_bytes"], "flops": work["flops"]}
+        return roof, step
+
+    def e2e(self, flush, stream):
+        """The same step through the eager public API with host buffers: pinned host ->
+        device copies of the step's inputs and a device -> host copy of the output inside
+        the timed region."""
+        torch, t, wl = self.torch, self.t, self.wl
+        host_in = {k: t[k].cpu().pin_memory() for k in ("q", "k", "v", "cu_seqlens_q", "cache_seqlens", "page_table")}
+        dev_in = {k: torch.empty_like(t[k]) for k in host_in}
+        host_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+        d2h = host_out.numel() * host_out.element_size()
+
+        def e2e_step():
+            for k2, v2 in host_in.items():
+                dev_in[k2].copy_(v2, non_blocking=True)
+            self.eng.prepare(dev_in["cu_seqlens_q"], dev_in["cache_seqlens"], dev_in["page_table"], wl.total_tokens,
+                             self.slots, self.max_q)
+            kp_e, vp_e = (dev_in["k"], dev_in["v"]) if wl.name == "ragged" else (t["k_pool"], t["v_pool"])
+            self.eng.forward(dev_in["q"], dev_in["k"], dev_in["v"], kp_e, vp_e, self.out, None, **self.scales)
+            host_out.copy_(self.out, non_blocking=True)
+
+        for _ in range(max(1, self.args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        e_s = [torch.cuda.Event(enable_timing=True) for _ in range(self.args.steps)]
+        e_e = [torch.cuda.Event(enable_timing=True) for _ in range(self.args.steps)]
+        for i in range(self.args.steps):
+            flush.fill_(float(i))
+            e_s[i].record(stream)
+            e2e_step()
+            e_e[i].record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in zip(e_s, e_e)) / self.args.steps, h2d, d2h
+
+    def summary(self, ms, phase_ms, peaks):
+        roof, step = self.rooflines(ms, phase_ms, peaks)
+        return {"workload": self.wl.description, "kv_dtype": "e4m3" if self.fp8 else "bf16",
+                "new_tokens": self.wl.total_tokens, "value": self.wl.total_tokens / (ms / 1e3),
+                "unit": "tokens/s", "ms_per_step": ms, "phases_ms": phase_ms, "roofline": roof,
+                "step_roofline": step, "plan": self.plan}
+
+
+# the other BASELINE workloads (and variants) timed beside the headline one
+CONFIGS = [
+    ("worked", "worked", {}),
+    ("decode", "decode", {}),
+    ("prefill", "prefill", {}),
+    ("mixed", "mixed", {}),
+    ("cascade", "cascade", {}),
+    ("cascade_off", "cascade", {"enable_cascade": False}),
+    ("decode_e4m3", "decode", {"fp8": True}),
+]
+
+
+def run_configs(args, dev, flush, stream, peaks, headline_key):
+    """Every entry of CONFIGS but the headline one: the same timed step (K graph replays,
+    L2 flushed before each) and phases, one workload at a time."""
+    import torch
+
+    out = {}
+    for key, name, kw in CONFIGS:
+        if key == headline_key:
+            continue
+        b = Bench(name, args, dev, **kw)
+        b.warm_and_capture(flush)
+        ms = b.time_steps(flush, stream)
+        out[key] = b.summary(ms, b.phases(flush, stream), peaks)
+        del b
+        torch.cuda.empty_cache()
+    if "cascade" in out and "cascade_off" in out:
+        on, off = out["cascade"], out["cascade_off"]
+        out["cascade"]["vs_no_cascade"] = {
+            "speedup": off["ms_per_step"] / on["ms_per_step"],
+            "ms_per_step_without_prefix_pass": off["ms_per_step"],
+            "kv_bytes_prefix_once": on["step_roofline"]["bytes"],
+            "kv_bytes_without_sharing": algorithmic_work(W_of("cascade", args.seed))["kv_bytes_without_sharing"],
+        }
+    return out
+
+
+def W_of(name, seed):
+    from paged_variable_length_gb300 import workloads as W
+
+    return W.WORKLOADS[name](seed)
+
+
 def run_ours(args):
     import torch
 
     from paged_variable_length_gb300 import build as libbuild
     from paged_variable_length_gb300 import pva
-    from paged_variable_length_gb300 import workloads as W
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -330,66 +585,22 @@ def run_ours(args):
         dist.barrier()
     pva.load()
 
-    wl = W.WORKLOADS[args.workload](args.seed + rank)
     fp8 = args.kv_dtype == "e4m3"
-    work = algorithmic_work(wl, 1 if fp8 else 2)
     dev = torch.device("cuda", local)
-    t = W.make_tensors(wl, dev)
-    scales = {}
-    if fp8:
-        t["k_pool"], t["v_pool"], ks, vs = W.make_fp8_pools(wl, dev)
-        scales = {"k_scale": ks, "v_scale": vs}
-    slots = None
-    if wl.name == "ragged":
-        # contiguous K/V: the batch's own k / v rows are the keys, nothing is stored
-        t["k_pool"], t["v_pool"] = t["k"], t["v"]
-        slots = torch.full((wl.total_tokens,), -1, dtype=torch.int64, device=dev)
-    max_q = max(wl.q_lens)
-    eng = pva.PagedAttention(wl.num_qo_heads, wl.num_kv_heads, wl.head_dim, wl.page_size, wl.num_pages,
-                             max_batch=wl.batch, max_tokens=wl.total_tokens, max_kv_len=max(wl.kv_lens),
-                             device=dev, kv_dtype=pva.KV_E4M3 if fp8 else pva.KV_BF16)
-    out = torch.empty_like(t["q"])
-    lse = torch.empty(t["q"].shape[:2], dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
-
-    def step():
-        eng.prepare(t["cu_seqlens_q"], t["cache_seqlens"], t["page_table"], wl.total_tokens, slots, max_q)
-        eng.forward(t["q"], t["k"], t["v"], t["k_pool"], t["v_pool"], out, lse, **scales)
-
-    for _ in range(args.warmup):
-        flush.fill_(1.0)
-        step()
-    torch.cuda.synchronize()
-    bits = pva.attn_get_device_status(eng.meta)
-    if bits:
-        raise RuntimeError(f"device error bits: {pva.deverr_names(bits)}")
-    plan = pva.attn_debug_plan_counts(eng.meta)
-
-    # The step is captured once as a CUDA graph and replayed: the library makes no
-    # host-device synchronisation and allocates nothing, so the whole prepare + forward
-    # is capturable, and the device time below is free of Python launch gaps (the e2e
-    # figure further down goes through the eager host API instead).
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        step()
-    graph.replay()
-    torch.cuda.synchronize()
+    peaks = load_peaks()
+    b = Bench(args.workload, args, dev, rank=rank, fp8=fp8)
+    wl = b.wl
+    b.warm_and_capture(flush)
 
     # ---- timed region: K steps, L2 flushed before each (outside the events)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    clocks = ClockSampler(local, enabled=not args.no_clocks)
+    clocks = ClockSampler(local, enabled=not args.no_clocks, directory=args.clocks_dir)
     clocks.wait_first_sample()
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    for i in range(args.steps):
-        flush.fill_(float(i))
-        starts[i].record(stream)
-        graph.replay()
-        ends[i].record(stream)
-    torch.cuda.synchronize()
+    ms = b.time_steps(flush, stream)
     if dist is not None:
         dist.barrier()
     # the timed region is short next to the sampler's period: keep the same step
@@ -397,85 +608,26 @@ def run_ours(args):
     t_end = time.perf_counter() + 1.0
     while time.perf_counter() < t_end:
         for _ in range(50):
-            graph.replay()
+            b.graph.replay()
         torch.cuda.synchronize()
     clock_info = clocks.stop()
-    times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms = sum(times) / len(times)
     ms = max_over_ranks(ms, dist, dev)
     value = job_tokens_per_s(wl.total_tokens, world, ms)
 
-    # ---- per-kernel durations (events between the library's launches), same steps
-    kev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
-    pev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
-    for e in kev + pev:
-        e.record(stream)
-    phase = {"prepare": [], "store": [], "tensor_core": [], "decode": [], "merge": []}
-    pgraph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(pgraph):
-        pev[0].record()
-        eng.prepare(t["cu_seqlens_q"], t["cache_seqlens"], t["page_table"], wl.total_tokens, slots, max_q)
-        pev[1].record()
-        pva.attn_set_timing_events(eng.meta, kev)
-        eng.forward(t["q"], t["k"], t["v"], t["k_pool"], t["v_pool"], out, lse, **scales)
-    pva.attn_set_timing_events(eng.meta, None)
-    for i in range(args.steps):
-        flush.fill_(float(i))
-        pgraph.replay()
-        torch.cuda.synchronize()
-        phase["prepare"].append(pev[0].elapsed_time(pev[1]))
-        for j, name in enumerate(["store", "tensor_core", "decode", "merge"]):
-            phase[name].append(kev[j].elapsed_time(kev[j + 1]))
-    phase_ms = {k: (sum(v) / len(v) if v else 0.0) for k, v in phase.items()}
-
-    peaks = load_peaks()
-    # dominant kernel: the phase with the largest share of the step
-    dom = max(("tensor_core", "decode"), key=lambda k: phase_ms[k])
-    if dom == "tensor_core" and work["flops"] > 0:
-        roof = {"bound": "tensor", "achieved": work["flops"] / (phase_ms[dom] / 1e3) / 1e12,
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
-    else:
-        roof = {"bound": "hbm", "achieved": work["attn_bytes"] / (phase_ms[dom] / 1e3) / 1e9,
-                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = ncu_traffic(dom, args.workload if not fp8 else args.workload + "-e4m3")
-    roof["kernel"] = dom
-    roof["peak_source"] = peaks["source"]
-    roof_time_s = max(work["flops"] / (peaks["bf16_tflops"] * 1e12), work["step_bytes"] / (peaks["hbm_gbs"] * 1e9))
-
-    # ---- end to end through the public API with host buffers (pinned), copies inside the timed region
-    host_in = {k: t[k].cpu().pin_memory() for k in ("q", "k", "v", "cu_seqlens_q", "cache_seqlens", "page_table")}
-    dev_in = {k: torch.empty_like(t[k]) for k in host_in}
-    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
-    d2h = host_out.numel() * host_out.element_size()
-
-    def e2e_step():
-        for k2, v2 in host_in.items():
-            dev_in[k2].copy_(v2, non_blocking=True)
-        eng.prepare(dev_in["cu_seqlens_q"], dev_in["cache_seqlens"], dev_in["page_table"], wl.total_tokens, slots,
-                    max_q)
-        kp_e, vp_e = (dev_in["k"], dev_in["v"]) if wl.name == "ragged" else (t["k_pool"], t["v_pool"])
-        eng.forward(dev_in["q"], dev_in["k"], dev_in["v"], kp_e, vp_e, out, None, **scales)
-        host_out.copy_(out, non_blocking=True)
-
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
-    torch.cuda.synchronize()
-    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    for i in range(args.steps):
-        flush.fill_(float(i))
-        e_s[i].record(stream)
-        e2e_step()
-        e_e[i].record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = sum(s.elapsed_time(e) for s, e in zip(e_s, e_e)) / args.steps
+    phase_ms = b.phases(flush, stream)
+    roof, step_roof = b.rooflines(ms, phase_ms, peaks)
+    e2e_ms, h2d, d2h = b.e2e(flush, stream)
     e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+    plan = b.plan
 
     base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        base = cpu_baseline(wl, {k: v.cpu() for k, v in dict(t, **scales).items()}, args.cpu_budget_s)
+        base = cpu_baseline(wl, {k: v.cpu() for k, v in dict(b.t, **b.scales).items()}, args.cpu_budget_s)
+    del b
+    torch.cuda.empty_cache()
+    configs = None
+    if world == 1 and not args.no_configs:
+        configs = run_configs(args, dev, flush, stream, peaks, args.workload + ("_e4m3" if fp8 else ""))
 
     if rank == 0:
         line = {
@@ -484,15 +636,15 @@ def run_ours(args):
             "vs_baseline": None, "dtype": "f16 MMA on e4m3 KV" if fp8 else "bf16", "data": "synthetic",
             "config": job_config(wl, args, world),
             "roofline": roof,
-            "step_roofline": {"roofline_time_us": roof_time_s * 1e6, "frac_of_step": roof_time_s / (ms / 1e3),
-                              "bytes": work["step_bytes"], "flops": work["flops"]},
+            "step_roofline": step_roof,
             "phases_ms": phase_ms,
             "plan": plan,
             "gpu_launches": int(args.steps * (1 + plan.get("kernels_per_forward", 2))),
-            "e2e": {"value": job_tokens_per_s(wl.total_tokens, world, e2e_ms), "unit": "tokens/s", "ms_per_step": e2e_ms,
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "e2e": {"value": job_tokens_per_s(wl.total_tokens, world, e2e_ms), "unit": "tokens/s",
+                    "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "clocks": clock_info,
             "cpu_baseline": base,
+            "configs": configs,
         }
         print(json.dumps(line))
     if dist is not None:

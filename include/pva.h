@@ -200,8 +200,9 @@ PVA_API pva_status attn_prepare_metadata(const pva_config* cfg, const int32_t* c
  * workspace_bytes; the returned meta is used with attn_forward as usual.
  * Limits and behaviour:
  *   - The first call on a device looks up that device's copy of the scratch
- *     area (with that device current); make that first call before any stream
- *     capture on the device.
+ *     area (with that device current), and so does the first call after the
+ *     device's context was created anew (cudaDeviceReset); make that first call
+ *     before any stream capture on the device.
  *   - When the plan for cfg does not fit, the number of split-KV units is
  *     lowered (down to one per SM) until it does; when it still does not fit,
  *     the call returns PVA_ERR_WORKSPACE_TOO_SMALL and launches nothing.

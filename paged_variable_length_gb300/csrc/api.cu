@@ -1,6 +1,7 @@
 // The C ABI of libpva.so (declared in include/pva.h): argument checks that need
 // no GPU, workspace planning, and kernel launches.  The host never reads device
 // data here except in the two documented debug helpers.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -42,14 +43,18 @@ pva_status check_config(const pva_config* c) {
 }
 
 // target_units > 0 replaces the number of split-KV units the plan aims for (and with
-// it the partial-slot capacity); 0 keeps the default of four per decode CTA.
+// it the unit and partial-slot capacity); 0 keeps the default of four per decode CTA.
+// The default leaves room for the balanced split too (it cuts the key line at most once
+// per decode CTA: one more unit per cut, at most two partial slots per cut); with fewer
+// units the prepare kernel plans the queue of split-KV chunks instead.
 Layout make_layout(const pva_config* c, int sm_count, int target_units = 0) {
     Layout L{};
     const int G = c->num_qo_heads / c->num_kv_heads;
     const int TB = kDecRows / G;
     const int TM = kPreRows / G;
     const int cps = decode_ctas_per_sm(c->num_kv_heads, c->head_dim);
-    L.target_units = target_units > 0 ? target_units : 4 * sm_count * cps;
+    L.dec_ctas = sm_count * cps;
+    L.target_units = target_units > 0 ? target_units : 4 * L.dec_ctas;
     L.max_dec_groups = (int32_t)(c->max_tokens / TB + c->max_batch + 1);
     L.max_dec_units = L.max_dec_groups + L.target_units + 1;
     L.max_partial = 2 * L.target_units + 2;
@@ -85,7 +90,6 @@ Layout make_layout(const pva_config* c, int sm_count, int target_units = 0) {
     L.req_scratch = take(sizeof(int32_t) * 4 * (size_t)(c->max_batch + 1));
     L.casc_groups = take(sizeof(CascGroup) * (size_t)L.max_casc_groups);
     L.casc_members = take(sizeof(int32_t) * 2 * 2 * (size_t)c->max_batch);  // (token, slot) per member per level
-    L.dec_ctas = sm_count * cps;
     L.dec_first = take(sizeof(int32_t) * ((size_t)L.dec_ctas + 1));
     L.total = off;
     return L;
@@ -166,7 +170,41 @@ static __device__ __align__(256) uint8_t g_static_workspace[PVA_STATIC_WORKSPACE
 
 constexpr int kMaxDevices = 64;
 std::mutex g_static_mu;
-void* g_static_ptr[kMaxDevices];  // device address of g_static_workspace, per device, once looked up
+// Device address of g_static_workspace per device, with the CUDA context it was looked up
+// in: a context created anew (after cudaDeviceReset) has its own copy of the module.
+struct StaticArea {
+    unsigned long long ctx_id;
+    void* ptr;
+};
+StaticArea g_static_area[kMaxDevices];
+
+// Identifier of the calling thread's current CUDA context (0 when it cannot be read; the
+// address is then looked up on every call).  Through the driver's entry points, resolved
+// once.
+unsigned long long current_context_id() {
+    using GetCurrent = CUresult (*)(CUcontext*);
+    using GetId = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(f);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+        get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
 
 // Host checks of attn_prepare_metadata's arguments other than the workspace.
 pva_status check_prepare_args(const pva_config* cfg, const int32_t* cu_seqlens_q, const int32_t* cache_seqlens,
@@ -324,17 +362,24 @@ pva_status attn_prepare_metadata_static(const pva_config* cfg, const int32_t* cu
     if (dev < 0 || dev >= kMaxDevices) return PVA_ERR_UNSUPPORTED;
     void* ws = nullptr;
     {
+        // host code only knows the array by a host-side stand-in: its device address comes
+        // from the runtime, once per device and context (with that device current)
         std::lock_guard<std::mutex> lock(g_static_mu);
-        if (g_static_ptr[dev] == nullptr) {
+        const unsigned long long ctx = current_context_id();
+        StaticArea& a = g_static_area[dev];
+        if (a.ptr == nullptr || ctx == 0 || a.ctx_id != ctx) {
             void* p = nullptr;
             if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || p == nullptr) return PVA_ERR_CUDA;
-            g_static_ptr[dev] = p;
+            a.ptr = p;
+            a.ctx_id = ctx;
         }
-        ws = g_static_ptr[dev];
+        ws = a.ptr;
     }
     const int sms = device_sm_count();
     if (sms <= 0) return PVA_ERR_CUDA;
     // the default plan, or one aiming for fewer split-KV units when that does not fit
+    // (below one unit per decode CTA the prepare kernel plans the unit queue, whose
+    // capacity follows the target, instead of the balanced split)
     Layout lay = make_layout(cfg, sms);
     for (int t = lay.target_units; lay.total > PVA_STATIC_WORKSPACE_BYTES && t > sms;) {
         t = t / 2 > sms ? t / 2 : sms;

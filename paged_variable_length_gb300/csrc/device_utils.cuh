@@ -206,25 +206,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-// 2^x on the FMA/ALU pipes, for x <= ~64 (inputs below -126 give ~2^-126, i.e. 0 for a
-// softmax weight; the clamp keeps the exponent arithmetic below from wrapping).  Range
-// reduction 2^x = 2^r * 2^f with r = round(x) obtained by adding 1.5 * 2^23 (the
-// integer lands in the low mantissa bits), f = x - r in [-0.5, 0.5];
-// 2^f from a cubic fitted here to minimise the relative error on [-0.5, 0.5] (weighted
-// least squares with Lawson reweighting: max relative error 7.6e-5, far below the bf16
-// rounding of the weights it feeds); the exponent is added back as integer bits.
-// Running part of a row's exponentials here instead of on the special-function unit
-// lets both pipes work at once.
-__device__ __forceinline__ float exp2_poly(float x) {
-    x = fmaxf(x, -126.f);
-    const float t = x + 12582912.f;  // 1.5 * 2^23
-    const float r = t - 12582912.f;
-    const float f = x - r;
-    float p = fmaf(fmaf(fmaf(0.0551702156662941f, f, 0.24260781705379486f), f, 0.693260908126831f), f,
-                   0.9999282956123352f);
-    return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
-}
-
 // ---------------------------------------------------------------- packed fp32 pairs (sm_100 family)
 
 // max(a, b, c) in one instruction.

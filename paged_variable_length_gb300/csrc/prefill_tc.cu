@@ -27,10 +27,12 @@
 //     a row's max grows by more than 2^8, and normalised once at the end.
 // TMEM: per Q tile h, S_h at columns 256h .. 256h+127 (P_h aliases its first
 // 64 columns) and O_h at 256h+128 .. 256h+255.
-// FP8 pools (F8): the MMAs take f16 operands (kind::f16 needs one type for both): the
-// producers load E4M3 K/V rows into registers, convert them (exactly) to f16 and store
-// the operand tiles; Q lands as bf16 and each softmax thread converts its own row in
-// place at the start of a unit (exact inside f16's range); P is packed as f16.
+// FP8 pools (F8): the MMAs take f16 operands (kind::f16 needs one type for both): each
+// producer lane async-copies its rows' E4M3 bytes of a K and a V tile into a
+// shared-memory staging area (kStage8), and once its own copies have landed converts
+// exactly those bytes to f16 (exact: every E4M3 value is an f16 value) into the
+// swizzled operand tiles; Q lands as bf16 and each softmax thread converts its own row
+// in place at the start of a unit (exact inside f16's range); P is packed as f16.
 // k_scale of the unit's kv head folds into the softmax scale, v_scale into 1/l.
 // Every wait is bounded; a timeout sets PVA_DEVERR_TIMEOUT and the CTA winds
 // down (outstanding copies and MMAs waited for, TMEM freed) without trapping.

@@ -33,8 +33,8 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBuckets = 256;  // cost classes for the longest-first ordering of work items
-constexpr int kCmpPages = 8;
-constexpr int kLineLimit = 1 << 29;  // the balanced decode split is used below this many keys   // page ids a lane compares per step of the shared-prefix search
+constexpr int kCmpPages = 8;         // page ids a lane compares per step of the shared-prefix search
+constexpr int kLineLimit = 1 << 29;  // the balanced decode split is used below this many keys
 
 // Per-request shared-memory arrays (dynamic shared memory, batch <= smem_batch), followed
 // by the open-addressing table of the shared-prefix search when cascade detection runs.
@@ -683,19 +683,8 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         const int pair_units = max(pt[0], 1);
         // Units aimed for: the decode tails start on the SMs the prefix pass leaves free, so
         // the pass gets about the share of the SMs its tensor-core time takes beside the
-        // tails' HBM time.  Per-SM rates measured on GB300: ~6.9 TFLOP/s in the tensor-core
-        // kernel (1/1.6 of that with FP8 pools) and ~36 GB/s of decode streaming; with
-        // 4 D Hq FLOPs per (member, key) and 2 Hkv D es bytes per tail key the time ratio is
-        // pairs * G * 72 / (tail keys * es * 6900).  Measured on the cascade batch: 38 units
-        // for bf16 (step 86 us) and 76 for FP8 (87 us) were the best targets tried, and this
-        // gives 37 and 77; one per SM took 101 / 99 us.
-        int target = p.lay.casc_target;
-        if (s_work > 0) {
-            const float pre = (float)pt[1] * 16.f * (float)p.group * 72.f * (p.kv_fp8 ? 1.6f : 1.f);
-            const float tail = (float)s_work * (p.kv_fp8 ? 1.f : 2.f) * 6900.f;
-            const float r = pre / tail;
-            target = max(1, min(target, (int)((float)p.lay.casc_target * r / (1.f + r))));
-        }
+        // tails' HBM time (prefix_pass_target, with the per-SM rates measured on GB300).
+        const int target = prefix_pass_target(pt[1], s_work, p.group, p.kv_fp8, p.lay.casc_target);
         int uv[1] = {0};
         for (int g = g0; g < g1; ++g) {
             const CascGroup cg = scg[g];
@@ -756,9 +745,15 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     // decode kernel cuts its pieces from the group records (g0: the group's start on the
     // line) and dec_first (the group the CTA's share starts in).
     // (kept in shared memory and read where used: this kernel has 64 registers a thread)
+    // (the line is cut at most once per decode CTA: that many more units than groups, and
+    // at most two partial slots per cut; a workspace planned for fewer split-KV units than
+    // decode CTAs takes the unit queue instead)
     if (tid == 0) {
         int share = 0;
-        if (p.split_kv && tiles_total == 0 && Hkv <= kDecHeadBlock && s_work > 0 && s_work < kLineLimit / 2) {
+        const bool fits = p.lay.max_dec_units >= tot3[0] + p.lay.dec_ctas + 1 &&
+                          p.lay.max_partial >= 2 * p.lay.dec_ctas + 2;
+        if (p.split_kv && tiles_total == 0 && Hkv <= kDecHeadBlock && s_work > 0 && s_work < kLineLimit / 2 &&
+            fits) {
             const int per_cta = (tot3[2] + p.lay.dec_ctas - 1) / p.lay.dec_ctas;
             share = max(kMinDecShare, (per_cta + kDecKeysPerStage - 1) / kDecKeysPerStage * kDecKeysPerStage);
         }

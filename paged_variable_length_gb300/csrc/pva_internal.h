@@ -273,6 +273,39 @@ inline int split_ranges(int ext, int chunk, int* per_out) {
     return (ext + per - 1) / per;
 }
 
+// ---------------------------------------------------------------- GB300 tuning: prefix-pass size
+//
+// Rates of one GB300 SM measured in this library's kernels, used only to size the
+// shared-prefix pass against the decode tails that run beside it (no result depends on
+// them): the tensor-core kernel's prefix pass does ~6.9 TFLOP/s per SM (1/1.6 of that
+// with FP8 pools, whose operands it converts), the decode kernel streams ~36 GB/s per SM.
+// A (member, prefix key) pair costs 4 D Hq = 4 D G Hkv FLOPs and a tail key 2 Hkv D es
+// bytes, so prefix time / tail time = pairs * G * 2 * 36 / (tail keys * es * 6900)
+// (es = bytes per pool element), and the pass aims for that share of the SMs:
+// units = casc_target * r / (1 + r), at least 1.  On the 128-member cascade batch (4096
+// shared keys, tails U[16, 512], G 4; seed 0: 34 480 tail keys) this gives 36 units for
+// bf16 and 76 for FP8 pools on 152 SMs, next to the best targets measured there (38 and
+// 76); one unit per SM took 101 / 99 us against 86 / 87 us.
+constexpr float kTuneTcGflopsPerSm = 6900.f;  // tensor-core prefix pass, bf16, per SM (GFLOP/s)
+constexpr float kTuneFp8TcSlowdown = 1.6f;    // the same with FP8 pools is this much slower
+constexpr float kTuneDecodeGbsPerSm = 36.f;   // decode streaming per SM (GB/s)
+
+// Prefix-pass units to aim for: pair16 = (member, 16 prefix keys) pairs over all groups,
+// tail_keys = keys of the decode tails, group = G; at most casc_target, at least 1.
+#ifdef __CUDACC__
+__host__ __device__
+#endif
+inline int prefix_pass_target(long long pair16, unsigned long long tail_keys, int group, int kv_fp8,
+                              int casc_target) {
+    if (tail_keys == 0) return casc_target;
+    const float pre = (float)pair16 * 16.f * (float)group * 2.f * kTuneDecodeGbsPerSm *
+                      (kv_fp8 ? kTuneFp8TcSlowdown : 1.f);
+    const float tail = (float)tail_keys * (kv_fp8 ? 1.f : 2.f) * kTuneTcGflopsPerSm;
+    const float r = pre / tail;
+    const int t = (int)((float)casc_target * r / (1.f + r));
+    return t < 1 ? 1 : (t > casc_target ? casc_target : t);
+}
+
 // Entries (log2) of the prepare kernel's shared-memory hash table for shared-prefix
 // detection: more than twice the batch, so that open addressing always finds a free entry.
 #ifdef __CUDACC__

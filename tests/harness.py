@@ -1,9 +1,12 @@
 """Shared test helpers: run a workload through the CUDA library and the oracle,
 and compare them with the tolerances the parity bar states.
 
-Tolerances: the KV pool after the write is bit-exact; the bf16 output must
-satisfy |gpu - ref| <= 2e-2 + 1e-2 * |ref| elementwise against the fp32
-oracle (max-abs 2e-2 with a 1e-2 relative allowance); LSE within 1e-3.
+Tolerances: the KV pool after the write is bit-exact; against the fp32 oracle the
+bf16 output must have max-abs error <= 2e-2 and max-rel error <= 1e-2, the relative
+error of an element taken against max(|ref|, 1) (so below |ref| = 1 it is the absolute
+error, and no element near zero can fail on rounding alone); LSE within 1e-3 absolute.
+Every comparison is recorded (test, max-abs, max-rel, LSE) and listed at the end of
+the session.
 """
 from __future__ import annotations
 
@@ -14,9 +17,12 @@ import oracle
 from paged_variable_length_gb300 import pva
 from paged_variable_length_gb300 import workloads as W
 
-ATOL = 2e-2
-RTOL = 1e-2
+MAX_ABS = 2e-2
+MAX_REL = 1e-2
 LSE_ATOL = 1e-3
+
+# (test id, compared elements, max-abs, max-rel, LSE max-abs) of every assert_close call
+RECORDS: list = []
 
 
 def make_engine(wl: W.Workload, enable_split_kv=True, enable_cascade=True, min_cascade_pages=8, sm_scale=0.0,
@@ -54,23 +60,37 @@ def pool_bits(t):
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
+def error_figures(g: np.ndarray, ref: np.ndarray):
+    """(max-abs, max-rel) of g against ref; the relative error is taken against max(|ref|, 1)."""
+    if g.size == 0:
+        return 0.0, 0.0
+    err = np.abs(g.astype(np.float64) - ref.astype(np.float64))
+    rel = err / np.maximum(np.abs(ref.astype(np.float64)), 1.0)
+    return float(err.max()), float(rel.max())
+
+
 def assert_close(gpu_out, gpu_lse, ref_out, ref_lse, mask=None):
+    """Assert the stated bar (max-abs <= 2e-2, max-rel <= 1e-2, LSE <= 1e-3) and
+    return the max-abs error.  `mask` selects the compared rows (sampled checks)."""
+    import os
+
     g = gpu_out.float().cpu().numpy()
     ref = ref_out
     if mask is not None:
         g, ref = g[mask], ref[mask]
     assert np.isfinite(g).all(), "non-finite output"
-    err = np.abs(g - ref)
-    bound = ATOL + RTOL * np.abs(ref)
-    bad = err > bound
-    assert not bad.any(), (f"{bad.sum()} of {bad.size} outside |d| <= {ATOL} + {RTOL}|ref|; "
-                           f"max abs {err.max():.3e}")
+    max_abs, max_rel = error_figures(g, ref)
+    lerr = None
     if gpu_lse is not None:
         gl = gpu_lse.cpu().numpy()
         rl = ref_lse
         if mask is not None:
             m2 = mask.any(axis=-1) if mask.ndim == 3 else mask
             gl, rl = gl[m2], rl[m2]
-        lerr = np.abs(gl - rl)
-        assert lerr.max() <= LSE_ATOL, f"LSE max abs err {lerr.max():.3e}"
-    return float(err.max())
+        lerr = float(np.abs(gl - rl).max()) if gl.size else 0.0
+    RECORDS.append((os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0], int(g.size), max_abs, max_rel, lerr))
+    assert max_abs <= MAX_ABS, f"max-abs error {max_abs:.3e} > {MAX_ABS} (max-rel {max_rel:.3e})"
+    assert max_rel <= MAX_REL, f"max-rel error {max_rel:.3e} > {MAX_REL} (max-abs {max_abs:.3e})"
+    if lerr is not None:
+        assert lerr <= LSE_ATOL, f"LSE max abs err {lerr:.3e}"
+    return max_abs

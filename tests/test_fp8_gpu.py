@@ -2,8 +2,8 @@
 
 The pool after the quantising store is compared byte for byte (the quantisation is
 integer-valued work: one E4M3 code per element); the output against the oracle's
-fp32 attention over e4m3 * scale within the same 2e-2 + 1e-2 * |ref| bar as the bf16
-path (the kernels' f16 operands hold every E4M3 value, the activations' bf16 values
+fp32 attention over e4m3 * scale within the same bar as the bf16 path (max-abs 2e-2,
+max-rel 1e-2 relative to max(|ref|, 1)) (the kernels' f16 operands hold every E4M3 value, the activations' bf16 values
 and P more finely than the bf16 path does); LSE within 1e-3.
 """
 import numpy as np
