@@ -175,7 +175,9 @@ PVA_API size_t attn_workspace_size(const pva_config* cfg);
  *                  256-byte aligned, owned by the caller, not used
  *                  concurrently by another prepare/forward.
  * The arrays must stay unchanged until the last attn_forward using `meta`
- * (page_table and slot_mapping are read by the forward kernels).
+ * (the forward kernels read them: the page table, the lengths, and slot_mapping
+ * or, without one, the derived slots through the page table).  A page id of a
+ * derived slot outside the pool is flagged (PVA_DEVERR_PAGE_ID) by the forward.
  */
 PVA_API pva_status attn_prepare_metadata(const pva_config* cfg, const int32_t* cu_seqlens_q,
                                  const int32_t* cache_seqlens, const int32_t* page_table,
@@ -282,6 +284,21 @@ PVA_API pva_status attn_get_device_status(const pva_meta* meta, uint32_t* error_
  * result.
  */
 PVA_API pva_status attn_set_timing_events(pva_meta* meta, void* const* events, int32_t n);
+
+/*
+ * Test helper for the kernels' bounded waits: every wait inside the forward kernels
+ * (on a pipeline stage, the tensor core, the work queue) gives up after 2 s, sets
+ * PVA_DEVERR_TIMEOUT, waits (with the 2 s limit) for its CTA's own copies and MMAs,
+ * frees what it holds and returns, so a wedged kernel ends with a status instead of
+ * hanging the device.  This call shortens that limit for the forwards that use meta,
+ * so a test can make the waits run out on a healthy batch: limit_ns >= 0 is the new
+ * limit in ns (0: a wait gives up at once if its condition does not already hold);
+ * limit_ns < 0 restores the default.  The waits that drain a CTA's copies and MMAs
+ * before it leaves keep the default.  The next attn_prepare_metadata on the workspace
+ * also restores it, and clears the error word.  Synchronises the meta's stream, then
+ * writes the plan header; not for use inside a stream capture.
+ */
+PVA_API pva_status attn_debug_set_wait_limit(const pva_meta* meta, int64_t limit_ns);
 
 /*
  * Debug/test helper: copies plan counters to host (synchronising): counts[0]

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <cstddef>
 #include <cstring>
 #include <mutex>
 
@@ -118,6 +119,7 @@ ForwardParams forward_params(const MetaHost* h, const void* q, const void* k, co
     fp.page_table = h->page_table;
     fp.ld = h->ld;
     fp.slots = h->slots;
+    fp.tok_req = h->tok_req;
     fp.total_tokens = h->total_tokens;
     fp.page_size = h->cfg.page_size;
     fp.page_shift = ilog2(h->cfg.page_size);
@@ -253,7 +255,8 @@ pva_status prepare_in_workspace(const pva_config* cfg, const int32_t* cu_seqlens
     h.page_table = page_table;
     h.ld = ld_page_table;
     h.ws = static_cast<uint8_t*>(workspace);
-    h.slots = slot_mapping != nullptr ? slot_mapping : reinterpret_cast<const int64_t*>(h.ws + lay.slots);
+    h.slots = slot_mapping;
+    h.tok_req = slot_mapping != nullptr ? nullptr : reinterpret_cast<const int32_t*>(h.ws + lay.slots);
     h.stream = stream;
     h.lay = lay;
     h.n_events = 0;
@@ -268,7 +271,7 @@ pva_status prepare_in_workspace(const pva_config* cfg, const int32_t* cu_seqlens
     pp.page_table = page_table;
     pp.ld = ld_page_table;
     pp.user_slots = slot_mapping;
-    pp.derived_slots = slot_mapping != nullptr ? nullptr : reinterpret_cast<int64_t*>(h.ws + lay.slots);
+    pp.tok_req = slot_mapping != nullptr ? nullptr : reinterpret_cast<int32_t*>(h.ws + lay.slots);
     pp.batch = batch;
     pp.total_tokens = total_tokens;
     pp.max_q_len = mq;
@@ -472,6 +475,19 @@ pva_status attn_set_timing_events(pva_meta* meta, void* const* events, int32_t n
         h->events[i] = n == 5 ? events[i] : nullptr;
     }
     h->n_events = n;
+    return PVA_OK;
+}
+
+pva_status attn_debug_set_wait_limit(const pva_meta* meta, int64_t limit_ns) {
+    const MetaHost* h = meta_of(meta);
+    if (h == nullptr) return PVA_ERR_NOT_PREPARED;
+    // the header holds limit + 1 (0: the default); limits above ~4.29 s are capped
+    uint32_t v = 0;
+    if (limit_ns >= 0) v = (uint32_t)((limit_ns < 0xFFFFFFFEll ? limit_ns : 0xFFFFFFFEll) + 1);
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(h->stream)) != cudaSuccess) return PVA_ERR_CUDA;
+    if (cudaMemcpy(h->ws + h->lay.header + offsetof(PlanHeader, wait_override), &v, sizeof(v),
+                   cudaMemcpyHostToDevice) != cudaSuccess)
+        return PVA_ERR_CUDA;
     return PVA_OK;
 }
 

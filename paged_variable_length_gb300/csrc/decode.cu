@@ -84,6 +84,17 @@ __device__ __forceinline__ void abort_cta(DecSmemHead* sh, uint32_t* err) {
     dev::set_error(err, kErrTimeout);
 }
 
+// A work wait of one whole warp (every lane calls it, converged): the lanes' results are
+// voted, so the warp leaves together or not at all (its next steps -- warp MMAs, fragment
+// loads, warp syncs -- need every lane); lane 0 records the abort.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t limit, DecSmemHead* sh,
+                                          uint32_t* err) {
+    if (__all_sync(0xffffffffu, dev::mbar_wait(bar, parity, limit))) return true;
+    if ((threadIdx.x & 31) == 0) abort_cta(sh, err);
+    __syncwarp();
+    return false;
+}
+
 template <int D, bool F8>
 __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
     decode_kernel(ForwardParams p, int stages, int row_stride) {
@@ -93,6 +104,7 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
     uint8_t* ring = smem + ((sizeof(DecSmemHead) + 127) / 128) * 128;
     PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws + p.lay.header);
     uint32_t* err = &hdr->error_bits;
+    const uint64_t wlim = dev::wait_limit(hdr->wait_override);  // work waits (drains: the default)
 
     // a CTA serves HB = min(Hkv, 8) kv heads ("head block"); work item = (unit, head block)
     const int Hkv = p.num_kv_heads, G = p.group, Hq = p.num_qo_heads;
@@ -103,8 +115,8 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
     // rows staged back to back (no padding): one copy per stage and pool (see launch_d)
     const bool runs = row_stride == row_bytes;
     const int stage_bytes = 2 * kStageKeys * row_stride;
-    // Plan from the prepare kernel (finished before the store kernel began); pool rows,
-    // the work counter and the prefix-pass partials only after grid_dep_wait.
+    // Plan from the prepare kernel (complete before the store kernel released this grid);
+    // pool rows, the work counter and the prefix-pass partials only after grid_dep_wait.
     dev::grid_dep_launch();
     const int n_units = hdr->n_dec_units * n_hb;
     // after a tensor-core kernel with units the store kernel has already finished (see
@@ -238,15 +250,13 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
             if (u < n_units) du = units[u / n_hb];
         }
         while (true) {
-            if (!dev::mbar_wait(&sh->empty[stage], phase ^ 1)) {
-                abort_cta(sh, err);
-                break;
-            }
+            if (!warp_wait(&sh->empty[stage], phase ^ 1, wlim, sh, err)) break;
             if (u >= n_units) {
                 if (lane == 0) {
                     sh->info[stage].flags = kEnd;
                     dev::mbar_arrive(&sh->full[stage]);
                 }
+                armed &= ~(1u << stage);  // the end marker carries no copies (earlier ones were consumed)
                 break;
             }
             const int hb = u % n_hb;
@@ -284,12 +294,7 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
                 } else if (si_ == nst - 1 && u_next < n_units && du_next.k0 + r < du_next.k1) {
                     page_first = page_of(p.page_table + (int64_t)du_next.req * p.ld, du_next.k0 + r);
                 }
-                if (si_ != 0) {
-                    if (!dev::mbar_wait(&sh->empty[stage], phase ^ 1)) {
-                        abort_cta(sh, err);
-                        goto producer_done;
-                    }
-                }
+                if (si_ != 0 && !warp_wait(&sh->empty[stage], phase ^ 1, wlim, sh, err)) goto producer_done;
                 const int nk = min(kStageKeys, du.k1 - k);
                 if (lane == 0) {
                     StageInfo& si = sh->info[stage];
@@ -339,11 +344,11 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
             g_cur = g_next;
         }
     producer_done:
-        // drain: every copy this warp issued must land before the CTA may exit
-        if (sh->abort_flag) {
-            for (int s = 0; s < stages; ++s)
-                if (armed & (1u << s)) (void)dev::mbar_wait(&sh->full[s], (armed_par >> s) & 1u);
-        }
+        // drain: every copy this warp issued must land before the CTA may exit -- also when
+        // it ends normally, since a consumer may still give up on a stage in flight (a stage
+        // the consumers already took has completed and returns at once)
+        for (int s = 0; s < stages; ++s)
+            if (armed & (1u << s)) (void)dev::mbar_wait(&sh->full[s], (armed_par >> s) & 1u);
         if (wait_late) dev::grid_dep_wait();
         return;
     }
@@ -364,10 +369,7 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
     uint32_t phase = 0;
 
     while (true) {
-        if (!dev::mbar_wait(&sh->full[stage], phase)) {
-            abort_cta(sh, err);
-            return;
-        }
+        if (!warp_wait(&sh->full[stage], phase, wlim, sh, err)) return;
         const StageInfo si = sh->info[stage];
         if (si.flags & kEnd) break;
         const int rows = si.ntok * G;

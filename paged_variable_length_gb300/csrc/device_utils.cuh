@@ -73,14 +73,25 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete; false after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Wait for the phase with the given parity to complete; false after limit_ns.  A limit
+// of 0 polls once (without the suspension a try_wait may take) and gives up at once if
+// the phase is not complete: a test of the timeout path uses it, so that a wait that has
+// to wait at all expires.  Waits that drain a CTA's own copies and MMAs before it leaves
+// always take the default limit.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
+    if (limit_ns == 0) return mbar_test_wait(bar, parity);
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer() - t0 > kWaitLimitNs) return false;
+        if (globaltimer() - t0 > limit_ns) return false;
     }
+}
+
+// The limit of a kernel's work waits: the plan header's override (set only by the debug
+// call attn_debug_set_wait_limit; the field holds limit + 1, 0 = none), else kWaitLimitNs.
+__device__ __forceinline__ uint64_t wait_limit(uint32_t override_plus1) {
+    return override_plus1 ? (uint64_t)(override_plus1 - 1u) : kWaitLimitNs;
 }
 
 // ---------------------------------------------------------------- bulk async copy (TMA, 1-D)

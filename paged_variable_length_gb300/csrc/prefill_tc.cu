@@ -94,12 +94,20 @@ struct Bars {
     int32_t uq[4];
     uint32_t tmem_base;
     int32_t abort_flag;
+    uint64_t wait_limit;  // of the work waits (the drains before the CTA leaves: the default)
 };
 
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Bars* b, uint32_t* err) {
-    if (dev::mbar_wait(bar, parity)) return true;
-    b->abort_flag = 1;
-    dev::set_error(err, kErrTimeout);
+// A work wait of one whole warp (every lane calls it, converged): the lanes' results are
+// voted, so the warp leaves together or not at all -- its next steps (warp-wide tensor-core
+// loads, warp syncs) need every lane.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint64_t wlim, Bars* b,
+                                              uint32_t* err) {
+    if (__all_sync(0xffffffffu, dev::mbar_wait(bar, parity, wlim))) return true;
+    if ((threadIdx.x & 31) == 0) {
+        b->abort_flag = 1;
+        dev::set_error(err, kErrTimeout);
+    }
+    __syncwarp();
     return false;
 }
 
@@ -107,8 +115,9 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ba
 // that order), one at a time: entry k is filled by one producer thread when the CTA
 // starts its unit k-1, so a CTA never holds more than one unit in reserve and the
 // grid finishes together.  Every role reads every entry; -1 ends the kernel.
-__device__ __forceinline__ void queue_push(Bars* b, int k, int32_t* counter, int n_units, uint32_t* err) {
-    if (k >= 4 && !dev::mbar_wait(&b->uq_empty[k & 3], ((k >> 2) & 1) ^ 1)) {
+__device__ __forceinline__ void queue_push(Bars* b, int k, int32_t* counter, int n_units, uint64_t wlim,
+                                           uint32_t* err) {
+    if (k >= 4 && !dev::mbar_wait(&b->uq_empty[k & 3], ((k >> 2) & 1) ^ 1, wlim)) {
         b->abort_flag = 1;
         dev::set_error(err, kErrTimeout);
     }
@@ -117,18 +126,18 @@ __device__ __forceinline__ void queue_push(Bars* b, int k, int32_t* counter, int
     dev::mbar_arrive(&b->uq_full[k & 3]);
 }
 
-// All lanes of the calling warp read entry k and lane 0 releases it (single: only the
-// calling thread reads, for a role that runs on one thread).
-__device__ __forceinline__ int queue_read(Bars* b, int k, int lane, uint32_t* err, bool single = false) {
+// All lanes of the calling warp (converged) read entry k and lane 0 releases it; the wait
+// is voted, so every lane gets the same entry (or -1).
+__device__ __forceinline__ int queue_read(Bars* b, int k, int lane, uint64_t wlim, uint32_t* err) {
     int v = -1;
-    if (dev::mbar_wait(&b->uq_full[k & 3], (k >> 2) & 1)) {
+    if (__all_sync(0xffffffffu, dev::mbar_wait(&b->uq_full[k & 3], (k >> 2) & 1, wlim))) {
         v = b->uq[k & 3];
-    } else {
+    } else if (lane == 0) {
         b->abort_flag = 1;
         dev::set_error(err, kErrTimeout);
     }
-    if (!single) __syncwarp();
-    if (single || lane == 0) dev::mbar_arrive(&b->uq_empty[k & 3]);
+    __syncwarp();
+    if (lane == 0) dev::mbar_arrive(&b->uq_empty[k & 3]);
     return v;
 }
 
@@ -173,12 +182,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws + p.lay.header);
     uint32_t* err = &hdr->error_bits;
     // The plan was written by the prepare kernel, which finished before the store
-    // kernel began; the pool rows and the work counter come from the store kernel, which
-    // may still run (programmatic launch): they are read only after grid_dep_wait.  An
-    // idle CTA waits too, so that this grid never completes before its predecessor.  The
-    // dependents (the decode kernel) are released only after that wait, so that when
-    // they start the store kernel has finished: decode does not wait for this grid
-    // before its own work, only before it exits.
+    // kernel released this grid; the pool rows and the work counter come from the store
+    // kernel, which may still run (programmatic launch): they are read only after
+    // grid_dep_wait.  An idle CTA waits too, so that this grid never completes before its
+    // predecessor.  The dependents (the decode kernel) are released only after that wait,
+    // so that when they start the store kernel has finished: decode does not wait for
+    // this grid before its own work, only before it exits.
     const int n_units = hdr->n_pre_tiles;
     if ((hdr->error_bits & kErrFatal) || n_units == 0 || (int)blockIdx.x >= n_units) {
         // an idle CTA releases the dependents at once: with no unit at all the decode
@@ -219,6 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             dev::mbar_init(&b->uq_empty[s], kQueueReaders);
         }
         b->abort_flag = 0;
+        b->wait_limit = dev::wait_limit(hdr->wait_override);
         dev::fence_barrier_init();
     }
     if (warp == kMmaWarp) {
@@ -229,6 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = b->tmem_base;
+    const uint64_t wlim = b->wait_limit;  // of the work waits, in a register for every role
     dev::grid_dep_wait();
     dev::grid_dep_launch();
 
@@ -301,18 +312,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         uint32_t it = 0;
         const bool fetcher = pwarp == 0 && lane == 0;
-        if (fetcher) queue_push(b, 0, counter, n_units, err);
-        for (int uc = 0;; ++uc) {
-            const int u = queue_read(b, uc, lane, err);
+        uint64_t* q_land = F8 ? &b->q_raw : &b->q_full;
+        // Leaving early (a wait that gave up) must not strand a Q tile loaded by TMA: the
+        // thread that loads one remembers its phase's parity until a later unit's q_empty wait
+        // shows it consumed, and waits for it before the CTA leaves; every producer arrives on
+        // the Q phase of the unit it leaves in, so that the phase can complete.
+        int tma_pending = -1;  // parity of this thread's TMA-loaded Q phase not yet seen consumed
+        int q_arrived = 0;     // Q phases this thread has arrived on
+        int uc = 0;
+        if (fetcher) queue_push(b, 0, counter, n_units, wlim, err);
+        for (;; ++uc) {
+            const int u = queue_read(b, uc, lane, wlim, err);
             if (u < 0 || b->abort_flag) break;
-            if (fetcher) queue_push(b, uc + 1, counter, n_units, err);
+            if (fetcher) queue_push(b, uc + 1, counter, n_units, wlim, err);
             const PreTile pt = units[u];
             const UnitView uv = unit_view(pt);
             const int32_t* prow =
                 p.page_table + (int64_t)(uv.casc ? cgroups[-1 - pt.req].leader : pt.req) * p.ld;
             // ---- Q: row r = token (or cascade member) r / G, head r % G of each tile
-            if (uc > 0 && !wait_or_abort(&b->q_empty, (uc - 1) & 1, b, err)) break;
-            uint64_t* q_land = F8 ? &b->q_raw : &b->q_full;
+            if (uc > 0 && !wait_or_abort(&b->q_empty, (uc - 1) & 1, wlim, b, err)) break;
+            tma_pending = -1;  // the Q tiles of every earlier unit have been consumed
             if (q_tma && !uv.casc) {
                 // consecutive tokens: the G heads of a kv head are adjacent rows of q, so a tile
                 // half is one tensor box (tokens past the batch read as zeros; rows of tokens
@@ -328,6 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tc::tma_load_3d(smem + L::kQ + h * L::kTile + x * kRegion, &q_map, x * 64, pt.kvh * G,
                                             pt.tok0 + h * TM, q_land);
                     }
+                    tma_pending = uc & 1;
                 }
             } else
             for (int h = 0; h < 2; ++h) {
@@ -347,6 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 copy_tile(smem + L::kQ + h * L::kTile, oq[0], oq[1], p.q);
             }
             issue(q_land);
+            ++q_arrived;
             // ---- K and V tiles
             const int kv_end = uv.key_end;
             const int nkt = (kv_end - uv.key_base + kPreKeys - 1) / kPreKeys;
@@ -431,9 +452,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t ph = (it >> 1) & 1;
                     tile_pages(j + 1, pg);
                     asm volatile("cp.async.wait_group 0;" ::: "memory");  // this lane's copies of tile j
-                    if (!(ok = wait_or_abort(&b->k_empty[st], ph ^ 1, b, err))) break;
+                    if (!(ok = wait_or_abort(&b->k_empty[st], ph ^ 1, wlim, b, err))) break;
                     convert(valid, stage8, smem + L::kK + st * L::kTile, &b->k_full[st]);
-                    if (!(ok = wait_or_abort(&b->v_empty[st], ph ^ 1, b, err))) break;
+                    if (!(ok = wait_or_abort(&b->v_empty[st], ph ^ 1, wlim, b, err))) break;
                     convert(valid, stage8 + kPreRows * D, smem + L::kV + st * L::kTile, &b->v_full[st]);
                     if (j + 1 < nkt) valid = load_tile(j + 1, pg);
                 }
@@ -489,13 +510,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                  "l"(base + off[m] + 64));
                             }
                         };
-                        if (!wait_or_abort(&b->k_empty[st], ph ^ 1, b, err)) {
+                        if (!wait_or_abort(&b->k_empty[st], ph ^ 1, wlim, b, err)) {
                             ok = false;
                             break;
                         }
                         copy_g8(smem + L::kK + st * L::kTile, p.k_pool);
                         issue(&b->k_full[st]);
-                        if (!wait_or_abort(&b->v_empty[st], ph ^ 1, b, err)) {
+                        if (!wait_or_abort(&b->v_empty[st], ph ^ 1, wlim, b, err)) {
                             ok = false;
                             break;
                         }
@@ -510,7 +531,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
         }
-        // copies still in flight must land before the CTA may leave
+        // After an abort, this thread arrives on the Q phase of the unit it left in (so that
+        // the phase can complete); then its TMA-loaded Q tile and its async copies must land
+        // before the CTA may leave.  (Not at a normal end: a phase completed by those
+        // arrivals would put the barrier two phases ahead of a warp still waiting on the
+        // one before, which shares its parity.)
+        if (b->abort_flag && q_arrived == uc) issue(q_land);
+        if (tma_pending >= 0) (void)dev::mbar_wait(q_land, (uint32_t)tma_pending);
         asm volatile("cp.async.wait_group 0;" ::: "memory");
     } else if (warp == kMmaWarp) {
         // ============================================================== MMA issuer (one warp)
@@ -525,9 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t q_lo = tc::smem_desc_lo(dev::smem_u32(smem + L::kQ), 16);
         const uint32_t k_lo = tc::smem_desc_lo(dev::smem_u32(smem + L::kK), 16);
         const uint32_t v_lo = tc::smem_desc_lo(dev::smem_u32(smem + L::kV), kRegion);
-        auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-            return __all_sync(0xffffffffu, wait_or_abort(bar, parity, b, err));
-        };
+        auto wait = [&](uint64_t* bar, uint32_t parity) -> bool { return wait_or_abort(bar, parity, wlim, b, err); };
         uint32_t it = 0;                      // KV tiles across units
         uint32_t n_p[2] = {0, 0};             // P tiles consumed per Q tile
         uint32_t n_units_h[2] = {0, 0};       // units that had Q tile h
@@ -562,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             return true;
         };
         for (int uc = 0; ok; ++uc) {
-            const int u = __shfl_sync(0xffffffffu, queue_read(b, uc, lane, err), 0);
+            const int u = __shfl_sync(0xffffffffu, queue_read(b, uc, lane, wlim, err), 0);
             if (u < 0) break;
             const UnitView uv = unit_view(units[u]);
             const int nkt0 = uv.nk[0];
@@ -642,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t n_s = 0;   // S tiles seen by this warpgroup
         uint32_t n_u = 0;   // units with this Q tile
         for (int k = 0;; ++k) {
-            const int u = queue_read(b, k, lane, err);
+            const int u = queue_read(b, k, lane, wlim, err);
             if (u < 0 || b->abort_flag) break;
             const PreTile pt = units[u];
             const UnitView uv = unit_view(pt);
@@ -651,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (F8) {
                 // this thread's row of Q tile h, bf16 -> f16 in place (both regions; every
                 // warp takes part in every unit: q_full counts the eight softmax warps)
-                if (!wait_or_abort(&b->q_raw, k & 1, b, err)) break;
+                if (!wait_or_abort(&b->q_raw, k & 1, wlim, b, err)) break;
 #pragma unroll
                 for (int x = 0; x < D / 64; ++x) {
 #pragma unroll
@@ -677,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m = -INFINITY, l = 0.f;
             bool ok = true;
             for (int j = 0; j < nk; ++j, ++n_s) {
-                if (!wait_or_abort(&b->s_full[h], n_s & 1, b, err)) {
+                if (!wait_or_abort(&b->s_full[h], n_s & 1, wlim, b, err)) {
                     ok = false;
                     break;
                 }
@@ -765,7 +790,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
             // ---- epilogue: O / l -> bf16 rows of out, LSE
-            if (!wait_or_abort(&b->o_ready[h], n_u & 1, b, err)) break;
+            if (!wait_or_abort(&b->o_ready[h], n_u & 1, wlim, b, err)) break;
             tc::fence_after_sync();
             const float inv = l > 0.f ? (F8 ? p.v_scale[pt.kvh] : 1.f) / l : 0.f;
             const int64_t orow = (valid && !uv.casc)

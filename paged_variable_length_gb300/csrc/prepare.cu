@@ -21,7 +21,8 @@
 //      cut into near-equal chunks;
 //   3. work lists, longest item first: decode units, prefill tile pairs with
 //      their causal KV extents, and the prefix-pass units of the cascade groups;
-//   4. slot_mapping derived from the page table when the caller passed none.
+//   4. when the caller passed no slot_mapping: the request of every new token, from
+//      which the store kernel derives each token's slot through the page table.
 #include <cuda_runtime.h>
 
 #include "device_utils.cuh"
@@ -375,6 +376,9 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     __shared__ int s_share;  // balanced decode split: keys per CTA (0: the unit queue)
     __shared__ int s_line;   // balanced decode split: length of the key line
 
+    // the store kernel that follows may set up its CTAs now: it reads nothing this kernel
+    // writes before its grid_dep_wait
+    dev::grid_dep_launch();
     const int tid = threadIdx.x;
     const int B = p.batch;
     const int TB = p.dec_tokens, TM = p.pre_tokens, Hkv = p.num_kv_heads, ps = p.page_size;
@@ -409,28 +413,6 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     // each thread owns a contiguous run of requests for the counting passes
     const int chunk_req = (B + kThreads - 1) / kThreads;
     const int r0 = min(B, tid * chunk_req), r1 = min(B, r0 + chunk_req);
-    // derived slot of a single-token request (one request per thread): its page id is
-    // requested here and used only at the end, so the load overlaps the passes below
-    int32_t d_page = 0;
-    int d_tok = -1, d_pos = 0;
-    if (p.derived_slots != nullptr && chunk_req == 1 && tid < B) {
-        const int n = cu[tid + 1] - cu[tid], L = lens[tid];
-        if (n == 1 && valid_req(n, L)) {
-            d_pos = L - 1;
-            d_tok = cu[tid];
-            d_page = p.page_table[(int64_t)tid * p.ld + d_pos / ps];
-        }
-    }
-    // page-table rows the shared-prefix search may compare: pulled into L2 now
-    if (casc && chunk_req == 1 && tid < B) {
-        const int n = cu[tid + 1] - cu[tid], L = lens[tid];
-        const int pages = (n == 1 && valid_req(n, L)) ? (L - n) / ps : 0;
-        if (pages >= p.min_cascade_pages) {
-            const char* row = reinterpret_cast<const char*>(p.page_table + (int64_t)tid * p.ld);
-            for (int off = 0; off < pages * 4; off += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + off));
-        }
-    }
-
     // ---- pass 0: shared-prefix groups among single-token decodes.  Requests are keyed
     // by their first page; the lowest-numbered request with a key leads its group; the
     // group's prefix is the run of pages every member shares with the leader (whole pages
@@ -506,9 +488,17 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         // matched by construction), one warp per member: lanes read consecutive page ids,
         // so each load instruction is one line of each row, 256 ids per step.  The group
         // prefix is the smallest mismatch, or the smallest member's page count.
+        // The rows about to be compared (members' and leaders' page ids up to the pages
+        // compared) are requested into L2 here, all at once, so that the warps' compare steps
+        // below, one member after another, mostly find them there.  Only rows of requests
+        // that share a first page are touched: a batch without such requests reads no row.
         for (int i = tid; i < B; i += kThreads) {
             const int ld = leader[i];
-            lim[i] = (ld >= 0 && ld != i) ? min(lcp[i], lcp[ld]) : 0;
+            const int l = (ld >= 0 && ld != i) ? min(lcp[i], lcp[ld]) : 0;
+            lim[i] = l;
+            const int pf = l > 0 ? l : ((ld == i && cnt[i] >= 2) ? lcp[i] : 0);
+            const char* row = reinterpret_cast<const char*>(p.page_table + (int64_t)i * p.ld);
+            for (int off = 4; off < pf * 4; off += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + off));
         }
         __syncthreads();
         for (int i = tid; i < B; i += kThreads)
@@ -613,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     int cnt[3] = {0, 0, 0};  // decode groups, prefill tile pairs x kv heads, decode key line
     unsigned long long work = 0, line = 0;
     int max_ntok = 0;
-    if (tid == 0 && p.cu[0] != 0) err |= kErrCu;
+    if (tid == 0 && cu[0] != 0) err |= kErrCu;
     if (tid == 0 && B > p.max_batch) err |= kErrLimits;
     if (tid == 0 && p.total_tokens > p.max_tokens) err |= kErrLimits;
     for (int i = r0; i < r1; ++i) {
@@ -951,27 +941,19 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         }
     }
 
-    // ---- derived slot mapping: the new tokens are each request's last q_len positions
-    if (run && p.derived_slots != nullptr) {
-        uint32_t perr = 0;
-        if (d_tok >= 0) {  // single-token request, page id loaded at the start
-            int64_t slot = -1;
-            if (d_page < 0 || d_page >= p.num_pages) perr |= kErrPage;
-            else slot = (int64_t)d_page * ps + d_pos % ps;
-            p.derived_slots[d_tok] = slot;
+    // ---- the request of every new token, from which the store kernel derives the slot
+    // mapping when the caller passed none (its many warps then load the page ids side by
+    // side; here, one thread per token would wait for them one after another)
+    if (run && p.tok_req != nullptr) {
+        // each thread a contiguous run of tokens: one search for its first token's request
+        // (request i with cu[i] <= t < cu[i+1]), then a walk
+        const int per = (p.total_tokens + kThreads - 1) / kThreads;
+        const int t0 = min(p.total_tokens, tid * per), t1 = min(p.total_tokens, t0 + per);
+        int i = t0 < t1 ? find_bucket(cu, B, t0) : 0;
+        for (int t = t0; t < t1; ++t) {
+            while (cu[i + 1] <= t) ++i;
+            p.tok_req[t] = i;
         }
-        for (int t = tid; t < p.total_tokens; t += kThreads) {
-            const int i = find_bucket(cu, B, t);  // request i with cu[i] <= t < cu[i+1]
-            const int n = cu[i + 1] - cu[i], L = lens[i];
-            if (n == 1 && chunk_req == 1) continue;  // written above
-            const int pos = L - n + (t - cu[i]);
-            const int64_t page = p.page_table[(int64_t)i * p.ld + pos / ps];
-            int64_t slot = -1;
-            if (page < 0 || page >= p.num_pages) perr |= kErrPage;
-            else slot = page * ps + pos % ps;
-            p.derived_slots[t] = slot;
-        }
-        if (perr) atomicOr(&s_err, perr);
     }
     __syncthreads();
     if (tid == 0) {
@@ -987,6 +969,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         hdr->n_casc_units = ok ? s_casc_units : 0;
         hdr->max_group_tokens = ok ? s_max_ntok : 0;
         hdr->dec_share = ok ? s_share : 0;
+        hdr->wait_override = 0;
     }
 }
 

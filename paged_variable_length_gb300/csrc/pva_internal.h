@@ -51,7 +51,9 @@ struct PlanHeader {
     int32_t n_casc_units;
     int32_t max_group_tokens;  // most tokens in one decode group (bounds the merge's rows)
     int32_t dec_share;         // keys per decode CTA of the balanced split; 0: the work queue
-    int32_t pad[53];           // pad[0] / pad[1]: decode / tensor-core work counters
+    uint32_t wait_override;    // tests only: wait limit in ns + 1 for the forward kernels' work
+                               // waits (attn_debug_set_wait_limit); 0 (set by prepare): default
+    int32_t pad[52];           // pad[0] / pad[1]: decode / tensor-core work counters
 };
 static_assert(sizeof(PlanHeader) == 256, "header is one 256-byte line");
 
@@ -134,7 +136,7 @@ struct Layout {
     size_t dec_units;
     size_t dec_groups;
     size_t pre_tiles;
-    size_t slots;        // int64 [max_tokens] derived slot mapping
+    size_t slots;        // int32 [max_tokens]: request of each new token (the slot mapping is derived from it)
     size_t partial_o;    // fp32 [max_partial][rows_per_slot][D]
     size_t partial_lse;  // fp32 [max_partial][rows_per_slot]
     size_t req_scratch;  // int32 [max_batch * 4] prepare scratch
@@ -160,7 +162,7 @@ struct PrepareParams {
     const int32_t* page_table;
     int64_t ld;
     const int64_t* user_slots;   // may be null
-    int64_t* derived_slots;
+    int32_t* tok_req;            // request of each new token, written when user_slots is null
     int32_t batch;
     int32_t total_tokens;
     int32_t max_q_len;
@@ -197,7 +199,8 @@ struct ForwardParams {
     const int32_t* seqlens;
     const int32_t* page_table;
     int64_t ld;
-    const int64_t* slots;        // user or derived
+    const int64_t* slots;        // the caller's slot mapping, or null: derived from tok_req
+    const int32_t* tok_req;      // request of each new token (when slots is null)
     int32_t total_tokens;
     int32_t page_size;
     int32_t page_shift;          // log2(page_size)
@@ -238,7 +241,8 @@ struct MetaHost {
     const int32_t* seqlens;
     const int32_t* page_table;
     int64_t ld;
-    const int64_t* slots;
+    const int64_t* slots;        // the caller's slot mapping or null
+    const int32_t* tok_req;      // per-token request index in the workspace (slots null)
     uint8_t* ws;
     void* stream;
     void* events[5];           // optional timing events (attn_set_timing_events)

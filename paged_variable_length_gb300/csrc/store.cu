@@ -9,6 +9,9 @@
 // warp moves one token's K row (or V row) with 16-byte vector accesses: reads
 // stream past L1, writes stay in L2 for the attention kernels that follow.  Into an
 // FP8 pool each element is quantised on the way (x / scale of its kv head, to E4M3).
+// Without a caller slot_mapping each warp derives its token's slot from the page table
+// (the token's request comes from the plan): the new tokens are the request's last
+// q_len positions.
 #include <cuda_runtime.h>
 
 #include "device_utils.cuh"
@@ -21,8 +24,13 @@ constexpr int kThreads = 256;
 
 __global__ void __launch_bounds__(kThreads) store_kernel(ForwardParams p, int row_vecs) {
     PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws + p.lay.header);
-    // the attention kernel that follows may set up its CTAs now; it reads nothing this
-    // kernel writes before its grid_dep_wait
+    // Launched programmatically: the kernel before it (the prepare kernel, or the previous
+    // forward's last kernel, which may still read the pool) must have finished before the
+    // plan, the slots or the pool are touched.  Only then may the attention kernel that
+    // follows set up its CTAs: it reads the plan before its own grid_dep_wait, so the plan
+    // must be complete when it starts, and it reads nothing this kernel writes before that
+    // wait.
+    dev::grid_dep_wait();
     dev::grid_dep_launch();
     // the attention kernels that follow fetch their work from these counters
     if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -35,7 +43,22 @@ __global__ void __launch_bounds__(kThreads) store_kernel(ForwardParams p, int ro
     if (job >= 2 * (int64_t)p.total_tokens) return;
     const int64_t t = job >> 1;
     const bool is_v = job & 1;
-    const int64_t slot = p.slots[t];
+    int64_t slot;
+    if (p.slots != nullptr) {
+        slot = p.slots[t];
+    } else {
+        // slot mapping derived from the page table: the new tokens of request i are its last
+        // q_len positions (prepare recorded each token's request)
+        const int i = p.tok_req[t];
+        const int c0 = p.cu[i], n = p.cu[i + 1] - c0, L = p.seqlens[i];
+        const int pos = L - n + (int)(t - c0);
+        const int64_t page = p.page_table[(int64_t)i * p.ld + (pos >> p.page_shift)];
+        if (page < 0 || page >= p.num_pages) {
+            if (lane == 0 && !is_v) dev::set_error(&hdr->error_bits, kErrPage);
+            return;
+        }
+        slot = (page << p.page_shift) + (pos & (p.page_size - 1));
+    }
     if (slot == -1) return;
     if (slot < 0 || slot >= p.num_slots) {
         if (lane == 0 && !is_v) dev::set_error(&hdr->error_bits, kErrSlot);
@@ -78,8 +101,7 @@ cudaError_t launch_store(const ForwardParams& p, int head_dim, cudaStream_t s) {
     const int row_vecs = p.num_kv_heads * head_dim * 2 / 16;
     const int64_t jobs = 2 * (int64_t)p.total_tokens;
     const int64_t blocks = (jobs + kThreads / 32 - 1) / (kThreads / 32);
-    store_kernel<<<(unsigned)blocks, kThreads, 0, s>>>(p, row_vecs);
-    return cudaGetLastError();
+    return launch_programmatic(store_kernel, (unsigned)blocks, (unsigned)kThreads, 0, s, p, row_vecs);
 }
 
 }  // namespace pva

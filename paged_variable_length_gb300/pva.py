@@ -26,7 +26,8 @@ DEVERR = {
 # Every function include/pva.h declares; the CPU tests check the library exports each one.
 EXPORTS = ("attn_abi_version", "attn_status_string", "attn_workspace_size", "attn_prepare_metadata",
            "attn_forward", "attn_store_kvcache", "attn_get_device_status", "attn_debug_plan_counts",
-           "attn_set_timing_events", "attn_prepare_metadata_static", "attn_forward_fp8kv", "attn_store_kvcache_fp8kv")
+           "attn_set_timing_events", "attn_prepare_metadata_static", "attn_forward_fp8kv", "attn_store_kvcache_fp8kv",
+           "attn_debug_set_wait_limit")
 
 
 class PvaError(RuntimeError):
@@ -86,6 +87,8 @@ def load(path: str | None = None):
         lib.attn_get_device_status.restype = ctypes.c_int
         lib.attn_set_timing_events.argtypes = [MP, ctypes.POINTER(ctypes.c_void_p), i32]
         lib.attn_set_timing_events.restype = ctypes.c_int
+        lib.attn_debug_set_wait_limit.argtypes = [MP, i64]
+        lib.attn_debug_set_wait_limit.restype = ctypes.c_int
         lib.attn_debug_plan_counts.argtypes = [MP, ctypes.POINTER(ctypes.c_int64), i32]
         lib.attn_debug_plan_counts.restype = i32
         _lib = lib
@@ -195,6 +198,12 @@ def attn_debug_plan_counts(meta: Meta) -> dict:
     keys = ("dec_units", "dec_groups", "pre_tiles", "casc_groups", "casc_tiles", "split_chunk", "partial_slots",
             "kernels_per_forward")
     return {keys[i]: int(arr[i]) for i in range(n)}
+
+
+def attn_debug_set_wait_limit(meta: Meta, limit_ns: int) -> None:
+    """Tests only: the forward kernels' wait limit for this meta (ns; 0 = give up at once,
+    negative = the default 2 s).  Synchronises; the next prepare restores the default."""
+    _check(load().attn_debug_set_wait_limit(ctypes.byref(meta), int(limit_ns)), "attn_debug_set_wait_limit")
 
 
 def attn_set_timing_events(meta: Meta, events) -> None:
