@@ -134,7 +134,8 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
     const DecGroup* dgroups = reinterpret_cast<const DecGroup*>(p.ws + p.lay.dec_groups);
     // Balanced split (share > 0, planned only when no tensor-core unit precedes this grid):
     // the decode groups' keys lie end to end on one line, each group padded to whole
-    // stages, and this CTA takes the line's keys [line_lo, line_hi).  Its pieces are cut
+    // stages and followed by a gap (kDecPieceCost keys, charged for a piece start, that
+    // nobody processes), and this CTA takes the line's keys [line_lo, line_hi).  Its pieces are cut
     // from the group records; a piece that starts at a share boundary inside a group is
     // that group's split (boundary index - index of the boundary before the group).
     const int share = hdr->dec_share;

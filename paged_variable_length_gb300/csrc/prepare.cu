@@ -346,7 +346,7 @@ __device__ __noinline__ void emit_balanced_groups(const PrepareParams& p, const 
             dg.g0 = g0;
             dg.pad1 = dg.pad2 = dg.pad3 = dg.pad4 = dg.pad5 = 0;
             store_record(&groups[gi], dg);
-            const int e16 = g0 + (kv_end + kDecKeysPerStage - 1) / kDecKeysPerStage * kDecKeysPerStage;
+            const int e16 = g0 + (kv_end + kDecKeysPerStage - 1) / kDecKeysPerStage * kDecKeysPerStage + kDecPieceCost;
             for (int c = (g0 + share - 1) / share; c * share < e16 && c <= p.lay.dec_ctas; ++c) dec_first[c] = gi;
             g0 = e16;
             if (pieces > 1) pi += pieces;
@@ -624,7 +624,8 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
             for (int g = 0; g < ng; ++g) {
                 const int ext = L - n + min((g + 1) * TB, n) - lp;
                 work += (unsigned long long)ext;
-                line += (unsigned long long)((ext + kDecKeysPerStage - 1) / kDecKeysPerStage * kDecKeysPerStage);
+                line += (unsigned long long)((ext + kDecKeysPerStage - 1) / kDecKeysPerStage * kDecKeysPerStage +
+                                             kDecPieceCost);
             }
         }
     }
@@ -728,9 +729,10 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         chunk = (int)(c > (unsigned long long)kMinSplitChunk ? c : (unsigned long long)kMinSplitChunk);
     }
     // ---- balanced split: with no tensor-core unit every decode CTA starts at once, so the
-    // decode groups' keys (each group padded to whole 16-key stages) are laid end to end on
-    // one line and CTA c takes the line's keys [c * share, (c + 1) * share): equal work per
-    // CTA, and a group is cut only where a CTA's share ends (fewer partials than queued
+    // decode groups' keys (each group padded to whole 16-key stages and followed by a gap of
+    // kDecPieceCost keys, the cost of starting a piece) are laid end to end on one line and
+    // CTA c takes the line's keys [c * share, (c + 1) * share): equal work per CTA, and a
+    // group is cut only where a CTA's share ends (fewer partials than queued
     // units of one chunk each, which also left the grid's last units as a tail).  The
     // decode kernel cuts its pieces from the group records (g0: the group's start on the
     // line) and dec_first (the group the CTA's share starts in).
@@ -774,7 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
                     const int pieces = 1 + (g0 + ext - 1) / share - g0 / share;
                     cnt2[0] += pieces;
                     if (pieces > 1) cnt2[1] += pieces;
-                    g0 += (ext + kDecKeysPerStage - 1) / kDecKeysPerStage * kDecKeysPerStage;
+                    g0 += (ext + kDecKeysPerStage - 1) / kDecKeysPerStage * kDecKeysPerStage + kDecPieceCost;
                     continue;
                 }
                 int per;

@@ -25,6 +25,12 @@ constexpr int kMinSplitChunk = 256;
 constexpr int kMaxCascChunks = 8;
 constexpr int kDecHeadBlock = 8;     // kv heads one decode CTA serves (more: several CTAs per unit)
 constexpr int kMinDecShare = 128;    // fewest keys a decode CTA gets in the balanced split
+// Keys the balanced split charges for starting a group's piece: on the key line each group is
+// followed by a gap of this many keys that no CTA processes, so a CTA whose share holds more
+// group starts gets fewer keys (a piece start cost ~0.9 us on the decode workload, about the
+// time of 9 keys of 4 KiB at one SM's streaming rate; measured per CTA: one piece 111.0 us,
+// two 112.1, three 113.0).
+constexpr int kDecPieceCost = 16;
 
 // Error bits the kernels OR into the plan's error word (same values as pva.h).
 constexpr uint32_t kErrCu = PVA_DEVERR_CU_SEQLENS;

@@ -1,34 +1,40 @@
 """Host check of the balanced decode split's arithmetic (CPU, no GPU).
 
 The prepare kernel lays the decode groups' keys end to end on one line (each group
-padded to whole 16-key stages) and gives CTA c the line's keys [c * share,
+padded to whole 16-key stages and followed by a gap of kDecPieceCost keys that no CTA
+processes, the cost of starting a piece) and gives CTA c the line's keys [c * share,
 (c + 1) * share); it counts a group's pieces as one plus the share boundaries inside
 the group and records, per CTA, the group its share starts in.  The decode kernel cuts
 its pieces from those records.  This test restates both rules in Python and checks, for
 random batches, that every key of every group is covered exactly once and that a group's
 split indices are exactly 0 .. pieces - 1 (so every partial slot is written once).
 """
+import os
 import random
+import re
 
 import pytest
 
-STAGE, MIN_SHARE = 16, 128
+_HDR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "paged_variable_length_gb300",
+                    "csrc", "pva_internal.h")
+_CONST = lambda name: int(re.search(name + r"\s*=\s*(\d+)", open(_HDR).read()).group(1))
+STAGE, MIN_SHARE, PIECE_COST = _CONST("kDecKeysPerStage"), _CONST("kMinDecShare"), _CONST("kDecPieceCost")
 
 
-def _plan(exts, n_ctas, min_share=MIN_SHARE):
+def _plan(exts, n_ctas, min_share=MIN_SHARE, cost=PIECE_COST):
     r16 = lambda x: (x + STAGE - 1) // STAGE * STAGE
-    line = sum(r16(e) for e in exts)
+    line = sum(r16(e) + cost for e in exts)
     share = max(min_share, r16((line + n_ctas - 1) // n_ctas))
     g0s, x = [], 0
     for e in exts:
         g0s.append(x)
-        x += r16(e)
+        x += r16(e) + cost
     pieces = [1 + (g0 + e - 1) // share - g0 // share for g0, e in zip(g0s, exts)]
     first = [None] * (n_ctas + 1)
     for c in range((line + share - 1) // share, n_ctas + 1):
         first[c] = len(exts)
     for g, (g0, e) in enumerate(zip(g0s, exts)):
-        end, c = g0 + r16(e), (g0 + share - 1) // share
+        end, c = g0 + r16(e) + cost, (g0 + share - 1) // share
         while c * share < end and c <= n_ctas:
             assert first[c] is None, "two groups claim one CTA"
             first[c] = g
@@ -85,6 +91,6 @@ def test_decode_workload_shape():
     rng = random.Random(0)
     exts = [rng.randint(512, 4096) for _ in range(64)]
     share, g0s, pieces, first = _plan(exts, 152)
-    line = sum((e + STAGE - 1) // STAGE * STAGE for e in exts)
+    line = sum((e + STAGE - 1) // STAGE * STAGE + PIECE_COST for e in exts)
     assert share * 152 >= line > share * 151 - share
     assert sum(pieces) <= len(exts) + 152
