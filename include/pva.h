@@ -156,8 +156,9 @@ PVA_API size_t attn_workspace_size(const pva_config* cfg);
  * shared-prefix (cascade) groups.  One kernel launch on `stream`, no sync.
  * Shared prefixes are found among single-token decodes whose page-table rows start
  * with the same run of at least min_cascade_pages pages lying before their query, and
- * inside such a group among members whose rows continue with a further such run (two
- * levels of the prefix tree); each prefix is read once per group by the forward.
+ * inside such a group among members whose rows continue with a further such run, and
+ * inside those again (three levels of the prefix tree); each shared run is read once per
+ * group by the forward.
  * Detection runs for batches of 2 to 1536 requests.
  *
  *   cu_seqlens_q   int32 [batch+1]  request i's new tokens are q[cu[i] : cu[i+1]]

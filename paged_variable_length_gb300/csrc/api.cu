@@ -60,7 +60,9 @@ Layout make_layout(const pva_config* c, int sm_count, int target_units = 0) {
     L.max_dec_units = L.max_dec_groups + L.target_units + 1;
     L.max_partial = 2 * L.target_units + 2;
     L.max_pre_tiles = (int32_t)((c->max_tokens / TM + c->max_batch + 1) * (int64_t)c->num_kv_heads);
-    // two levels of groups (top level and sub-groups), each at most one per two requests
+    // up to three levels of groups, each at most one per two requests; the prepare kernel
+    // numbers no more than max_batch + 1 records in all (a deeper level that would need
+    // more is not formed: its requests read those keys as tails)
     L.max_casc_groups = c->enable_cascade ? c->max_batch + 1 : 1;
     // at most one prefix-pass unit per SM; the prepare kernel aims for fewer, weighing the
     // prefix pass against the decode tails that run beside it
@@ -90,7 +92,7 @@ Layout make_layout(const pva_config* c, int sm_count, int target_units = 0) {
     L.partial_lse = take(sizeof(float) * (size_t)L.max_partial * L.rows_per_slot);
     L.req_scratch = take(sizeof(int32_t) * 4 * (size_t)(c->max_batch + 1));
     L.casc_groups = take(sizeof(CascGroup) * (size_t)L.max_casc_groups);
-    L.casc_members = take(sizeof(int32_t) * 2 * 2 * (size_t)c->max_batch);  // (token, slot) per member per level
+    L.casc_members = take(sizeof(int32_t) * 2 * 3 * (size_t)c->max_batch);  // (token, slot) per member per level
     L.dec_first = take(sizeof(int32_t) * ((size_t)L.dec_ctas + 1));
     L.total = off;
     return L;

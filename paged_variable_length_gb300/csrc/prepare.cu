@@ -128,40 +128,62 @@ __device__ __forceinline__ int casc_pair_units(int members, int TM, int Hkv) {
     return (((members + TM - 1) / TM) + 1) / 2 * Hkv;
 }
 
-// Level 2 of the shared-prefix search (pass 0 of the kernel below): inside a group,
-// members keyed by the page right after the group's prefix; the lowest-numbered one
-// leads its sub-group, whose prefix extends the group's by the run of pages every
-// sub-member shares with it (again at least min_pages, again whole pages before each
-// member's query).  Its prefix pass covers keys [group prefix, sub-group prefix) only.
-// The arrays of level 1 that are no longer needed hold level 2's: the page after the
-// prefix (kFirst), pages before the query then the sub-prefix (kLcp), counts then next
-// free member slots (kCnt); the hash table is reused.  Sub-group records are numbered
-// after the n_groups top-level ones; returns how many there are.  A function of its
-// own (not inlined), so that its registers do not weigh on the rest of the kernel,
-// which runs 1024 threads and so has 64 registers each.
-__device__ __noinline__ int find_sub_groups(int32_t* dyn, int stride, int32_t* hkey, int32_t* hval, int hbits,
-                                            CascGroup* scg, CascGroup* cgroups, const int32_t* page_table,
-                                            int64_t ld_table, int64_t num_pages, int min_pages, int B, int ps,
-                                            int r0, int r1, int n_groups, int members1, int (*s_tmp2)[2]) {
+// What the shared-prefix search of every level needs besides its own arrays (set once, in
+// shared memory: passed as one pointer, so that the calls below keep few values live in
+// the 64-register kernel).
+struct SearchCtx {
+    int32_t* dyn;
+    int32_t* hkey;
+    int32_t* hval;
+    CascGroup* scg;
+    CascGroup* cgroups;
+    const int32_t* page_table;
+    int64_t ld_table;
+    int64_t num_pages;
+    int stride, hbits, min_pages, B, ps, max_groups;
+};
+
+// One level deeper in the shared-prefix tree (pass 0 of the kernel below; level 2 inside
+// the top-level groups, level 3 inside level 2's): inside a parent group, members keyed by
+// the page right after the parent's prefix; the lowest-numbered one leads its sub-group,
+// whose prefix extends the parent's by the run of pages every sub-member shares with it
+// (again at least min_pages, again whole pages before each member's query).  Its prefix
+// pass covers keys [parent prefix, sub-group prefix) only.  parent[i]: request i's group
+// at the parent level (-1: none).  Scratch arrays: the page after the parent's prefix
+// (page2), pages before the query then the sub-prefix (pg2), counts then next free member
+// slots (cnt2, kept for the member lists); outputs: the sub-leader (lead2) and sub-group
+// id (cgid2, -1: none) of each request; the hash table is reused.  Sub-group records are
+// numbered after the n_groups already found, their member lists after `members0` entries;
+// a level whose groups would exceed max_groups records in all is not formed (its requests
+// run the rest as tails).  Returns how many there are and their member entries in
+// *members_total.  A function of its own (not inlined), so that its registers do not
+// weigh on the rest of the kernel, which runs 1024 threads and so has 64 registers each.
+__device__ __noinline__ int find_next_level(const SearchCtx* cx, const int32_t* parent, int32_t* page2, int32_t* pg2,
+                                            int32_t* cnt2, int32_t* lead2, int32_t* cgid2, int n_groups,
+                                            int members0, int (*s_tmp2)[2], int* members_total) {
     const int tid = threadIdx.x, lane = tid & 31;
+    int32_t* dyn = cx->dyn;
+    int32_t* hkey = cx->hkey;
+    int32_t* hval = cx->hval;
+    CascGroup* scg = cx->scg;
+    CascGroup* cgroups = cx->cgroups;
+    const int32_t* page_table = cx->page_table;
+    const int64_t ld_table = cx->ld_table, num_pages = cx->num_pages;
+    const int stride = cx->stride, hbits = cx->hbits, min_pages = cx->min_pages, B = cx->B, ps = cx->ps;
+    const int max_groups = cx->max_groups;
+    const int chunk_req = (B + kThreads - 1) / kThreads;
+    const int r0 = min(B, tid * chunk_req), r1 = min(B, r0 + chunk_req);
     const int HT = 1 << hbits;
     auto sa = [&](int a) { return dyn + a * stride; };
     const int32_t* cu = sa(kCu);
     const int32_t* lens = sa(kLen);
-    int32_t* first = sa(kFirst);
-    int32_t* lcp = sa(kLcp);
-    int32_t* cnt = sa(kCnt);
-    int32_t* page2 = first;
-    int32_t* pg2 = lcp;
-    int32_t* cnt2 = cnt;
-    int32_t* lead2 = sa(kLeader2);
-    int32_t* cgid2 = sa(kCgid2);  // pages compared per member until the sub-groups are numbered
+    *members_total = 0;
     for (int h = tid; h < HT; h += kThreads) {
         hkey[h] = -1;
         hval[h] = 0x7fffffff;
     }
     for (int i = tid; i < B; i += kThreads) {
-        const int g = sa(kCgid)[i];
+        const int g = parent[i];
         int pg = -1, pages = 0;
         if (g >= 0) {
             const int n = cu[i + 1] - cu[i], L = lens[i];
@@ -184,7 +206,7 @@ __device__ __noinline__ int find_sub_groups(int32_t* dyn, int stride, int32_t* h
     // is dropped below)
     auto key2 = [&](int i) -> int {
         return page2[i] < 0 ? -1
-                            : (int)(((uint32_t)page2[i] * 2654435761u ^ (uint32_t)sa(kCgid)[i] * 0x9E3779B9u) &
+                            : (int)(((uint32_t)page2[i] * 2654435761u ^ (uint32_t)parent[i] * 0x9E3779B9u) &
                                     0x7fffffffu);
     };
     int dup = 0;  // some key met twice (in a warp, or already in the table)
@@ -219,7 +241,7 @@ __device__ __noinline__ int find_sub_groups(int32_t* dyn, int stride, int32_t* h
     for (int i0 = 0; i0 < B; i0 += kThreads) {
         const int i = i0 + tid;
         int ld = (i < B && page2[i] >= 0) ? hval[lead2[i]] : -1;
-        if (ld >= 0 && (sa(kCgid)[ld] != sa(kCgid)[i] || page2[ld] != page2[i])) ld = -1;
+        if (ld >= 0 && (parent[ld] != parent[i] || page2[ld] != page2[i])) ld = -1;
         const unsigned peers = __match_any_sync(0xffffffffu, ld);
         if (i < B) lead2[i] = ld;
         if (ld >= 0 && lane == __ffs(peers) - 1) atomicAdd(&cnt2[ld], __popc(peers));
@@ -237,7 +259,7 @@ __device__ __noinline__ int find_sub_groups(int32_t* dyn, int stride, int32_t* h
         const int warp = tid >> 5;
         for (int i = warp; i < B; i += kWarps) {
             const int l = cgid2[i];
-            const int g = sa(kCgid)[i];
+            const int g = parent[i];
             if (l <= 0 || g < 0) continue;  // warp-uniform
             const int start = scg[g].prefix_len / ps + 1;  // page start - 1 matched by the key
             if (l <= start) continue;
@@ -268,7 +290,7 @@ __device__ __noinline__ int find_sub_groups(int32_t* dyn, int stride, int32_t* h
     __syncthreads();
     auto is_sub_leader = [&](int i) {
         if (lead2[i] != i || cnt2[i] < 2) return false;
-        return pg2[i] - scg[sa(kCgid)[i]].prefix_len / ps >= min_pages;
+        return pg2[i] - scg[parent[i]].prefix_len / ps >= min_pages;
     };
     int hv[2] = {0, 0};
     for (int i = r0; i < r1; ++i)
@@ -278,13 +300,18 @@ __device__ __noinline__ int find_sub_groups(int32_t* dyn, int stride, int32_t* h
         }
     int ht[2];
     block_scan<2>(hv, ht, s_tmp2);
+    if (n_groups + ht[0] > max_groups) {  // no room for this level's records: not formed
+        for (int i = tid; i < B; i += kThreads) cgid2[i] = -1;
+        __syncthreads();
+        return 0;
+    }
     {
-        int gid = n_groups + hv[0], moff = members1 + hv[1];
+        int gid = n_groups + hv[0], moff = members0 + hv[1];
         for (int i = r0; i < r1; ++i) {
             if (!is_sub_leader(i)) continue;
             CascGroup cg;
             cg.leader = i;
-            cg.key_base = scg[sa(kCgid)[i]].prefix_len;
+            cg.key_base = scg[parent[i]].prefix_len;
             cg.prefix_len = pg2[i] * ps;
             cg.n_members = cnt2[i];
             cg.member_off = moff;
@@ -292,7 +319,7 @@ __device__ __noinline__ int find_sub_groups(int32_t* dyn, int stride, int32_t* h
             cg.chunk_keys = 0;
             cg.unit_off = 0;
             cg.n_units = 0;
-            cg.level = 1;
+            cg.level = scg[parent[i]].level + 1;
             cg.pad0 = cg.pad1 = 0;
             store_record(&cgroups[gid], cg);
             scg[gid] = cg;
@@ -303,6 +330,7 @@ __device__ __noinline__ int find_sub_groups(int32_t* dyn, int stride, int32_t* h
         }
     }
     const int n_new = ht[0];
+    *members_total = ht[1];
     __syncthreads();
     for (int i = tid; i < B; i += kThreads) {
         const int ld = lead2[i];
@@ -375,6 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     __shared__ int s_max_ntok;
     __shared__ int s_share;  // balanced decode split: keys per CTA (0: the unit queue)
     __shared__ int s_line;   // balanced decode split: length of the key line
+    __shared__ SearchCtx s_cx;  // the deeper levels' shared-prefix search
 
     // the store kernel that follows may set up its CTAs now: it reads nothing this kernel
     // writes before its grid_dep_wait
@@ -418,7 +447,13 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     // group's prefix is the run of pages every member shares with the leader (whole pages
     // that lie strictly before each member's query, so no causal mask ever applies to it).
     int n_cgroups = 0;
-    int n_sub = 0;  // sub-groups among them
+    int n_sub = 0;   // level-2 groups among them
+    int n_sub3 = 0;  // level-3 groups among them
+    // level 3's per-request arrays (a = 0: its leader, 1: group id, 2: member-slot cursors)
+    // live in the workspace's per-request scratch, unused on this path (detection needs the
+    // per-request arrays in shared memory); read only when a level-3 group exists.
+    // (Addressed where used: this kernel has 64 registers a thread.)
+    auto g3 = [&](int a) { return reinterpret_cast<int32_t*>(p.ws + p.lay.req_scratch) + a * (B + 1); };
     // shared-memory copy of the cascade group records (after the hash table)
     CascGroup* scg = reinterpret_cast<CascGroup*>(dyn + kNumArrays * stride +
                                                   2 * (casc ? (1 << casc_hash_bits(p.smem_batch)) : 0));
@@ -575,18 +610,52 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         }
         const int members1 = gt[1];  // member-list entries of the top-level groups
         __syncthreads();
-        // ---- level 2: sub-groups inside each group (find_sub_groups)
+        // ---- level 2: sub-groups inside each group, then level 3 inside those (the
+        // level-1 scratch arrays kFirst / kLcp serve both searches in turn)
         if (n_cgroups > 0) {
-            n_sub = find_sub_groups(dyn, stride, hkey, hval, hbits, scg, cgroups, p.page_table, p.ld, p.num_pages,
-                                    p.min_cascade_pages, B, ps, r0, r1, n_cgroups, members1, s_tmp2);
-            n_cgroups += n_sub;
+            if (tid == 0) {
+                s_cx.dyn = dyn;
+                s_cx.hkey = hkey;
+                s_cx.hval = hval;
+                s_cx.scg = scg;
+                s_cx.cgroups = cgroups;
+                s_cx.page_table = p.page_table;
+                s_cx.ld_table = p.ld;
+                s_cx.num_pages = p.num_pages;
+                s_cx.stride = stride;
+                s_cx.hbits = hbits;
+                s_cx.min_pages = p.min_cascade_pages;
+                s_cx.B = B;
+                s_cx.ps = ps;
+                // records the searches may number in all: the shared-memory copy holds smem_batch + 1
+                s_cx.max_groups = min(p.smem_batch + 1, p.lay.max_casc_groups);
+            }
+            __syncthreads();
+            // level 2 inside the top-level groups, then (when it found any) level 3 inside level
+            // 2's, through one call site (a second one cost the kernel registers)
+            int members = members1;
+            for (int level = 2; level <= 3; ++level) {
+                const bool l2 = level == 2;
+                int m_new = 0;
+                const int n_new = find_next_level(&s_cx, l2 ? sa(kCgid) : sa(kCgid2), sa(kFirst), sa(kLcp),
+                                                  l2 ? sa(kCnt) : g3(2), l2 ? sa(kLeader2) : g3(0),
+                                                  l2 ? sa(kCgid2) : g3(1), n_cgroups, members, s_tmp2, &m_new);
+                n_cgroups += n_new;
+                members += m_new;
+                if (l2) n_sub = n_new;
+                else n_sub3 = n_new;
+                if (n_new == 0) break;
+            }
         }
         }  // some candidates share a first page
     }
     auto casc_of = [&](int i) { return casc && n_cgroups > 0 ? sa(kCgid)[i] : -1; };
     auto casc2_of = [&](int i) { return casc && n_cgroups > 0 ? sa(kCgid2)[i] : -1; };
+    auto casc3_of = [&](int i) { return n_sub3 > 0 ? g3(1)[i] : -1; };
     // keys before request i's decode tail: its deepest shared prefix (0 for no group)
     auto prefix_of = [&](int i) {
+        const int g3 = casc3_of(i);
+        if (g3 >= 0) return scg[g3].prefix_len;
         const int g2 = casc2_of(i);
         if (g2 >= 0) return scg[g2].prefix_len;
         const int g = casc_of(i);
@@ -594,8 +663,8 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     };
     // prefix partial slots of request i (its groups' chunks)
     auto prefix_parts = [&](int i) {
-        const int g = casc_of(i), g2 = casc2_of(i);
-        return (g >= 0 ? scg[g].n_chunks : 0) + (g2 >= 0 ? scg[g2].n_chunks : 0);
+        const int g = casc_of(i), g2 = casc2_of(i), g3 = casc3_of(i);
+        return (g >= 0 ? scg[g].n_chunks : 0) + (g2 >= 0 ? scg[g2].n_chunks : 0) + (g3 >= 0 ? scg[g3].n_chunks : 0);
     };
 
     // ---- pass 1: validate, count decode groups and prefill tiles, sum decode key extents
@@ -657,11 +726,12 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
 
     // ---- cascade groups: key chunks of each prefix (about `target` prefix-pass units in
     // total, see below), unit ranges, member lists.  A member takes one
-    // partial slot per chunk of each of its groups; with sub-groups in the batch each
-    // level gets at most half the chunks, so no member needs more than kMaxCascChunks.
+    // partial slot per chunk of each of its groups; with deeper levels in the batch each
+    // level gets at most a half (two levels) or a third (three) of the chunks, so no member
+    // needs more than kMaxCascChunks.
     if (casc && n_cgroups > 0) {
         const int ng = n_cgroups;
-        const int nc_cap = n_sub > 0 ? kMaxCascChunks / 2 : kMaxCascChunks;
+        const int nc_cap = kMaxCascChunks / (1 + (n_sub > 0) + (n_sub3 > 0));
         const int gch = (ng + kThreads - 1) / kThreads;
         const int g0 = min(ng, tid * gch), g1 = min(ng, g0 + gch);
         int pv[2] = {0, 0};  // pair units; (member, 16 prefix keys) pairs
@@ -706,11 +776,13 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         if (tid == 0) s_casc_units = ut[0];
         // each member takes a slot of its group's member list (filled when its decode
         // group is written below); the first-page array is free again
-        // (and of its sub-group's: the slot goes to kLcp, free since level 2 was numbered)
+        // (and of its sub-group's: the slot goes to kLcp, free since the searches ended; of
+        // its level-3 group's: the slot replaces its own lead3 entry, read only by itself)
         for (int i = tid; i < B; i += kThreads) {
             if (sa(kCgid)[i] < 0) continue;
             sa(kFirst)[i] = atomicAdd(&sa(kMpos)[sa(kLeader)[i]], 1);
             if (sa(kCgid2)[i] >= 0) sa(kLcp)[i] = atomicAdd(&sa(kCnt)[sa(kLeader2)[i]], 1);
+            if (casc3_of(i) >= 0) g3(0)[i] = atomicAdd(&g3(2)[g3(0)[i]], 1);
         }
     }
     __syncthreads();
@@ -887,7 +959,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
             if (p.use_prefill && n > TB) continue;  // prefill units: emitted below
             const int ng = (n + TB - 1) / TB;
             const int lp = prefix_of(i);
-            const int cg = casc_of(i), cg2 = casc2_of(i);
+            const int cg = casc_of(i), cg2 = casc2_of(i), cg3 = casc3_of(i);
             const int npre = prefix_parts(i);
             for (int g = 0; g < ng; ++g) {
                 const int a0 = g * TB, na = min(TB, n - a0);
@@ -914,6 +986,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
                 // then the sub-group's)
                 if (cg >= 0) cmembers[sa(kFirst)[i]] = make_int2(dg.tok0, pi + s);
                 if (cg2 >= 0) cmembers[sa(kLcp)[i]] = make_int2(dg.tok0, pi + s + scg[cg].n_chunks);
+                if (cg3 >= 0) cmembers[g3(0)[i]] = make_int2(dg.tok0, pi + s + scg[cg].n_chunks + scg[cg2].n_chunks);
                 for (int u = 0; u < s; ++u) {
                     DecUnit du;
                     du.group = gi;

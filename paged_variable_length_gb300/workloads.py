@@ -189,6 +189,40 @@ def cascade_tree(seed: int = 0, branches: int = 8, per_branch: int = 16, root: i
                                 f"ps{page_size}, {num_pages}-page pool")
 
 
+def cascade_tree3(seed: int = 0, fanout=(4, 4), per_leaf: int = 8, runs=(1024, 1024, 1024), lo: int = 16,
+                  hi: int = 512, page_size: int = 16, num_pages: int = 20000) -> Workload:
+    """A three-level prefix tree of single-token decodes: every row starts with the same
+    ``runs[0]``-token run of pages; ``fanout[0]`` branches each add a ``runs[1]``-token run
+    of their own; inside each branch ``fanout[1]`` twigs add a ``runs[2]``-token run; each
+    twig holds ``per_leaf`` rows, which end in private tails of U[lo, hi] tokens.  Default:
+    4 x 4 twigs of 8 rows (128 decodes), 1024 tokens a level; Hq 32, Hkv 8, D 128;
+    page_size 16 over a 20000-page pool."""
+    rng = np.random.default_rng(seed)
+    if any(r % page_size for r in runs):
+        raise ValueError("the shared runs are whole pages")
+    perm = [int(x) for x in rng.permutation(num_pages)]
+    take = lambda k: [perm.pop() for _ in range(k)]
+    root_pages = take(runs[0] // page_size)
+    rows, kv_lens = [], []
+    for _ in range(fanout[0]):
+        branch_pages = root_pages + take(runs[1] // page_size)
+        for _ in range(fanout[1]):
+            twig_pages = branch_pages + take(runs[2] // page_size)
+            for _ in range(per_leaf):
+                L = sum(runs) + int(rng.integers(lo, hi + 1))
+                rows.append(twig_pages + take(math.ceil(L / page_size) - len(twig_pages)))
+                kv_lens.append(L)
+    table = np.zeros((len(rows), max(len(r) for r in rows)), np.int32)
+    for i, r in enumerate(rows):
+        table[i, :len(r)] = r
+    return Workload("cascade_tree3", [1] * len(rows), kv_lens, 32, 8, 128, page_size, num_pages, table, 1.0, seed,
+                    shared_prefix_pages=runs[0] // page_size,
+                    extra={"fanout": tuple(fanout), "runs": tuple(runs), "per_leaf": per_leaf},
+                    description=f"cascade tree, three levels: {fanout[0]}x{fanout[1]}x{per_leaf} decodes, "
+                                f"{runs[0]}/{runs[1]}/{runs[2]}-token shared runs, tails U[{lo},{hi}], "
+                                f"Hq32/Hkv8/D128, ps{page_size}, {num_pages}-page pool")
+
+
 def ragged_prefill(seed: int = 0, batch: int = 8, lo: int = 256, hi: int = 4096) -> Workload:
     """The prefill workload's requests (8 fresh prefills, len U[256,4096], Hq 32, Hkv 8,
     D 128) over contiguous K/V: page_size 1, the "pool" is the batch's own k / v rows and
@@ -237,6 +271,7 @@ WORKLOADS = {
     "mixed": mixed,
     "cascade": cascade,
     "cascade_tree": cascade_tree,
+    "cascade_tree3": cascade_tree3,
     "specdec": spec_decode,
     "ragged": ragged_prefill,
 }

@@ -148,13 +148,15 @@ def _fp8_sampled(wl, n_rows=1500, seed=0):
     return pva.attn_debug_plan_counts(eng.meta)
 
 
-@pytest.mark.parametrize("name", ["prefill", "mixed", "cascade", "cascade_tree", "specdec"])
+@pytest.mark.parametrize("name", ["prefill", "mixed", "cascade", "cascade_tree", "cascade_tree3", "specdec"])
 def test_fp8_full_size_workloads(name):
     counts = _fp8_sampled(W.WORKLOADS[name](0))
     if name == "cascade":
         assert counts["casc_groups"] >= 1, "the shared prefix should run as a prefix pass"
     if name == "cascade_tree":
         assert counts["casc_groups"] == 9, "a root group and 8 branch sub-groups"
+    if name == "cascade_tree3":
+        assert counts["casc_groups"] == 21, "a root group, 4 branches and 16 twigs"
     if name in ("prefill", "mixed"):
         assert counts["pre_tiles"] > 0, "prefills should run on the tensor-core kernel"
 
@@ -167,6 +169,14 @@ def test_fp8_shared_prefix_groups():
     wl = _cascade_batch(seed=4)
     _fp8_case(wl)
     _fp8_case(wl, enable_cascade=False)
+
+
+def test_fp8_three_level_prefix_tree():
+    """Three levels of shared prefixes (two twigs under one branch, a partial sharer, a
+    member a level deeper than any group) in one FP8 batch."""
+    from test_parity_gpu import _tree3_batch
+
+    _fp8_case(_tree3_batch(seed=4))
 
 
 def test_fp8_two_level_prefix_tree():

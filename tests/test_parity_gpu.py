@@ -365,6 +365,72 @@ def test_two_level_prefix_tree_head_layouts(Hq, Hkv, D):
     assert pva.attn_debug_plan_counts(eng.meta)["casc_groups"] == 5
 
 
+def _tree3_batch(seed=0, Hq=32, Hkv=8, D=128, ps=16):
+    """Three levels of shared prefixes.  Root R (9 pages) holds branch R1 (8 more shared
+    pages), in which twig R1a shares 10 more pages (5 members, one cut short after 8 of
+    them: the twig's prefix stops at the shortest) and twig R1b 8 more (2 members); R1 also
+    has members with private pages after it, and one member goes a fourth level deeper
+    (shared with nobody: its tail).  Branch R2 (12 more pages) has 3 members and no twig.
+    Plus a member of R alone, an unrelated decode and a prefill: 1 root group, 2 branches,
+    2 twigs."""
+    rng = np.random.default_rng(seed)
+    P = 1200
+    perm = list(rng.permutation(P))
+    take = lambda k: [int(perm.pop()) for _ in range(k)]
+    rows, q_lens, kv_lens = [], [], []
+
+    def add(shared, tail):
+        L = len(shared) * ps + tail
+        rows.append(shared + take((L + ps - 1) // ps - len(shared)))
+        q_lens.append(1)
+        kv_lens.append(L)
+
+    root = take(9)
+    r1, r2 = root + take(8), root + take(12)
+    r1a, r1b = r1 + take(10), r1 + take(8)
+    for tail in (1, 17, 40):
+        add(r1a, tail)
+    add(r1a[:len(r1) + 8], 33)                  # in the twig for 8 of its 10 pages
+    for tail in (5, 61):
+        add(r1b, tail)
+    for tail in (2, 29):
+        add(r1, tail)
+    add(r1a + take(9), 3)                      # a fourth shared level would start here: nobody shares it
+    for tail in (8, 44, 90):
+        add(r2, tail)
+    add(root, 70)
+    add([], 300)                                # unrelated decode
+    L = 180                                     # a prefill in the same batch
+    rows.append(take((L + ps - 1) // ps)); q_lens.append(L); kv_lens.append(L)
+    return _table_workload(q_lens, kv_lens, rows, Hq, Hkv, D, ps, P, seed)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_three_level_prefix_tree_matches_the_oracle(seed):
+    wl = _tree3_batch(seed)
+    _, eng = _full_check(wl)
+    counts = pva.attn_debug_plan_counts(eng.meta)
+    assert counts["casc_groups"] == 5, counts
+    _full_check(wl, enable_cascade=False)
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(28, 4, 128), (16, 4, 64)])
+def test_three_level_prefix_tree_head_layouts(Hq, Hkv, D):
+    wl = _tree3_batch(3, Hq=Hq, Hkv=Hkv, D=D)
+    _, eng = _full_check(wl)
+    assert pva.attn_debug_plan_counts(eng.meta)["casc_groups"] == 5
+
+
+def test_full_size_three_level_prefix_tree():
+    """128 decodes: 1024 shared tokens, 4 branches of 1024 more, 4 twigs of 1024 more each."""
+    wl = W.cascade_tree3(0)
+    t = W.make_tensors(wl, DEV)
+    eng = make_engine(wl)
+    eng.prepare(t["cu_seqlens_q"], t["cache_seqlens"], t["page_table"], wl.total_tokens)
+    assert pva.attn_debug_plan_counts(eng.meta)["casc_groups"] == 1 + 4 + 16
+    _sampled_check(wl)
+
+
 def test_sub_group_larger_than_a_tile_pair():
     """A sub-group of 70 members (G 4: 32 member rows per tile) under a 27-page root
     (432 keys: the sub-group's keys start off a 128-key boundary), a second sub-group of
@@ -490,10 +556,12 @@ def test_ragged_full_size_workload():
 def _random_forest(seed, Hq=32, Hkv=8, D=128, ps=16, min_pages=8):
     """Random shared-prefix forests: 1-3 roots of min_pages-1 .. min_pages+5 pages (some too
     short for a group), each with 1-3 branches of min_pages-1 .. min_pages+3 further
-    pages, leaves that sometimes share a third run (a level below the second: it must run
-    as part of their tails), leaves cut short inside a shared run, multi-token decodes
+    pages, leaves that sometimes share a third run (a third level when long enough) and
+    a fourth (below the deepest level detected: it runs as part of their tails), leaves cut
+    short inside a shared run, multi-token decodes
     (never prefix members), unrelated decodes and a prefill."""
     rng = np.random.default_rng(1000 + seed)
+    rng4 = np.random.default_rng(3000 + seed)
     P = 4000
     perm = [int(x) for x in rng.permutation(P)]
     take = lambda k: [perm.pop() for _ in range(int(k))]
@@ -510,8 +578,13 @@ def _random_forest(seed, Hq=32, Hkv=8, D=128, ps=16, min_pages=8):
         for _ in range(int(rng.integers(1, 5))):
             branch = root + take(rng.integers(min_pages - 1, min_pages + 4))
             third = branch + take(rng.integers(1, 12)) if rng.random() < 0.4 else None
+            # (the fourth runs draw from a generator of their own: the forests of the other
+            # draws stay what they were)
+            fourth = third + take(rng4.integers(1, 12)) if third is not None and rng4.random() < 0.5 else None
             for _ in range(int(rng.integers(2, 7))):
                 shared = third if third is not None and rng.random() < 0.6 else branch
+                if fourth is not None and shared is third and rng4.random() < 0.5:
+                    shared = fourth
                 if rng.random() < 0.2:  # shares only part of the run
                     shared = shared[:int(rng.integers(1, len(shared) + 1))]
                 n = 1 if rng.random() < 0.85 else int(rng.integers(2, 4))
