@@ -58,21 +58,15 @@ def parse():
 # what they were at capture time; after any change the roofline reports null.
 NCU_TRAFFIC = {
     ("decode", "decode"): {
-        "bytes": 617.566208e6,
+        "bytes": 617.533440e6,
         "sources": ['paged_variable_length_gb300/csrc/decode.cu', 'paged_variable_length_gb300/csrc/device_utils.cuh', 'paged_variable_length_gb300/csrc/pva_internal.h'],
-        "sha256_16": "d22e27864064e1e0",
+        "sha256_16": "2f6f7404ef847958",
         "summary": "profiles/decode_kernel_decode_workload.md",
     },
-    ("decode", "decode-e4m3"): {
-        "bytes": 310.656512e6,
-        "sources": ['paged_variable_length_gb300/csrc/decode.cu', 'paged_variable_length_gb300/csrc/device_utils.cuh', 'paged_variable_length_gb300/csrc/pva_internal.h'],
-        "sha256_16": "d22e27864064e1e0",
-        "summary": "profiles/decode_kernel_fp8_decode_workload.md",
-    },
     ("tensor_core", "prefill"): {
-        "bytes": 220.372992e6,
+        "bytes": 219.442944e6,
         "sources": ['paged_variable_length_gb300/csrc/prefill_tc.cu', 'paged_variable_length_gb300/csrc/device_utils.cuh', 'paged_variable_length_gb300/csrc/tc_utils.cuh', 'paged_variable_length_gb300/csrc/pva_internal.h'],
-        "sha256_16": "d7afb9e03a9ef989",
+        "sha256_16": "aea784ccc5c7a3d4",
         "summary": "profiles/prefill_kernel_prefill_workload.md",
     },
 }
