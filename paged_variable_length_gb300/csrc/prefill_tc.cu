@@ -479,35 +479,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int key = uv.key_base + j * kPreKeys + r;
                             pg[m] = (r < kPreRows && key < kv_end) ? prow[kTok ? key : key >> p.page_shift] : 0;
                         }
-                        int64_t off[kG8];
+                        // each row's slot as 32 bits (a pool that fits in HBM has fewer than 2^32
+                        // slots; kNoSlot: the row is not copied), the address formed at the copy:
+                        // the producer warps run in 104 registers
+                        constexpr uint32_t kNoSlot = 0xFFFFFFFFu;
+                        uint32_t sl[kG8];
                         bool bad = false;
 #pragma unroll
                         for (int m = 0; m < kG8; ++m) {
                             const int r = pwarp * 4 + grp + 12 * m;
                             const int key = uv.key_base + j * kPreKeys + r;
-                            off[m] = -1;
+                            sl[m] = kNoSlot;
                             if (r < kPreRows && key < kv_end) {
                                 int64_t page = pg[m];
                                 if (page < 0 || page >= p.num_pages) {
                                     bad = true;
                                     page = 0;
                                 }
-                                const int64_t slot = kTok ? page : (page << p.page_shift) + (key & ps_mask);
-                                off[m] = (slot * p.num_kv_heads + pt.kvh) * D + c8 * 8;
+                                sl[m] = (uint32_t)(kTok ? page : (page << p.page_shift) + (key & ps_mask));
                             }
                         }
                         if (bad) dev::set_error(err, kErrPage);
+                        const int64_t slot_elems = (int64_t)p.num_kv_heads * D;
                         auto copy_g8 = [&](uint8_t* tile, const uint16_t* base) {
                             const uint32_t t0 = dev::smem_u32(tile);
+                            const uint16_t* b0 = base + (int64_t)pt.kvh * D + c8 * 8;
 #pragma unroll
                             for (int m = 0; m < kG8; ++m) {
                                 const int r = pwarp * 4 + grp + 12 * m;
-                                if (off[m] < 0) continue;
+                                if (sl[m] == kNoSlot) continue;
+                                const uint16_t* src = b0 + (int64_t)sl[m] * slot_elems;
                                 const uint32_t d = t0 + r * 128 + ((c8 ^ (r & 7)) << 4);
-                                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(base + off[m]));
+                                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src));
                                 if (D == 128)
                                     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d + kRegion),
-                                                 "l"(base + off[m] + 64));
+                                                 "l"(src + 64));
                             }
                         };
                         if (!wait_or_abort(&b->k_empty[st], ph ^ 1, wlim, b, err)) {
