@@ -11,8 +11,9 @@
 //   0. shared-prefix (cascade) groups: single-token decodes whose page tables start
 //      with the same run of pages ("Source walkthrough: Attention backends",
 //      section 3.3: the shared part is computed once and merged by log-sum-exp), and
-//      inside each group sub-groups whose rows continue with a further shared run (two
-//      levels of the prefix tree the page describes its multi-level form over);
+//      inside each group sub-groups whose rows continue with a further shared run, and
+//      inside those a third level (three levels of the prefix tree the page describes
+//      its multi-level form over);
 //   1. validate cu_seqlens_q / cache_seqlens (error word, never a trap) and
 //      classify each request: q_len * G <= 16 rows -> decode groups (the
 //      warp-MMA streaming kernel), otherwise -> 128-row tensor-core tiles;
