@@ -341,6 +341,196 @@ __device__ __noinline__ int find_next_level(const SearchCtx* cx, const int32_t* 
     return n_new;
 }
 
+// Pass 0 of the kernel below once some candidates share a first page: each member's
+// prefix with its leader (page-id compare), the top-level group records and each
+// member's group id.  Out of line, like the chunk planning below and the deeper levels
+// (find_next_level): most batches have no shared first page, and this code, inlined, lay
+// between the passes every batch runs, where the instruction fetch streamed through it
+// (3 to 8 us more per prepare, measured with the forward's kernels queued behind it).
+// Returns the number of groups and of their member-list entries.
+__device__ __noinline__ int2 build_prefix_groups(const PrepareParams& p, int32_t* dyn, int (*s_tmp2)[2]) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int B = p.batch, ps = p.page_size, stride = p.smem_batch + 1;
+    const int chunk_req = (B + kThreads - 1) / kThreads;
+    const int r0 = min(B, tid * chunk_req), r1 = min(B, r0 + chunk_req);
+    auto sa = [&](int a) { return dyn + a * stride; };
+    const int hbits = casc_hash_bits(p.smem_batch);
+    int32_t* hkey = dyn + kNumArrays * stride;
+    int32_t* hval = hkey + (1 << hbits);
+    CascGroup* scg = reinterpret_cast<CascGroup*>(hval + (1 << hbits));
+    CascGroup* cgroups = reinterpret_cast<CascGroup*>(p.ws + p.lay.casc_groups);
+    int32_t* first = sa(kFirst);
+    int32_t* leader = sa(kLeader);
+    int32_t* lcp = sa(kLcp);
+    int32_t* cnt = sa(kCnt);
+    int32_t* lim = sa(kMpos);
+    int n_cgroups = 0;
+    // Every member compares pages 1 .. lim-1 of its row with the leader's (page 0
+    // matched by construction), one warp per member: lanes read consecutive page ids,
+    // so each load instruction is one line of each row, 256 ids per step.  The group
+    // prefix is the smallest mismatch, or the smallest member's page count.
+    // The rows about to be compared (members' and leaders' page ids up to the pages
+    // compared) are requested into L2 here, all at once, so that the warps' compare steps
+    // below, one member after another, mostly find them there.  Only rows of requests
+    // that share a first page are touched: a batch without such requests reads no row.
+    for (int i = tid; i < B; i += kThreads) {
+        const int ld = leader[i];
+        const int l = (ld >= 0 && ld != i) ? min(lcp[i], lcp[ld]) : 0;
+        lim[i] = l;
+        const int pf = l > 0 ? l : ((ld == i && cnt[i] >= 2) ? lcp[i] : 0);
+        const char* row = reinterpret_cast<const char*>(p.page_table + (int64_t)i * p.ld);
+        for (int off = 4; off < pf * 4; off += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + off));
+    }
+    __syncthreads();
+    for (int i = tid; i < B; i += kThreads)
+        if (lim[i] > 0) atomicMin(&lcp[leader[i]], lim[i]);
+    {
+        constexpr int kU = kCmpPages;  // 8 ids per lane per step
+        const int warp = tid >> 5;
+        for (int i = warp; i < B; i += kWarps) {
+            const int l = lim[i];
+            if (l <= 1) continue;  // warp-uniform: i is the same for the whole warp
+            const int ld = leader[i];
+            const int32_t* ri = p.page_table + (int64_t)i * p.ld;
+            const int32_t* rl = p.page_table + (int64_t)ld * p.ld;
+            int mis = l;
+            for (int k0 = 1; k0 < l; k0 += 32 * kU) {
+                int va[kU], vb[kU];
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int k = k0 + u * 32 + lane;
+                    va[u] = k < l ? ri[k] : 0;
+                    vb[u] = k < l ? rl[k] : 0;
+                }
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int k = k0 + u * 32 + lane;
+                    if (k < l && va[u] != vb[u]) mis = min(mis, k);
+                }
+            }
+            mis = __reduce_min_sync(0xffffffffu, mis);
+            if (lane == 0 && mis < l) atomicMin(&lcp[ld], mis);
+        }
+    }
+    __syncthreads();
+    // group ids in leader order (a deterministic plan) and member slot ranges
+    int gv[2] = {0, 0};
+    for (int i = r0; i < r1; ++i)
+        if (is_group_leader(leader, cnt, lcp, i, p.min_cascade_pages)) {
+            gv[0] += 1;
+            gv[1] += cnt[i];
+        }
+    int gt[2];
+    block_scan<2>(gv, gt, s_tmp2);
+    {
+        int gid = gv[0], moff = gv[1];
+        for (int i = r0; i < r1; ++i) {
+            if (!is_group_leader(leader, cnt, lcp, i, p.min_cascade_pages)) continue;
+            sa(kCgid)[i] = gid;
+            CascGroup cg;
+            cg.leader = i;
+            cg.prefix_len = lcp[i] * ps;
+            cg.n_members = cnt[i];
+            cg.member_off = moff;
+            cg.n_chunks = 0;
+            cg.chunk_keys = 0;
+            cg.unit_off = 0;
+            cg.n_units = 0;
+            cg.key_base = 0;
+            cg.level = 0;
+            cg.pad0 = cg.pad1 = 0;
+            store_record(&cgroups[gid], cg);
+            scg[gid] = cg;
+            sa(kMpos)[i] = moff;  // next free member slot of the group
+            moff += cnt[i];
+            ++gid;
+        }
+    }
+    n_cgroups = gt[0];
+    __syncthreads();
+    // members take the group id of their leader (-1 when the leader leads no group)
+    for (int i = tid; i < B; i += kThreads) {
+        const int ld = leader[i];
+        if (ld >= 0 && ld != i)
+            sa(kCgid)[i] = is_group_leader(leader, cnt, lcp, ld, p.min_cascade_pages) ? sa(kCgid)[ld] : -1;
+    }
+    __syncthreads();
+    return make_int2(n_cgroups, gt[1]);  // groups, member-list entries
+}
+
+// Key chunks of each group's prefix (about `target` prefix-pass units in total, see
+// below), unit ranges, member lists.  A member takes one partial slot per chunk of each
+// of its groups; with deeper levels in the batch each level gets at most a half (two
+// levels) or a third (three) of the chunks, so no member needs more than
+// kMaxCascChunks.  Out of line for the reason given above.
+__device__ __noinline__ void plan_prefix_chunks(const PrepareParams& p, int32_t* dyn, int3 ng3,
+                                                unsigned long long work, int (*s_tmp2)[2], int (*s_tmp1)[1],
+                                                int* s_casc_units) {
+    const int tid = threadIdx.x;
+    const int B = p.batch, stride = p.smem_batch + 1, TM = p.pre_tokens, Hkv = p.num_kv_heads;
+    const int n_cgroups = ng3.x, n_sub = ng3.y, n_sub3 = ng3.z;
+    auto sa = [&](int a) { return dyn + a * stride; };
+    auto g3 = [&](int a) { return reinterpret_cast<int32_t*>(p.ws + p.lay.req_scratch) + a * (B + 1); };
+    auto casc3_of = [&](int i) { return n_sub3 > 0 ? g3(1)[i] : -1; };
+    const int hbits = casc_hash_bits(p.smem_batch);
+    CascGroup* scg = reinterpret_cast<CascGroup*>(dyn + kNumArrays * stride + 2 * (1 << hbits));
+    CascGroup* cgroups = reinterpret_cast<CascGroup*>(p.ws + p.lay.casc_groups);
+    const int ng = n_cgroups;
+    const int nc_cap = kMaxCascChunks / (1 + (n_sub > 0) + (n_sub3 > 0));
+    const int gch = (ng + kThreads - 1) / kThreads;
+    const int g0 = min(ng, tid * gch), g1 = min(ng, g0 + gch);
+    int pv[2] = {0, 0};  // pair units; (member, 16 prefix keys) pairs
+    for (int g = g0; g < g1; ++g) {
+        pv[0] += casc_pair_units(scg[g].n_members, TM, Hkv);
+        pv[1] += scg[g].n_members * ((scg[g].prefix_len - scg[g].key_base) / 16);
+    }
+    int pt[2];
+    block_scan<2>(pv, pt, s_tmp2);
+    const int pair_units = max(pt[0], 1);
+    // Units aimed for: the decode tails start on the SMs the prefix pass leaves free, so
+    // the pass gets about the share of the SMs its tensor-core time takes beside the
+    // tails' HBM time (prefix_pass_target, with the per-SM rates measured on GB300).
+    const int target = prefix_pass_target(pt[1], work, p.group, p.kv_fp8, p.lay.casc_target);
+    int uv[1] = {0};
+    for (int g = g0; g < g1; ++g) {
+        const CascGroup cg = scg[g];
+        const int span = cg.prefix_len - cg.key_base;
+        int nc = (target + pair_units - 1) / pair_units;
+        nc = max(1, min(nc, min(nc_cap, (span + kPreKeys - 1) / kPreKeys)));
+        const int ck = ((span + nc - 1) / nc + kPreKeys - 1) / kPreKeys * kPreKeys;
+        uv[0] += (span + ck - 1) / ck * casc_pair_units(cg.n_members, TM, Hkv);
+    }
+    int ut[1];
+    block_scan<1>(uv, ut, s_tmp1);
+    int uoff = uv[0];
+    for (int g = g0; g < g1; ++g) {
+        CascGroup cg = scg[g];
+        const int span = cg.prefix_len - cg.key_base;
+        int nc = (target + pair_units - 1) / pair_units;
+        nc = max(1, min(nc, min(nc_cap, (span + kPreKeys - 1) / kPreKeys)));
+        const int ck = ((span + nc - 1) / nc + kPreKeys - 1) / kPreKeys * kPreKeys;
+        cg.chunk_keys = ck;
+        cg.n_chunks = (span + ck - 1) / ck;
+        cg.unit_off = uoff;
+        cg.n_units = cg.n_chunks * casc_pair_units(cg.n_members, TM, Hkv);
+        sa(kCUoff)[g] = uoff;
+        uoff += cg.n_units;
+        store_record(&cgroups[g], cg);
+        scg[g] = cg;
+    }
+    if (tid == 0) *s_casc_units = ut[0];
+    // each member takes a slot of its group's member list (filled when its decode
+    // group is written below); the first-page array is free again
+    // (and of its sub-group's: the slot goes to kLcp, free since the searches ended; of
+    // its level-3 group's: the slot replaces its own lead3 entry, read only by itself)
+    for (int i = tid; i < B; i += kThreads) {
+        if (sa(kCgid)[i] < 0) continue;
+        sa(kFirst)[i] = atomicAdd(&sa(kMpos)[sa(kLeader)[i]], 1);
+        if (sa(kCgid2)[i] >= 0) sa(kLcp)[i] = atomicAdd(&sa(kCnt)[sa(kLeader2)[i]], 1);
+        if (casc3_of(i) >= 0) g3(0)[i] = atomicAdd(&g3(2)[g3(0)[i]], 1);
+    }
+}
+
 // Pass 3 of the balanced decode split (see the kernel below): the decode groups of this
 // thread's requests with their start on the key line (g0) and their pieces (one, plus one
 // per CTA share boundary inside the group), and dec_first: for every CTA whose share
@@ -520,135 +710,47 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         }
         // no two candidates share a first page (the usual decode batch): no groups
         if (__syncthreads_or(has_member)) {
-        // Every member compares pages 1 .. lim-1 of its row with the leader's (page 0
-        // matched by construction), one warp per member: lanes read consecutive page ids,
-        // so each load instruction is one line of each row, 256 ids per step.  The group
-        // prefix is the smallest mismatch, or the smallest member's page count.
-        // The rows about to be compared (members' and leaders' page ids up to the pages
-        // compared) are requested into L2 here, all at once, so that the warps' compare steps
-        // below, one member after another, mostly find them there.  Only rows of requests
-        // that share a first page are touched: a batch without such requests reads no row.
-        for (int i = tid; i < B; i += kThreads) {
-            const int ld = leader[i];
-            const int l = (ld >= 0 && ld != i) ? min(lcp[i], lcp[ld]) : 0;
-            lim[i] = l;
-            const int pf = l > 0 ? l : ((ld == i && cnt[i] >= 2) ? lcp[i] : 0);
-            const char* row = reinterpret_cast<const char*>(p.page_table + (int64_t)i * p.ld);
-            for (int off = 4; off < pf * 4; off += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + off));
-        }
-        __syncthreads();
-        for (int i = tid; i < B; i += kThreads)
-            if (lim[i] > 0) atomicMin(&lcp[leader[i]], lim[i]);
-        {
-            constexpr int kU = kCmpPages;  // 8 ids per lane per step
-            const int warp = tid >> 5;
-            for (int i = warp; i < B; i += kWarps) {
-                const int l = lim[i];
-                if (l <= 1) continue;  // warp-uniform: i is the same for the whole warp
-                const int ld = leader[i];
-                const int32_t* ri = p.page_table + (int64_t)i * p.ld;
-                const int32_t* rl = p.page_table + (int64_t)ld * p.ld;
-                int mis = l;
-                for (int k0 = 1; k0 < l; k0 += 32 * kU) {
-                    int va[kU], vb[kU];
-#pragma unroll
-                    for (int u = 0; u < kU; ++u) {
-                        const int k = k0 + u * 32 + lane;
-                        va[u] = k < l ? ri[k] : 0;
-                        vb[u] = k < l ? rl[k] : 0;
-                    }
-#pragma unroll
-                    for (int u = 0; u < kU; ++u) {
-                        const int k = k0 + u * 32 + lane;
-                        if (k < l && va[u] != vb[u]) mis = min(mis, k);
-                    }
+            const int2 c = build_prefix_groups(p, dyn, s_tmp2);
+            n_cgroups = c.x;
+            const int members1 = c.y;
+            // ---- level 2: sub-groups inside each group, then level 3 inside those (the
+            // level-1 scratch arrays kFirst / kLcp serve both searches in turn)
+            if (n_cgroups > 0) {
+                if (tid == 0) {
+                    s_cx.dyn = dyn;
+                    s_cx.hkey = hkey;
+                    s_cx.hval = hval;
+                    s_cx.scg = scg;
+                    s_cx.cgroups = cgroups;
+                    s_cx.page_table = p.page_table;
+                    s_cx.ld_table = p.ld;
+                    s_cx.num_pages = p.num_pages;
+                    s_cx.stride = stride;
+                    s_cx.hbits = hbits;
+                    s_cx.min_pages = p.min_cascade_pages;
+                    s_cx.B = B;
+                    s_cx.ps = ps;
+                    // records the searches may number in all: the shared-memory copy holds smem_batch + 1
+                    s_cx.max_groups = min(p.smem_batch + 1, p.lay.max_casc_groups);
                 }
-                mis = __reduce_min_sync(0xffffffffu, mis);
-                if (lane == 0 && mis < l) atomicMin(&lcp[ld], mis);
+                __syncthreads();
+                // level 2 inside the top-level groups, then (when it found any) level 3 inside level
+                // 2's, through one call site (a second one cost the kernel registers)
+                int members = members1;
+                for (int level = 2; level <= 3; ++level) {
+                    const bool l2 = level == 2;
+                    int m_new = 0;
+                    const int n_new = find_next_level(&s_cx, l2 ? sa(kCgid) : sa(kCgid2), sa(kFirst), sa(kLcp),
+                                                      l2 ? sa(kCnt) : g3(2), l2 ? sa(kLeader2) : g3(0),
+                                                      l2 ? sa(kCgid2) : g3(1), n_cgroups, members, s_tmp2, &m_new);
+                    n_cgroups += n_new;
+                    members += m_new;
+                    if (l2) n_sub = n_new;
+                    else n_sub3 = n_new;
+                    if (n_new == 0) break;
+                }
             }
         }
-        __syncthreads();
-        // group ids in leader order (a deterministic plan) and member slot ranges
-        int gv[2] = {0, 0};
-        for (int i = r0; i < r1; ++i)
-            if (is_group_leader(leader, cnt, lcp, i, p.min_cascade_pages)) {
-                gv[0] += 1;
-                gv[1] += cnt[i];
-            }
-        int gt[2];
-        block_scan<2>(gv, gt, s_tmp2);
-        {
-            int gid = gv[0], moff = gv[1];
-            for (int i = r0; i < r1; ++i) {
-                if (!is_group_leader(leader, cnt, lcp, i, p.min_cascade_pages)) continue;
-                sa(kCgid)[i] = gid;
-                CascGroup cg;
-                cg.leader = i;
-                cg.prefix_len = lcp[i] * ps;
-                cg.n_members = cnt[i];
-                cg.member_off = moff;
-                cg.n_chunks = 0;
-                cg.chunk_keys = 0;
-                cg.unit_off = 0;
-                cg.n_units = 0;
-                cg.key_base = 0;
-                cg.level = 0;
-                cg.pad0 = cg.pad1 = 0;
-                store_record(&cgroups[gid], cg);
-                scg[gid] = cg;
-                sa(kMpos)[i] = moff;  // next free member slot of the group
-                moff += cnt[i];
-                ++gid;
-            }
-        }
-        n_cgroups = gt[0];
-        __syncthreads();
-        // members take the group id of their leader (-1 when the leader leads no group)
-        for (int i = tid; i < B; i += kThreads) {
-            const int ld = leader[i];
-            if (ld >= 0 && ld != i)
-                sa(kCgid)[i] = is_group_leader(leader, cnt, lcp, ld, p.min_cascade_pages) ? sa(kCgid)[ld] : -1;
-        }
-        const int members1 = gt[1];  // member-list entries of the top-level groups
-        __syncthreads();
-        // ---- level 2: sub-groups inside each group, then level 3 inside those (the
-        // level-1 scratch arrays kFirst / kLcp serve both searches in turn)
-        if (n_cgroups > 0) {
-            if (tid == 0) {
-                s_cx.dyn = dyn;
-                s_cx.hkey = hkey;
-                s_cx.hval = hval;
-                s_cx.scg = scg;
-                s_cx.cgroups = cgroups;
-                s_cx.page_table = p.page_table;
-                s_cx.ld_table = p.ld;
-                s_cx.num_pages = p.num_pages;
-                s_cx.stride = stride;
-                s_cx.hbits = hbits;
-                s_cx.min_pages = p.min_cascade_pages;
-                s_cx.B = B;
-                s_cx.ps = ps;
-                // records the searches may number in all: the shared-memory copy holds smem_batch + 1
-                s_cx.max_groups = min(p.smem_batch + 1, p.lay.max_casc_groups);
-            }
-            __syncthreads();
-            // level 2 inside the top-level groups, then (when it found any) level 3 inside level
-            // 2's, through one call site (a second one cost the kernel registers)
-            int members = members1;
-            for (int level = 2; level <= 3; ++level) {
-                const bool l2 = level == 2;
-                int m_new = 0;
-                const int n_new = find_next_level(&s_cx, l2 ? sa(kCgid) : sa(kCgid2), sa(kFirst), sa(kLcp),
-                                                  l2 ? sa(kCnt) : g3(2), l2 ? sa(kLeader2) : g3(0),
-                                                  l2 ? sa(kCgid2) : g3(1), n_cgroups, members, s_tmp2, &m_new);
-                n_cgroups += n_new;
-                members += m_new;
-                if (l2) n_sub = n_new;
-                else n_sub3 = n_new;
-                if (n_new == 0) break;
-            }
-        }
-        }  // some candidates share a first page
     }
     auto casc_of = [&](int i) { return casc && n_cgroups > 0 ? sa(kCgid)[i] : -1; };
     auto casc2_of = [&](int i) { return casc && n_cgroups > 0 ? sa(kCgid2)[i] : -1; };
@@ -725,67 +827,9 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         if (tid == 0) tile_off[B] = tot3[1];
     }
 
-    // ---- cascade groups: key chunks of each prefix (about `target` prefix-pass units in
-    // total, see below), unit ranges, member lists.  A member takes one
-    // partial slot per chunk of each of its groups; with deeper levels in the batch each
-    // level gets at most a half (two levels) or a third (three) of the chunks, so no member
-    // needs more than kMaxCascChunks.
-    if (casc && n_cgroups > 0) {
-        const int ng = n_cgroups;
-        const int nc_cap = kMaxCascChunks / (1 + (n_sub > 0) + (n_sub3 > 0));
-        const int gch = (ng + kThreads - 1) / kThreads;
-        const int g0 = min(ng, tid * gch), g1 = min(ng, g0 + gch);
-        int pv[2] = {0, 0};  // pair units; (member, 16 prefix keys) pairs
-        for (int g = g0; g < g1; ++g) {
-            pv[0] += casc_pair_units(scg[g].n_members, TM, Hkv);
-            pv[1] += scg[g].n_members * ((scg[g].prefix_len - scg[g].key_base) / 16);
-        }
-        int pt[2];
-        block_scan<2>(pv, pt, s_tmp2);
-        const int pair_units = max(pt[0], 1);
-        // Units aimed for: the decode tails start on the SMs the prefix pass leaves free, so
-        // the pass gets about the share of the SMs its tensor-core time takes beside the
-        // tails' HBM time (prefix_pass_target, with the per-SM rates measured on GB300).
-        const int target = prefix_pass_target(pt[1], s_work, p.group, p.kv_fp8, p.lay.casc_target);
-        int uv[1] = {0};
-        for (int g = g0; g < g1; ++g) {
-            const CascGroup cg = scg[g];
-            const int span = cg.prefix_len - cg.key_base;
-            int nc = (target + pair_units - 1) / pair_units;
-            nc = max(1, min(nc, min(nc_cap, (span + kPreKeys - 1) / kPreKeys)));
-            const int ck = ((span + nc - 1) / nc + kPreKeys - 1) / kPreKeys * kPreKeys;
-            uv[0] += (span + ck - 1) / ck * casc_pair_units(cg.n_members, TM, Hkv);
-        }
-        int ut[1];
-        block_scan<1>(uv, ut, s_tmp1);
-        int uoff = uv[0];
-        for (int g = g0; g < g1; ++g) {
-            CascGroup cg = scg[g];
-            const int span = cg.prefix_len - cg.key_base;
-            int nc = (target + pair_units - 1) / pair_units;
-            nc = max(1, min(nc, min(nc_cap, (span + kPreKeys - 1) / kPreKeys)));
-            const int ck = ((span + nc - 1) / nc + kPreKeys - 1) / kPreKeys * kPreKeys;
-            cg.chunk_keys = ck;
-            cg.n_chunks = (span + ck - 1) / ck;
-            cg.unit_off = uoff;
-            cg.n_units = cg.n_chunks * casc_pair_units(cg.n_members, TM, Hkv);
-            sa(kCUoff)[g] = uoff;
-            uoff += cg.n_units;
-            store_record(&cgroups[g], cg);
-            scg[g] = cg;
-        }
-        if (tid == 0) s_casc_units = ut[0];
-        // each member takes a slot of its group's member list (filled when its decode
-        // group is written below); the first-page array is free again
-        // (and of its sub-group's: the slot goes to kLcp, free since the searches ended; of
-        // its level-3 group's: the slot replaces its own lead3 entry, read only by itself)
-        for (int i = tid; i < B; i += kThreads) {
-            if (sa(kCgid)[i] < 0) continue;
-            sa(kFirst)[i] = atomicAdd(&sa(kMpos)[sa(kLeader)[i]], 1);
-            if (sa(kCgid2)[i] >= 0) sa(kLcp)[i] = atomicAdd(&sa(kCnt)[sa(kLeader2)[i]], 1);
-            if (casc3_of(i) >= 0) g3(0)[i] = atomicAdd(&g3(2)[g3(0)[i]], 1);
-        }
-    }
+    // ---- shared-prefix groups: key chunks, unit ranges, member lists (out of line)
+    if (casc && n_cgroups > 0)
+        plan_prefix_chunks(p, dyn, make_int3(n_cgroups, n_sub, n_sub3), s_work, s_tmp2, s_tmp1, &s_casc_units);
     __syncthreads();
     const int tiles_total = tot3[1] + s_casc_units;
     if (tot3[0] > p.lay.max_dec_groups || tiles_total > p.lay.max_pre_tiles) {
