@@ -179,10 +179,12 @@ __device__ __noinline__ int find_next_level(const SearchCtx* cx, const int32_t* 
     const int32_t* cu = sa(kCu);
     const int32_t* lens = sa(kLen);
     *members_total = 0;
+    #pragma unroll 1
     for (int h = tid; h < HT; h += kThreads) {
         hkey[h] = -1;
         hval[h] = 0x7fffffff;
     }
+    #pragma unroll 1
     for (int i = tid; i < B; i += kThreads) {
         const int g = parent[i];
         int pg = -1, pages = 0;
@@ -211,6 +213,7 @@ __device__ __noinline__ int find_next_level(const SearchCtx* cx, const int32_t* 
                                     0x7fffffffu);
     };
     int dup = 0;  // some key met twice (in a warp, or already in the table)
+    #pragma unroll 1
     for (int i0 = 0; i0 < B; i0 += kThreads) {
         const int i = i0 + tid;
         const int f = i < B ? key2(i) : -1;
@@ -235,10 +238,12 @@ __device__ __noinline__ int find_next_level(const SearchCtx* cx, const int32_t* 
     // no two members of a group continue with the same page: no sub-group (the usual
     // case; the rest of the search is skipped)
     if (!__syncthreads_or(dup)) {
+        #pragma unroll 1
         for (int i = tid; i < B; i += kThreads) cgid2[i] = -1;
         __syncthreads();
         return 0;
     }
+    #pragma unroll 1
     for (int i0 = 0; i0 < B; i0 += kThreads) {
         const int i = i0 + tid;
         int ld = (i < B && page2[i] >= 0) ? hval[lead2[i]] : -1;
@@ -248,16 +253,19 @@ __device__ __noinline__ int find_next_level(const SearchCtx* cx, const int32_t* 
         if (ld >= 0 && lane == __ffs(peers) - 1) atomicAdd(&cnt2[ld], __popc(peers));
     }
     __syncthreads();
+    #pragma unroll 1
     for (int i = tid; i < B; i += kThreads) {
         const int ld = lead2[i];
         cgid2[i] = (ld >= 0 && ld != i) ? min(pg2[i], pg2[ld]) : 0;
     }
     __syncthreads();
+    #pragma unroll 1
     for (int i = tid; i < B; i += kThreads)
         if (cgid2[i] > 0) atomicMin(&pg2[lead2[i]], cgid2[i]);
     {
         constexpr int kU = kCmpPages;
         const int warp = tid >> 5;
+        #pragma unroll 1
         for (int i = warp; i < B; i += kWarps) {
             const int l = cgid2[i];
             const int g = parent[i];
@@ -268,6 +276,7 @@ __device__ __noinline__ int find_next_level(const SearchCtx* cx, const int32_t* 
             const int32_t* ri = page_table + (int64_t)i * ld_table;
             const int32_t* rl = page_table + (int64_t)ld * ld_table;
             int mis = l;
+            #pragma unroll 1
             for (int k0 = start; k0 < l; k0 += 32 * kU) {
                 int va[kU], vb[kU];
 #pragma unroll
@@ -287,6 +296,7 @@ __device__ __noinline__ int find_next_level(const SearchCtx* cx, const int32_t* 
         }
     }
     __syncthreads();
+    #pragma unroll 1
     for (int i = tid; i < B; i += kThreads) cgid2[i] = -1;
     __syncthreads();
     auto is_sub_leader = [&](int i) {
@@ -294,6 +304,7 @@ __device__ __noinline__ int find_next_level(const SearchCtx* cx, const int32_t* 
         return pg2[i] - scg[parent[i]].prefix_len / ps >= min_pages;
     };
     int hv[2] = {0, 0};
+    #pragma unroll 1
     for (int i = r0; i < r1; ++i)
         if (is_sub_leader(i)) {
             hv[0] += 1;
@@ -302,12 +313,14 @@ __device__ __noinline__ int find_next_level(const SearchCtx* cx, const int32_t* 
     int ht[2];
     block_scan<2>(hv, ht, s_tmp2);
     if (n_groups + ht[0] > max_groups) {  // no room for this level's records: not formed
+        #pragma unroll 1
         for (int i = tid; i < B; i += kThreads) cgid2[i] = -1;
         __syncthreads();
         return 0;
     }
     {
         int gid = n_groups + hv[0], moff = members0 + hv[1];
+        #pragma unroll 1
         for (int i = r0; i < r1; ++i) {
             if (!is_sub_leader(i)) continue;
             CascGroup cg;
@@ -333,6 +346,7 @@ __device__ __noinline__ int find_next_level(const SearchCtx* cx, const int32_t* 
     const int n_new = ht[0];
     *members_total = ht[1];
     __syncthreads();
+    #pragma unroll 1
     for (int i = tid; i < B; i += kThreads) {
         const int ld = lead2[i];
         if (ld >= 0 && ld != i) cgid2[i] = cgid2[ld];
@@ -373,6 +387,7 @@ __device__ __noinline__ int2 build_prefix_groups(const PrepareParams& p, int32_t
     // compared) are requested into L2 here, all at once, so that the warps' compare steps
     // below, one member after another, mostly find them there.  Only rows of requests
     // that share a first page are touched: a batch without such requests reads no row.
+    #pragma unroll 1
     for (int i = tid; i < B; i += kThreads) {
         const int ld = leader[i];
         const int l = (ld >= 0 && ld != i) ? min(lcp[i], lcp[ld]) : 0;
@@ -382,11 +397,13 @@ __device__ __noinline__ int2 build_prefix_groups(const PrepareParams& p, int32_t
         for (int off = 4; off < pf * 4; off += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + off));
     }
     __syncthreads();
+    #pragma unroll 1
     for (int i = tid; i < B; i += kThreads)
         if (lim[i] > 0) atomicMin(&lcp[leader[i]], lim[i]);
     {
         constexpr int kU = kCmpPages;  // 8 ids per lane per step
         const int warp = tid >> 5;
+        #pragma unroll 1
         for (int i = warp; i < B; i += kWarps) {
             const int l = lim[i];
             if (l <= 1) continue;  // warp-uniform: i is the same for the whole warp
@@ -394,6 +411,7 @@ __device__ __noinline__ int2 build_prefix_groups(const PrepareParams& p, int32_t
             const int32_t* ri = p.page_table + (int64_t)i * p.ld;
             const int32_t* rl = p.page_table + (int64_t)ld * p.ld;
             int mis = l;
+            #pragma unroll 1
             for (int k0 = 1; k0 < l; k0 += 32 * kU) {
                 int va[kU], vb[kU];
 #pragma unroll
@@ -415,6 +433,7 @@ __device__ __noinline__ int2 build_prefix_groups(const PrepareParams& p, int32_t
     __syncthreads();
     // group ids in leader order (a deterministic plan) and member slot ranges
     int gv[2] = {0, 0};
+    #pragma unroll 1
     for (int i = r0; i < r1; ++i)
         if (is_group_leader(leader, cnt, lcp, i, p.min_cascade_pages)) {
             gv[0] += 1;
@@ -424,6 +443,7 @@ __device__ __noinline__ int2 build_prefix_groups(const PrepareParams& p, int32_t
     block_scan<2>(gv, gt, s_tmp2);
     {
         int gid = gv[0], moff = gv[1];
+        #pragma unroll 1
         for (int i = r0; i < r1; ++i) {
             if (!is_group_leader(leader, cnt, lcp, i, p.min_cascade_pages)) continue;
             sa(kCgid)[i] = gid;
@@ -449,6 +469,7 @@ __device__ __noinline__ int2 build_prefix_groups(const PrepareParams& p, int32_t
     n_cgroups = gt[0];
     __syncthreads();
     // members take the group id of their leader (-1 when the leader leads no group)
+    #pragma unroll 1
     for (int i = tid; i < B; i += kThreads) {
         const int ld = leader[i];
         if (ld >= 0 && ld != i)
@@ -480,6 +501,7 @@ __device__ __noinline__ void plan_prefix_chunks(const PrepareParams& p, int32_t*
     const int gch = (ng + kThreads - 1) / kThreads;
     const int g0 = min(ng, tid * gch), g1 = min(ng, g0 + gch);
     int pv[2] = {0, 0};  // pair units; (member, 16 prefix keys) pairs
+    #pragma unroll 1
     for (int g = g0; g < g1; ++g) {
         pv[0] += casc_pair_units(scg[g].n_members, TM, Hkv);
         pv[1] += scg[g].n_members * ((scg[g].prefix_len - scg[g].key_base) / 16);
@@ -492,6 +514,7 @@ __device__ __noinline__ void plan_prefix_chunks(const PrepareParams& p, int32_t*
     // tails' HBM time (prefix_pass_target, with the per-SM rates measured on GB300).
     const int target = prefix_pass_target(pt[1], work, p.group, p.kv_fp8, p.lay.casc_target);
     int uv[1] = {0};
+    #pragma unroll 1
     for (int g = g0; g < g1; ++g) {
         const CascGroup cg = scg[g];
         const int span = cg.prefix_len - cg.key_base;
@@ -503,6 +526,7 @@ __device__ __noinline__ void plan_prefix_chunks(const PrepareParams& p, int32_t*
     int ut[1];
     block_scan<1>(uv, ut, s_tmp1);
     int uoff = uv[0];
+    #pragma unroll 1
     for (int g = g0; g < g1; ++g) {
         CascGroup cg = scg[g];
         const int span = cg.prefix_len - cg.key_base;
@@ -523,6 +547,7 @@ __device__ __noinline__ void plan_prefix_chunks(const PrepareParams& p, int32_t*
     // group is written below); the first-page array is free again
     // (and of its sub-group's: the slot goes to kLcp, free since the searches ended; of
     // its level-3 group's: the slot replaces its own lead3 entry, read only by itself)
+    #pragma unroll 1
     for (int i = tid; i < B; i += kThreads) {
         if (sa(kCgid)[i] < 0) continue;
         sa(kFirst)[i] = atomicAdd(&sa(kMpos)[sa(kLeader)[i]], 1);
@@ -542,11 +567,14 @@ __device__ __noinline__ void emit_balanced_groups(const PrepareParams& p, const 
                                                   int line, int n_groups, DecGroup* groups) {
     int32_t* dec_first = reinterpret_cast<int32_t*>(p.ws + p.lay.dec_first);
     if (threadIdx.x == 0)  // CTAs whose share starts past the line: no group
+        #pragma unroll 1
         for (int c = (line + share - 1) / share; c <= p.lay.dec_ctas; ++c) dec_first[c] = n_groups;
+    #pragma unroll 1
     for (int i = r0; i < r1; ++i) {
         const int c0 = cu[i], n = cu[i + 1] - c0, L = lens[i];
         if (n <= 0 || (p.use_prefill && n > TB)) continue;
         const int ng = (n + TB - 1) / TB;
+        #pragma unroll 1
         for (int g = 0; g < ng; ++g) {
             const int a0 = g * TB, na = min(TB, n - a0);
             const int kv_end = L - n + a0 + na;
@@ -566,6 +594,7 @@ __device__ __noinline__ void emit_balanced_groups(const PrepareParams& p, const 
             dg.pad1 = dg.pad2 = dg.pad3 = dg.pad4 = dg.pad5 = 0;
             store_record(&groups[gi], dg);
             const int e16 = g0 + (kv_end + kDecKeysPerStage - 1) / kDecKeysPerStage * kDecKeysPerStage + kDecPieceCost;
+            #pragma unroll 1
             for (int c = (g0 + share - 1) / share; c * share < e16 && c <= p.lay.dec_ctas; ++c) dec_first[c] = gi;
             g0 = e16;
             if (pieces > 1) pi += pieces;
@@ -619,6 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     // pass works from shared memory; the step runs with cold caches, so each dependent
     // global round trip costs a DRAM latency.
     if (small) {
+        #pragma unroll 1
         for (int i = tid; i <= B; i += kThreads) {
             sa(kCu)[i] = p.cu[i];
             if (i < B) sa(kLen)[i] = p.seqlens[i];
@@ -658,10 +688,12 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         const int HT = 1 << hbits;  // > 2 * batch: the probe below always meets a free entry
         int32_t* hkey = dyn + kNumArrays * stride;
         int32_t* hval = hkey + HT;
+        #pragma unroll 1
         for (int h = tid; h < HT; h += kThreads) {
             hkey[h] = -1;
             hval[h] = 0x7fffffff;
         }
+        #pragma unroll 1
         for (int i = tid; i < B; i += kThreads) {
             const int n = cu[i + 1] - cu[i], L = lens[i];
             const bool ok = n == 1 && valid_req(n, L);
@@ -677,6 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         // with equal keys act once (lowest lane, which holds the lowest request index), so
         // a group of many requests does not serialise on one shared-memory address.
         const int lane = tid & 31;
+        #pragma unroll 1
         for (int i0 = 0; i0 < B; i0 += kThreads) {  // uniform trip count: whole warps take part
             const int i = i0 + tid;
             const int f = i < B ? first[i] : -1;
@@ -698,6 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         }
         __syncthreads();
         int has_member = 0;
+        #pragma unroll 1
         for (int i0 = 0; i0 < B; i0 += kThreads) {
             const int i = i0 + tid;
             const int ld = (i < B && first[i] >= 0) ? hval[leader[i]] : -1;
@@ -778,6 +812,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     if (tid == 0 && cu[0] != 0) err |= kErrCu;
     if (tid == 0 && B > p.max_batch) err |= kErrLimits;
     if (tid == 0 && p.total_tokens > p.max_tokens) err |= kErrLimits;
+    #pragma unroll 1
     for (int i = r0; i < r1; ++i) {
         const int c0 = cu[i], c1 = cu[i + 1], L = lens[i];
         const int n = c1 - c0;
@@ -793,6 +828,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
             cnt[0] += ng;
             max_ntok = max(max_ntok, min(n, TB));
             const int lp = prefix_of(i);
+            #pragma unroll 1
             for (int g = 0; g < ng; ++g) {
                 const int ext = L - n + min((g + 1) * TB, n) - lp;
                 work += (unsigned long long)ext;
@@ -815,6 +851,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     int32_t* tile_off = small ? sa(kToff) : reinterpret_cast<int32_t*>(p.ws + p.lay.req_scratch);
     {
         int toff = cnt[1], goff = cnt[0];
+        #pragma unroll 1
         for (int i = r0; i < r1; ++i) {
             tile_off[i] = toff;
             if (small) sa(kGoff)[i] = goff;
@@ -872,6 +909,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
 
     // ---- pass 2: units and partial slots per thread's requests, and the unit cost
     // histogram (a group's units all have length `per` but the last)
+    #pragma unroll 1
     for (int b = tid; b < kBuckets; b += kThreads) {
         s_hist_u[b] = 0;
         s_hist_t[b] = 0;
@@ -881,12 +919,14 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     if (!fatal) {
         const int share = s_share;
         int g0 = cnt[2];  // balanced split: this thread's first group's start on the line
+        #pragma unroll 1
         for (int i = r0; i < r1; ++i) {
             const int n = cu[i + 1] - cu[i], L = lens[i];
             if (n <= 0 || (p.use_prefill && n > TB)) continue;
             const int ng = (n + TB - 1) / TB;
             const int lp = prefix_of(i);
             const int npre = prefix_parts(i);
+            #pragma unroll 1
             for (int g = 0; g < ng; ++g) {
                 const int ext = L - n + min((g + 1) * TB, n) - lp;
                 if (share > 0) {  // pieces: one, plus one per CTA share boundary inside the group
@@ -954,6 +994,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         return (pt.kv_end1 - pt.kv_end0 + kPreKeys - 1) / kPreKeys;
     };
     if (run) {
+        #pragma unroll 1
         for (int x = tid; x < tiles_total; x += kThreads) {
             PreTile pt;
             atomicAdd(&s_hist_t[cost_bucket(make_tile(x, pt))], 1);
@@ -998,6 +1039,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         emit_balanced_groups(p, cu, lens, r0, r1, TB, cnt[0], cnt2[1], cnt[2], s_share, s_line, tot3[0], groups);
     } else if (run) {
         int gi = cnt[0], pi = cnt2[1];
+        #pragma unroll 1
         for (int i = r0; i < r1; ++i) {
             const int c0 = cu[i], n = cu[i + 1] - c0, L = lens[i];
             if (n <= 0) continue;
@@ -1006,6 +1048,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
             const int lp = prefix_of(i);
             const int cg = casc_of(i), cg2 = casc2_of(i), cg3 = casc3_of(i);
             const int npre = prefix_parts(i);
+            #pragma unroll 1
             for (int g = 0; g < ng; ++g) {
                 const int a0 = g * TB, na = min(TB, n - a0);
                 const int kv_end = L - n + a0 + na;
@@ -1054,6 +1097,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
             }
         }
         // prefill tile pairs, then cascade prefix units, in parallel over the unit index
+        #pragma unroll 1
         for (int x = tid; x < tiles_total; x += kThreads) {
             PreTile pt;
             const int b = cost_bucket(make_tile(x, pt));
@@ -1070,6 +1114,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         const int per = (p.total_tokens + kThreads - 1) / kThreads;
         const int t0 = min(p.total_tokens, tid * per), t1 = min(p.total_tokens, t0 + per);
         int i = t0 < t1 ? find_bucket(cu, B, t0) : 0;
+        #pragma unroll 1
         for (int t = t0; t < t1; ++t) {
             while (cu[i + 1] <= t) ++i;
             p.tok_req[t] = i;
