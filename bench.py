@@ -64,9 +64,9 @@ NCU_TRAFFIC = {
         "summary": "profiles/decode_kernel_decode_workload.md",
     },
     ("tensor_core", "prefill"): {
-        "bytes": 219.442944e6,
+        "bytes": 219.720960e6,
         "sources": ['paged_variable_length_gb300/csrc/prefill_tc.cu', 'paged_variable_length_gb300/csrc/device_utils.cuh', 'paged_variable_length_gb300/csrc/tc_utils.cuh', 'paged_variable_length_gb300/csrc/pva_internal.h'],
-        "sha256_16": "aea784ccc5c7a3d4",
+        "sha256_16": "1198d80cd3594772",
         "summary": "profiles/prefill_kernel_prefill_workload.md",
     },
 }
