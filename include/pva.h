@@ -167,7 +167,9 @@ PVA_API size_t attn_workspace_size(const pva_config* cfg);
  *   slot_mapping   int64 [total_tokens] pool slot of each new token, -1 = do not
  *                  store; or NULL to derive it from the page table (the new
  *                  tokens are positions kv_len - q_len .. kv_len - 1)
- *   batch, total_tokens   host values; total_tokens must equal cu[batch]
+ *   batch, total_tokens   host values; total_tokens must equal cu[batch].  With
+ *                  batch 0, cache_seqlens and page_table are not read and may be
+ *                  NULL (ld_page_table is then ignored)
  *   max_q_len      host upper bound on any request's q_len (<= 0: unknown,
  *                  taken as total_tokens); lets the forward skip the prefill
  *                  kernel for decode-only batches.  A request above it sets

@@ -216,9 +216,11 @@ pva_status check_prepare_args(const pva_config* cfg, const int32_t* cu_seqlens_q
                               pva_meta* meta) {
     pva_status st = check_config(cfg);
     if (st != PVA_OK) return st;
-    if (meta == nullptr || cu_seqlens_q == nullptr || cache_seqlens == nullptr || page_table == nullptr)
+    if (meta == nullptr || cu_seqlens_q == nullptr) return PVA_ERR_INVALID_ARG;
+    // an empty batch reads neither the lengths nor the page table
+    if (batch > 0 && (cache_seqlens == nullptr || page_table == nullptr || ld_page_table <= 0))
         return PVA_ERR_INVALID_ARG;
-    if (batch < 0 || total_tokens < 0 || ld_page_table <= 0) return PVA_ERR_INVALID_ARG;
+    if (batch < 0 || total_tokens < 0 || (batch == 0 && total_tokens != 0)) return PVA_ERR_INVALID_ARG;
     if (batch > cfg->max_batch || total_tokens > cfg->max_tokens) return PVA_ERR_INVALID_ARG;
     return PVA_OK;
 }

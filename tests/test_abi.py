@@ -101,6 +101,21 @@ def test_null_pointers_are_rejected_on_the_host(lib):
     assert st == 1
 
 
+def test_empty_batch_needs_no_lengths_or_page_table(lib):
+    """batch 0 reads neither array: NULL passes the argument checks and the call stops at the
+    next one (a 16-byte workspace is too small: nothing is launched, with or without a
+    device), while new tokens claimed for an empty batch are refused."""
+    cfg = _cfg()
+    meta = pva.Meta()
+    dummy = ctypes.c_void_p(256)
+    st = lib.attn_prepare_metadata(ctypes.byref(cfg), dummy, None, None, 0, None, 0, 0, 0, dummy, 16, None,
+                                   ctypes.byref(meta))
+    assert st in (3, 4)  # PVA_ERR_WORKSPACE_TOO_SMALL, or PVA_ERR_CUDA without a device
+    st = lib.attn_prepare_metadata(ctypes.byref(cfg), dummy, None, None, 0, None, 0, 3, 0, dummy, 16, None,
+                                   ctypes.byref(meta))
+    assert st == 1
+
+
 def test_misaligned_workspace_and_oversized_batch_are_rejected(lib):
     cfg = _cfg()
     meta = pva.Meta()

@@ -608,3 +608,48 @@ def test_random_prefix_forests(seed):
     _, eng = _full_check(wl)
     assert pva.attn_debug_plan_counts(eng.meta)["casc_groups"] >= 1
     _full_check(wl, enable_cascade=False)
+
+
+# ------------------------------------------------------------------ edge cases
+
+
+@pytest.mark.parametrize("case", [
+    (32, 8, 128, 64, [1, 200, 1, 3], [5000, 260, 64, 3]),   # pages of 64 slots
+    (16, 4, 64, 128, [1, 1, 130], [9000, 255, 700]),          # pages of 128 slots, the largest built
+])
+def test_large_pages(case):
+    Hq, Hkv, D, ps, ql, kl = case
+    _full_check(W.custom(ql, kl, Hq, Hkv, D, ps, seed=ps))
+
+
+def test_batch_at_capacity():
+    """A batch exactly at the configured max_batch, max_tokens and max_kv_len (the plan's
+    capacities at their smallest)."""
+    rng = np.random.default_rng(5)
+    ql = [1] * 30 + [64, 33]
+    kl = [int(x) for x in rng.integers(1, 3000, size=30)] + [64, 3000]
+    wl = W.custom(ql, kl, 32, 8, 128, 16, seed=5)
+    _full_check(wl, max_batch=wl.batch, max_tokens=wl.total_tokens, max_kv_len=max(kl))
+
+
+def test_empty_batch_and_no_new_tokens():
+    """No request at all, and requests that all bring zero new tokens: prepare and forward
+    succeed, write nothing and leave the status clean."""
+    wl = W.custom([1, 2], [10, 40], 32, 8, 128, 16, seed=3)
+    eng = make_engine(wl)
+    t = W.make_tensors(wl, DEV)
+    k0, v0 = t["k_pool"].clone(), t["v_pool"].clone()
+    out = torch.full_like(t["q"], 7.0)
+    none = lambda x: x[:0]  # empty views that keep a valid address
+    cu0 = torch.zeros(1, dtype=torch.int32, device=DEV)
+    eng.prepare(cu0, none(t["cache_seqlens"]), none(t["page_table"]), 0, None, 0)
+    eng.forward(none(t["q"]), none(t["k"]), none(t["v"]), t["k_pool"], t["v_pool"], none(out), None)
+    torch.cuda.synchronize()
+    assert pva.attn_get_device_status(eng.meta) == 0
+    cu = torch.zeros(3, dtype=torch.int32, device=DEV)
+    eng.prepare(cu, t["cache_seqlens"], t["page_table"], 0, None, 0)
+    eng.forward(none(t["q"]), none(t["k"]), none(t["v"]), t["k_pool"], t["v_pool"], none(out), None)
+    torch.cuda.synchronize()
+    assert pva.attn_get_device_status(eng.meta) == 0
+    assert torch.equal(t["k_pool"], k0) and torch.equal(t["v_pool"], v0)
+    assert torch.all(out == 7.0)
