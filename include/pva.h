@@ -113,7 +113,7 @@ typedef struct pva_config {
     int32_t num_kv_heads;       /* Hkv; Hq % Hkv == 0 and Hq / Hkv <= 16 */
     int32_t head_dim;           /* D: 64 or 128 */
     int32_t page_size;          /* 1, 2, 4, ..., 128 (a power of two) */
-    int64_t num_pages;          /* pool capacity in pages */
+    int64_t num_pages;          /* pool capacity in pages; num_pages * page_size < 2^32 */
     float sm_scale;             /* softmax scale; <= 0 selects 1/sqrt(head_dim) */
     int32_t max_batch;          /* upper bound on requests per batch */
     int32_t max_tokens;         /* upper bound on new tokens per batch */

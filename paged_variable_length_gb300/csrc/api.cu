@@ -38,7 +38,8 @@ pva_status check_config(const pva_config* c) {
     if (c->num_qo_heads % c->num_kv_heads != 0) return PVA_ERR_INVALID_ARG;
     if (!is_pow2(c->page_size) || c->page_size > 128) return PVA_ERR_UNSUPPORTED;
     if (!decode_supported(c->num_qo_heads, c->num_kv_heads, c->head_dim)) return PVA_ERR_UNSUPPORTED;
-    if ((int64_t)c->num_pages * c->page_size > ((int64_t)1 << 40)) return PVA_ERR_UNSUPPORTED;
+    // the tensor-core kernel's gathers keep a slot in 32 bits (all ones marks a row not copied)
+    if ((int64_t)c->num_pages * c->page_size >= ((int64_t)1 << 32)) return PVA_ERR_UNSUPPORTED;
     if (c->kv_dtype != PVA_KV_BF16 && c->kv_dtype != PVA_KV_E4M3) return PVA_ERR_UNSUPPORTED;
     return PVA_OK;
 }

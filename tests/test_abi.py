@@ -77,7 +77,8 @@ def _cfg(**kw):
 
 @pytest.mark.parametrize("bad", [dict(head_dim=96), dict(page_size=24), dict(page_size=256),
                                  dict(num_qo_heads=30), dict(num_qo_heads=64, num_kv_heads=2),
-                                 dict(num_kv_heads=12, num_qo_heads=24), dict(num_pages=0)])
+                                 dict(num_kv_heads=12, num_qo_heads=24), dict(num_pages=0),
+                                 dict(num_pages=1 << 28)])  # 2^32 slots of 16
 def test_unsupported_or_invalid_config_is_rejected_on_the_host(lib, bad):
     cfg = _cfg(**bad)
     assert pva.attn_workspace_size(cfg) == 0
