@@ -55,6 +55,8 @@ CASES = [
     (16, 1, 128, 32, [1, 5, 1], [4096, 5, 31]),            # MQA
     (16, 16, 64, 2, [1, 1, 7], [9, 1, 7]),                 # MHA
     (32, 2, 128, 8, [1, 1], [3000, 5]),                    # group 16
+    (32, 8, 128, 64, [1, 200, 1, 3], [5000, 260, 64, 3]),  # pages of 64 slots
+    (32, 16, 128, 128, [1, 1, 70], [3000, 129, 200]),      # pages of 128 slots, two head blocks
 ]
 
 

@@ -57,6 +57,7 @@ CASES = [
     (16, 1, 128, 32, [1, 5, 1], [4096, 5, 31]),                # MQA
     (16, 16, 64, 2, [1, 1, 7], [9, 1, 7]),                     # MHA (group 1)
     (32, 2, 128, 8, [1, 1], [3000, 5]),                        # group 16
+    (32, 16, 128, 128, [1, 1, 70], [3000, 129, 200]),          # two head blocks (Hkv 16), 128-slot pages
 ]
 
 
