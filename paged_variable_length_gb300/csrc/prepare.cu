@@ -105,6 +105,15 @@ __device__ void block_scan(int (&v)[N], int (&total)[N], int (*warp_tmp)[N]) {
     __syncthreads();
 }
 
+// block_scan of two counters, out of line: one copy of the code serves the shared-prefix
+// steps (where the kernel's cold instruction fetch dominates) and pass 2.  Returns this
+// thread's exclusive offsets (x, y) and the block totals (z, w).
+__device__ __noinline__ int4 block_scan2(int a, int b, int (*warp_tmp)[2]) {
+    int v[2] = {a, b}, total[2];
+    block_scan<2>(v, total, warp_tmp);
+    return make_int4(v[0], v[1], total[0], total[1]);
+}
+
 // Index i with off[i] <= x < off[i+1] (off ascending, off[0] <= x); among equal offsets
 // the last one, so that entries of width zero are passed over.
 __device__ __forceinline__ int find_bucket(const int32_t* off, int count, int x) {
@@ -311,7 +320,10 @@ __device__ __noinline__ int find_next_level(const SearchCtx* cx, const int32_t* 
             hv[1] += cnt2[i];
         }
     int ht[2];
-    block_scan<2>(hv, ht, s_tmp2);
+    {
+        const int4 r = block_scan2(hv[0], hv[1], s_tmp2);
+        hv[0] = r.x, hv[1] = r.y, ht[0] = r.z, ht[1] = r.w;
+    }
     if (n_groups + ht[0] > max_groups) {  // no room for this level's records: not formed
         #pragma unroll 1
         for (int i = tid; i < B; i += kThreads) cgid2[i] = -1;
@@ -440,7 +452,10 @@ __device__ __noinline__ int2 build_prefix_groups(const PrepareParams& p, int32_t
             gv[1] += cnt[i];
         }
     int gt[2];
-    block_scan<2>(gv, gt, s_tmp2);
+    {
+        const int4 r = block_scan2(gv[0], gv[1], s_tmp2);
+        gv[0] = r.x, gv[1] = r.y, gt[0] = r.z, gt[1] = r.w;
+    }
     {
         int gid = gv[0], moff = gv[1];
         #pragma unroll 1
@@ -507,7 +522,10 @@ __device__ __noinline__ void plan_prefix_chunks(const PrepareParams& p, int32_t*
         pv[1] += scg[g].n_members * ((scg[g].prefix_len - scg[g].key_base) / 16);
     }
     int pt[2];
-    block_scan<2>(pv, pt, s_tmp2);
+    {
+        const int4 r = block_scan2(pv[0], pv[1], s_tmp2);
+        pv[0] = r.x, pv[1] = r.y, pt[0] = r.z, pt[1] = r.w;
+    }
     const int pair_units = max(pt[0], 1);
     // Units aimed for: the decode tails start on the SMs the prefix pass leaves free, so
     // the pass gets about the share of the SMs its tensor-core time takes beside the
@@ -524,7 +542,10 @@ __device__ __noinline__ void plan_prefix_chunks(const PrepareParams& p, int32_t*
         uv[0] += (span + ck - 1) / ck * casc_pair_units(cg.n_members, TM, Hkv);
     }
     int ut[1];
-    block_scan<1>(uv, ut, s_tmp1);
+    {
+        const int4 r = block_scan2(uv[0], 0, s_tmp2);
+        uv[0] = r.x, ut[0] = r.z;
+    }
     int uoff = uv[0];
     #pragma unroll 1
     for (int g = g0; g < g1; ++g) {
@@ -951,7 +972,10 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         }
     }
     int tot2[2];
-    block_scan<2>(cnt2, tot2, s_tmp2);
+    {
+        const int4 r = block_scan2(cnt2[0], cnt2[1], s_tmp2);
+        cnt2[0] = r.x, cnt2[1] = r.y, tot2[0] = r.z, tot2[1] = r.w;
+    }
     const bool over = tot2[0] > p.lay.max_dec_units || tot2[1] > p.lay.max_partial;
     if (over && tid == 0) atomicOr(&s_err, kErrLimits);
     const bool run = !fatal && !over;
