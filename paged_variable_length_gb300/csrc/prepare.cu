@@ -153,6 +153,36 @@ struct SearchCtx {
     int stride, hbits, min_pages, B, ps, max_groups;
 };
 
+// First index k in [start, l) at which two page-table rows differ, one warp: lanes read
+// consecutive ids, kCmpPages each per step.  The search stops after the step that finds
+// one, and never reads past *bound, the group's prefix as far as the other warps have
+// found it (it only falls, and a mismatch at or past it changes no minimum).  Returns a
+// value >= min(l, *bound) when the rows agree up to there.  Warp-uniform.
+__device__ __forceinline__ int first_mismatch(const int32_t* ri, const int32_t* rl, int start, int l,
+                                              const volatile int32_t* bound, int lane) {
+    int mis = l;
+    #pragma unroll 1
+    for (int k0 = start;; k0 += 32 * kCmpPages) {
+        l = min(l, __shfl_sync(0xffffffffu, *bound, 0));
+        if (k0 >= l) break;
+        int va[kCmpPages], vb[kCmpPages];
+#pragma unroll
+        for (int u = 0; u < kCmpPages; ++u) {
+            const int k = k0 + u * 32 + lane;
+            va[u] = k < l ? ri[k] : 0;
+            vb[u] = k < l ? rl[k] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < kCmpPages; ++u) {
+            const int k = k0 + u * 32 + lane;
+            if (k < l && va[u] != vb[u]) mis = min(mis, k);
+        }
+        mis = __reduce_min_sync(0xffffffffu, mis);
+        if (mis < l) break;
+    }
+    return mis;
+}
+
 // One level deeper in the shared-prefix tree (pass 0 of the kernel below; level 2 inside
 // the top-level groups, level 3 inside level 2's): inside a parent group, members keyed by
 // the page right after the parent's prefix; the lowest-numbered one leads its sub-group,
@@ -272,7 +302,6 @@ __device__ __noinline__ int find_next_level(const SearchCtx* cx, const int32_t* 
     for (int i = tid; i < B; i += kThreads)
         if (cgid2[i] > 0) atomicMin(&pg2[lead2[i]], cgid2[i]);
     {
-        constexpr int kU = kCmpPages;
         const int warp = tid >> 5;
         #pragma unroll 1
         for (int i = warp; i < B; i += kWarps) {
@@ -286,16 +315,16 @@ __device__ __noinline__ int find_next_level(const SearchCtx* cx, const int32_t* 
             const int32_t* rl = page_table + (int64_t)ld * ld_table;
             int mis = l;
             #pragma unroll 1
-            for (int k0 = start; k0 < l; k0 += 32 * kU) {
-                int va[kU], vb[kU];
+            for (int k0 = start; k0 < l; k0 += 32 * kCmpPages) {
+                int va[kCmpPages], vb[kCmpPages];
 #pragma unroll
-                for (int u = 0; u < kU; ++u) {
+                for (int u = 0; u < kCmpPages; ++u) {
                     const int k = k0 + u * 32 + lane;
                     va[u] = k < l ? ri[k] : 0;
                     vb[u] = k < l ? rl[k] : 0;
                 }
 #pragma unroll
-                for (int u = 0; u < kU; ++u) {
+                for (int u = 0; u < kCmpPages; ++u) {
                     const int k = k0 + u * 32 + lane;
                     if (k < l && va[u] != vb[u]) mis = min(mis, k);
                 }
@@ -393,8 +422,9 @@ __device__ __noinline__ int2 build_prefix_groups(const PrepareParams& p, int32_t
     int n_cgroups = 0;
     // Every member compares pages 1 .. lim-1 of its row with the leader's (page 0
     // matched by construction), one warp per member: lanes read consecutive page ids,
-    // so each load instruction is one line of each row, 256 ids per step.  The group
-    // prefix is the smallest mismatch, or the smallest member's page count.
+    // so each load instruction is one line of each row, 256 ids per step, up to the
+    // first mismatch or the group's prefix as found so far.  The group prefix is the
+    // smallest mismatch, or the smallest member's page count.
     // The rows about to be compared (members' and leaders' page ids up to the pages
     // compared) are requested into L2 here, all at once, so that the warps' compare steps
     // below, one member after another, mostly find them there.  Only rows of requests
@@ -413,32 +443,14 @@ __device__ __noinline__ int2 build_prefix_groups(const PrepareParams& p, int32_t
     for (int i = tid; i < B; i += kThreads)
         if (lim[i] > 0) atomicMin(&lcp[leader[i]], lim[i]);
     {
-        constexpr int kU = kCmpPages;  // 8 ids per lane per step
         const int warp = tid >> 5;
         #pragma unroll 1
         for (int i = warp; i < B; i += kWarps) {
             const int l = lim[i];
             if (l <= 1) continue;  // warp-uniform: i is the same for the whole warp
             const int ld = leader[i];
-            const int32_t* ri = p.page_table + (int64_t)i * p.ld;
-            const int32_t* rl = p.page_table + (int64_t)ld * p.ld;
-            int mis = l;
-            #pragma unroll 1
-            for (int k0 = 1; k0 < l; k0 += 32 * kU) {
-                int va[kU], vb[kU];
-#pragma unroll
-                for (int u = 0; u < kU; ++u) {
-                    const int k = k0 + u * 32 + lane;
-                    va[u] = k < l ? ri[k] : 0;
-                    vb[u] = k < l ? rl[k] : 0;
-                }
-#pragma unroll
-                for (int u = 0; u < kU; ++u) {
-                    const int k = k0 + u * 32 + lane;
-                    if (k < l && va[u] != vb[u]) mis = min(mis, k);
-                }
-            }
-            mis = __reduce_min_sync(0xffffffffu, mis);
+            const int mis = first_mismatch(p.page_table + (int64_t)i * p.ld, p.page_table + (int64_t)ld * p.ld, 1,
+                                           l, &lcp[ld], lane);
             if (lane == 0 && mis < l) atomicMin(&lcp[ld], mis);
         }
     }
