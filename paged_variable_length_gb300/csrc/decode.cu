@@ -652,6 +652,7 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1)
 // reads than they saved (merge of the cascade batch 10.2 -> 16.4 us at 8 warps).
 // Launched programmatically after the decode kernel, whose grid it waits for.
 constexpr int kMergeThreads = 1024;
+constexpr int kHoist = 2;  // parts whose columns each lane loads before the LSE reductions
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(ForwardParams p) {
@@ -688,6 +689,20 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(ForwardParams p) {
         {
             const int row = (it / n_groups) * kWarps + warp;
             if (row >= rows) continue;
+            // the first kHoist parts' columns are requested together with the LSEs, so that
+            // the usual split counts take one round trip to L2, not two
+            float hv[kHoist][kPer];
+#pragma unroll
+            for (int k = 0; k < kHoist; ++k) {
+                const float* sp = pob + ((int64_t)k * rps + row) * D + lane * kPer;
+                if constexpr (kPer == 4) {
+                    const float4 v = k < np ? __ldcg(reinterpret_cast<const float4*>(sp)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    hv[k][0] = v.x, hv[k][1] = v.y, hv[k][2] = v.z, hv[k][3] = v.w;
+                } else {
+                    const float2 v = k < np ? __ldcg(reinterpret_cast<const float2*>(sp)) : make_float2(0.f, 0.f);
+                    hv[k][0] = v.x, hv[k][1] = v.y;
+                }
+            }
             const float lfirst = lane < np ? __ldcg(plb + (int64_t)lane * rps + row) : -INFINITY;
             float mx = lfirst;
             for (int s0 = 32; s0 < np; s0 += 32)
@@ -706,8 +721,20 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(ForwardParams p) {
                 wsum += w;
                 const int cnt = min(32, np - s0);
                 const float* src = pob + ((int64_t)s0 * rps + row) * D + lane * kPer;
-#pragma unroll 8
-                for (int k = 0; k < cnt; ++k) {
+                int k = 0;
+                if (s0 == 0) {
+#pragma unroll
+                    for (int h = 0; h < kHoist; ++h) {
+                        const float wk = __shfl_sync(0xffffffffu, w, h);
+                        if (h < cnt) {
+#pragma unroll
+                            for (int c = 0; c < kPer; ++c) acc[c] += wk * hv[h][c];
+                        }
+                    }
+                    k = kHoist;
+                }
+#pragma unroll 4
+                for (; k < cnt; ++k) {
                     const float wk = __shfl_sync(0xffffffffu, w, k);
                     const float* sp = src + (int64_t)k * rps * D;
                     if constexpr (kPer == 4) {
