@@ -58,9 +58,9 @@ def parse():
 # what they were at capture time; after any change the roofline reports null.
 NCU_TRAFFIC = {
     ("decode", "decode"): {
-        "bytes": 617.533440e6,
+        "bytes": 617.257472e6,
         "sources": ['paged_variable_length_gb300/csrc/decode.cu', 'paged_variable_length_gb300/csrc/device_utils.cuh', 'paged_variable_length_gb300/csrc/pva_internal.h'],
-        "sha256_16": "2f6f7404ef847958",
+        "sha256_16": "b88e677d84d563c6",
         "summary": "profiles/decode_kernel_decode_workload.md",
     },
     ("tensor_core", "prefill"): {
