@@ -554,7 +554,7 @@ def test_ragged_full_size_workload():
     assert_close(out, lse, ref_o, ref_l, mask=sel)
 
 
-def _random_forest(seed, Hq=32, Hkv=8, D=128, ps=16, min_pages=8):
+def _random_forest(seed, Hq=32, Hkv=8, D=128, ps=16, min_pages=8, P=4000):
     """Random shared-prefix forests: 1-3 roots of min_pages-1 .. min_pages+5 pages (some too
     short for a group), each with 1-3 branches of min_pages-1 .. min_pages+3 further
     pages, leaves that sometimes share a third run (a third level when long enough) and
@@ -563,7 +563,6 @@ def _random_forest(seed, Hq=32, Hkv=8, D=128, ps=16, min_pages=8):
     (never prefix members), unrelated decodes and a prefill."""
     rng = np.random.default_rng(1000 + seed)
     rng4 = np.random.default_rng(3000 + seed)
-    P = 4000
     perm = [int(x) for x in rng.permutation(P)]
     take = lambda k: [perm.pop() for _ in range(int(k))]
     rows, ql, kl = [], [], []
@@ -606,6 +605,17 @@ def test_random_prefix_forests(seed):
     layouts = [(32, 8, 128), (28, 4, 128), (16, 4, 64), (32, 32, 128)]
     Hq, Hkv, D = layouts[seed % len(layouts)]
     wl = _random_forest(seed, Hq=Hq, Hkv=Hkv, D=D)
+    _, eng = _full_check(wl)
+    assert pva.attn_debug_plan_counts(eng.meta)["casc_groups"] >= 1
+    _full_check(wl, enable_cascade=False)
+
+
+@pytest.mark.parametrize("ps,P,seed", [(1, 40000, 0), (1, 40000, 3), (64, 2000, 1), (128, 1000, 2)])
+def test_random_prefix_forests_other_page_sizes(ps, P, seed):
+    """The same forests over token slots (shared runs of 7 to 30 slots: prefix chunks far
+    shorter than a 128-key tile) and over pages of 64 and 128 slots (a shared page holds
+    half a tile or a whole one)."""
+    wl = _random_forest(seed, ps=ps, P=P)
     _, eng = _full_check(wl)
     assert pva.attn_debug_plan_counts(eng.meta)["casc_groups"] >= 1
     _full_check(wl, enable_cascade=False)
