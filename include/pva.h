@@ -157,8 +157,9 @@ PVA_API size_t attn_workspace_size(const pva_config* cfg);
  * Shared prefixes are found among single-token decodes whose page-table rows start
  * with the same run of at least min_cascade_pages pages lying before their query, and
  * inside such a group among members whose rows continue with a further such run, and
- * inside those again (three levels of the prefix tree); each shared run is read once per
- * group by the forward.
+ * so on inside those (up to eight levels of the prefix tree; runs below the eighth are
+ * read as part of each member's own keys); each shared run is read once per group by
+ * the forward.
  * Detection runs for batches of 2 to 1536 requests.
  *
  *   cu_seqlens_q   int32 [batch+1]  request i's new tokens are q[cu[i] : cu[i+1]]
@@ -307,8 +308,8 @@ PVA_API pva_status attn_debug_set_wait_limit(const pva_meta* meta, int64_t limit
  * Debug/test helper: copies plan counters to host (synchronising): counts[0]
  * decode units, [1] decode merge groups, [2] prefill tiles, [3] cascade
  * groups, [4] cascade prefix tiles, [5] split-KV chunk (keys), [6] partial
- * slots used, [7] kernels one attn_forward launches.  Returns the number of
- * entries written (<= n).
+ * slots used, [7] kernels one attn_forward launches, [8] levels of the shared-prefix
+ * tree found (0: none).  Returns the number of entries written (<= n).
  */
 PVA_API int32_t attn_debug_plan_counts(const pva_meta* meta, int64_t* counts, int32_t n);
 

@@ -61,7 +61,7 @@ Layout make_layout(const pva_config* c, int sm_count, int target_units = 0) {
     L.max_dec_units = L.max_dec_groups + L.target_units + 1;
     L.max_partial = 2 * L.target_units + 2;
     L.max_pre_tiles = (int32_t)((c->max_tokens / TM + c->max_batch + 1) * (int64_t)c->num_kv_heads);
-    // up to three levels of groups, each at most one per two requests; the prepare kernel
+    // up to kMaxCascLevels levels of groups, each at most one per two requests; the prepare kernel
     // numbers no more than max_batch + 1 records in all (a deeper level that would need
     // more is not formed: its requests read those keys as tails)
     L.max_casc_groups = c->enable_cascade ? c->max_batch + 1 : 1;
@@ -70,8 +70,8 @@ Layout make_layout(const pva_config* c, int sm_count, int target_units = 0) {
     L.casc_target = sm_count;
     if (c->enable_cascade) {
         // every member of a group takes one partial slot per prefix chunk of each of its
-        // (up to two) groups, at most kMaxCascChunks in all (with sub-groups in a batch each
-        // level takes at most half); the prefix pass has at most (member tiles / 2 +
+        // groups (one a level), at most kMaxCascChunks in all (with n levels in a batch each
+        // level takes at most 1/n of them); the prefix pass has at most (member tiles / 2 +
         // groups) x kv heads x chunks units per level
         L.max_partial += c->max_batch * kMaxCascChunks;
         L.max_pre_tiles += (int32_t)((2 * (c->max_batch / (2 * TM)) + L.max_casc_groups + 2) *
@@ -93,7 +93,8 @@ Layout make_layout(const pva_config* c, int sm_count, int target_units = 0) {
     L.partial_lse = take(sizeof(float) * (size_t)L.max_partial * L.rows_per_slot);
     L.req_scratch = take(sizeof(int32_t) * 4 * (size_t)(c->max_batch + 1));
     L.casc_groups = take(sizeof(CascGroup) * (size_t)L.max_casc_groups);
-    L.casc_members = take(sizeof(int32_t) * 2 * 3 * (size_t)c->max_batch);  // (token, slot) per member per level
+    L.casc_members = take(sizeof(int32_t) * 2 * kMaxCascLevels * (size_t)c->max_batch);  // (token, slot) per member per level
+    L.casc_deep = take(sizeof(int32_t) * 3 * (kMaxCascLevels - 2) * (size_t)(c->max_batch + 1));
     L.dec_first = take(sizeof(int32_t) * ((size_t)L.dec_ctas + 1));
     L.total = off;
     return L;
@@ -502,9 +503,10 @@ int32_t attn_debug_plan_counts(const pva_meta* meta, int64_t* counts, int32_t n)
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(h->stream)) != cudaSuccess) return 0;
     PlanHeader hdr{};
     if (cudaMemcpy(&hdr, h->ws + h->lay.header, sizeof(hdr), cudaMemcpyDeviceToHost) != cudaSuccess) return 0;
-    const int64_t vals[8] = {hdr.n_dec_units, hdr.n_dec_groups, hdr.n_pre_tiles, hdr.n_casc_groups,
-                             hdr.n_casc_tiles, hdr.split_chunk, hdr.n_partial_slots, h->kernels_per_forward};
-    const int m = n < 8 ? n : 8;
+    const int64_t vals[9] = {hdr.n_dec_units, hdr.n_dec_groups,     hdr.n_pre_tiles,        hdr.n_casc_groups,
+                             hdr.n_casc_tiles, hdr.split_chunk,      hdr.n_partial_slots,    h->kernels_per_forward,
+                             hdr.n_casc_levels};
+    const int m = n < 9 ? n : 9;
     for (int i = 0; i < m; ++i) counts[i] = vals[i];
     return m;
 }

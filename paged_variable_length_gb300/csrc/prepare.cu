@@ -12,8 +12,8 @@
 //      with the same run of pages ("Source walkthrough: Attention backends",
 //      section 3.3: the shared part is computed once and merged by log-sum-exp), and
 //      inside each group sub-groups whose rows continue with a further shared run, and
-//      inside those a third level (three levels of the prefix tree the page describes
-//      its multi-level form over);
+//      so on inside those, up to kMaxCascLevels levels of the prefix tree the page
+//      describes its multi-level form over;
 //   1. validate cu_seqlens_q / cache_seqlens (error word, never a trap) and
 //      classify each request: q_len * G <= 16 rows -> decode groups (the
 //      warp-MMA streaming kernel), otherwise -> 128-row tensor-core tiles;
@@ -138,6 +138,14 @@ __device__ __forceinline__ int casc_pair_units(int members, int TM, int Hkv) {
     return (((members + TM - 1) / TM) + 1) / 2 * Hkv;
 }
 
+// Per-request arrays of shared-prefix level L >= 3 in the workspace (a = 0: the request's
+// leader at that level, later its member-list slot; 1: its group id, -1 for none; 2:
+// member counts, then member-list cursors, indexed by leader).  Levels 1 and 2 keep theirs
+// in shared memory.
+__device__ __forceinline__ int32_t* deep_level(const PrepareParams& p, int L, int a) {
+    return reinterpret_cast<int32_t*>(p.ws + p.lay.casc_deep) + ((L - 3) * 3 + a) * (p.batch + 1);
+}
+
 // What the shared-prefix search of every level needs besides its own arrays (set once, in
 // shared memory: passed as one pointer, so that the calls below keep few values live in
 // the 64-register kernel).
@@ -184,7 +192,8 @@ __device__ __forceinline__ int first_mismatch(const int32_t* ri, const int32_t* 
 }
 
 // One level deeper in the shared-prefix tree (pass 0 of the kernel below; level 2 inside
-// the top-level groups, level 3 inside level 2's): inside a parent group, members keyed by
+// the top-level groups, level 3 inside level 2's, and so on): inside a parent group,
+// members keyed by
 // the page right after the parent's prefix; the lowest-numbered one leads its sub-group,
 // whose prefix extends the parent's by the run of pages every sub-member shares with it
 // (again at least min_pages, again whole pages before each member's query).  Its prefix
@@ -508,23 +517,19 @@ __device__ __noinline__ int2 build_prefix_groups(const PrepareParams& p, int32_t
 
 // Key chunks of each group's prefix (about `target` prefix-pass units in total, see
 // below), unit ranges, member lists.  A member takes one partial slot per chunk of each
-// of its groups; with deeper levels in the batch each level gets at most a half (two
-// levels) or a third (three) of the chunks, so no member needs more than
-// kMaxCascChunks.  Out of line for the reason given above.
-__device__ __noinline__ void plan_prefix_chunks(const PrepareParams& p, int32_t* dyn, int3 ng3,
-                                                unsigned long long work, int (*s_tmp2)[2], int (*s_tmp1)[1],
+// of its groups; with n levels in the batch each level gets at most 1/n of the chunks,
+// so no member needs more than kMaxCascChunks.  Out of line for the reason given above.
+__device__ __noinline__ void plan_prefix_chunks(const PrepareParams& p, int32_t* dyn, int n_cgroups,
+                                                int n_levels, unsigned long long work, int (*s_tmp2)[2],
                                                 int* s_casc_units) {
     const int tid = threadIdx.x;
     const int B = p.batch, stride = p.smem_batch + 1, TM = p.pre_tokens, Hkv = p.num_kv_heads;
-    const int n_cgroups = ng3.x, n_sub = ng3.y, n_sub3 = ng3.z;
     auto sa = [&](int a) { return dyn + a * stride; };
-    auto g3 = [&](int a) { return reinterpret_cast<int32_t*>(p.ws + p.lay.req_scratch) + a * (B + 1); };
-    auto casc3_of = [&](int i) { return n_sub3 > 0 ? g3(1)[i] : -1; };
     const int hbits = casc_hash_bits(p.smem_batch);
     CascGroup* scg = reinterpret_cast<CascGroup*>(dyn + kNumArrays * stride + 2 * (1 << hbits));
     CascGroup* cgroups = reinterpret_cast<CascGroup*>(p.ws + p.lay.casc_groups);
     const int ng = n_cgroups;
-    const int nc_cap = kMaxCascChunks / (1 + (n_sub > 0) + (n_sub3 > 0));
+    const int nc_cap = kMaxCascChunks / max(n_levels, 1);
     const int gch = (ng + kThreads - 1) / kThreads;
     const int g0 = min(ng, tid * gch), g1 = min(ng, g0 + gch);
     int pv[2] = {0, 0};  // pair units; (member, 16 prefix keys) pairs
@@ -576,16 +581,22 @@ __device__ __noinline__ void plan_prefix_chunks(const PrepareParams& p, int32_t*
         scg[g] = cg;
     }
     if (tid == 0) *s_casc_units = ut[0];
-    // each member takes a slot of its group's member list (filled when its decode
-    // group is written below); the first-page array is free again
-    // (and of its sub-group's: the slot goes to kLcp, free since the searches ended; of
-    // its level-3 group's: the slot replaces its own lead3 entry, read only by itself)
+    // each member takes a slot of its group's member list at every level it belongs to
+    // (filled when its decode group is written below): level 1's goes to the first-page
+    // array, free again; level 2's to kLcp, free since the searches ended; a deeper level's
+    // replaces the request's own leader entry at that level, read only by itself
     #pragma unroll 1
     for (int i = tid; i < B; i += kThreads) {
         if (sa(kCgid)[i] < 0) continue;
         sa(kFirst)[i] = atomicAdd(&sa(kMpos)[sa(kLeader)[i]], 1);
-        if (sa(kCgid2)[i] >= 0) sa(kLcp)[i] = atomicAdd(&sa(kCnt)[sa(kLeader2)[i]], 1);
-        if (casc3_of(i) >= 0) g3(0)[i] = atomicAdd(&g3(2)[g3(0)[i]], 1);
+        if (n_levels < 2 || sa(kCgid2)[i] < 0) continue;
+        sa(kLcp)[i] = atomicAdd(&sa(kCnt)[sa(kLeader2)[i]], 1);
+        #pragma unroll 1
+        for (int L = 3; L <= n_levels; ++L) {
+            if (deep_level(p, L, 1)[i] < 0) break;
+            int32_t* lead = deep_level(p, L, 0);
+            lead[i] = atomicAdd(&deep_level(p, L, 2)[lead[i]], 1);
+        }
     }
 }
 
@@ -651,7 +662,6 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     __shared__ unsigned long long s_work;
     __shared__ int s_tmp3[kWarps][3];
     __shared__ int s_tmp2[kWarps][2];
-    __shared__ int s_tmp1[kWarps][1];
     __shared__ int s_hist_u[kBuckets];
     __shared__ int s_hist_t[kBuckets];
     __shared__ int s_casc_units;
@@ -703,13 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
     // group's prefix is the run of pages every member shares with the leader (whole pages
     // that lie strictly before each member's query, so no causal mask ever applies to it).
     int n_cgroups = 0;
-    int n_sub = 0;   // level-2 groups among them
-    int n_sub3 = 0;  // level-3 groups among them
-    // level 3's per-request arrays (a = 0: its leader, 1: group id, 2: member-slot cursors)
-    // live in the workspace's per-request scratch, unused on this path (detection needs the
-    // per-request arrays in shared memory); read only when a level-3 group exists.
-    // (Addressed where used: this kernel has 64 registers a thread.)
-    auto g3 = [&](int a) { return reinterpret_cast<int32_t*>(p.ws + p.lay.req_scratch) + a * (B + 1); };
+    int n_levels = 0;  // deepest level with a group (0: none)
     // shared-memory copy of the cascade group records (after the hash table)
     CascGroup* scg = reinterpret_cast<CascGroup*>(dyn + kNumArrays * stride +
                                                   2 * (casc ? (1 << casc_hash_bits(p.smem_batch)) : 0));
@@ -782,9 +786,10 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
             const int2 c = build_prefix_groups(p, dyn, s_tmp2);
             n_cgroups = c.x;
             const int members1 = c.y;
-            // ---- level 2: sub-groups inside each group, then level 3 inside those (the
-            // level-1 scratch arrays kFirst / kLcp serve both searches in turn)
+            // ---- level 2: sub-groups inside each group, then level 3 inside those, and so
+            // on (the level-1 scratch arrays kFirst / kLcp serve every search in turn)
             if (n_cgroups > 0) {
+                n_levels = 1;
                 if (tid == 0) {
                     s_cx.dyn = dyn;
                     s_cx.hkey = hkey;
@@ -803,40 +808,54 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
                     s_cx.max_groups = min(p.smem_batch + 1, p.lay.max_casc_groups);
                 }
                 __syncthreads();
-                // level 2 inside the top-level groups, then (when it found any) level 3 inside level
-                // 2's, through one call site (a second one cost the kernel registers)
+                // level 2 inside the top-level groups, then (while the last level found any)
+                // each next level inside the one before, through one call site (a second one
+                // cost the kernel registers)
                 int members = members1;
-                for (int level = 2; level <= 3; ++level) {
+                #pragma unroll 1
+                for (int level = 2; level <= kMaxCascLevels; ++level) {
                     const bool l2 = level == 2;
                     int m_new = 0;
-                    const int n_new = find_next_level(&s_cx, l2 ? sa(kCgid) : sa(kCgid2), sa(kFirst), sa(kLcp),
-                                                      l2 ? sa(kCnt) : g3(2), l2 ? sa(kLeader2) : g3(0),
-                                                      l2 ? sa(kCgid2) : g3(1), n_cgroups, members, s_tmp2, &m_new);
+                    const int n_new = find_next_level(
+                        &s_cx, l2 ? sa(kCgid) : level == 3 ? sa(kCgid2) : deep_level(p, level - 1, 1), sa(kFirst),
+                        sa(kLcp), l2 ? sa(kCnt) : deep_level(p, level, 2), l2 ? sa(kLeader2) : deep_level(p, level, 0),
+                        l2 ? sa(kCgid2) : deep_level(p, level, 1), n_cgroups, members, s_tmp2, &m_new);
                     n_cgroups += n_new;
                     members += m_new;
-                    if (l2) n_sub = n_new;
-                    else n_sub3 = n_new;
                     if (n_new == 0) break;
+                    n_levels = level;
                 }
             }
         }
     }
-    auto casc_of = [&](int i) { return casc && n_cgroups > 0 ? sa(kCgid)[i] : -1; };
-    auto casc2_of = [&](int i) { return casc && n_cgroups > 0 ? sa(kCgid2)[i] : -1; };
-    auto casc3_of = [&](int i) { return n_sub3 > 0 ? g3(1)[i] : -1; };
+    // request i's group at level L (-1: none; a member at level L is one at every level
+    // above it)
+    auto casc_at = [&](int i, int L) {
+        if (L > n_levels) return -1;
+        return L == 1 ? sa(kCgid)[i] : L == 2 ? sa(kCgid2)[i] : deep_level(p, L, 1)[i];
+    };
+    auto casc_of = [&](int i) { return casc_at(i, 1); };
     // keys before request i's decode tail: its deepest shared prefix (0 for no group)
     auto prefix_of = [&](int i) {
-        const int g3 = casc3_of(i);
-        if (g3 >= 0) return scg[g3].prefix_len;
-        const int g2 = casc2_of(i);
-        if (g2 >= 0) return scg[g2].prefix_len;
-        const int g = casc_of(i);
-        return g >= 0 ? scg[g].prefix_len : 0;
+        int lp = 0;
+        #pragma unroll 1
+        for (int L = 1; L <= n_levels; ++L) {
+            const int g = casc_at(i, L);
+            if (g < 0) break;
+            lp = scg[g].prefix_len;
+        }
+        return lp;
     };
     // prefix partial slots of request i (its groups' chunks)
     auto prefix_parts = [&](int i) {
-        const int g = casc_of(i), g2 = casc2_of(i), g3 = casc3_of(i);
-        return (g >= 0 ? scg[g].n_chunks : 0) + (g2 >= 0 ? scg[g2].n_chunks : 0) + (g3 >= 0 ? scg[g3].n_chunks : 0);
+        int np = 0;
+        #pragma unroll 1
+        for (int L = 1; L <= n_levels; ++L) {
+            const int g = casc_at(i, L);
+            if (g < 0) break;
+            np += scg[g].n_chunks;
+        }
+        return np;
     };
 
     // ---- pass 1: validate, count decode groups and prefill tiles, sum decode key extents
@@ -901,7 +920,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
 
     // ---- shared-prefix groups: key chunks, unit ranges, member lists (out of line)
     if (casc && n_cgroups > 0)
-        plan_prefix_chunks(p, dyn, make_int3(n_cgroups, n_sub, n_sub3), s_work, s_tmp2, s_tmp1, &s_casc_units);
+        plan_prefix_chunks(p, dyn, n_cgroups, n_levels, s_work, s_tmp2, &s_casc_units);
     __syncthreads();
     const int tiles_total = tot3[1] + s_casc_units;
     if (tot3[0] > p.lay.max_dec_groups || tiles_total > p.lay.max_pre_tiles) {
@@ -1084,7 +1103,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
             if (p.use_prefill && n > TB) continue;  // prefill units: emitted below
             const int ng = (n + TB - 1) / TB;
             const int lp = prefix_of(i);
-            const int cg = casc_of(i), cg2 = casc2_of(i), cg3 = casc3_of(i);
+            const int cg = casc_of(i);
             const int npre = prefix_parts(i);
             #pragma unroll 1
             for (int g = 0; g < ng; ++g) {
@@ -1108,11 +1127,20 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
                 dg.pad1 = dg.pad2 = dg.pad3 = dg.pad4 = dg.pad5 = 0;
                 store_record(&groups[gi], dg);
                 // member list entries of a shared-prefix member (one new token): its q row and
-                // the partial slot of chunk 0 of each of its groups (the group's chunks first,
-                // then the sub-group's)
-                if (cg >= 0) cmembers[sa(kFirst)[i]] = make_int2(dg.tok0, pi + s);
-                if (cg2 >= 0) cmembers[sa(kLcp)[i]] = make_int2(dg.tok0, pi + s + scg[cg].n_chunks);
-                if (cg3 >= 0) cmembers[g3(0)[i]] = make_int2(dg.tok0, pi + s + scg[cg].n_chunks + scg[cg2].n_chunks);
+                // the partial slot of chunk 0 of each of its groups, level by level (each
+                // level's chunks after those of the level above)
+                if (cg >= 0) {
+                    int slot = pi + s;
+                    cmembers[sa(kFirst)[i]] = make_int2(dg.tok0, slot);
+                    slot += scg[cg].n_chunks;
+                    #pragma unroll 1
+                    for (int lv = 2; lv <= n_levels; ++lv) {
+                        const int gl = casc_at(i, lv);
+                        if (gl < 0) break;
+                        cmembers[lv == 2 ? sa(kLcp)[i] : deep_level(p, lv, 0)[i]] = make_int2(dg.tok0, slot);
+                        slot += scg[gl].n_chunks;
+                    }
+                }
                 for (int u = 0; u < s; ++u) {
                     DecUnit du;
                     du.group = gi;
@@ -1168,6 +1196,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_kernel(PrepareParams p) {
         hdr->n_partial_slots = ok ? tot2[1] : 0;
         hdr->split_chunk = chunk;
         hdr->n_casc_groups = ok ? n_cgroups : 0;
+        hdr->n_casc_levels = ok ? n_levels : 0;
         hdr->n_casc_tiles = ok ? s_casc_units : 0;
         hdr->n_casc_units = ok ? s_casc_units : 0;
         hdr->max_group_tokens = ok ? s_max_ntok : 0;

@@ -23,6 +23,12 @@ constexpr int kPreKeys = 128;
 constexpr int kMinSplitChunk = 256;
 // Most key chunks one shared prefix is cut into for the cascade prefix pass.
 constexpr int kMaxCascChunks = 8;
+// Deepest level of the shared-prefix tree detected (level 1: a run of leading pages shared
+// by a group; level L + 1: a further run shared by some members of a level-L group).
+// With n levels in a batch each level's prefixes are cut into at most kMaxCascChunks / n
+// chunks, so every level keeps at least one.
+constexpr int kMaxCascLevels = 8;
+static_assert(kMaxCascLevels <= kMaxCascChunks, "every level keeps one prefix chunk");
 constexpr int kDecHeadBlock = 8;     // kv heads one decode CTA serves (more: several CTAs per unit)
 constexpr int kMinDecShare = 128;    // fewest keys a decode CTA gets in the balanced split
 // Keys the balanced split charges for starting a group's piece: on the key line each group is
@@ -59,7 +65,8 @@ struct PlanHeader {
     int32_t dec_share;         // keys per decode CTA of the balanced split; 0: the work queue
     uint32_t wait_override;    // tests only: wait limit in ns + 1 for the forward kernels' work
                                // waits (attn_debug_set_wait_limit); 0 (set by prepare): default
-    int32_t pad[52];           // pad[0] / pad[1]: decode / tensor-core work counters
+    int32_t n_casc_levels;     // deepest shared-prefix level with a group (0: none)
+    int32_t pad[51];           // pad[0] / pad[1]: decode / tensor-core work counters
 };
 static_assert(sizeof(PlanHeader) == 256, "header is one 256-byte line");
 
@@ -147,7 +154,8 @@ struct Layout {
     size_t partial_lse;  // fp32 [max_partial][rows_per_slot]
     size_t req_scratch;  // int32 [max_batch * 4] prepare scratch
     size_t casc_groups;  // CascGroup [max_casc_groups]
-    size_t casc_members; // int2 [max_batch]: member's token, partial slot of its prefix chunk 0
+    size_t casc_members; // int2 [kMaxCascLevels * max_batch]: member's token, partial slot of its prefix chunk 0
+    size_t casc_deep;    // int32 [3 * (kMaxCascLevels - 2) * (max_batch + 1)]: levels 3 and deeper, per request
     size_t dec_first;    // int32 [dec_ctas + 1]: balanced split, first group of each CTA's keys
     size_t total;
     int32_t max_dec_units;

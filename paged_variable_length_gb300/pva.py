@@ -193,10 +193,10 @@ def attn_get_device_status(meta: Meta) -> int:
 
 
 def attn_debug_plan_counts(meta: Meta) -> dict:
-    arr = (ctypes.c_int64 * 8)()
-    n = load().attn_debug_plan_counts(ctypes.byref(meta), arr, 8)
+    arr = (ctypes.c_int64 * 9)()
+    n = load().attn_debug_plan_counts(ctypes.byref(meta), arr, 9)
     keys = ("dec_units", "dec_groups", "pre_tiles", "casc_groups", "casc_tiles", "split_chunk", "partial_slots",
-            "kernels_per_forward")
+            "kernels_per_forward", "casc_levels")
     return {keys[i]: int(arr[i]) for i in range(n)}
 
 

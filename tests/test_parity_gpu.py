@@ -432,6 +432,69 @@ def test_full_size_three_level_prefix_tree():
     _sampled_check(wl)
 
 
+def _deep_tree(seed, depth, fanout=2, Hq=32, Hkv=8, D=128, ps=16, min_pages=8):
+    """A shared-prefix tree `depth` levels deep: every node extends its parent's pages by a
+    run of min_pages to min_pages + 3 pages and has `fanout` child nodes (the deepest
+    nodes three single-token decodes each, with private tails); about half of the inner
+    nodes (all of them in a chain, fanout 1, where otherwise two levels would share one
+    prefix) also have a decode that ends there.  Plus an unrelated decode and a prefill."""
+    rng = np.random.default_rng(7000 + seed)
+    P = 1500 if ps > 1 else 8000
+    perm = [int(x) for x in rng.permutation(P)]
+    take = lambda k: [perm.pop() for _ in range(int(k))]
+    rows, q_lens, kv_lens = [], [], []
+
+    def add(shared, tail, n=1):
+        L = len(shared) * ps + tail
+        rows.append(shared + take((L + ps - 1) // ps - len(shared)))
+        q_lens.append(n)
+        kv_lens.append(L)
+
+    def node(shared, level):
+        run = shared + take(rng.integers(min_pages, min_pages + 4))
+        if level == depth:
+            for _ in range(3):
+                add(run, int(rng.integers(1, 60)))
+            return
+        for _ in range(fanout):
+            node(run, level + 1)
+        if fanout == 1 or rng.random() < 0.5:
+            add(run, int(rng.integers(1, 60)))
+
+    node([], 1)
+    add([], 400)                                # unrelated decode
+    L = 150                                     # a prefill in the same batch
+    rows.append(take((L + ps - 1) // ps)); q_lens.append(L); kv_lens.append(L)
+    order = rng.permutation(len(rows))          # requests in any order
+    rows = [rows[i] for i in order]
+    return _table_workload([q_lens[i] for i in order], [kv_lens[i] for i in order], rows, Hq, Hkv, D, ps, P, seed)
+
+
+@pytest.mark.parametrize("depth,fanout", [(4, 2), (6, 2), (8, 1)])
+def test_deep_prefix_trees(depth, fanout):
+    """Trees of 4, 6 and 8 levels: every level is found, and each member merges one
+    partial per level with its tail."""
+    wl = _deep_tree(depth, depth, fanout)
+    _, eng = _full_check(wl)
+    assert pva.attn_debug_plan_counts(eng.meta)["casc_levels"] == depth
+    _full_check(wl, enable_cascade=False)
+
+
+def test_prefix_tree_deeper_than_the_levels_found():
+    """A chain of 11 nested shared runs: the first eight are prefix levels, the rest are
+    read as part of each member's own keys."""
+    wl = _deep_tree(11, 11, fanout=1)
+    _, eng = _full_check(wl)
+    assert pva.attn_debug_plan_counts(eng.meta)["casc_levels"] == 8
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,ps", [(28, 4, 128, 16), (16, 4, 64, 16), (32, 8, 128, 64), (32, 8, 128, 1)])
+def test_deep_prefix_tree_layouts(Hq, Hkv, D, ps):
+    wl = _deep_tree(20 + ps, 5, 2, Hq=Hq, Hkv=Hkv, D=D, ps=ps)
+    _, eng = _full_check(wl)
+    assert pva.attn_debug_plan_counts(eng.meta)["casc_levels"] == 5
+
+
 def test_sub_group_larger_than_a_tile_pair():
     """A sub-group of 70 members (G 4: 32 member rows per tile) under a 27-page root
     (432 keys: the sub-group's keys start off a 128-key boundary), a second sub-group of
@@ -558,8 +621,8 @@ def _random_forest(seed, Hq=32, Hkv=8, D=128, ps=16, min_pages=8, P=4000):
     """Random shared-prefix forests: 1-3 roots of min_pages-1 .. min_pages+5 pages (some too
     short for a group), each with 1-3 branches of min_pages-1 .. min_pages+3 further
     pages, leaves that sometimes share a third run (a third level when long enough) and
-    a fourth (below the deepest level detected: it runs as part of their tails), leaves cut
-    short inside a shared run, multi-token decodes
+    a fourth (a fourth level when long enough), leaves cut short inside a shared run,
+    multi-token decodes
     (never prefix members), unrelated decodes and a prefill."""
     rng = np.random.default_rng(1000 + seed)
     rng4 = np.random.default_rng(3000 + seed)
