@@ -188,3 +188,15 @@ def test_fp8_two_level_prefix_tree():
 
     wl = _tree_batch(seed=2)
     _fp8_case(wl)
+
+
+def test_fp8_deep_prefix_tree():
+    """Six levels of shared prefixes (two child runs under every node) in one FP8 batch."""
+    from test_parity_gpu import _deep_tree
+
+    wl = _deep_tree(31, 6, 2)
+    t = W.make_tensors(wl, DEV)
+    eng = make_engine(wl, kv_dtype=pva.KV_E4M3)
+    eng.prepare(t["cu_seqlens_q"], t["cache_seqlens"], t["page_table"], wl.total_tokens)
+    assert pva.attn_debug_plan_counts(eng.meta)["casc_levels"] == 6
+    _fp8_case(wl)
