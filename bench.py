@@ -36,7 +36,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="decode",
                     choices=["worked", "decode", "prefill", "mixed", "cascade", "cascade_tree", "cascade_tree3",
-                             "specdec", "ragged"])
+                             "cascade_deep", "specdec", "ragged"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -536,6 +536,7 @@ CONFIGS = [
     ("cascade_off", "cascade", {"enable_cascade": False}),
     ("cascade_tree", "cascade_tree", {}),
     ("cascade_tree3", "cascade_tree3", {}),
+    ("cascade_deep", "cascade_deep", {}),
     ("decode_e4m3", "decode", {"fp8": True}),
 ]
 

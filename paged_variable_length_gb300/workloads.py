@@ -223,6 +223,44 @@ def cascade_tree3(seed: int = 0, fanout=(4, 4), per_leaf: int = 8, runs=(1024, 1
                                 f"Hq32/Hkv8/D128, ps{page_size}, {num_pages}-page pool")
 
 
+def cascade_deep(seed: int = 0, levels: int = 6, run: int = 512, per_leaf: int = 4, lo: int = 16, hi: int = 512,
+                 page_size: int = 16, num_pages: int = 20000) -> Workload:
+    """A binary prefix tree ``levels`` deep of single-token decodes: every row starts with
+    the same ``run``-token run of pages, and at each further level the rows of a node split
+    into two halves that each add a ``run``-token run of their own; each of the
+    2^(levels-1) leaves holds ``per_leaf`` rows, which end in private tails of U[lo, hi]
+    tokens.  Default: six levels of 512 tokens, 32 leaves of 4 rows (128 decodes); Hq 32,
+    Hkv 8, D 128; page_size 16 over a 20000-page pool."""
+    rng = np.random.default_rng(seed)
+    if run % page_size:
+        raise ValueError("the shared runs are whole pages")
+    perm = [int(x) for x in rng.permutation(num_pages)]
+    take = lambda k: [perm.pop() for _ in range(k)]
+    rows, kv_lens = [], []
+
+    def node(pages, level):
+        pages = pages + take(run // page_size)
+        if level == levels:
+            for _ in range(per_leaf):
+                L = levels * run + int(rng.integers(lo, hi + 1))
+                rows.append(pages + take(math.ceil(L / page_size) - len(pages)))
+                kv_lens.append(L)
+            return
+        for _ in range(2):
+            node(pages, level + 1)
+
+    node([], 1)
+    table = np.zeros((len(rows), max(len(r) for r in rows)), np.int32)
+    for i, r in enumerate(rows):
+        table[i, :len(r)] = r
+    return Workload("cascade_deep", [1] * len(rows), kv_lens, 32, 8, 128, page_size, num_pages, table, 1.0, seed,
+                    shared_prefix_pages=run // page_size,
+                    extra={"levels": levels, "run": run, "per_leaf": per_leaf},
+                    description=f"cascade tree, {levels} levels: binary, {2 ** (levels - 1)}x{per_leaf} decodes, "
+                                f"{run}-token shared run a level, tails U[{lo},{hi}], Hq32/Hkv8/D128, "
+                                f"ps{page_size}, {num_pages}-page pool")
+
+
 def ragged_prefill(seed: int = 0, batch: int = 8, lo: int = 256, hi: int = 4096) -> Workload:
     """The prefill workload's requests (8 fresh prefills, len U[256,4096], Hq 32, Hkv 8,
     D 128) over contiguous K/V: page_size 1, the "pool" is the batch's own k / v rows and
@@ -272,6 +310,7 @@ WORKLOADS = {
     "cascade": cascade,
     "cascade_tree": cascade_tree,
     "cascade_tree3": cascade_tree3,
+    "cascade_deep": cascade_deep,
     "specdec": spec_decode,
     "ragged": ragged_prefill,
 }

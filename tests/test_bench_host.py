@@ -110,3 +110,19 @@ def test_work_model_counts_a_prefix_tree_once():
     rp, bp = root // wl.page_size, branch // wl.page_size
     assert len({tuple(r[:rp]) for r in wl.page_table}) == 1
     assert len({tuple(r[rp:rp + bp]) for r in wl.page_table}) == branches
+
+
+def test_work_model_counts_a_deep_prefix_tree_once():
+    """Six binary levels: every node's run once, every private tail once."""
+    levels, run, per_leaf = 6, 64, 2
+    wl = W.cascade_deep(0, levels=levels, run=run, per_leaf=per_leaf, lo=16, hi=40, num_pages=2000)
+    work = bench.algorithmic_work(wl)
+    row = wl.num_kv_heads * wl.head_dim * 2
+    nodes = 2 ** levels - 1
+    tails = [L - levels * run for L in wl.kv_lens]
+    assert len(tails) == 2 ** (levels - 1) * per_leaf and min(tails) >= 16
+    assert work["kv_bytes"] == 2 * (nodes * run + sum(tails)) * row
+    # the page table has the tree's structure: 2^(l-1) distinct runs at level l
+    rp = run // wl.page_size
+    for lv in range(levels):
+        assert len({tuple(r[lv * rp:(lv + 1) * rp]) for r in wl.page_table}) == 2 ** lv

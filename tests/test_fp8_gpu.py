@@ -150,7 +150,8 @@ def _fp8_sampled(wl, n_rows=1500, seed=0):
     return pva.attn_debug_plan_counts(eng.meta)
 
 
-@pytest.mark.parametrize("name", ["prefill", "mixed", "cascade", "cascade_tree", "cascade_tree3", "specdec"])
+@pytest.mark.parametrize("name", ["prefill", "mixed", "cascade", "cascade_tree", "cascade_tree3", "cascade_deep",
+                                  "specdec"])
 def test_fp8_full_size_workloads(name):
     counts = _fp8_sampled(W.WORKLOADS[name](0))
     if name == "cascade":
@@ -159,6 +160,8 @@ def test_fp8_full_size_workloads(name):
         assert counts["casc_groups"] == 9, "a root group and 8 branch sub-groups"
     if name == "cascade_tree3":
         assert counts["casc_groups"] == 21, "a root group, 4 branches and 16 twigs"
+    if name == "cascade_deep":
+        assert counts["casc_levels"] == 6, "a binary tree six levels deep"
     if name in ("prefill", "mixed"):
         assert counts["pre_tiles"] > 0, "prefills should run on the tensor-core kernel"
 

@@ -432,6 +432,17 @@ def test_full_size_three_level_prefix_tree():
     _sampled_check(wl)
 
 
+def test_full_size_six_level_prefix_tree():
+    """128 decodes in a binary prefix tree six levels deep, 512 shared tokens a level."""
+    wl = W.cascade_deep(0)
+    t = W.make_tensors(wl, DEV)
+    eng = make_engine(wl)
+    eng.prepare(t["cu_seqlens_q"], t["cache_seqlens"], t["page_table"], wl.total_tokens)
+    counts = pva.attn_debug_plan_counts(eng.meta)
+    assert counts["casc_levels"] == 6 and counts["casc_groups"] == 1 + 2 + 4 + 8 + 16 + 32, counts
+    _sampled_check(wl)
+
+
 def _deep_tree(seed, depth, fanout=2, Hq=32, Hkv=8, D=128, ps=16, min_pages=8):
     """A shared-prefix tree `depth` levels deep: every node extends its parent's pages by a
     run of min_pages to min_pages + 3 pages and has `fanout` child nodes (the deepest
