@@ -58,15 +58,15 @@ def parse():
 # what they were at capture time; after any change the roofline reports null.
 NCU_TRAFFIC = {
     ("decode", "decode"): {
-        "bytes": 617.257472e6,
+        "bytes": 617.539328e6,
         "sources": ['paged_variable_length_gb300/csrc/decode.cu', 'paged_variable_length_gb300/csrc/device_utils.cuh', 'paged_variable_length_gb300/csrc/pva_internal.h'],
-        "sha256_16": "b88e677d84d563c6",
+        "sha256_16": "613cd1f6c6e4c52d",
         "summary": "profiles/decode_kernel_decode_workload.md",
     },
     ("tensor_core", "prefill"): {
-        "bytes": 219.720960e6,
+        "bytes": 220.163328e6,
         "sources": ['paged_variable_length_gb300/csrc/prefill_tc.cu', 'paged_variable_length_gb300/csrc/device_utils.cuh', 'paged_variable_length_gb300/csrc/tc_utils.cuh', 'paged_variable_length_gb300/csrc/pva_internal.h'],
-        "sha256_16": "1198d80cd3594772",
+        "sha256_16": "8f5604412ac531c8",
         "summary": "profiles/prefill_kernel_prefill_workload.md",
     },
 }
